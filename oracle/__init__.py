@@ -1,0 +1,17 @@
+"""Test infrastructure: a float64 CPU oracle for exact attention forward.
+
+Only the test-suite, the package's ``smoke()`` check and the benchmark's CPU
+baseline leg may import this package.  The library's own compute path never
+imports, calls or links anything in here, and nothing in here imports the
+library.
+"""
+
+from .attention_ref import (  # noqa: F401
+    masked_attention,
+    prefill,
+    prefill_rows,
+    gather_sequence,
+    decode,
+    decode_partials,
+    combine,
+)

@@ -1,0 +1,426 @@
+"""Pins for the float64 oracle: checks against what the pages and mathematics
+fix, none of which re-types the oracle's own formula.
+
+* the worked example printed on "FlashAttention for inference: tiled prefill
+  and split-KV decoding", §"A worked example by hand" (tests/golden);
+* brute force with scalar loops, ``math.exp`` and ``math.fsum``;
+* a library routine: torch's float64 CPU ``scaled_dot_product_attention``;
+* closed forms and invariants (q = 0, first row, V = 1, key shift, GQA as
+  repeated MHA, paged == contiguous, decode == last prefill row);
+* the chunk-combine identity (§"The online softmax, with every symbol
+  defined", combining partial results) over random chunkings;
+* the page's toy run (§"Toy run: tiling and splitting are exact"), re-created
+  here with a test-only tiled prefill and split-KV decode;
+* planted mistakes: each mutation of the oracle below must break a pin.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import attention_ref as ref
+from exact_io_aware_order_gb300 import workloads as W
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+TOL = 1e-13
+
+
+def _f64(t):
+    return t.to(torch.float64).numpy() if isinstance(t, torch.Tensor) else np.asarray(t, np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Test-only restatement of the online softmax update (page §"The online
+# softmax ...", reconstructed from the prefill pseudo-code and the worked
+# example): m_j = max(m_{j-1}, max s_j); c_j = exp(m_{j-1} - m_j);
+# l_j = c_j l_{j-1} + sum exp(s_j - m_j); o~_j = c_j o~_{j-1} + sum exp(s_j - m_j) v_j.
+# ---------------------------------------------------------------------------
+
+def _online_blocks(scores, values, block):
+    """Returns the per-block trace [(m, c, l, otilde)] and final (o, lse)."""
+    m, l, ot = -math.inf, 0.0, np.zeros(values.shape[1:])
+    trace = []
+    for b0 in range(0, len(scores), block):
+        s = np.asarray(scores[b0:b0 + block], np.float64)
+        vb = np.asarray(values[b0:b0 + block], np.float64)
+        m_new = max(m, float(s.max()))
+        c = math.exp(m - m_new) if m != -math.inf else 0.0
+        p = np.exp(s - m_new)
+        l = c * l + p.sum()
+        ot = c * ot + (p[:, None] * vb).sum(0) if vb.ndim == 2 else c * ot + (p * vb).sum()
+        m = m_new
+        trace.append((m, c, l, np.array(ot, copy=True)))
+    return trace, ot / l, m + math.log(l)
+
+
+# ---------------------------------------------------------------------------
+# Worked example.
+# ---------------------------------------------------------------------------
+
+def test_worked_example_direct(golden):
+    g = golden("worked_example.txt")
+    s = np.array(g["scores"])
+    v = np.array(g["values"])[:, None]
+    # d = 1, q = 1, k = s, scale = 1 makes the scores exactly s.
+    o, lse = oracle.masked_attention(np.ones((1, 1)), s[:, None], v, 1.0)
+    assert abs(o[0, 0] - g["result_o"]) <= 0.5e-4
+    assert abs(math.exp(lse[0]) - g["exp_sum"]) <= 0.5e-3
+    assert np.allclose(np.exp(s), g["exp_scores"], atol=0.5e-3)
+
+
+def test_worked_example_blocks_and_combine(golden):
+    g = golden("worked_example.txt")
+    s = np.array(g["scores"])
+    v = np.array(g["values"])
+    trace, o, lse = _online_blocks(s, v, 2)
+    (m1, _, l1, ot1), (m2, c2, l2, ot2) = trace
+    assert m1 == g["block1_m"] and m2 == g["block2_m"]
+    assert abs(l1 - g["block1_l"]) <= 0.5e-4
+    assert abs(float(ot1) - g["block1_otilde"]) <= 0.5e-4
+    assert abs(float(ot1) / l1 - g["block1_interim"]) <= 0.5e-4
+    assert abs(c2 - g["block2_c"]) <= 0.5e-4
+    assert abs(l2 - g["block2_l"]) <= 0.5e-4
+    assert abs(float(ot2) - g["block2_otilde"]) <= 0.5e-4
+    assert abs(float(o) - g["result_o"]) <= 0.5e-4
+    # The oracle's per-block results merged by its combine rule give the same
+    # answer as the oracle on the whole row.
+    parts = [oracle.masked_attention(np.ones((1, 1)), s[i:i + 2, None], v[i:i + 2, None], 1.0)
+             for i in (0, 2)]
+    oc, lc = oracle.combine(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    ow, lw = oracle.masked_attention(np.ones((1, 1)), s[:, None], v[:, None], 1.0)
+    assert abs(oc[0, 0] - g["result_o"]) <= 0.5e-4
+    assert abs(oc[0, 0] - ow[0, 0]) <= TOL and abs(lc[0] - lw[0]) <= TOL
+    assert abs(lse - lw[0]) <= TOL
+
+
+# ---------------------------------------------------------------------------
+# Brute force: scalar loops with math.exp / math.fsum.
+# ---------------------------------------------------------------------------
+
+def _brute_prefill(q, k, v, scale, causal):
+    B, nq, N, d = q.shape
+    nkv = k.shape[1]
+    g = nq // nkv
+    o = np.zeros(q.shape)
+    lse = np.zeros((B, nq, N))
+    for b in range(B):
+        for h in range(nq):
+            kh = h // g
+            for i in range(N):
+                js = range(i + 1) if causal else range(N)
+                sc = [scale * math.fsum(q[b, h, i, t] * k[b, kh, j, t] for t in range(d)) for j in js]
+                m = max(sc)
+                z = math.fsum(math.exp(x - m) for x in sc)
+                lse[b, h, i] = m + math.log(z)
+                for t in range(d):
+                    o[b, h, i, t] = math.fsum(math.exp(x - lse[b, h, i]) * v[b, kh, j, t]
+                                              for x, j in zip(sc, js))
+    return o, lse
+
+
+def _pin_bruteforce():
+    worst = 0.0
+    for (B, nq, nkv, N, d, causal) in [(1, 1, 1, 1, 4, True), (1, 2, 1, 2, 3, True),
+                                       (2, 2, 2, 3, 8, True), (1, 4, 2, 5, 8, False),
+                                       (1, 3, 1, 17, 5, True), (1, 2, 2, 33, 8, True),
+                                       (1, 2, 1, 17, 8, False)]:
+        x = W.make_prefill(B, nq, nkv, N, d, seed=N + d)
+        q, k, v = _f64(x.q), _f64(x.k), _f64(x.v)
+        ob, lb = _brute_prefill(q, k, v, x.scale, causal)
+        oo, lo = oracle.prefill(x.q, x.k, x.v, x.scale, causal)
+        worst = max(worst, np.abs(ob - oo).max(), np.abs(lb - lo).max())
+    return worst
+
+
+def test_bruteforce_tiny_shapes():
+    assert _pin_bruteforce() <= TOL
+
+
+# ---------------------------------------------------------------------------
+# Library routine: torch float64 SDPA (GQA expressed by repeating K/V).
+# ---------------------------------------------------------------------------
+
+def _pin_sdpa():
+    worst = 0.0
+    for (B, nq, nkv, N, d, causal) in [(1, 4, 2, 300, 64, True), (2, 6, 3, 129, 32, False),
+                                       (1, 7, 1, 200, 128, True)]:
+        x = W.make_prefill(B, nq, nkv, N, d, seed=7)
+        g = nq // nkv
+        q = x.q.double()
+        k = x.k.double().repeat_interleave(g, dim=1)
+        v = x.v.double().repeat_interleave(g, dim=1)
+        ref_o = torch.nn.functional.scaled_dot_product_attention(
+            q, k, v, is_causal=causal, scale=x.scale).numpy()
+        oo, lo = oracle.prefill(x.q, x.k, x.v, x.scale, causal)
+        worst = max(worst, np.abs(ref_o - oo).max())
+        # LSE through scipy's logsumexp over the masked score matrix.
+        from scipy.special import logsumexp
+        sc = (q @ k.transpose(-1, -2)).numpy() * x.scale
+        if causal:
+            sc = np.where(np.tril(np.ones((N, N), bool)), sc, -np.inf)
+        worst = max(worst, np.abs(logsumexp(sc, axis=-1) - lo).max())
+    return worst
+
+
+def test_library_sdpa_float64():
+    assert _pin_sdpa() <= 1e-12
+
+
+# ---------------------------------------------------------------------------
+# Closed forms and invariants.
+# ---------------------------------------------------------------------------
+
+def _pin_closed_forms():
+    worst = 0.0
+    x = W.make_prefill(1, 2, 1, 70, 16, seed=3)
+    N = 70
+    # q = 0: every score is 0, LSE_i = ln(i+1), O_i = mean(v_0..v_i).
+    q0 = torch.zeros_like(x.q)
+    o, lse = oracle.prefill(q0, x.k, x.v, x.scale, True)
+    v = _f64(x.v)[0, 0]
+    prefix_mean = np.cumsum(v, axis=0) / np.arange(1, N + 1)[:, None]
+    worst = max(worst, np.abs(lse[0, 0] - np.log(np.arange(1, N + 1))).max(),
+                np.abs(o[0, 1] - prefix_mean).max())
+    # Row 0 of causal prefill: O_0 = v_0, LSE_0 = s_00.
+    o, lse = oracle.prefill(x.q, x.k, x.v, x.scale, True)
+    s00 = x.scale * math.fsum(_f64(x.q)[0, 0, 0] * _f64(x.k)[0, 0, 0])
+    worst = max(worst, np.abs(o[0, 0, 0] - v[0]).max(), abs(lse[0, 0, 0] - s00))
+    # V = 1 gives O = 1.
+    o1, _ = oracle.prefill(x.q, x.k, torch.ones_like(x.v), x.scale, True)
+    worst = max(worst, np.abs(o1 - 1.0).max())
+    # Adding c to every key leaves O unchanged and shifts LSE_i by scale q_i.c.
+    c = torch.linspace(-0.5, 0.5, 16, dtype=torch.float64)
+    ks = x.k.double() + c
+    o2, lse2 = oracle.prefill(x.q, ks, x.v, x.scale, True)
+    shift = x.scale * (_f64(x.q) @ c.numpy())
+    worst = max(worst, np.abs(o2 - o).max() / 1e2, np.abs(lse2 - lse - shift).max() / 1e2)
+    return worst
+
+
+def test_closed_forms():
+    assert _pin_closed_forms() <= TOL
+
+
+def _pin_gqa():
+    """GQA equals MHA with each kv head repeated g times (consecutive groups)."""
+    x = W.make_prefill(1, 6, 2, 40, 8, seed=5)
+    o, lse = oracle.prefill(x.q, x.k, x.v, x.scale, True)
+    om, lm = oracle.prefill(x.q, x.k.repeat_interleave(3, dim=1),
+                            x.v.repeat_interleave(3, dim=1), x.scale, True)
+    return max(np.abs(o - om).max(), np.abs(lse - lm).max())
+
+
+def test_gqa_is_repeated_mha():
+    assert _pin_gqa() <= TOL
+
+
+def test_decode_equals_last_prefill_row_and_paged_equals_contiguous():
+    N, nq, nkv, d = 97, 4, 2, 16
+    x = W.make_prefill(1, nq, nkv, N, d, seed=11)
+    op, lp = oracle.prefill(x.q, x.k, x.v, x.scale, True)
+    # Contiguous cache (B, L, n_kv, d) holding the same keys/values.
+    kc = x.k[0].permute(1, 0, 2).unsqueeze(0).contiguous()
+    vc = x.v[0].permute(1, 0, 2).unsqueeze(0).contiguous()
+    q = x.q[:, :, N - 1]
+    od, ld = oracle.decode(q, kc, vc, None, [N], x.scale)
+    assert np.abs(od - op[:, :, N - 1]).max() <= TOL
+    assert np.abs(ld - lp[:, :, N - 1]).max() <= TOL
+    # The same tokens laid out in a paged cache through a permuted block table.
+    bs = 8
+    nb = (N + bs - 1) // bs
+    perm = torch.randperm(nb + 3, generator=torch.Generator().manual_seed(2))
+    kp = torch.zeros(nb + 3, bs, nkv, d, dtype=torch.float64)
+    vp = torch.zeros_like(kp)
+    table = torch.zeros(1, nb, dtype=torch.int32)
+    for j in range(nb):
+        t0, t1 = j * bs, min(N, (j + 1) * bs)
+        kp[perm[j], :t1 - t0] = kc[0, t0:t1].double()
+        vp[perm[j], :t1 - t0] = vc[0, t0:t1].double()
+        table[0, j] = int(perm[j])
+    # Slots past the last token hold NaN: they must never be read.
+    kp[perm[nb - 1], N - (nb - 1) * bs:] = float("nan")
+    vp[perm[nb - 1], N - (nb - 1) * bs:] = float("nan")
+    og, lg = oracle.decode(q, kp, vp, table, [N], x.scale, bs)
+    assert np.abs(og - od).max() <= TOL and np.abs(lg - ld).max() <= TOL
+
+
+def test_empty_sequence_and_empty_split():
+    x = W.make_decode_contiguous(2, 4, 2, 16, 5, seed=1)
+    lens = [0, 5]
+    o, lse = oracle.decode(x.q, x.k_cache, x.v_cache, None, lens, x.scale)
+    assert np.all(o[0] == 0.0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(lse[1]))
+    ranges = [[(0, 0), (0, 0)], [(0, 3), (3, 3)]]
+    op, lp = oracle.decode_partials(x.q, x.k_cache, x.v_cache, None, lens, x.scale, 0, ranges)
+    assert np.all(np.isneginf(lp[:, 0])) and np.all(op[:, 0] == 0)
+    assert np.all(np.isneginf(lp[1, 1])) and np.all(op[1, 1] == 0)
+    oc, lc = oracle.combine(op, lp)
+    assert np.all(oc[0] == 0.0) and np.all(np.isneginf(lc[0]))
+
+
+# ---------------------------------------------------------------------------
+# Chunk-combine identity.
+# ---------------------------------------------------------------------------
+
+def _pin_combine():
+    rng = np.random.default_rng(0)
+    worst = 0.0
+    x = W.make_decode_contiguous(1, 6, 2, 32, 300, seed=4)
+    o_full, l_full = oracle.decode(x.q, x.k_cache, x.v_cache, None, [300], x.scale)
+    for trial in range(6):
+        cuts = np.sort(rng.choice(np.arange(0, 301), size=rng.integers(1, 7), replace=True))
+        bounds = [0] + cuts.tolist() + [300]
+        ranges = [[(bounds[i], bounds[i + 1]) for i in range(len(bounds) - 1)] + [(0, 0)]]
+        op, lp = oracle.decode_partials(x.q, x.k_cache, x.v_cache, None, [300], x.scale, 0, ranges)
+        oc, lc = oracle.combine(op, lp)
+        worst = max(worst, np.abs(oc - o_full).max(), np.abs(lc - l_full).max())
+        perm = rng.permutation(op.shape[0])           # order of chunks is irrelevant
+        oc2, lc2 = oracle.combine(op[perm], lp[perm])
+        worst = max(worst, np.abs(oc2 - oc).max(), np.abs(lc2 - lc).max())
+    return worst
+
+
+def test_combine_identity_random_chunkings():
+    assert _pin_combine() <= TOL
+
+
+def test_combine_matches_softmax_over_chunks_rule():
+    """The page's merge rule: weights = softmax of the LSEs over the chunk axis."""
+    rng = np.random.default_rng(1)
+    o_parts = rng.standard_normal((5, 3, 7))
+    lse_parts = rng.standard_normal((5, 3)) * 4
+    w = torch.softmax(torch.as_tensor(lse_parts), dim=0).numpy()
+    o, lse = oracle.combine(o_parts, lse_parts)
+    assert np.abs(o - (w[..., None] * o_parts).sum(0)).max() <= TOL
+    assert np.abs(lse - torch.logsumexp(torch.as_tensor(lse_parts), 0).numpy()).max() <= TOL
+
+
+# ---------------------------------------------------------------------------
+# The page's toy run, re-created with test-only tiled / split restatements.
+# ---------------------------------------------------------------------------
+
+def _tiled_prefill_head(q, k, v, scale, tile):
+    """FA-2 loop order with the online softmax, causal, float64 (test-only)."""
+    N, d = q.shape
+    o = np.zeros((N, d))
+    lse = np.zeros(N)
+    for i0 in range(0, N, tile):
+        qi = q[i0:i0 + tile]
+        r = qi.shape[0]
+        m = np.full(r, -np.inf)
+        l = np.zeros(r)
+        acc = np.zeros((r, d))
+        for j0 in range(0, min(N, i0 + r), tile):
+            s = scale * qi @ k[j0:j0 + tile].T
+            rows = np.arange(i0, i0 + r)[:, None]
+            cols = np.arange(j0, j0 + s.shape[1])[None, :]
+            s = np.where(cols <= rows, s, -np.inf)
+            m_new = np.maximum(m, s.max(1))
+            p = np.exp(s - m_new[:, None])
+            c = np.exp(m - m_new)
+            l = c * l + p.sum(1)
+            acc = c[:, None] * acc + p @ v[j0:j0 + tile]
+            m = m_new
+        o[i0:i0 + r] = acc / l[:, None]
+        lse[i0:i0 + r] = m + np.log(l)
+    return o, lse
+
+
+def test_toy_run_tiled_prefill(golden):
+    g = golden("toy_run.txt")
+    N, d, tile = int(g["prefill_seqlen"]), int(g["prefill_head_dim"]), int(g["prefill_tile"])
+    x = W.make_prefill(1, 1, 1, N, d, seed=0)
+    q, k, v = _f64(x.q)[0, 0], _f64(x.k)[0, 0], _f64(x.v)[0, 0]
+    ot, lt = _tiled_prefill_head(q, k, v, x.scale, tile)
+    oo, lo = oracle.prefill(x.q, x.k, x.v, x.scale, True)
+    # The page measured 1.1e-15; allow a little more for our own summation order.
+    assert np.abs(ot - oo[0, 0]).max() <= 100 * g["prefill_max_abs_diff"]
+    assert np.abs(lt - lo[0, 0]).max() <= TOL
+
+
+def test_toy_run_split_decode(golden):
+    g = golden("toy_run.txt")
+    H, L, chunk = int(g["decode_query_heads"]), int(g["decode_cache_len"]), int(g["decode_chunk"])
+    x = W.make_decode_contiguous(1, H, H, 128, L, seed=0)
+    q = _f64(x.q)[0]
+    kc, vc = _f64(x.k_cache)[0], _f64(x.v_cache)[0]
+    o_parts, l_parts = [], []
+    for t0 in range(0, L, chunk):              # each chunk: its own online softmax
+        oh, lh = [], []
+        for h in range(H):
+            s = x.scale * kc[t0:t0 + chunk, h] @ q[h]
+            _, o, lse = _online_blocks(s, vc[t0:t0 + chunk, h], 64)
+            oh.append(o)
+            lh.append(lse)
+        o_parts.append(np.stack(oh))
+        l_parts.append(np.array(lh))
+    o_parts, l_parts = np.stack(o_parts), np.stack(l_parts)
+    w = np.exp(l_parts - l_parts.max(0))       # merge by LSE weights (test-only)
+    o_split = (w[..., None] * o_parts).sum(0) / w.sum(0)[..., None]
+    oo, lo = oracle.decode(x.q, x.k_cache, x.v_cache, None, [L], x.scale)
+    assert np.abs(o_split - oo[0]).max() <= 100 * g["decode_max_abs_diff"]
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: every mutation must break at least one pin.
+# ---------------------------------------------------------------------------
+
+def _pins():
+    return {"bruteforce": (_pin_bruteforce, TOL), "sdpa": (_pin_sdpa, 1e-12),
+            "closed": (_pin_closed_forms, TOL), "gqa": (_pin_gqa, TOL),
+            "combine": (_pin_combine, TOL)}
+
+
+def _any_pin_fails():
+    failed = []
+    for name, (fn, tol) in _pins().items():
+        try:
+            err = fn()
+        except Exception:  # a crash counts as a caught mistake
+            err = math.inf
+        if not (err <= tol):
+            failed.append(name)
+    return failed
+
+
+def test_pins_pass_unmutated():
+    assert _any_pin_fails() == []
+
+
+@pytest.mark.parametrize("mutation", ["gqa_modulo", "strict_mask", "no_scale", "lse_no_max",
+                                      "combine_unweighted", "gqa_off_by_one"])
+def test_planted_mistake_is_caught(monkeypatch, mutation):
+    orig_ma = ref.masked_attention
+    orig_comb = ref.combine
+    if mutation == "gqa_modulo":
+        monkeypatch.setattr(ref, "_kv_head", lambda h, nq, nkv: h % nkv)
+    elif mutation == "gqa_off_by_one":
+        monkeypatch.setattr(ref, "_kv_head", lambda h, nq, nkv: min(nkv - 1, (h + 1) // (nq // nkv)))
+    elif mutation == "strict_mask":
+        def strict(r0, r1, ncols):
+            return np.arange(ncols)[None, :] < np.arange(r0, r1)[:, None]
+        monkeypatch.setattr(ref, "_causal_allowed", strict)
+    elif mutation == "no_scale":
+        monkeypatch.setattr(ref, "masked_attention",
+                            lambda q, k, v, scale, allowed=None: orig_ma(q, k, v, 1.0, allowed))
+    elif mutation == "lse_no_max":
+        def bad(q, k, v, scale, allowed=None):
+            o, lse = orig_ma(q, k, v, scale, allowed)
+            s = scale * (ref._f64(q) @ ref._f64(k).T) if len(k) else None
+            if s is not None:
+                if allowed is not None:
+                    s = np.where(allowed, s, -np.inf)
+                lse = lse - s.max(axis=1)     # dropped the max term
+            return o, lse
+        monkeypatch.setattr(ref, "masked_attention", bad)
+    elif mutation == "combine_unweighted":
+        monkeypatch.setattr(ref, "combine", lambda o, l: (ref._f64(o).mean(0), ref._f64(l).max(0)))
+        monkeypatch.setattr(oracle, "combine", ref.combine)
+    failed = _any_pin_fails()
+    monkeypatch.setattr(ref, "masked_attention", orig_ma)
+    monkeypatch.setattr(ref, "combine", orig_comb)
+    assert failed, f"mutation {mutation} was not caught by any pin"
