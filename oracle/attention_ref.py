@@ -158,13 +158,16 @@ def prefill_rows(q, k, v, scale: float, causal: bool,
     dv = v.shape[3]
     o = np.zeros((len(rows), dv))
     lse = np.zeros((len(rows),))
+    groups: dict = {}
     for idx, (b, h, i) in enumerate(rows):
-        kh = _kv_head(h, n_q, n_kv)
-        ncols = i + 1 if causal else N
-        ob, lb = masked_attention(_f64(q[b, h, i:i + 1]), _f64(k[b, kh, :ncols]),
-                                  _f64(v[b, kh, :ncols]), scale, None)
-        o[idx] = ob[0]
-        lse[idx] = lb[0]
+        groups.setdefault((b, _kv_head(h, n_q, n_kv)), []).append((idx, h, i))
+    for (b, kh), members in groups.items():
+        kb, vb = _f64(k[b, kh]), _f64(v[b, kh])      # upcast once per (sequence, kv head)
+        for idx, h, i in members:
+            ncols = i + 1 if causal else N
+            ob, lb = masked_attention(_f64(q[b, h, i:i + 1]), kb[:ncols], vb[:ncols], scale, None)
+            o[idx] = ob[0]
+            lse[idx] = lb[0]
     return o, lse
 
 

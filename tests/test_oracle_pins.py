@@ -424,3 +424,16 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
     monkeypatch.setattr(ref, "masked_attention", orig_ma)
     monkeypatch.setattr(ref, "combine", orig_comb)
     assert failed, f"mutation {mutation} was not caught by any pin"
+
+
+def test_sampled_rows_match_full_prefill():
+    """The sampled-row entry point (used at sizes where every row is too slow)
+    agrees with the pinned full prefill, causal and not, with GQA."""
+    x = W.make_prefill(2, 6, 2, 90, 16, seed=9)
+    rows = [(b, h, i) for b in range(2) for h in range(6) for i in (0, 1, 31, 64, 89)]
+    for causal in (True, False):
+        of, lf = oracle.prefill(x.q, x.k, x.v, x.scale, causal)
+        orow, lrow = oracle.prefill_rows(x.q, x.k, x.v, x.scale, causal, rows)
+        for n, (b, h, i) in enumerate(rows):
+            assert np.abs(orow[n] - of[b, h, i]).max() <= TOL
+            assert abs(lrow[n] - lf[b, h, i]) <= TOL
