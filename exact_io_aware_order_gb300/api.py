@@ -1,0 +1,187 @@
+"""Python binding of the C ABI in ``include/attn.h``.
+
+Argument marshalling only: shape/dtype checks, output allocation with torch,
+raw pointers and the current CUDA stream passed to ``libattn.so``.  Nothing
+here computes any part of attention.
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from ._lib import check, lib
+
+_BF16 = torch.bfloat16
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
+            causal: bool = True, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, stream=None):
+    """Attention forward over whole sequences (``attn_prefill``).
+
+    q: (B, n_q, N, d) bf16; k, v: (B, n_kv, N, d) bf16.  Returns
+    (O (B, n_q, N, d) fp32, LSE (B, n_q, N) fp32, natural log).
+    """
+    _need(q, "q", _BF16, 4)
+    _need(k, "k", _BF16, 4)
+    _need(v, "v", _BF16, 4)
+    B, n_q, N, d = q.shape
+    n_kv = k.shape[1]
+    if k.shape != (B, n_kv, N, d) or v.shape != k.shape:
+        raise ValueError("k and v must be (B, n_kv, N, d) matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, n_q, N, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, n_q, N), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, 4)
+    _need(lse, "lse", torch.float32, 3)
+    st = lib().attn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr(), B, n_q, n_kv, N, d, float(scale), int(bool(causal)),
+                            _stream(stream))
+    check("attn_prefill", st)
+    return out, lse
+
+
+def decode_num_splits(batch: int, n_kv_heads: int, max_kv_len: int, num_sms: int = 0) -> int:
+    """The split-count policy (``attn_decode_num_splits``)."""
+    return int(lib().attn_decode_num_splits(int(batch), int(n_kv_heads), int(max_kv_len),
+                                            int(num_sms)))
+
+
+def split_ranges(kv_len: int, num_splits: int):
+    """Token range of every split under the library's split rule:
+    c = roundup(ceil(len / S), 16); split s covers [s*c, min((s+1)*c, len))."""
+    per = -(-kv_len // num_splits)
+    c = -(-per // 16) * 16
+    return [(min(s * c, kv_len), min(s * c + c, kv_len)) for s in range(num_splits)]
+
+
+def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   kv_lens: torch.Tensor, block_table: Optional[torch.Tensor] = None,
+                   num_splits: int = 0, max_kv_len: Optional[int] = None,
+                   scale: Optional[float] = None, o_partial: Optional[torch.Tensor] = None,
+                   lse_partial: Optional[torch.Tensor] = None, stream=None):
+    """Split-KV single-token decode (``attn_decode_splitkv``).
+
+    q: (B, n_q, d) bf16.  Paged: k_cache, v_cache (num_blocks, block_size,
+    n_kv, d) with block_table (B, max_blocks) int32; contiguous (block_table
+    None): (B, L, n_kv, d).  kv_lens: (B,) int32 on the device.
+    Returns (o_partial (S, B, n_q, d), lse_partial (S, B, n_q)), fp32.
+    """
+    _need(q, "q", _BF16, 3)
+    _need(k_cache, "k_cache", _BF16, 4)
+    _need(v_cache, "v_cache", _BF16, 4)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must have the same shape")
+    B, n_q, d = q.shape
+    n_kv = k_cache.shape[2]
+    if k_cache.shape[3] != d or kv_lens.shape[0] != B:
+        raise ValueError("cache head_dim or kv_lens length does not match q")
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, 2)
+        if block_table.shape[0] != B:
+            raise ValueError("block_table must have one row per sequence")
+        num_blocks, block_size = k_cache.shape[0], k_cache.shape[1]
+        max_blocks = block_table.shape[1]
+        if max_kv_len is None:
+            max_kv_len = max_blocks * block_size
+        bt_ptr = block_table.data_ptr()
+    else:
+        if k_cache.shape[0] != B:
+            raise ValueError("a contiguous cache must be (B, L, n_kv, d)")
+        num_blocks, block_size, max_blocks = 0, 0, 0
+        max_kv_len = k_cache.shape[1]
+        bt_ptr = None
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if num_splits == 0:
+        num_splits = decode_num_splits(B, n_kv, max_kv_len)
+    if o_partial is None:
+        o_partial = torch.empty((num_splits, B, n_q, d), dtype=torch.float32, device=q.device)
+    if lse_partial is None:
+        lse_partial = torch.empty((num_splits, B, n_q), dtype=torch.float32, device=q.device)
+    _need(o_partial, "o_partial", torch.float32, 4)
+    _need(lse_partial, "lse_partial", torch.float32, 3)
+    if o_partial.shape[0] != num_splits or lse_partial.shape[0] != num_splits:
+        raise ValueError("partial buffers must have num_splits rows")
+    st = lib().attn_decode_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), bt_ptr,
+                                   kv_lens.data_ptr(), int(num_splits), o_partial.data_ptr(),
+                                   lse_partial.data_ptr(), B, n_q, n_kv, d, block_size,
+                                   max_blocks, num_blocks, int(max_kv_len), float(scale),
+                                   _stream(stream))
+    check("attn_decode_splitkv", st)
+    return o_partial, lse_partial
+
+
+def combine(o_partial: torch.Tensor, lse_partial: torch.Tensor,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None):
+    """Merge split partials by their LSE weights (``attn_combine``).
+
+    o_partial: (S, B, n_q, d) fp32; lse_partial: (S, B, n_q) fp32.
+    Returns (O (B, n_q, d), LSE (B, n_q)), fp32.
+    """
+    _need(o_partial, "o_partial", torch.float32, 4)
+    _need(lse_partial, "lse_partial", torch.float32, 3)
+    S, B, n_q, d = o_partial.shape
+    if lse_partial.shape != (S, B, n_q):
+        raise ValueError("lse_partial must be (S, B, n_q)")
+    if out is None:
+        out = torch.empty((B, n_q, d), dtype=torch.float32, device=o_partial.device)
+    if lse is None:
+        lse = torch.empty((B, n_q), dtype=torch.float32, device=o_partial.device)
+    _need(out, "out", torch.float32, 3)
+    _need(lse, "lse", torch.float32, 2)
+    st = lib().attn_combine(o_partial.data_ptr(), lse_partial.data_ptr(), S, B, n_q, d,
+                            out.data_ptr(), lse.data_ptr(), _stream(stream))
+    check("attn_combine", st)
+    return out, lse
+
+
+def decode(q, k_cache, v_cache, kv_lens, block_table=None, num_splits: int = 0,
+           max_kv_len: Optional[int] = None, scale: Optional[float] = None, stream=None):
+    """Split-KV decode followed by the combine: returns (O (B, n_q, d), LSE (B, n_q))."""
+    op, lp = decode_splitkv(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len,
+                            scale, stream=stream)
+    return combine(op, lp, stream=stream)
+
+
+def check_device_status(stream=None) -> None:
+    """Synchronises the stream and raises if a kernel recorded an error."""
+    check("attn_check_device_status", lib().attn_check_device_status(_stream(stream)))
+
+
+def set_wait_timeout_ns(timeout_ns: int) -> int:
+    """Sets the bound on any kernel-side wait; returns the previous bound."""
+    return int(lib().attn_set_wait_timeout_ns(int(timeout_ns)))
+
+
+def selftest_bounded_wait(stream=None) -> int:
+    """Runs the bounded-wait self-test kernel; returns its attn_status code."""
+    return int(lib().attn_selftest_bounded_wait(_stream(stream)))

@@ -1,0 +1,228 @@
+// C ABI of the attention library: argument validation, per-device state
+// (error word, architecture check) and kernel launches on the caller's stream.
+// The operations themselves are defined in include/attn.h.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <cuda_runtime.h>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One 32-bit error word per device; kernels atomically OR error bits into it.
+__device__ uint32_t g_attn_error_word;
+
+struct DeviceState {
+  std::once_flag once;
+  bool ok = false;         // sm_103 and the symbol address resolved
+  bool arch_ok = false;
+  uint32_t* err_word = nullptr;
+  int num_sms = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+// Resolves per-device state once per device, with that device current.
+DeviceState* device_state(int* status) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *status = ATTN_ERR_LAUNCH;
+    return nullptr;
+  }
+  DeviceState* s = &g_dev[dev];
+  std::call_once(s->once, [s, dev] {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return;
+    s->num_sms = sms;
+    s->arch_ok = (major == 10 && minor == 3);
+    if (!s->arch_ok) return;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_error_word) != cudaSuccess) return;
+    s->err_word = static_cast<uint32_t*>(p);
+    s->ok = true;
+  });
+  if (!s->arch_ok) {
+    *status = ATTN_ERR_ARCH;
+    return nullptr;
+  }
+  if (!s->ok) {
+    *status = ATTN_ERR_LAUNCH;
+    return nullptr;
+  }
+  *status = ATTN_OK;
+  return s;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+attn::LaunchCtx make_ctx(void* stream, const DeviceState* s) {
+  attn::LaunchCtx c;
+  c.stream = static_cast<cudaStream_t>(stream);
+  c.err_word = s->err_word;
+  c.timeout_ns = g_timeout_ns.load();
+  c.num_sms = s->num_sms;
+  return c;
+}
+
+bool valid_scale(float scale) { return std::isfinite(scale) && scale > 0.f; }
+
+int split_policy(int batch, int n_kv_heads, int max_kv_len, int num_sms) {
+  if (batch <= 0 || n_kv_heads <= 0 || max_kv_len <= 0 || num_sms <= 0) return 1;
+  // Aim for about four resident decode CTAs' worth of work per SM, but keep
+  // every split at least 256 tokens long (the split results then dominate
+  // the partial-output traffic only by a small factor).
+  const long long pairs = (long long)batch * n_kv_heads;
+  const long long target = 4LL * num_sms;
+  long long splits = (target + pairs - 1) / pairs;
+  const long long max_useful = (max_kv_len + 255) / 256;
+  if (splits > max_useful) splits = max_useful;
+  if (splits < 1) splits = 1;
+  if (splits > ATTN_MAX_SPLITS) splits = ATTN_MAX_SPLITS;
+  return static_cast<int>(splits);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_NULL: return "ATTN_ERR_NULL: a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "ATTN_ERR_SHAPE: a size or the scale is out of range";
+    case ATTN_ERR_HEADDIM: return "ATTN_ERR_HEADDIM: head_dim must be 64 or 128";
+    case ATTN_ERR_GQA: return "ATTN_ERR_GQA: n_q_heads must be a multiple of n_kv_heads (decode: ratio <= 16)";
+    case ATTN_ERR_SPLITS: return "ATTN_ERR_SPLITS: num_splits out of range";
+    case ATTN_ERR_ALIGN: return "ATTN_ERR_ALIGN: a pointer is misaligned";
+    case ATTN_ERR_ARCH: return "ATTN_ERR_ARCH: the current device is not sm_103 (GB300)";
+    case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH: a CUDA call or kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel-side bounded wait gave up";
+    case ATTN_ERR_DEVICE: return "ATTN_ERR_DEVICE: a kernel saw a bad block-table entry or kv_len";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+const char* attn_version(void) { return "0.1.0 sm_103a"; }
+
+uint64_t attn_set_wait_timeout_ns(uint64_t timeout_ns) {
+  if (timeout_ns < 1000) timeout_ns = 1000;
+  return g_timeout_ns.exchange(timeout_ns);
+}
+
+int attn_decode_num_splits(int batch, int n_kv_heads, int max_kv_len, int num_sms) {
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 1;
+    }
+  }
+  return split_policy(batch, n_kv_heads, max_kv_len, num_sms);
+}
+
+int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o, float* lse,
+                 int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim, float scale,
+                 int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || seqlen < 1 || seqlen > (1 << 24) ||
+      (long long)batch * n_q_heads > (1LL << 20) || !valid_scale(scale))
+    return ATTN_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  attn::PrefillArgs a{q, k, v, o, lse, batch, n_q_heads, n_kv_heads, seqlen, head_dim, scale,
+                      causal ? 1 : 0};
+  if (attn::launch_prefill(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                        const int32_t* block_table, const int32_t* kv_lens, int num_splits,
+                        float* o_partial, float* lse_partial, int batch, int n_q_heads,
+                        int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                        int num_blocks, int max_kv_len, float scale, void* stream) {
+  if (!q || !k_cache || !v_cache || !kv_lens || !o_partial || !lse_partial) return ATTN_ERR_NULL;
+  const bool paged = block_table != nullptr;
+  if (batch < 1 || batch > 65535 || n_q_heads < 1 || n_kv_heads < 1 || n_kv_heads > 65535 ||
+      max_kv_len < 0 || !valid_scale(scale))
+    return ATTN_ERR_SHAPE;
+  if (paged && (block_size < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+                (long long)block_size * max_blocks_per_seq > (1LL << 30)))
+    return ATTN_ERR_SHAPE;
+  if (!paged && max_kv_len < 1) return ATTN_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 16) return ATTN_ERR_GQA;
+  if (num_splits < 0 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(o_partial, 16) || !aligned(lse_partial, 4) || !aligned(kv_lens, 4) ||
+      (paged && !aligned(block_table, 4)))
+    return ATTN_ERR_ALIGN;
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  if (num_splits == 0) num_splits = split_policy(batch, n_kv_heads, max_kv_len, ds->num_sms);
+  attn::DecodeArgs a{q, k_cache, v_cache, block_table, kv_lens, num_splits, o_partial, lse_partial,
+                     batch, n_q_heads, n_kv_heads, head_dim, paged ? block_size : 0,
+                     paged ? max_blocks_per_seq : 0, paged ? num_blocks : 0, max_kv_len, scale};
+  if (attn::launch_decode(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+int attn_combine(const float* o_partial, const float* lse_partial, int num_splits, int batch,
+                 int n_q_heads, int head_dim, float* o, float* lse, void* stream) {
+  if (!o_partial || !lse_partial || !o || !lse) return ATTN_ERR_NULL;
+  if (batch < 1 || n_q_heads < 1 || (long long)batch * n_q_heads > (1LL << 31) - 1)
+    return ATTN_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (num_splits < 1 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
+  if (!aligned(o_partial, 16) || !aligned(lse_partial, 4) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  attn::CombineArgs a{o_partial, lse_partial, num_splits, batch, n_q_heads, head_dim, o, lse};
+  if (attn::launch_combine(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+int attn_check_device_status(void* stream) {
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ds->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(ds->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+  }
+  if (word & attn::kErrTimeout) return ATTN_ERR_TIMEOUT;
+  if (word) return ATTN_ERR_DEVICE;
+  return ATTN_OK;
+}
+
+int attn_selftest_bounded_wait(void* stream) {
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  if (attn::launch_wait_selftest(make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return attn_check_device_status(stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal launch interface shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// Device error word bits (read back and cleared by attn_check_device_status).
+constexpr uint32_t kErrTimeout = 1u;     // a bounded wait gave up
+constexpr uint32_t kErrBlockIndex = 2u;  // a block-table entry outside [0, num_blocks)
+constexpr uint32_t kErrKvLen = 4u;       // a kv_len outside [0, capacity]
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  uint32_t* err_word;   // device address of this device's error word
+  uint64_t timeout_ns;  // bound on any single kernel-side wait
+  int num_sms;
+};
+
+struct PrefillArgs {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  float* o;
+  float* lse;
+  int batch, n_q_heads, n_kv_heads, seqlen, head_dim;
+  float scale;
+  int causal;
+};
+
+struct DecodeArgs {
+  const uint16_t* q;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  const int32_t* block_table;
+  const int32_t* kv_lens;
+  int num_splits;
+  float* o_partial;
+  float* lse_partial;
+  int batch, n_q_heads, n_kv_heads, head_dim;
+  int block_size, max_blocks_per_seq, num_blocks, max_kv_len;
+  float scale;
+};
+
+struct CombineArgs {
+  const float* o_partial;
+  const float* lse_partial;
+  int num_splits, batch, n_q_heads, head_dim;
+  float* o;
+  float* lse;
+};
+
+// Each returns cudaSuccess or the launch error.  Arguments are already
+// validated by the caller.
+cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx);
+cudaError_t launch_decode(const DecodeArgs& a, const LaunchCtx& ctx);
+cudaError_t launch_combine(const CombineArgs& a, const LaunchCtx& ctx);
+cudaError_t launch_wait_selftest(const LaunchCtx& ctx);
+
+// Split rule shared by the decode kernel's documentation and the host:
+// c = roundup(ceil(len / S), 16); split s covers [s*c, min((s+1)*c, len)).
+constexpr int kSplitGranule = 16;
+
+}  // namespace attn

@@ -1,0 +1,456 @@
+// Split-KV single-token decode and the LSE combine, sm_103a.
+//
+// Page "FlashAttention for inference: tiled prefill and split-KV decoding",
+// section "Decode: a different bottleneck": the key/value sequence of each
+// (sequence, kv head) is split into chunks, one thread block per chunk; each
+// block loads every key/value row of its chunk once and uses it for all
+// g = n_q / n_kv query heads of that kv head (GQA-aware sharing), streams a
+// paged or contiguous cache, and writes its partial output with its
+// log-sum-exp.  A second small kernel merges the partials by their LSE
+// weights (section "The online softmax, with every symbol defined", combining
+// partial results; the merge rule of section "Minimal implementation").
+//
+// Design for GB300.  Decode is HBM-bound, so the kernel is built to stream:
+//   * one producer warp issues one 256-byte bulk async copy per cache row
+//     (cp.async.bulk, completing on an mbarrier) into a 3-stage ring of
+//     64-token stages -- paged and contiguous caches take the same path;
+//   * four consumer warps each take 16 tokens of a stage.  With g query rows
+//     sharing the rows, q K^T and P V are small dense products (M = 16 padded
+//     rows); they run on mma.sync m16n8k16 (bf16 in, fp32 accumulate) so the
+//     ALU work stays far below the memory time;
+//   * rows sit at a 16-byte padded pitch, so every ldmatrix is conflict-free;
+//   * row max / row sum use quad shuffles; at the end the warps merge their
+//     (m, l, O) states through shared memory.
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kStageTokens = 64;   // tokens per ring stage
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;  // 16 tokens each per stage
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct DecodeSmem {
+  static constexpr int kRowBytes = D * 2 + 16;                 // padded pitch
+  static constexpr int kStageBytes = kStageTokens * kRowBytes;  // one of K or V
+  static constexpr int kQBytes = 16 * kRowBytes;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kStages * kStageBytes;
+  static constexpr int kQOff = 2 * kStages * kStageBytes;
+  static constexpr int kBarOff = kQOff + kQBytes;              // 2*kStages barriers
+  static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;
+  static constexpr int kTotal = kMiscOff + 16;
+  // Merge scratch reuses the K/V ring once the stream is done.
+  static constexpr int kMergeO = 0;                                  // [warps][16][D] f32
+  static constexpr int kMergeM = kConsumerWarps * 16 * D * 4;        // [warps][16]
+  static constexpr int kMergeL = kMergeM + kConsumerWarps * 16 * 4;  // [warps][16]
+  static_assert(kMergeL + kConsumerWarps * 16 * 4 <= kQOff, "merge scratch fits in the ring");
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_ns) {
+  using L = DecodeSmem<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int S = a.num_splits;
+  const int g = a.n_q_heads / a.n_kv_heads;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- this split's token range (split rule: see the C header) ----
+  const bool paged = a.block_table != nullptr;
+  const long long capacity =
+      paged ? (long long)a.max_blocks_per_seq * a.block_size : (long long)a.max_kv_len;
+  int len = a.kv_lens[b];
+  if (len < 0 || (long long)len > capacity) {
+    if (threadIdx.x == 0) atomicOr(err_word, kErrKvLen);
+    len = len < 0 ? 0 : (int)capacity;
+  }
+  const int per = (len + S - 1) / S;
+  const int chunk = (per + kSplitGranule - 1) / kSplitGranule * kSplitGranule;
+  const int t0 = min(split * chunk, len);
+  const int t1 = min(t0 + chunk, len);
+  const int n_tok = t1 - t0;
+
+  float* o_out = a.o_partial + (((size_t)split * a.batch + b) * a.n_q_heads + (size_t)kvh * g) * D;
+  float* lse_out = a.lse_partial + ((size_t)split * a.batch + b) * a.n_q_heads + (size_t)kvh * g;
+  if (n_tok <= 0) {  // empty split: o = 0, lse = -inf
+    for (int i = threadIdx.x; i < g * D; i += blockDim.x) o_out[i] = 0.f;
+    for (int i = threadIdx.x; i < g; i += blockDim.x) lse_out[i] = -INFINITY;
+    return;
+  }
+  const int n_stage_iters = (n_tok + kStageTokens - 1) / kStageTokens;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff);
+  const uint32_t full0 = smem_u32(&bars[0]);
+  const uint32_t empty0 = smem_u32(&bars[kStages]);
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{abort_flag, err_word, timeout_ns};
+
+  if (warp == 0) {
+    // ================= producer: stream rows into the ring =================
+    const int32_t* table = paged ? a.block_table + (size_t)b * a.max_blocks_per_seq : nullptr;
+    for (int it = 0; it < n_stage_iters; ++it) {
+      const int st = it % kStages;
+      if (it >= kStages) {
+        if (!mbar_wait_warp(empty0 + 8 * st, ((it / kStages) - 1) & 1, ctl)) break;
+      }
+      const int base = t0 + it * kStageTokens;
+      const int cnt = min(kStageTokens, t1 - base);
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)cnt * 2u * D * 2u);
+      __syncwarp();
+      for (int i = lane; i < cnt; i += 32) {
+        const int t = base + i;
+        size_t row;
+        if (paged) {
+          int blk = table[t / a.block_size];
+          if (blk < 0 || blk >= a.num_blocks) {
+            atomicOr(err_word, kErrBlockIndex);
+            blk = 0;  // keep the copy in bounds; the result is flagged invalid
+          }
+          row = (size_t)blk * a.block_size + (t % a.block_size);
+        } else {
+          row = (size_t)b * a.max_kv_len + t;
+        }
+        const size_t off = (row * a.n_kv_heads + kvh) * D;
+        const uint32_t dk = smem_u32(smem + L::kKOff + st * L::kStageBytes + i * L::kRowBytes);
+        const uint32_t dv = smem_u32(smem + L::kVOff + st * L::kStageBytes + i * L::kRowBytes);
+        bulk_load(dk, a.k_cache + off, D * 2, full0 + 8 * st);
+        bulk_load(dv, a.v_cache + off, D * 2, full0 + 8 * st);
+      }
+    }
+    // Wait for copies still in flight before the CTA may leave (abort path only:
+    // on the normal path the consumers have waited on every stage).
+    if (*abort_flag) {
+      for (int it = max(0, n_stage_iters - kStages); it < n_stage_iters; ++it) {
+        WaitCtl drain{abort_flag, err_word, timeout_ns};
+        volatile uint32_t no_abort = 0u;
+        drain.abort_flag = &no_abort;
+        mbar_wait(full0 + 8 * (it % kStages), (it / kStages) & 1, drain);
+      }
+    }
+  } else {
+    // ================= consumers =================
+    const int cw = warp - 1;
+    const int ctid = threadIdx.x - 32;
+    uint8_t* sq = smem + L::kQOff;
+    // q rows of this kv head's g query heads; rows g..15 are zero.
+    const uint16_t* qsrc = a.q + ((size_t)b * a.n_q_heads + (size_t)kvh * g) * D;
+    for (int i = ctid; i < 16 * (D / 8); i += 32 * kConsumerWarps) {
+      const int r = i / (D / 8), c = i % (D / 8);
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (r < g) val = *reinterpret_cast<const uint4*>(qsrc + (size_t)r * D + c * 8);
+      *reinterpret_cast<uint4*>(sq + r * L::kRowBytes + c * 16) = val;
+    }
+    consumer_sync();
+    // Q as A fragments, one set per 16-wide k step of the head dimension.
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int r = (lane & 15);
+      const int c = kk * 16 + (lane >> 4) * 8;
+      ldsm_x4(smem_u32(sq + r * L::kRowBytes + c * 2), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+    }
+    const float sl2 = a.scale * kLog2e;
+    float m_r[2] = {-INFINITY, -INFINITY};  // running max (log2 domain) of rows gid, gid+8
+    float l_r[2] = {0.f, 0.f};
+    float acc[D / 8][4];
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    const int quad = lane & 3;
+
+    for (int it = 0; it < n_stage_iters; ++it) {
+      const int st = it % kStages;
+      if (!mbar_wait_warp(full0 + 8 * st, (it / kStages) & 1, ctl)) break;
+      const int base = t0 + it * kStageTokens;
+      const int cnt = min(kStageTokens, t1 - base);
+      const int vc = min(16, cnt - cw * 16);  // valid tokens of this warp's 16
+      if (vc > 0) {
+        uint8_t* sk = smem + L::kKOff + st * L::kStageBytes + cw * 16 * L::kRowBytes;
+        uint8_t* sv = smem + L::kVOff + st * L::kStageBytes + cw * 16 * L::kRowBytes;
+        if (vc < 16) {  // stale rows past the end: zero V so 0 * (old data) stays 0
+          for (int i = lane; i < (16 - vc) * (D / 8); i += 32) {
+            const int r = vc + i / (D / 8), c = i % (D / 8);
+            *reinterpret_cast<uint4*>(sv + r * L::kRowBytes + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+        }
+        // ---- S = q K^T for 16 tokens (two n-tiles of 8) ----
+        float s[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          // lanes 0-7: tokens 0-7 @ d 16kk; 8-15: tokens 0-7 @ d+8; 16-23: tokens 8-15 @ d; 24-31: tokens 8-15 @ d+8
+          const int r = (lane & 7) + ((lane >> 4) << 3);
+          const int c = kk * 16 + ((lane >> 3) & 1) * 8;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(smem_u32(sk + r * L::kRowBytes + c * 2), b0, b1, b2, b3);
+          mma16816(s[0], qa[kk], b0, b1);
+          mma16816(s[1], qa[kk], b2, b3);
+        }
+        // ---- mask tokens past the end, online softmax update ----
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tok = n * 8 + quad * 2 + (e & 1);
+            if (tok >= vc) s[n][e] = -INFINITY;
+            mx[e >> 1] = fmaxf(mx[e >> 1], s[n][e]);
+          }
+        float corr[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+          const float m_new = fmaxf(m_r[r], mx[r] * sl2);  // finite: token 0 is valid
+          corr[r] = ex2_approx(m_r[r] - m_new);            // exp2(-inf) = 0 on the first stage
+          m_r[r] = m_new;
+        }
+        float rs[2] = {0.f, 0.f};
+        uint32_t pa[4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const float p0 = ex2_approx(fmaf(s[n][0], sl2, -m_r[0]));
+          const float p1 = ex2_approx(fmaf(s[n][1], sl2, -m_r[0]));
+          const float p2 = ex2_approx(fmaf(s[n][2], sl2, -m_r[1]));
+          const float p3 = ex2_approx(fmaf(s[n][3], sl2, -m_r[1]));
+          rs[0] += p0 + p1;
+          rs[1] += p2 + p3;
+          pa[2 * n + 0] = pack_bf16x2(p0, p1);  // row gid,   tokens 8n + 2q, +1
+          pa[2 * n + 1] = pack_bf16x2(p2, p3);  // row gid+8
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 1);
+          rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 2);
+          l_r[r] = l_r[r] * corr[r] + rs[r];
+        }
+        // A fragment of P: {row g tok 2q..}, {row g+8 tok 2q..}, {row g tok 8+2q..}, {row g+8 tok 8+2q..}
+        const uint32_t pfrag[4] = {pa[0], pa[1], pa[2], pa[3]};
+        // ---- O = corr * O + P V ----
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+          // lanes 0-7: tok 0-7 @ d 16j; 8-15: tok 8-15 @ 16j; 16-23: tok 0-7 @ 16j+8; 24-31: tok 8-15 @ 16j+8
+          const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int c = j * 16 + (lane >> 4) * 8;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(smem_u32(sv + r * L::kRowBytes + c * 2), b0, b1, b2, b3);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float* o = acc[2 * j + h];
+            o[0] *= corr[0];
+            o[1] *= corr[0];
+            o[2] *= corr[1];
+            o[3] *= corr[1];
+          }
+          mma16816(acc[2 * j + 0], pfrag, b0, b1);
+          mma16816(acc[2 * j + 1], pfrag, b2, b3);
+        }
+        if (vc < 16) fence_proxy_async_smem();  // generic writes above precede the next copy
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    }
+
+    // ================= merge the consumer warps' states =================
+    consumer_sync();  // every warp is done reading the ring
+    float* mo = reinterpret_cast<float*>(smem + L::kMergeO) + (size_t)cw * 16 * D;
+    float* mm = reinterpret_cast<float*>(smem + L::kMergeM);
+    float* ml = reinterpret_cast<float*>(smem + L::kMergeL);
+    const int gid = lane >> 2;
+    if (quad == 0) {
+      mm[cw * 16 + gid] = m_r[0];
+      mm[cw * 16 + gid + 8] = m_r[1];
+      ml[cw * 16 + gid] = l_r[0];
+      ml[cw * 16 + gid + 8] = l_r[1];
+    }
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      const int col = j * 8 + quad * 2;
+      mo[gid * D + col] = acc[j][0];
+      mo[gid * D + col + 1] = acc[j][1];
+      mo[(gid + 8) * D + col] = acc[j][2];
+      mo[(gid + 8) * D + col + 1] = acc[j][3];
+    }
+    consumer_sync();
+    if (!*abort_flag) {
+      for (int i = ctid; i < g * D; i += 32 * kConsumerWarps) {
+        const int r = i / D, c = i % D;
+        float m = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, mm[w * 16 + r]);
+        float lsum = 0.f, osum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float f = ex2_approx(mm[w * 16 + r] - m);  // 0 for a warp that saw no token
+          lsum += f * ml[w * 16 + r];
+          osum += f * reinterpret_cast<float*>(smem + L::kMergeO)[((size_t)w * 16 + r) * D + c];
+        }
+        o_out[(size_t)r * D + c] = osum / lsum;
+        if (c == 0) lse_out[r] = (m + __log2f(lsum)) * kLn2;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Combine: one 128-thread block per (sequence, query head); warps take every
+// 4th split, lanes own 4 consecutive head-dim elements per D/4 lanes.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
+  constexpr int kLanesPerRow = D / 4;               // float4 per lane
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;   // splits handled per warp step
+  const int bh = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = a.num_splits;
+  const size_t stride_s = (size_t)a.batch * a.n_q_heads;
+  __shared__ float s_max[4], s_sum[4];
+  __shared__ float4 s_o[4][kRowsPerWarp][kLanesPerRow];
+
+  // 1) max over splits
+  float mx = -INFINITY;
+  for (int s = threadIdx.x; s < S; s += 128) mx = fmaxf(mx, a.lse_partial[(size_t)s * stride_s + bh]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) s_max[warp] = mx;
+  __syncthreads();
+  mx = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
+  float4* out = reinterpret_cast<float4*>(a.o + (size_t)bh * D);
+  if (mx == -INFINITY) {  // every split empty
+    for (int i = threadIdx.x; i < D / 4; i += 128) out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x == 0) a.lse[bh] = -INFINITY;
+    return;
+  }
+  // 2) weighted sum of partial outputs
+  const int sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  for (int s = warp * kRowsPerWarp + sub; s < S; s += 4 * kRowsPerWarp) {
+    const float w = ex2_approx((a.lse_partial[(size_t)s * stride_s + bh] - mx) * kLog2e);
+    const float4 v = reinterpret_cast<const float4*>(a.o_partial + ((size_t)s * stride_s + bh) * D)[li];
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+    if (li == 0) wsum += w;
+  }
+  s_o[warp][sub][li] = acc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  if (lane == 0) s_sum[warp] = wsum;
+  __syncthreads();
+  const float W = s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3];
+  for (int i = threadIdx.x; i < kLanesPerRow; i += 128) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < 4; ++w)
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        const float4 v = s_o[w][r][i];
+        t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+      }
+    const float inv = 1.f / W;
+    out[i] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
+  }
+  if (threadIdx.x == 0) a.lse[bh] = mx + logf(W);
+}
+
+__global__ void wait_selftest_kernel(uint32_t* err_word, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0u;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{&abort_flag, err_word, timeout_ns};
+  mbar_wait(smem_u32(&bar), 0, ctl);  // no one arrives: must give up after timeout_ns
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_arrive(smem_u32(&bar));  // complete the phase before exit
+}
+
+template <int D>
+cudaError_t launch_decode_t(const DecodeArgs& a, const LaunchCtx& ctx) {
+  using L = DecodeSmem<D>;
+  static bool configured[64] = {};  // the attribute is per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = true;
+  }
+  dim3 grid(a.num_splits, a.n_kv_heads, a.batch);
+  decode_splitkv_kernel<D><<<grid, kThreads, L::kTotal, ctx.stream>>>(a, ctx.err_word, ctx.timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, const LaunchCtx& ctx) {
+  return a.head_dim == 128 ? launch_decode_t<128>(a, ctx) : launch_decode_t<64>(a, ctx);
+}
+
+cudaError_t launch_combine(const CombineArgs& a, const LaunchCtx& ctx) {
+  const unsigned nbh = (unsigned)a.batch * (unsigned)a.n_q_heads;
+  if (a.head_dim == 128)
+    combine_kernel<128><<<nbh, 128, 0, ctx.stream>>>(a);
+  else
+    combine_kernel<64><<<nbh, 128, 0, ctx.stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(const LaunchCtx& ctx) {
+  wait_selftest_kernel<<<1, 32, 0, ctx.stream>>>(ctx.err_word, ctx.timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,190 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention forward library.
+ *
+ * What it computes is defined on the explainer page "FlashAttention for
+ * inference: tiled prefill and split-KV decoding" (pofe.ai):
+ *   - attention itself: S = Q K^T * scale, P = softmax(S), O = P V
+ *     (section "The bottleneck it attacks"), computed exactly up to rounding
+ *     with the online softmax of section "The online softmax, with every
+ *     symbol defined";
+ *   - causal prefill in FlashAttention-2 loop order, one thread block per
+ *     query tile, tiles above the diagonal skipped, each row's log-sum-exp
+ *     written (section "Prefill: tiles, loop order and the tensor cores");
+ *   - split-KV single-token decode over a grouped-query, optionally paged
+ *     cache, with per-split partial outputs and LSEs (section "Decode: a
+ *     different bottleneck");
+ *   - the merge of partial results by their LSE weights (section "The online
+ *     softmax ...", combining partial results, and the merge rule in section
+ *     "Minimal implementation").
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer, allocated and owned by the
+ *     caller.  The library never allocates, never frees and never
+ *     synchronises (except attn_check_device_status), and launches all work
+ *     on the caller's stream (`stream` is a cudaStream_t; NULL = the legacy
+ *     default stream).
+ *   - bf16 tensors are passed as `const attn_bf16*` (the raw 16-bit pattern).
+ *   - All arrays are dense and row-major in the order their shape is written.
+ *   - LSE values are natural logarithms of sums of exp(scaled score); an
+ *     empty key set yields LSE = -inf and O = 0.
+ *   - Arguments are validated before anything is launched; on any error the
+ *     call returns a nonzero attn_status and launches nothing.
+ *   - Kernel-side waits are bounded; a timeout, a block-table entry outside
+ *     [0, num_blocks) or a kv_len above the cache capacity is recorded in a
+ *     per-device error word that attn_check_device_status reports.
+ *   - Grouped-query attention: g = n_q_heads / n_kv_heads query heads share a
+ *     key/value head; query head h reads key/value head h / g.
+ */
+#ifndef ATTN_SM103_H
+#define ATTN_SM103_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t attn_bf16; /* bfloat16 bit pattern */
+
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = 1,     /* a required pointer is NULL                          */
+  ATTN_ERR_SHAPE = 2,    /* a size is out of range (batch, heads, seqlen, ...)   */
+  ATTN_ERR_HEADDIM = 3,  /* head_dim not supported (64 and 128 are)             */
+  ATTN_ERR_GQA = 4,      /* n_q_heads not a multiple of n_kv_heads, or g > 16 in decode */
+  ATTN_ERR_SPLITS = 5,   /* num_splits < 0 or above the supported maximum        */
+  ATTN_ERR_ALIGN = 6,    /* a pointer is not aligned as documented               */
+  ATTN_ERR_ARCH = 7,     /* the current device is not sm_103 (GB300)             */
+  ATTN_ERR_LAUNCH = 8,   /* a CUDA runtime call or kernel launch failed          */
+  ATTN_ERR_TIMEOUT = 9,  /* a kernel's bounded wait gave up (device error word)  */
+  ATTN_ERR_DEVICE = 10   /* bad block-table entry or kv_len seen by a kernel     */
+} attn_status;
+
+/* Name of a status code; never NULL. */
+const char* attn_status_string(int status);
+
+/*
+ * attn_prefill -- attention forward over whole sequences (causal prefill).
+ *
+ * Page: "FlashAttention for inference: tiled prefill and split-KV decoding",
+ * section "Prefill: tiles, loop order and the tensor cores" (loop order,
+ * causal skipping, the per-row log-sum-exp output) and the layout of
+ * section "Minimal implementation" (batch, heads, seq, head_dim).
+ *
+ *   q   : (batch, n_q_heads,  seqlen, head_dim) bf16, 16-byte aligned
+ *   k, v: (batch, n_kv_heads, seqlen, head_dim) bf16, 16-byte aligned
+ *   o   : (batch, n_q_heads,  seqlen, head_dim) fp32 output, 16-byte aligned
+ *   lse : (batch, n_q_heads,  seqlen) fp32 output (natural log), 4-byte aligned
+ *   scale: multiplies q.k (pass 1/sqrt(head_dim) for standard attention)
+ *   causal: nonzero -> row i attends to keys j <= i; zero -> to every key.
+ * Limits: head_dim in {64, 128}; 1 <= seqlen <= 2^24; batch*n_q_heads <= 2^20;
+ *   n_q_heads % n_kv_heads == 0.  bf16 inputs, fp32 accumulation, P rounded
+ *   to bf16 before the P*V product.
+ * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
+ */
+int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+                 float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen,
+                 int head_dim, float scale, int causal, void* stream);
+
+/*
+ * attn_decode_num_splits -- the split-count policy for single-token decode.
+ *
+ * Page: same, section "Decode: a different bottleneck": splitting the key/value
+ * sequence restores parallelism at small batch, adds only reduction overhead
+ * at large batch, so the split count is chosen from batch, heads and length.
+ * Returns a value in [1, ATTN_MAX_SPLITS] (1 for non-positive arguments).
+ * num_sms <= 0 means "query the current device".  Pure host function.
+ */
+#define ATTN_MAX_SPLITS 1024
+int attn_decode_num_splits(int batch, int n_kv_heads, int max_kv_len, int num_sms);
+
+/*
+ * attn_decode_splitkv -- split-KV single-token decode (partial results).
+ *
+ * Page: same, section "Decode: a different bottleneck" (split-KV, GQA-aware
+ * key/value sharing, paged caches) and section "Minimal implementation" for
+ * the cache, block-table and cache-length layouts.
+ *
+ *   q          : (batch, n_q_heads, head_dim) bf16, one query token per sequence,
+ *                16-byte aligned
+ *   k_cache,
+ *   v_cache    : paged (block_table != NULL): (num_blocks, block_size, n_kv_heads, head_dim)
+ *                contiguous (block_table == NULL): (batch, max_kv_len, n_kv_heads, head_dim)
+ *                bf16, 16-byte aligned
+ *   block_table: (batch, max_blocks_per_seq) int32 physical block ids, or NULL
+ *   kv_lens    : (batch,) int32 tokens already cached per sequence (0 allowed);
+ *                must not exceed max_blocks_per_seq*block_size (paged) or
+ *                max_kv_len (contiguous) -- a larger value is clamped and flagged
+ *   num_splits : number of splits S >= 1, or 0 for attn_decode_num_splits(batch,
+ *                n_kv_heads, max_kv_len, 0) (the caller must size the partials for it)
+ *   o_partial  : (S, batch, n_q_heads, head_dim) fp32 output, 16-byte aligned
+ *   lse_partial: (S, batch, n_q_heads) fp32 output, 4-byte aligned
+ *   block_size, max_blocks_per_seq, num_blocks: paged cache geometry (ignored
+ *                when block_table is NULL); block_size must be >= 1
+ *   max_kv_len : contiguous cache length; for a paged cache, the largest kv_len
+ *                (used only by the num_splits = 0 policy)
+ *   scale      : multiplies q.k
+ * Split rule: with c = roundup(ceil(kv_len / S), 16), split s of a sequence
+ * covers tokens [s*c, min((s+1)*c, kv_len)); an empty split writes o = 0 and
+ * lse = -inf.  Each split's (o, lse) is attention restricted to its tokens.
+ * Limits: head_dim in {64, 128}; n_q_heads / n_kv_heads <= 16.
+ * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _SPLITS, _ALIGN, _ARCH, _LAUNCH.
+ */
+int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                        const int32_t* block_table, const int32_t* kv_lens, int num_splits,
+                        float* o_partial, float* lse_partial, int batch, int n_q_heads,
+                        int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                        int num_blocks, int max_kv_len, float scale, void* stream);
+
+/*
+ * attn_combine -- merge per-split partial results by their LSE weights.
+ *
+ * Page: same, section "The online softmax, with every symbol defined" (the
+ * rule for combining independent partial results: lambda = log sum_k
+ * exp(lambda_k), o = sum_k exp(lambda_k - lambda) o_k) and the merge rule in
+ * section "Minimal implementation" (a softmax over the split axis).
+ *
+ *   o_partial  : (num_splits, batch, n_q_heads, head_dim) fp32, 16-byte aligned
+ *   lse_partial: (num_splits, batch, n_q_heads) fp32, 4-byte aligned
+ *   o          : (batch, n_q_heads, head_dim) fp32 output, 16-byte aligned
+ *   lse        : (batch, n_q_heads) fp32 output, 4-byte aligned
+ * Splits with lse = -inf carry zero weight; if all are -inf, o = 0, lse = -inf.
+ * Limits: 1 <= num_splits <= ATTN_MAX_SPLITS; head_dim in {64, 128}.
+ * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _SPLITS, _ALIGN, _ARCH, _LAUNCH.
+ */
+int attn_combine(const float* o_partial, const float* lse_partial, int num_splits, int batch,
+                 int n_q_heads, int head_dim, float* o, float* lse, void* stream);
+
+/*
+ * attn_check_device_status -- synchronises `stream`, then reads and clears the
+ * current device's error word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a bounded
+ * wait gave up), ATTN_ERR_DEVICE (bad block-table entry or kv_len), or
+ * ATTN_ERR_LAUNCH (a CUDA error, e.g. from an earlier launch).  Meant for
+ * tests and debugging: it blocks the host.
+ */
+int attn_check_device_status(void* stream);
+
+/*
+ * attn_set_wait_timeout_ns -- upper bound, in nanoseconds, on any single
+ * kernel-side wait (default 2e9).  Values below 1000 are raised to 1000.
+ * Host-side setting read at each launch; not thread-safe against concurrent
+ * launches.  Returns the previous value.
+ */
+uint64_t attn_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * attn_selftest_bounded_wait -- launches one CTA that waits on a barrier no
+ * one arrives at, with the current timeout, then returns the resulting
+ * device status (ATTN_ERR_TIMEOUT when the bounded wait works).  Synchronises
+ * `stream`.  Exercises the give-up path without faulting or hanging the GPU.
+ */
+int attn_selftest_bounded_wait(void* stream);
+
+/* Library version string, e.g. "0.1.0 sm_103a". */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SM103_H */

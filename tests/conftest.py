@@ -31,3 +31,18 @@ def read_golden(name: str) -> dict:
 @pytest.fixture(scope="session")
 def golden():
     return read_golden
+
+
+@pytest.fixture(scope="session")
+def dev():
+    """cuda:0 with the library built; GPU tests fail loudly without a device."""
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from exact_io_aware_order_gb300 import build
+
+    build.build()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d

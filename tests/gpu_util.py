@@ -1,0 +1,30 @@
+"""Shared helpers for the GPU parity tests (tolerances and comparisons)."""
+
+import numpy as np
+import torch
+
+# Acceptance bar for bf16 inputs with fp32 accumulation against the float64
+# oracle: O max-abs 2e-2 and mean-abs 2e-3, LSE max-abs 1e-3.
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
+
+
+def nan_like(shape, device):
+    return torch.full(shape, float("nan"), dtype=torch.float32, device=device)
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    """Element-wise parity: returns (max|dO|, mean|dO|, max|dLSE|)."""
+    o = o_gpu.detach().double().cpu().numpy() if isinstance(o_gpu, torch.Tensor) else o_gpu
+    lse = lse_gpu.detach().double().cpu().numpy() if isinstance(lse_gpu, torch.Tensor) else lse_gpu
+    assert o.shape == o_ref.shape, (what, o.shape, o_ref.shape)
+    assert np.isfinite(o).all(), f"{what}: non-finite output (unwritten element?)"
+    # -inf LSE (empty key set) must match exactly; finite ones within tolerance.
+    inf_ref = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse), inf_ref), f"{what}: -inf pattern of LSE differs"
+    assert np.isfinite(lse[~inf_ref]).all(), f"{what}: non-finite LSE"
+    err = np.abs(o - o_ref)
+    lerr = np.abs(lse[~inf_ref] - lse_ref[~inf_ref]).max() if (~inf_ref).any() else 0.0
+    emax, emean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
+    assert emax <= O_MAX and emean <= O_MEAN and lerr <= LSE_MAX, \
+        f"{what}: max|dO|={emax:.3e} mean|dO|={emean:.3e} max|dLSE|={lerr:.3e}"
+    return emax, emean, float(lerr)

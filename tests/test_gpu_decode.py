@@ -1,0 +1,181 @@
+"""Parity of split-KV decode (attn_decode_splitkv) and the combine
+(attn_combine), through the C ABI, against the float64 oracle: the combined
+result and every split's partial result, contiguous and paged caches, the
+split-count sweep, edge cases, and the kernels' own error reporting."""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_order_gb300 as attn
+from exact_io_aware_order_gb300 import workloads as W
+from exact_io_aware_order_gb300._lib import AttnError, status_codes
+import oracle
+from gpu_util import compare, nan_like
+
+pytestmark = pytest.mark.gpu
+
+
+def split_rule(kv_len, S):
+    """The header's split rule, restated here: c = roundup(ceil(len/S), 16)."""
+    if kv_len == 0:
+        return [(0, 0)] * S
+    c = ((kv_len + S - 1) // S + 15) // 16 * 16
+    return [(min(s * c, kv_len), min(min(s * c, kv_len) + c, kv_len)) for s in range(S)]
+
+
+def run_decode(d, dev, S):
+    q = d.q.to(dev)
+    kc, vc = d.k_cache.to(dev), d.v_cache.to(dev)
+    lens = d.kv_lens.to(dev)
+    bt = d.block_table.to(dev) if d.block_table is not None else None
+    B, Hq, D = q.shape
+    op, lp = nan_like((S, B, Hq, D), dev), nan_like((S, B, Hq), dev)
+    attn.decode_splitkv(q, kc, vc, lens, bt, num_splits=S, max_kv_len=d.max_kv_len, scale=d.scale,
+                        o_partial=op, lse_partial=lp)
+    o, lse = nan_like((B, Hq, D), dev), nan_like((B, Hq), dev)
+    attn.combine(op, lp, out=o, lse=lse)
+    attn.check_device_status()
+    return op, lp, o, lse
+
+
+def check_all(d, op, lp, o, lse, S, what):
+    bt = d.block_table
+    lens = d.kv_lens.tolist()
+    o_ref, lse_ref = oracle.decode(d.q, d.k_cache, d.v_cache, bt, lens, d.scale, d.block_size)
+    res = compare(o, lse, o_ref, lse_ref, what + " combined")
+    ranges = [split_rule(n, S) for n in lens]
+    op_ref, lp_ref = oracle.decode_partials(d.q, d.k_cache, d.v_cache, bt, lens, d.scale,
+                                            d.block_size, ranges)
+    compare(op, lp, op_ref, lp_ref, what + " partials")
+    return res
+
+
+@pytest.mark.parametrize("S", [1, 16, 64, 148])
+def test_qwen_decode_split_sweep(dev, S):
+    """28 / 4 heads, head_dim 128, contiguous 30720-token cache."""
+    d = W.qwen_decode(30720)
+    op, lp, o, lse = run_decode(d, dev, S)
+    check_all(d, op, lp, o, lse, S, f"qwen S={S}")
+
+
+def test_paged_batched_decode_auto_splits(dev):
+    """16 sequences, lengths uniform in [1024, 32768], 32 / 8 heads, 16-token blocks."""
+    d = W.llama_paged_decode()
+    S = attn.decode_num_splits(16, 8, d.max_kv_len)
+    op, lp, o, lse = run_decode(d, dev, S)
+    check_all(d, op, lp, o, lse, S, f"paged S={S}")
+
+
+@pytest.mark.parametrize("lens,S,bs,D,Hq,Hkv", [
+    ([0, 1, 15, 16, 17], 3, 16, 128, 8, 2),
+    ([63, 64, 65, 200], 2, 16, 64, 4, 4),
+    ([5, 1000], 100, 16, 128, 16, 1),        # many empty splits, g = 16
+    ([1, 2, 3], 1, 1, 128, 2, 1),            # one-token blocks
+    ([777, 1], 5, 7, 64, 6, 3),              # odd block size
+    ([4096], 1, 64, 128, 28, 4),
+])
+def test_paged_edge_cases(dev, lens, S, bs, D, Hq, Hkv):
+    d = W.make_decode_paged(len(lens), Hq, Hkv, D, lens, block_size=bs, seed=sum(lens) + S,
+                            extra_blocks=3)
+    op, lp, o, lse = run_decode(d, dev, S)
+    check_all(d, op, lp, o, lse, S, f"paged lens={lens} S={S}")
+
+
+@pytest.mark.parametrize("kv_len,L,S", [(1, 1, 1), (100, 300, 4), (30720, 30720, 7),
+                                        (2049, 4096, 33)])
+def test_contiguous_edge_cases(dev, kv_len, L, S):
+    d = W.make_decode_contiguous(2, 8, 2, 128, kv_len, seed=kv_len, max_kv_len=L)
+    op, lp, o, lse = run_decode(d, dev, S)
+    check_all(d, op, lp, o, lse, S, f"contig len={kv_len} L={L} S={S}")
+
+
+def test_slots_past_the_end_are_never_read(dev):
+    """NaN in cache slots beyond kv_len (paged tail and contiguous tail) must not
+    reach the output."""
+    d = W.make_decode_paged(2, 8, 2, 128, [37, 50], block_size=16, seed=3)
+    for b, n in enumerate(d.kv_lens.tolist()):
+        last = int(d.block_table[b, (n - 1) // 16])
+        d.k_cache[last, n % 16 or 16:] = float("nan")
+        d.v_cache[last, n % 16 or 16:] = float("nan")
+    op, lp, o, lse = run_decode(d, dev, 3)
+    check_all(d, op, lp, o, lse, 3, "nan tail paged")
+    c = W.make_decode_contiguous(1, 4, 1, 64, 90, seed=4, max_kv_len=200)
+    c.k_cache[:, 90:] = float("nan")
+    c.v_cache[:, 90:] = float("nan")
+    op, lp, o, lse = run_decode(c, dev, 2)
+    check_all(c, op, lp, o, lse, 2, "nan tail contiguous")
+
+
+def test_split_count_does_not_change_the_result(dev):
+    d = W.make_decode_contiguous(1, 28, 4, 128, 5000, seed=6)
+    outs = [run_decode(d, dev, S)[2:] for S in (1, 3, 64, 300)]
+    for o, lse in outs[1:]:
+        assert (o - outs[0][0]).abs().max().item() <= 2e-3
+        assert (lse - outs[0][1]).abs().max().item() <= 1e-4
+
+
+def test_decode_matches_last_prefill_row(dev):
+    x = W.make_prefill(1, 28, 4, 1111, 128, seed=8)
+    o_p, lse_p = attn.prefill(x.q.to(dev), x.k.to(dev), x.v.to(dev), x.scale, True)
+    kc = x.k[0].permute(1, 0, 2).unsqueeze(0).contiguous()
+    vc = x.v[0].permute(1, 0, 2).unsqueeze(0).contiguous()
+    d = W.DecodeInputs(x.q[:, :, -1].contiguous(), kc, vc, None,
+                       torch.tensor([1111], dtype=torch.int32), 0, x.scale, 1111)
+    _, _, o_d, lse_d = run_decode(d, dev, 9)
+    assert (o_d - o_p[:, :, -1]).abs().max().item() <= 1e-2
+    assert (lse_d - lse_p[:, :, -1]).abs().max().item() <= 1e-3
+
+
+def test_combine_kernel_on_arbitrary_partials(dev):
+    rng = np.random.default_rng(0)
+    for S, B, Hq, D in [(5, 2, 3, 128), (148, 1, 28, 128), (1, 4, 2, 64), (1024, 1, 2, 64),
+                        (1024, 1, 1, 64)]:
+        op = rng.standard_normal((S, B, Hq, D)).astype(np.float32)
+        lp = (rng.standard_normal((S, B, Hq)) * 5).astype(np.float32)
+        lp[rng.random((S, B, Hq)) < 0.2] = -np.inf            # empty splits
+        lp[:, 0, 0] = -np.inf                                 # one row with every split empty
+        op[np.isneginf(lp)] = 0.0
+        o, lse = attn.combine(torch.from_numpy(op).to(dev), torch.from_numpy(lp).to(dev))
+        attn.check_device_status()
+        o_ref, lse_ref = oracle.combine(op.astype(np.float64), lp.astype(np.float64))
+        ol, ll = o.double().cpu().numpy(), lse.double().cpu().numpy()
+        assert np.array_equal(np.isneginf(ll), np.isneginf(lse_ref))
+        fin = np.isfinite(lse_ref)
+        if fin.any():
+            assert np.abs(ll[fin] - lse_ref[fin]).max() <= 1e-5
+        assert np.abs(ol - o_ref).max() <= 1e-5
+        assert np.all(ol[~fin] == 0.0)
+
+
+def test_bad_block_table_entry_is_reported(dev):
+    """An out-of-range physical block id is caught by the kernel's own bounds
+    check (the copy is redirected to block 0) and reported as ATTN_ERR_DEVICE."""
+    d = W.make_decode_paged(1, 4, 1, 128, [40], block_size=16, seed=1)
+    d.block_table[0, 1] = d.k_cache.shape[0] + 5
+    with pytest.raises(AttnError) as e:
+        run_decode(d, dev, 2)
+    assert e.value.status == status_codes()["ATTN_ERR_DEVICE"]
+    attn.check_device_status()                                  # the word was cleared
+
+
+def test_kv_len_beyond_capacity_is_reported(dev):
+    d = W.make_decode_contiguous(1, 4, 1, 128, 64, seed=2)
+    d.kv_lens[0] = 65                                           # capacity is 64
+    with pytest.raises(AttnError) as e:
+        run_decode(d, dev, 2)
+    assert e.value.status == status_codes()["ATTN_ERR_DEVICE"]
+    attn.check_device_status()
+
+
+def test_bounded_wait_gives_up_and_reports(dev):
+    """A kernel waiting on a barrier nobody arrives at returns after the
+    timeout with ATTN_ERR_TIMEOUT; the context stays usable."""
+    old = attn.set_wait_timeout_ns(2_000_000)                    # 2 ms
+    try:
+        assert attn.selftest_bounded_wait() == status_codes()["ATTN_ERR_TIMEOUT"]
+    finally:
+        attn.set_wait_timeout_ns(old)
+    d = W.make_decode_contiguous(1, 4, 2, 128, 300, seed=3)
+    op, lp, o, lse = run_decode(d, dev, 2)
+    check_all(d, op, lp, o, lse, 2, "after timeout test")

@@ -1,0 +1,158 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+* libattn.so builds, loads and exports every function include/attn.h declares;
+* every status code has a name;
+* argument validation rejects bad calls with the documented status before
+  touching the device (fake, never-dereferenced addresses are used);
+* the split-count policy and the split rule behave as documented.
+"""
+
+import ctypes
+import os
+
+import pytest
+
+from exact_io_aware_order_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return _lib.lib()
+
+
+def test_exports_every_header_function(L):
+    names = _lib.header_functions()
+    assert {"attn_prefill", "attn_decode_splitkv", "attn_combine", "attn_decode_num_splits",
+            "attn_status_string", "attn_check_device_status"} <= set(names)
+    raw = ctypes.CDLL(_lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), f"{n} is declared in include/attn.h but not exported"
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_status_strings(L):
+    codes = _lib.status_codes()
+    assert codes["ATTN_OK"] == 0 and len(set(codes.values())) == len(codes)
+    for name, val in codes.items():
+        s = L.attn_status_string(val).decode()
+        assert s.startswith(name), (name, s)
+    assert L.attn_status_string(999).decode() == "ATTN_ERR_UNKNOWN"
+    assert L.attn_version().decode().endswith("sm_103a")
+
+
+# Fake 16-byte-aligned addresses; validation fails before any is used.
+P = 0x10000
+
+
+def _prefill(L, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, batch=1, hq=4, hkv=2, n=128, d=128, scale=0.1, causal=1)
+    a.update(kw)
+    return L.attn_prefill(a["q"], a["k"], a["v"], a["o"], a["lse"], a["batch"], a["hq"], a["hkv"],
+                          a["n"], a["d"], a["scale"], a["causal"], None)
+
+
+def test_prefill_validation(L):
+    c = _lib.status_codes()
+    assert _prefill(L, q=None) == c["ATTN_ERR_NULL"]
+    assert _prefill(L, lse=None) == c["ATTN_ERR_NULL"]
+    assert _prefill(L, n=0) == c["ATTN_ERR_SHAPE"]
+    assert _prefill(L, batch=0) == c["ATTN_ERR_SHAPE"]
+    assert _prefill(L, n=(1 << 24) + 1) == c["ATTN_ERR_SHAPE"]
+    assert _prefill(L, scale=0.0) == c["ATTN_ERR_SHAPE"]
+    assert _prefill(L, scale=float("nan")) == c["ATTN_ERR_SHAPE"]
+    assert _prefill(L, d=96) == c["ATTN_ERR_HEADDIM"]
+    assert _prefill(L, d=256) == c["ATTN_ERR_HEADDIM"]
+    assert _prefill(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
+    assert _prefill(L, q=P + 8) == c["ATTN_ERR_ALIGN"]
+    assert _prefill(L, o=P + 4) == c["ATTN_ERR_ALIGN"]
+    assert _prefill(L, lse=P + 2) == c["ATTN_ERR_ALIGN"]
+
+
+def _decode(L, **kw):
+    a = dict(q=P, k=P, v=P, bt=P, lens=P, S=4, op=P, lp=P, B=2, hq=8, hkv=2, d=128, bs=16,
+             mb=8, nb=16, maxlen=128, scale=0.1)
+    a.update(kw)
+    return L.attn_decode_splitkv(a["q"], a["k"], a["v"], a["bt"], a["lens"], a["S"], a["op"],
+                                 a["lp"], a["B"], a["hq"], a["hkv"], a["d"], a["bs"], a["mb"],
+                                 a["nb"], a["maxlen"], a["scale"], None)
+
+
+def test_decode_validation(L):
+    c = _lib.status_codes()
+    assert _decode(L, q=None) == c["ATTN_ERR_NULL"]
+    assert _decode(L, lens=None) == c["ATTN_ERR_NULL"]
+    assert _decode(L, B=0) == c["ATTN_ERR_SHAPE"]
+    assert _decode(L, bs=0) == c["ATTN_ERR_SHAPE"]
+    assert _decode(L, nb=0) == c["ATTN_ERR_SHAPE"]
+    assert _decode(L, bt=None, maxlen=0) == c["ATTN_ERR_SHAPE"]
+    assert _decode(L, scale=-1.0) == c["ATTN_ERR_SHAPE"]
+    assert _decode(L, d=80) == c["ATTN_ERR_HEADDIM"]
+    assert _decode(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
+    assert _decode(L, hq=34, hkv=2) == c["ATTN_ERR_GQA"]       # g = 17 > 16
+    assert _decode(L, S=-1) == c["ATTN_ERR_SPLITS"]
+    assert _decode(L, S=_lib.ATTN_MAX_SPLITS + 1) == c["ATTN_ERR_SPLITS"]
+    assert _decode(L, k=P + 8) == c["ATTN_ERR_ALIGN"]
+    assert _decode(L, op=P + 4) == c["ATTN_ERR_ALIGN"]
+    assert _decode(L, bt=P + 2) == c["ATTN_ERR_ALIGN"]
+
+
+def test_combine_validation(L):
+    c = _lib.status_codes()
+    f = L.attn_combine
+    assert f(None, P, 4, 1, 8, 128, P, P, None) == c["ATTN_ERR_NULL"]
+    assert f(P, P, 4, 0, 8, 128, P, P, None) == c["ATTN_ERR_SHAPE"]
+    assert f(P, P, 4, 1, 8, 32, P, P, None) == c["ATTN_ERR_HEADDIM"]
+    assert f(P, P, 0, 1, 8, 128, P, P, None) == c["ATTN_ERR_SPLITS"]
+    assert f(P, P, 1025, 1, 8, 128, P, P, None) == c["ATTN_ERR_SPLITS"]
+    assert f(P + 8, P, 4, 1, 8, 128, P, P, None) == c["ATTN_ERR_ALIGN"]
+
+
+def test_split_policy(L):
+    f = L.attn_decode_num_splits
+    assert f(0, 4, 1000, 152) == 1 and f(1, 4, 0, 152) == 1
+    for B, H, Lk, sms in [(1, 4, 30720, 152), (1, 8, 32768, 152), (16, 8, 32768, 152),
+                          (3, 1, 77, 152), (1, 1, 1000, 152), (256, 8, 30000, 152),
+                          (1, 4, 30720, 148)]:
+        s = f(B, H, Lk, sms)
+        assert 1 <= s <= _lib.ATTN_MAX_SPLITS
+        # splits never cut a sequence into chunks much shorter than 256 tokens
+        assert s == 1 or -(-Lk // s) >= 256 - 16
+        # small batch: enough (sequence, kv head, split) blocks to cover every SM
+        if B * H < sms and Lk >= 256 * sms:
+            assert B * H * s >= sms
+    # large batch: already enough (sequence, head) pairs -> one split
+    assert f(256, 8, 30000, 152) == 1
+
+
+def _rule(kv_len, S):
+    """The split rule as the header states it, restated independently."""
+    if kv_len == 0:
+        return [(0, 0)] * S
+    c = ((kv_len + S - 1) // S + 15) // 16 * 16
+    out = []
+    for s in range(S):
+        lo = min(s * c, kv_len)
+        out.append((lo, min(lo + c, kv_len)))
+    return out
+
+
+@pytest.mark.parametrize("kv_len,S", [(30720, 1), (30720, 16), (30720, 148), (1, 4), (17, 2),
+                                      (1000, 7), (0, 3), (15, 16)])
+def test_split_rule(kv_len, S):
+    from exact_io_aware_order_gb300.api import split_ranges
+
+    r = split_ranges(kv_len, S)
+    assert r == _rule(kv_len, S)
+    covered = [t for a, b in r for t in range(a, b)]
+    assert covered == list(range(kv_len))            # a partition, in order
+
+
+def test_header_documents_each_entry_point():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    for name in ["attn_prefill", "attn_decode_splitkv", "attn_combine", "attn_decode_num_splits"]:
+        block = text[:text.index(name + "(")]
+        doc = block[block.rindex("/*"):]
+        assert "Page:" in doc or "section" in doc, f"{name} lacks its citation"
