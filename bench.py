@@ -1,0 +1,494 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+  * causal prefill of one Qwen2.5-7B-shaped attention layer (batch 1, 28 query
+    / 4 key-value heads, head_dim 128, N = 8192 tokens): attn_prefill;
+  * one split-KV single-token decode over a 30720-token contiguous cache of the
+    same layer shape (auto split count): attn_decode_splitkv + attn_combine.
+The headline value is causal-prefill attention TFLOP/s (4 N^2 d heads, halved
+for causal); the decode HBM GB/s is reported beside it.  Inputs are resident
+in HBM when the timed region starts; the decode cache rotates over four copies
+(4 x 62.9 MB > L2) and the prefill writes a 117 MB output each step, so no
+step reads warm L2 data from the step before.
+
+`--impl reference` times the float64 CPU oracle (the only other place this file
+runs anything under oracle/) on a bounded sample of the same workload.
+
+N > 1 GPUs (torchrun): one independent replica per GPU ("replicas only": the
+path needs no exchange between GPUs), barrier + max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal prefill attention TFLOP/s (% BF16 peak); split-KV decode HBM GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "prefill_sm103_qwen_n8192.txt")
+PREFILL_SRC = os.path.join(ROOT, "exact_io_aware_order_gb300", "csrc", "prefill_sm103.cu")
+
+WORKLOADS = {
+    # name: (prefill (n_q, n_kv, N, d, spike), decode kind)
+    "qwen": dict(n_q=28, n_kv=4, seqlen=8192, d=128, spike=0.0, decode="qwen30720",
+                 desc="Qwen2.5-7B attention layer: causal prefill N=8192 (28/4 heads, d=128) + "
+                      "split-KV decode over a 30720-token contiguous cache"),
+    "llama-long": dict(n_q=32, n_kv=8, seqlen=32768, d=128, spike=0.01, decode="paged16",
+                       desc="Llama-3-8B attention layer: causal prefill N=32768 (32/8 heads, "
+                            "1% keys x8) + paged decode of 16 sequences, lengths U[1024,32768]"),
+}
+
+
+def prefill_flops(n_q: int, seqlen: int, d: int, batch: int = 1) -> float:
+    return 4.0 * batch * n_q * float(seqlen) ** 2 * d / 2.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the prefill kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+        sha = hashlib.sha256(open(PREFILL_SRC, "rb").read()).hexdigest()[:16]
+        vals = dict(line.split(":", 1) for line in text.splitlines() if ":" in line)
+        if vals.get("source_sha256_16", "").strip() != sha:
+            return None
+        return float(vals["dram_bytes_per_launch"].strip())
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", gpu_id, "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons), "samples": n}
+
+
+# ---------------------------------------------------------------------------
+# The GB300 arm.
+# ---------------------------------------------------------------------------
+def run_gb300(args, rank: int, world: int, dist):
+    import torch
+
+    import exact_io_aware_order_gb300 as attn
+    from exact_io_aware_order_gb300 import workloads as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    attn.lib()  # fail loudly if the library is missing
+    wl = WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+
+    # ---- inputs (seeded, synthetic), resident in HBM ----
+    x = W.make_prefill(1, wl["n_q"], wl["n_kv"], wl["seqlen"], wl["d"], seed=0,
+                       spike_frac=wl["spike"])
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    o = torch.empty((1, wl["n_q"], wl["seqlen"], wl["d"]), dtype=torch.float32, device=dev)
+    lse = torch.empty((1, wl["n_q"], wl["seqlen"]), dtype=torch.float32, device=dev)
+    if wl["decode"] == "qwen30720":
+        dec = W.qwen_decode(30720)
+    else:
+        dec = W.llama_paged_decode()
+    n_copies = 4
+    caches = []
+    for c in range(n_copies):  # rotate so no decode reads a cache left warm in L2
+        caches.append((dec.k_cache.to(dev), dec.v_cache.to(dev)))
+    dq = dec.q.to(dev)
+    dlens = dec.kv_lens.to(dev)
+    dbt = dec.block_table.to(dev) if dec.block_table is not None else None
+    B, Hq, D = dq.shape
+    S = attn.decode_num_splits(B, dec.n_kv, dec.max_kv_len)
+    op = torch.empty((S, B, Hq, D), dtype=torch.float32, device=dev)
+    lp = torch.empty((S, B, Hq), dtype=torch.float32, device=dev)
+    do = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    dl = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    tokens = int(dec.kv_lens.sum())
+    dec_bytes = (tokens * dec.n_kv * D * 2 * 2) + dq.numel() * 2 + do.numel() * 4 + dl.numel() * 4
+    flops = prefill_flops(wl["n_q"], wl["seqlen"], wl["d"])
+
+    def step(i, ev=None):
+        kc, vc = caches[i % n_copies]
+        if ev is not None:
+            ev[0].record()
+        attn.prefill(q, k, v, x.scale, True, out=o, lse=lse)
+        if ev is not None:
+            ev[1].record()
+        attn.decode_splitkv(dq, kc, vc, dlens, dbt, num_splits=S, max_kv_len=dec.max_kv_len,
+                            scale=dec.scale, o_partial=op, lse_partial=lp)
+        if ev is not None:
+            ev[2].record()
+        attn.combine(op, lp, out=do, lse=dl)
+        if ev is not None:
+            ev[3].record()
+
+    for i in range(args.warmup):
+        step(i)
+    attn.check_device_status()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    gpu_uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", "") or "")
+    sampler = ClockSampler(("GPU-" + gpu_uuid) if gpu_uuid and not gpu_uuid.startswith("GPU-")
+                           else (gpu_uuid or str(dev.index)))
+    time.sleep(0.15)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(args.steps):
+        step(i, evs[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    attn.check_device_status()
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    cmb_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    pre_total = sum(pre_ms)
+    dec_total = sum(dec_ms) + sum(cmb_ms)
+
+    # max over ranks of each timed quantity
+    def rmax(val: float) -> float:
+        if dist is None:
+            return val
+        t = torch.tensor([val], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    total_ms, pre_total, dec_total = rmax(total_ms), rmax(pre_total), rmax(dec_total)
+    avg_pre = statistics.mean(pre_ms)
+    avg_dec = statistics.mean(dec_ms)
+    prefill_tflops = world * flops * args.steps / (pre_total * 1e-3) / 1e12
+    decode_gbs = world * dec_bytes * args.steps / (dec_total * 1e-3) / 1e9
+    achieved = flops / (avg_pre * 1e-3) / 1e12
+    dec_achieved = dec_bytes / (avg_dec * 1e-3) / 1e9
+    traffic = profiled_traffic() if args.workload == "qwen" else None
+
+    result = {
+        "metric": METRIC, "value": round(prefill_tflops, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl["desc"], "batch": 1, "n_q_heads": wl["n_q"],
+                   "n_kv_heads": wl["n_kv"], "seqlen": wl["seqlen"], "head_dim": wl["d"],
+                   "decode_tokens": tokens, "decode_num_splits": S,
+                   "l2": "decode cache rotated over 4 copies (> L2); prefill writes a fresh "
+                         "output each step",
+                   "parallelism": f"replicas x{world}"},
+        "prefill_frac_of_bf16_peak": round(achieved / peaks["bf16_tflops"], 4),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": traffic,
+                     "kernel": "prefill_kernel<128>", "peak_source": peak_src + " bf16 burst",
+                     "flops_per_launch": flops, "avg_launch_ms": round(avg_pre, 4)},
+        "decode": {"value": round(decode_gbs, 1), "unit": "GB/s",
+                   "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 1),
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": round(dec_achieved / peaks["hbm_gbs"], 4),
+                                "kernel": "decode_splitkv_kernel<128>",
+                                "peak_source": peak_src + " hbm copy",
+                                "bytes_per_launch": dec_bytes,
+                                "avg_launch_us": round(avg_dec * 1e3, 2),
+                                "combine_avg_us": round(statistics.mean(cmb_ms) * 1e3, 2)}},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist)
+    return result
+
+
+def run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist):
+    """Same metric through the public API with pinned host buffers: every step
+    copies its inputs host->device and its outputs device->host."""
+    import torch
+
+    import exact_io_aware_order_gb300 as attn
+
+    pin = lambda t: t.contiguous().pin_memory()
+    hq, hk, hv = pin(x.q), pin(x.k), pin(x.v)
+    ho = torch.empty(tuple(x.q.shape), dtype=torch.float32).pin_memory()
+    hl = torch.empty(tuple(x.q.shape[:3]), dtype=torch.float32).pin_memory()
+    hdq, hkc, hvc, hlen = pin(dec.q), pin(dec.k_cache), pin(dec.v_cache), pin(dec.kv_lens)
+    hbt = pin(dec.block_table) if dec.block_table is not None else None
+    B, Hq, D = dec.q.shape
+    hdo = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+    hdl = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+    q, k, v = (torch.empty_like(t, device=dev) for t in (hq, hk, hv))
+    o = torch.empty(ho.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty(hl.shape, dtype=torch.float32, device=dev)
+    dq, kc, vc, dl_ = (torch.empty_like(t, device=dev) for t in (hdq, hkc, hvc, hlen))
+    dbt = torch.empty_like(hbt, device=dev) if hbt is not None else None
+    op = torch.empty((S, B, Hq, D), dtype=torch.float32, device=dev)
+    lp = torch.empty((S, B, Hq), dtype=torch.float32, device=dev)
+    do = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    dlo = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdq, hkc, hvc, hlen)) + \
+        (hbt.numel() * 4 if hbt is not None else 0)
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdo, hdl))
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        attn.prefill(q, k, v, x.scale, True, out=o, lse=lse)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        if ev is not None:
+            ev[1].record()
+        dq.copy_(hdq, non_blocking=True)
+        kc.copy_(hkc, non_blocking=True)
+        vc.copy_(hvc, non_blocking=True)
+        dl_.copy_(hlen, non_blocking=True)
+        if dbt is not None:
+            dbt.copy_(hbt, non_blocking=True)
+        attn.decode_splitkv(dq, kc, vc, dl_, dbt, num_splits=S, max_kv_len=dec.max_kv_len,
+                            scale=dec.scale, o_partial=op, lse_partial=lp)
+        attn.combine(op, lp, out=do, lse=dlo)
+        hdo.copy_(do, non_blocking=True)
+        hdl.copy_(dlo, non_blocking=True)
+        if ev is not None:
+            ev[2].record()
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        step()
+    n = max(3, min(args.steps, args.e2e_steps))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    for i in range(n):
+        step(evs[i])
+    torch.cuda.synchronize()
+    pre = sum(e[0].elapsed_time(e[1]) for e in evs)
+    dcd = sum(e[1].elapsed_time(e[2]) for e in evs)
+    if dist is not None:
+        t = torch.tensor([pre, dcd], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        pre, dcd = float(t[0]), float(t[1])
+    return {"value": round(world * flops * n / (pre * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "decode_value": round(world * dec_bytes * n / (dcd * 1e-3) / 1e9, 1),
+            "decode_unit": "GB/s (end to end, cache copied from host each step)"}
+
+
+# ---------------------------------------------------------------------------
+# The float64 CPU oracle (cpu_baseline leg and --impl reference).
+# ---------------------------------------------------------------------------
+def _cpu_worker(spec: dict) -> dict:
+    """Runs inside a fresh interpreter with BLAS threads pinned: times the
+    oracle on the requested sample and returns throughput figures."""
+    import numpy as np
+
+    from exact_io_aware_order_gb300 import workloads as W
+    import oracle
+
+    wl = WORKLOADS[spec["workload"]]
+    x = W.make_prefill(1, wl["n_q"], wl["n_kv"], wl["seqlen"], wl["d"], seed=0,
+                       spike_frac=wl["spike"])
+    g = wl["n_q"] // wl["n_kv"]
+    out = {}
+    if spec["kind"] == "heads":
+        h = spec["heads"]
+        nkv = -(-h // g)
+        t0 = time.perf_counter()
+        oracle.prefill(x.q[:, :h], x.k[:, :nkv], x.v[:, :nkv], x.scale, True)
+        dt = time.perf_counter() - t0
+        fl = prefill_flops(h, wl["seqlen"], wl["d"])
+        out["prefill_tflops"] = fl / dt / 1e12
+        out["prefill_s"] = dt
+        out["sample"] = f"all {wl['seqlen']} rows of {h} of {wl['n_q']} query heads"
+    else:  # per-step sampled rows, repeated
+        N = wl["seqlen"]
+        rows = [(0, 0, int(i)) for i in np.linspace(0, N - 1, spec["rows"]).round()]
+        fl = sum(4.0 * (i + 1) * wl["d"] for _, _, i in rows)
+        times = []
+        for _ in range(spec["repeats"]):
+            t0 = time.perf_counter()
+            oracle.prefill_rows(x.q, x.k, x.v, x.scale, True, rows)
+            times.append(time.perf_counter() - t0)
+        out["prefill_tflops"] = fl * len(times) / sum(times) / 1e12
+        out["prefill_s"] = sum(times)
+        out["step_times"] = times
+        out["sample"] = f"{spec['rows']} evenly spaced rows of query head 0 per step"
+    if spec.get("decode", True):
+        dec = W.qwen_decode(30720) if wl["decode"] == "qwen30720" else W.llama_paged_decode()
+        nb = spec.get("decode_seqs", dec.q.shape[0])
+        lens = dec.kv_lens.tolist()[:nb]
+        t0 = time.perf_counter()
+        oracle.decode(dec.q[:nb], dec.k_cache, dec.v_cache,
+                      dec.block_table[:nb] if dec.block_table is not None else None,
+                      lens, dec.scale, dec.block_size)
+        dt = time.perf_counter() - t0
+        byts = sum(lens) * dec.n_kv * dec.q.shape[2] * 4
+        out["decode_gbs"] = byts / dt / 1e9
+        out["decode_s"] = dt
+    return out
+
+
+def run_cpu(spec: dict) -> dict:
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ, OPENBLAS_NUM_THREADS=str(cores), OMP_NUM_THREADS=str(cores),
+               MKL_NUM_THREADS=str(cores), CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", json.dumps(spec)],
+                       env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("oracle worker failed:\n" + r.stderr[-2000:])
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    out["cores"] = cores
+    return out
+
+
+def run_reference(args, rank: int, world: int):
+    """Times the float64 oracle on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return None
+    wl = WORKLOADS[args.workload]
+    rows = 32 if args.workload == "qwen" else 8
+    spec = {"workload": args.workload, "kind": "rows", "rows": rows,
+            "repeats": args.warmup + args.steps, "decode": False}
+    r = run_cpu(spec)
+    times = r["step_times"][args.warmup:]
+    import numpy as np
+
+    fl = sum(4.0 * (i + 1) * wl["d"] for i in np.linspace(0, wl["seqlen"] - 1, rows).round())
+    value = fl * len(times) / sum(times) / 1e12
+    return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": wl["desc"], "batch": 1, "n_q_heads": wl["n_q"],
+                       "n_kv_heads": wl["n_kv"], "seqlen": wl["seqlen"], "head_dim": wl["d"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"],
+                             "kind": "oracle", "sample": r["sample"]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-heads", type=int, default=8,
+                    help="query heads in the cpu_baseline sample (whole rows, N tokens)")
+    ap.add_argument("--cpu-worker", type=str, default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+
+    if args.cpu_worker is not None:
+        print(json.dumps(_cpu_worker(json.loads(args.cpu_worker))))
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    # The CPU baseline runs before the first GPU call (its worker is a fresh
+    # interpreter either way), on rank 0 at N = 1 only.
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        spec = {"workload": args.workload, "kind": "heads", "heads": args.cpu_heads}
+        r = run_cpu(spec)
+        cpu = {"value": round(r["prefill_tflops"], 6), "unit": "TFLOP/s", "cores": r["cores"],
+               "kind": "oracle", "sample": r["sample"] + "; float64 numpy, BLAS threads = cores",
+               "seconds": round(r["prefill_s"], 2),
+               "decode_value": round(r["decode_gbs"], 3), "decode_unit": "GB/s",
+               "decode_seconds": round(r["decode_s"], 2)}
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    res = run_gb300(args, rank, world, dist)
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
