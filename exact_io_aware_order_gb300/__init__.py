@@ -15,5 +15,6 @@ from .api import (  # noqa: F401
     set_wait_timeout_ns,
     selftest_bounded_wait,
     split_ranges,
+    decode_noalloc,
 )
 from ._lib import AttnError, lib  # noqa: F401

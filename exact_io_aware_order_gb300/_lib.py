@@ -30,9 +30,12 @@ SIGNATURES = {
     "attn_check_device_status": (c_int, [c_void_p]),
     "attn_set_wait_timeout_ns": (c_uint64, [c_uint64]),
     "attn_selftest_bounded_wait": (c_int, [c_void_p]),
+    "attn_decode_noalloc": (c_int, [c_void_p] * 5 + [c_int] + [c_void_p] * 2 + [c_int] * 8
+                            + [c_float, c_void_p]),
 }
 
 ATTN_MAX_SPLITS = 1024
+ATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class AttnError(RuntimeError):

@@ -185,3 +185,44 @@ def set_wait_timeout_ns(timeout_ns: int) -> int:
 def selftest_bounded_wait(stream=None) -> int:
     """Runs the bounded-wait self-test kernel; returns its attn_status code."""
     return int(lib().attn_selftest_bounded_wait(_stream(stream)))
+
+
+def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   kv_lens: torch.Tensor, block_table: Optional[torch.Tensor] = None,
+                   num_splits: int = 0, max_kv_len: Optional[int] = None,
+                   scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, stream=None):
+    """Split-KV decode + combine with the partials in the library's fixed
+    device buffer (``attn_decode_noalloc``), for callers that cannot allocate
+    device memory on their decode path: pass ``out`` and ``lse`` to allocate
+    nothing at all.  Returns (O (B, n_q, d), LSE (B, n_q)), fp32."""
+    _need(q, "q", _BF16, 3)
+    _need(k_cache, "k_cache", _BF16, 4)
+    _need(v_cache, "v_cache", _BF16, 4)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    B, n_q, d = q.shape
+    n_kv = k_cache.shape[2]
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, 2)
+        num_blocks, block_size, max_blocks = k_cache.shape[0], k_cache.shape[1], block_table.shape[1]
+        if max_kv_len is None:
+            max_kv_len = max_blocks * block_size
+        bt_ptr = block_table.data_ptr()
+    else:
+        num_blocks, block_size, max_blocks = 0, 0, 0
+        max_kv_len = k_cache.shape[1]
+        bt_ptr = None
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, n_q, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, n_q), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, 3)
+    _need(lse, "lse", torch.float32, 2)
+    st = lib().attn_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), bt_ptr,
+                                   kv_lens.data_ptr(), int(num_splits), out.data_ptr(),
+                                   lse.data_ptr(), B, n_q, n_kv, d, block_size, max_blocks,
+                                   num_blocks, int(max_kv_len), float(scale), _stream(stream))
+    check("attn_decode_noalloc", st)
+    return out, lse

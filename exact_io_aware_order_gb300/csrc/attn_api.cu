@@ -92,6 +92,16 @@ int split_policy(int batch, int n_kv_heads, int max_kv_len, int num_sms) {
 
 }  // namespace
 
+namespace attn {
+int resolve_launch_ctx(void* stream, LaunchCtx* out) {
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  *out = make_ctx(stream, ds);
+  return ATTN_OK;
+}
+}  // namespace attn
+
 extern "C" {
 
 const char* attn_status_string(int status) {
@@ -107,6 +117,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH: a CUDA call or kernel launch failed";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel-side bounded wait gave up";
     case ATTN_ERR_DEVICE: return "ATTN_ERR_DEVICE: a kernel saw a bad block-table entry or kv_len";
+    case ATTN_ERR_SCRATCH: return "ATTN_ERR_SCRATCH: the split partials exceed the fixed scratch buffer";
     default: return "ATTN_ERR_UNKNOWN";
   }
 }

@@ -58,6 +58,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_combine(const CombineArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_wait_selftest(const LaunchCtx& ctx);
 
+// Resolves the current device's launch context (architecture check, error
+// word, SM count) for a call on `stream`; returns an attn_status code.
+int resolve_launch_ctx(void* stream, LaunchCtx* out);
+
 // Split rule shared by the decode kernel's documentation and the host:
 // c = roundup(ceil(len / S), 16); split s covers [s*c, min((s+1)*c, len)).
 constexpr int kSplitGranule = 16;

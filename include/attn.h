@@ -57,7 +57,8 @@ typedef enum attn_status {
   ATTN_ERR_ARCH = 7,     /* the current device is not sm_103 (GB300)             */
   ATTN_ERR_LAUNCH = 8,   /* a CUDA runtime call or kernel launch failed          */
   ATTN_ERR_TIMEOUT = 9,  /* a kernel's bounded wait gave up (device error word)  */
-  ATTN_ERR_DEVICE = 10   /* bad block-table entry or kv_len seen by a kernel     */
+  ATTN_ERR_DEVICE = 10,  /* bad block-table entry or kv_len seen by a kernel     */
+  ATTN_ERR_SCRATCH = 11  /* attn_decode_noalloc: partials exceed its fixed buffer */
 } attn_status;
 
 /* Name of a status code; never NULL. */
@@ -179,6 +180,48 @@ uint64_t attn_set_wait_timeout_ns(uint64_t timeout_ns);
  * `stream`.  Exercises the give-up path without faulting or hanging the GPU.
  */
 int attn_selftest_bounded_wait(void* stream);
+
+/*
+ * attn_decode_noalloc -- split-KV decode and combine in one call, for callers
+ * that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point: it is a convenience of
+ * this library.  Some callers may not call cudaMalloc on their decode path:
+ * a serving loop that reserved all device memory at start-up and forbids
+ * later allocations, a plugin inside a host framework that owns the device
+ * allocator and only hands it the tensors it needs, or a latency-critical step
+ * where cudaMalloc's implicit synchronisation is unacceptable.  Such a caller
+ * cannot provide the per-split partial buffers that attn_decode_splitkv
+ * writes and attn_combine reads.  This entry point keeps those partials in a
+ * fixed buffer of ATTN_NOALLOC_SCRATCH_BYTES compiled into the library (a
+ * file-scope device array): every GPU that loads the library holds it until
+ * the process exits.  It calls no allocating routine.
+ *
+ * Arguments are those of attn_decode_splitkv, except that the final results
+ * are written directly:
+ *   o   : (batch, n_q_heads, head_dim) fp32 output, 16-byte aligned
+ *   lse : (batch, n_q_heads) fp32 output (natural log), 4-byte aligned
+ * The results equal attn_decode_splitkv followed by attn_combine with the same
+ * num_splits (0 = the same policy).
+ * Limit: num_splits * batch * n_q_heads * (head_dim + 1) * 4 bytes, with the
+ *   output part rounded up to 256 bytes, must fit in ATTN_NOALLOC_SCRATCH_BYTES;
+ *   larger requests return ATTN_ERR_SCRATCH and launch nothing.
+ * Set-up: the first call on each device looks up the buffer's device address
+ *   (cudaGetSymbolAddress, once per device, with that device current); make
+ *   that first call before any stream capture begins.
+ * Sharing: every call reuses the same buffer, which keeps the previous call's
+ *   contents.  Each call overwrites every partial value it later reads, so
+ *   nothing needs clearing; but two calls whose kernels overlap on the GPU
+ *   (unordered streams, or concurrent host threads) race on the buffer and
+ *   give wrong results -- order them on one stream or with events.
+ * Errors: those of attn_decode_splitkv, plus ATTN_ERR_SCRATCH.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+int attn_decode_noalloc(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                        const int32_t* block_table, const int32_t* kv_lens, int num_splits,
+                        float* o, float* lse, int batch, int n_q_heads, int n_kv_heads,
+                        int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                        int max_kv_len, float scale, void* stream);
 
 /* Library version string, e.g. "0.1.0 sm_103a". */
 const char* attn_version(void);
