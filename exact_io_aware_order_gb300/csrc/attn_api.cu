@@ -77,12 +77,17 @@ bool valid_scale(float scale) { return std::isfinite(scale) && scale > 0.f; }
 
 int split_policy(int batch, int n_kv_heads, int max_kv_len, int num_sms) {
   if (batch <= 0 || n_kv_heads <= 0 || max_kv_len <= 0 || num_sms <= 0) return 1;
-  // Aim for about four resident decode CTAs' worth of work per SM, but keep
-  // every split at least 256 tokens long (the split results then dominate
-  // the partial-output traffic only by a small factor).
+  // Two decode CTAs are resident per SM.  One sequence: exactly one full wave
+  // of equal chunks.  Several sequences (lengths may differ): about four waves
+  // of smaller chunks so the block scheduler can balance long and short ones.
+  // Never cut chunks much below 256 tokens (a CTA must stream long enough to
+  // hide its start-up), and use one split once (sequence, kv head) pairs
+  // already fill the GPU.
+  const long long slots = 2LL * num_sms;
   const long long pairs = (long long)batch * n_kv_heads;
-  const long long target = 4LL * num_sms;
-  long long splits = (target + pairs - 1) / pairs;
+  if (pairs >= slots) return 1;
+  const long long waves = batch == 1 ? 1 : 4;
+  long long splits = (waves * slots + pairs - 1) / pairs;
   const long long max_useful = (max_kv_len + 255) / 256;
   if (splits > max_useful) splits = max_useful;
   if (splits < 1) splits = 1;

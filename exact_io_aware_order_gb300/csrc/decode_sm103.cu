@@ -11,17 +11,23 @@
 // partial results; the merge rule of section "Minimal implementation").
 //
 // Design for GB300.  Decode is HBM-bound, so the kernel is built to stream:
-//   * one producer warp issues one 256-byte bulk async copy per cache row
-//     (cp.async.bulk, completing on an mbarrier) into a 3-stage ring of
-//     64-token stages -- paged and contiguous caches take the same path;
+//   * a producer warp feeds a ring of 64-token stages with tiled TMA copies
+//     (128-byte swizzle): one box of 64 tokens x 64 dims (8 KB) for a
+//     contiguous cache, one box of 16 tokens (2 KB) per 16-token group of a
+//     paged cache whose block size is a multiple of 16.  Other block sizes
+//     fall back to plain loads by the producer warp;
 //   * four consumer warps each take 16 tokens of a stage.  With g query rows
 //     sharing the rows, q K^T and P V are small dense products (M = 16 padded
 //     rows); they run on mma.sync m16n8k16 (bf16 in, fp32 accumulate) so the
 //     ALU work stays far below the memory time;
-//   * rows sit at a 16-byte padded pitch, so every ldmatrix is conflict-free;
-//   * row max / row sum use quad shuffles; at the end the warps merge their
-//     (m, l, O) states through shared memory.
+//   * ldmatrix reads the swizzled rows without bank conflicts; row max / row
+//     sum use quad shuffles; the output is rescaled only when a row max grows
+//     by more than 2^8 (exact: the same stale max is used for l and O); at the
+//     end the warps merge their (m, l, O) states through shared memory.
 #include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -31,30 +37,43 @@
 namespace attn {
 namespace {
 
+#ifndef ATTN_DECODE_STAGES
+#define ATTN_DECODE_STAGES 3
+#endif
 constexpr int kStageTokens = 64;   // tokens per ring stage
-constexpr int kStages = 3;
+constexpr int kStages = ATTN_DECODE_STAGES;
 constexpr int kConsumerWarps = 4;  // 16 tokens each per stage
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// How the producer fills a stage.
+enum LoadMode : int { kLoadBox64 = 0, kLoadBox16 = 1, kLoadPlain = 2 };
 
 template <int D>
 struct DecodeSmem {
-  static constexpr int kRowBytes = D * 2 + 16;                 // padded pitch
-  static constexpr int kStageBytes = kStageTokens * kRowBytes;  // one of K or V
-  static constexpr int kQBytes = 16 * kRowBytes;
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kStages * kStageBytes;
-  static constexpr int kQOff = 2 * kStages * kStageBytes;
-  static constexpr int kBarOff = kQOff + kQBytes;              // 2*kStages barriers
+  static constexpr int kHalves = D / 64;                       // 128-byte swizzle spans per row
+  static constexpr int kHalfBytes = kStageTokens * 128;        // 64 rows x 128 B
+  static constexpr int kTileBytes = kHalves * kHalfBytes;      // K (or V) of one stage
+  static constexpr int kStageBytes = 2 * kTileBytes;           // K then V
+  static constexpr int kQRowBytes = D * 2 + 16;                // padded q rows
+  static constexpr int kRing = 0;
+  static constexpr int kQOff = kStages * kStageBytes;
+  static constexpr int kBarOff = kQOff + 16 * kQRowBytes;      // 2*kStages barriers
   static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;
-  static constexpr int kTotal = kMiscOff + 16;
-  // Merge scratch reuses the K/V ring once the stream is done.
+  static constexpr int kTotal = kMiscOff + 16 + 1024;          // + alignment slack
+  // Merge scratch reuses the ring once the stream is done.
   static constexpr int kMergeO = 0;                                  // [warps][16][D] f32
   static constexpr int kMergeM = kConsumerWarps * 16 * D * 4;        // [warps][16]
   static constexpr int kMergeL = kMergeM + kConsumerWarps * 16 * 4;  // [warps][16]
   static_assert(kMergeL + kConsumerWarps * 16 * 4 <= kQOff, "merge scratch fits in the ring");
 };
+
+// Byte offset of (row, 16-byte chunk c) inside one 128-byte-swizzled span.
+__device__ __forceinline__ uint32_t swz(int row, int c) {
+  return (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4));
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -76,6 +95,14 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -83,11 +110,22 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
 }
 
+struct DecodeKParams {
+  DecodeArgs a;
+  int mode;  // LoadMode
+  uint32_t* err_word;
+  uint64_t timeout_ns;
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads)
-decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_ns) {
+decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const DecodeKParams kp) {
   using L = DecodeSmem<D>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  const DecodeArgs& a = kp.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int S = a.num_splits;
   const int g = a.n_q_heads / a.n_kv_heads;
@@ -99,7 +137,7 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
       paged ? (long long)a.max_blocks_per_seq * a.block_size : (long long)a.max_kv_len;
   int len = a.kv_lens[b];
   if (len < 0 || (long long)len > capacity) {
-    if (threadIdx.x == 0) atomicOr(err_word, kErrKvLen);
+    if (threadIdx.x == 0 && split == 0) atomicOr(kp.err_word, kErrKvLen);
     len = len < 0 ? 0 : (int)capacity;
   }
   const int per = (len + S - 1) / S;
@@ -130,11 +168,15 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
     fence_mbar_init();
   }
   __syncthreads();
-  const WaitCtl ctl{abort_flag, err_word, timeout_ns};
+  const WaitCtl ctl{abort_flag, kp.err_word, kp.timeout_ns};
 
   if (warp == 0) {
     // ================= producer: stream rows into the ring =================
     const int32_t* table = paged ? a.block_table + (size_t)b * a.max_blocks_per_seq : nullptr;
+    if (lane == 0 && kp.mode != kLoadPlain) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+    }
     for (int it = 0; it < n_stage_iters; ++it) {
       const int st = it % kStages;
       if (it >= kStages) {
@@ -142,37 +184,75 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
       }
       const int base = t0 + it * kStageTokens;
       const int cnt = min(kStageTokens, t1 - base);
-      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)cnt * 2u * D * 2u);
-      __syncwarp();
-      for (int i = lane; i < cnt; i += 32) {
-        const int t = base + i;
-        size_t row;
-        if (paged) {
+      uint8_t* sk = smem + L::kRing + st * L::kStageBytes;
+      uint8_t* sv = sk + L::kTileBytes;
+      if (kp.mode == kLoadBox64) {
+        // Contiguous cache viewed as (D, n_kv, L, B): one 64-token box per half.
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)L::kStageBytes);
+#pragma unroll
+          for (int h = 0; h < L::kHalves; ++h) {
+            tma_load_4d(smem_u32(sk + h * L::kHalfBytes), &tm_k, full0 + 8 * st, h * 64, kvh, base, b);
+            tma_load_4d(smem_u32(sv + h * L::kHalfBytes), &tm_v, full0 + 8 * st, h * 64, kvh, base, b);
+          }
+        }
+      } else if (kp.mode == kLoadBox16) {
+        // Paged cache viewed as (D, n_kv, block_size, num_blocks): one box per
+        // 16-token group (a group never straddles a block: both are 16-aligned).
+        const int groups = (cnt + 15) >> 4;
+        if (lane == 0)
+          mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)groups * 16u * 2u * (uint32_t)D * 2u);
+        __syncwarp();
+        if (lane < groups) {
+          const int t = base + 16 * lane;
           int blk = table[t / a.block_size];
           if (blk < 0 || blk >= a.num_blocks) {
-            atomicOr(err_word, kErrBlockIndex);
+            atomicOr(kp.err_word, kErrBlockIndex);
             blk = 0;  // keep the copy in bounds; the result is flagged invalid
           }
-          row = (size_t)blk * a.block_size + (t % a.block_size);
-        } else {
-          row = (size_t)b * a.max_kv_len + t;
+          const int slot = t % a.block_size;
+#pragma unroll
+          for (int h = 0; h < L::kHalves; ++h) {
+            tma_load_4d(smem_u32(sk + h * L::kHalfBytes + lane * 2048), &tm_k, full0 + 8 * st,
+                        h * 64, kvh, slot, blk);
+            tma_load_4d(smem_u32(sv + h * L::kHalfBytes + lane * 2048), &tm_v, full0 + 8 * st,
+                        h * 64, kvh, slot, blk);
+          }
         }
-        const size_t off = (row * a.n_kv_heads + kvh) * D;
-        const uint32_t dk = smem_u32(smem + L::kKOff + st * L::kStageBytes + i * L::kRowBytes);
-        const uint32_t dv = smem_u32(smem + L::kVOff + st * L::kStageBytes + i * L::kRowBytes);
-        bulk_load(dk, a.k_cache + off, D * 2, full0 + 8 * st);
-        bulk_load(dv, a.v_cache + off, D * 2, full0 + 8 * st);
+      } else {
+        // Any other block size: plain 16-byte loads into the swizzled layout.
+        for (int i = lane; i < cnt * (D / 8); i += 32) {
+          const int r = i / (D / 8), c = i % (D / 8);
+          const int t = base + r;
+          size_t row;
+          if (paged) {
+            int blk = table[t / a.block_size];
+            if (blk < 0 || blk >= a.num_blocks) {
+              atomicOr(kp.err_word, kErrBlockIndex);
+              blk = 0;
+            }
+            row = (size_t)blk * a.block_size + (t % a.block_size);
+          } else {
+            row = (size_t)b * a.max_kv_len + t;
+          }
+          const size_t off = (row * a.n_kv_heads + kvh) * D + (size_t)c * 8;
+          const uint4 kval = *reinterpret_cast<const uint4*>(a.k_cache + off);
+          const uint4 vval = *reinterpret_cast<const uint4*>(a.v_cache + off);
+          const uint32_t o = (c >> 3) * L::kHalfBytes + swz(r, c & 7);
+          *reinterpret_cast<uint4*>(sk + o) = kval;
+          *reinterpret_cast<uint4*>(sv + o) = vval;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full0 + 8 * st);
       }
     }
     // Wait for copies still in flight before the CTA may leave (abort path only:
     // on the normal path the consumers have waited on every stage).
-    if (*abort_flag) {
-      for (int it = max(0, n_stage_iters - kStages); it < n_stage_iters; ++it) {
-        WaitCtl drain{abort_flag, err_word, timeout_ns};
-        volatile uint32_t no_abort = 0u;
-        drain.abort_flag = &no_abort;
+    if (*abort_flag && lane == 0) {
+      volatile uint32_t no_abort = 0u;
+      WaitCtl drain{&no_abort, kp.err_word, kp.timeout_ns};
+      for (int it = max(0, n_stage_iters - kStages); it < n_stage_iters; ++it)
         mbar_wait(full0 + 8 * (it % kStages), (it / kStages) & 1, drain);
-      }
     }
   } else {
     // ================= consumers =================
@@ -185,7 +265,7 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
       const int r = i / (D / 8), c = i % (D / 8);
       uint4 val = make_uint4(0, 0, 0, 0);
       if (r < g) val = *reinterpret_cast<const uint4*>(qsrc + (size_t)r * D + c * 8);
-      *reinterpret_cast<uint4*>(sq + r * L::kRowBytes + c * 16) = val;
+      *reinterpret_cast<uint4*>(sq + r * L::kQRowBytes + c * 16) = val;
     }
     consumer_sync();
     // Q as A fragments, one set per 16-wide k step of the head dimension.
@@ -194,7 +274,7 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
     for (int kk = 0; kk < D / 16; ++kk) {
       const int r = (lane & 15);
       const int c = kk * 16 + (lane >> 4) * 8;
-      ldsm_x4(smem_u32(sq + r * L::kRowBytes + c * 2), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+      ldsm_x4(smem_u32(sq + r * L::kQRowBytes + c * 2), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
     }
     const float sl2 = a.scale * kLog2e;
     float m_r[2] = {-INFINITY, -INFINITY};  // running max (log2 domain) of rows gid, gid+8
@@ -211,12 +291,14 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
       const int cnt = min(kStageTokens, t1 - base);
       const int vc = min(16, cnt - cw * 16);  // valid tokens of this warp's 16
       if (vc > 0) {
-        uint8_t* sk = smem + L::kKOff + st * L::kStageBytes + cw * 16 * L::kRowBytes;
-        uint8_t* sv = smem + L::kVOff + st * L::kStageBytes + cw * 16 * L::kRowBytes;
-        if (vc < 16) {  // stale rows past the end: zero V so 0 * (old data) stays 0
+        uint8_t* sk = smem + L::kRing + st * L::kStageBytes;
+        uint8_t* sv = sk + L::kTileBytes;
+        const int r0 = cw * 16;  // this warp's first row in the stage
+        if (vc < 16) {  // rows past the end: zero V so 0 * (old data) stays 0
           for (int i = lane; i < (16 - vc) * (D / 8); i += 32) {
-            const int r = vc + i / (D / 8), c = i % (D / 8);
-            *reinterpret_cast<uint4*>(sv + r * L::kRowBytes + c * 16) = make_uint4(0, 0, 0, 0);
+            const int r = r0 + vc + i / (D / 8), c = i % (D / 8);
+            *reinterpret_cast<uint4*>(sv + (c >> 3) * L::kHalfBytes + swz(r, c & 7)) =
+                make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
         }
@@ -227,10 +309,10 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // lanes 0-7: tokens 0-7 @ d 16kk; 8-15: tokens 0-7 @ d+8; 16-23: tokens 8-15 @ d; 24-31: tokens 8-15 @ d+8
-          const int r = (lane & 7) + ((lane >> 4) << 3);
-          const int c = kk * 16 + ((lane >> 3) & 1) * 8;
+          const int r = r0 + (lane & 7) + ((lane >> 4) << 3);
+          const int c = kk * 2 + ((lane >> 3) & 1);  // 16-byte chunk index over the row
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(smem_u32(sk + r * L::kRowBytes + c * 2), b0, b1, b2, b3);
+          ldsm_x4(smem_u32(sk + (c >> 3) * L::kHalfBytes + swz(r, c & 7)), b0, b1, b2, b3);
           mma16816(s[0], qa[kk], b0, b1);
           mma16816(s[1], qa[kk], b2, b3);
         }
@@ -244,14 +326,24 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
             if (tok >= vc) s[n][e] = -INFINITY;
             mx[e >> 1] = fmaxf(mx[e >> 1], s[n][e]);
           }
-        float corr[2];
+        bool grow = false;
+        float m_new[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
           mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-          const float m_new = fmaxf(m_r[r], mx[r] * sl2);  // finite: token 0 is valid
-          corr[r] = ex2_approx(m_r[r] - m_new);            // exp2(-inf) = 0 on the first stage
-          m_r[r] = m_new;
+          m_new[r] = fmaxf(m_r[r], mx[r] * sl2);  // finite: token 0 of the warp is valid
+          grow |= m_new[r] - m_r[r] > kRescaleThreshold;  // always true on the first stage
+        }
+        // Keep the stale max unless some row of the warp grew by more than 2^8.
+        const bool rescale = __any_sync(0xffffffffu, grow);
+        float corr[2] = {1.f, 1.f};
+        if (rescale) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            corr[r] = ex2_approx(m_r[r] - m_new[r]);  // exp2(-inf) = 0 on the first stage
+            m_r[r] = m_new[r];
+          }
         }
         float rs[2] = {0.f, 0.f};
         uint32_t pa[4];
@@ -272,24 +364,25 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
           rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 2);
           l_r[r] = l_r[r] * corr[r] + rs[r];
         }
+        if (rescale) {
+#pragma unroll
+          for (int j = 0; j < D / 8; ++j) {
+            acc[j][0] *= corr[0];
+            acc[j][1] *= corr[0];
+            acc[j][2] *= corr[1];
+            acc[j][3] *= corr[1];
+          }
+        }
         // A fragment of P: {row g tok 2q..}, {row g+8 tok 2q..}, {row g tok 8+2q..}, {row g+8 tok 8+2q..}
         const uint32_t pfrag[4] = {pa[0], pa[1], pa[2], pa[3]};
-        // ---- O = corr * O + P V ----
+        // ---- O += P V ----
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
           // lanes 0-7: tok 0-7 @ d 16j; 8-15: tok 8-15 @ 16j; 16-23: tok 0-7 @ 16j+8; 24-31: tok 8-15 @ 16j+8
-          const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
-          const int c = j * 16 + (lane >> 4) * 8;
+          const int r = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int c = j * 2 + (lane >> 4);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(smem_u32(sv + r * L::kRowBytes + c * 2), b0, b1, b2, b3);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float* o = acc[2 * j + h];
-            o[0] *= corr[0];
-            o[1] *= corr[0];
-            o[2] *= corr[1];
-            o[3] *= corr[1];
-          }
+          ldsm_x4_t(smem_u32(sv + (c >> 3) * L::kHalfBytes + swz(r, c & 7)), b0, b1, b2, b3);
           mma16816(acc[2 * j + 0], pfrag, b0, b1);
           mma16816(acc[2 * j + 1], pfrag, b2, b3);
         }
@@ -314,10 +407,8 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) {
       const int col = j * 8 + quad * 2;
-      mo[gid * D + col] = acc[j][0];
-      mo[gid * D + col + 1] = acc[j][1];
-      mo[(gid + 8) * D + col] = acc[j][2];
-      mo[(gid + 8) * D + col + 1] = acc[j][3];
+      *reinterpret_cast<float2*>(&mo[gid * D + col]) = make_float2(acc[j][0], acc[j][1]);
+      *reinterpret_cast<float2*>(&mo[(gid + 8) * D + col]) = make_float2(acc[j][2], acc[j][3]);
     }
     consumer_sync();
     if (!*abort_flag) {
@@ -341,56 +432,86 @@ decode_splitkv_kernel(const DecodeArgs a, uint32_t* err_word, uint64_t timeout_n
 }
 
 // ---------------------------------------------------------------------------
-// Combine: one 128-thread block per (sequence, query head); warps take every
-// 4th split, lanes own 4 consecutive head-dim elements per D/4 lanes.
+// Combine: one 256-thread block per (sequence, query head).  Each warp takes
+// every 8th split (four loads in flight per lane); lanes own 4 consecutive
+// head-dim elements.
 // ---------------------------------------------------------------------------
+constexpr int kCombineWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const CombineArgs a) {
   constexpr int kLanesPerRow = D / 4;               // float4 per lane
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;   // splits handled per warp step
+  constexpr int kStep = kCombineWarps * kRowsPerWarp;
   const int bh = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.num_splits;
   const size_t stride_s = (size_t)a.batch * a.n_q_heads;
-  __shared__ float s_max[4], s_sum[4];
-  __shared__ float4 s_o[4][kRowsPerWarp][kLanesPerRow];
+  __shared__ float s_max[kCombineWarps], s_sum[kCombineWarps];
+  __shared__ float4 s_o[kCombineWarps][kRowsPerWarp][kLanesPerRow];
 
   // 1) max over splits
   float mx = -INFINITY;
-  for (int s = threadIdx.x; s < S; s += 128) mx = fmaxf(mx, a.lse_partial[(size_t)s * stride_s + bh]);
+  for (int s = threadIdx.x; s < S; s += 32 * kCombineWarps)
+    mx = fmaxf(mx, a.lse_partial[(size_t)s * stride_s + bh]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane == 0) s_max[warp] = mx;
   __syncthreads();
-  mx = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
+  mx = s_max[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, s_max[w]);
   float4* out = reinterpret_cast<float4*>(a.o + (size_t)bh * D);
   if (mx == -INFINITY) {  // every split empty
-    for (int i = threadIdx.x; i < D / 4; i += 128) out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = threadIdx.x; i < D / 4; i += blockDim.x) out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (threadIdx.x == 0) a.lse[bh] = -INFINITY;
     return;
   }
-  // 2) weighted sum of partial outputs
+  // 2) weighted sum of partial outputs, four splits in flight per lane
   const int sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  for (int s = warp * kRowsPerWarp + sub; s < S; s += 4 * kRowsPerWarp) {
-    const float w = ex2_approx((a.lse_partial[(size_t)s * stride_s + bh] - mx) * kLog2e);
-    const float4 v = reinterpret_cast<const float4*>(a.o_partial + ((size_t)s * stride_s + bh) * D)[li];
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
-    if (li == 0) wsum += w;
+  int s = warp * kRowsPerWarp + sub;
+  for (; s + 3 * kStep < S; s += 4 * kStep) {
+    float w[4];
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const size_t idx = (size_t)(s + u * kStep) * stride_s + bh;
+      w[u] = a.lse_partial[idx];
+      v[u] = reinterpret_cast<const float4*>(a.o_partial + idx * D)[li];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float e = ex2_approx((w[u] - mx) * kLog2e);
+      acc.x = fmaf(e, v[u].x, acc.x);
+      acc.y = fmaf(e, v[u].y, acc.y);
+      acc.z = fmaf(e, v[u].z, acc.z);
+      acc.w = fmaf(e, v[u].w, acc.w);
+      if (li == 0) wsum += e;
+    }
+  }
+  for (; s < S; s += kStep) {
+    const size_t idx = (size_t)s * stride_s + bh;
+    const float e = ex2_approx((a.lse_partial[idx] - mx) * kLog2e);
+    const float4 v = reinterpret_cast<const float4*>(a.o_partial + idx * D)[li];
+    acc.x = fmaf(e, v.x, acc.x);
+    acc.y = fmaf(e, v.y, acc.y);
+    acc.z = fmaf(e, v.z, acc.z);
+    acc.w = fmaf(e, v.w, acc.w);
+    if (li == 0) wsum += e;
   }
   s_o[warp][sub][li] = acc;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   if (lane == 0) s_sum[warp] = wsum;
   __syncthreads();
-  const float W = s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3];
-  for (int i = threadIdx.x; i < kLanesPerRow; i += 128) {
+  float W = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) W += s_sum[w];
+  for (int i = threadIdx.x; i < kLanesPerRow; i += blockDim.x) {
     float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < 4; ++w)
+    for (int w = 0; w < kCombineWarps; ++w)
       for (int r = 0; r < kRowsPerWarp; ++r) {
         const float4 v = s_o[w][r][i];
         t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
@@ -416,6 +537,43 @@ __global__ void wait_selftest_kernel(uint32_t* err_word, uint64_t timeout_ns) {
   if (threadIdx.x == 0) mbar_arrive(smem_u32(&bar));  // complete the phase before exit
 }
 
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// A (D, n_kv, rows, planes) bf16 cache with boxes of 64 dims x 1 head x box_rows x 1.
+bool make_cache_map(CUtensorMap* m, const void* base, int D, int n_kv, long long rows,
+                    long long planes, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)n_kv, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t row = (cuuint64_t)D * 2;
+  cuuint64_t strides[3] = {row, row * (cuuint64_t)n_kv, row * (cuuint64_t)n_kv * (cuuint64_t)rows};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch_decode_t(const DecodeArgs& a, const LaunchCtx& ctx) {
   using L = DecodeSmem<D>;
@@ -428,8 +586,28 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const LaunchCtx& ctx) {
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
+  DecodeKParams kp;
+  kp.a = a;
+  kp.err_word = ctx.err_word;
+  kp.timeout_ns = ctx.timeout_ns;
+  CUtensorMap mk, mv;
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  if (a.block_table == nullptr) {
+    kp.mode = kLoadBox64;
+    if (!make_cache_map(&mk, a.k_cache, D, a.n_kv_heads, a.max_kv_len, a.batch, 64) ||
+        !make_cache_map(&mv, a.v_cache, D, a.n_kv_heads, a.max_kv_len, a.batch, 64))
+      return cudaErrorInvalidValue;
+  } else if (a.block_size % 16 == 0) {
+    kp.mode = kLoadBox16;
+    if (!make_cache_map(&mk, a.k_cache, D, a.n_kv_heads, a.block_size, a.num_blocks, 16) ||
+        !make_cache_map(&mv, a.v_cache, D, a.n_kv_heads, a.block_size, a.num_blocks, 16))
+      return cudaErrorInvalidValue;
+  } else {
+    kp.mode = kLoadPlain;
+  }
   dim3 grid(a.num_splits, a.n_kv_heads, a.batch);
-  decode_splitkv_kernel<D><<<grid, kThreads, L::kTotal, ctx.stream>>>(a, ctx.err_word, ctx.timeout_ns);
+  decode_splitkv_kernel<D><<<grid, kThreads, L::kTotal, ctx.stream>>>(mk, mv, kp);
   return cudaGetLastError();
 }
 
@@ -442,9 +620,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const LaunchCtx& ctx) {
 cudaError_t launch_combine(const CombineArgs& a, const LaunchCtx& ctx) {
   const unsigned nbh = (unsigned)a.batch * (unsigned)a.n_q_heads;
   if (a.head_dim == 128)
-    combine_kernel<128><<<nbh, 128, 0, ctx.stream>>>(a);
+    combine_kernel<128><<<nbh, 32 * kCombineWarps, 0, ctx.stream>>>(a);
   else
-    combine_kernel<64><<<nbh, 128, 0, ctx.stream>>>(a);
+    combine_kernel<64><<<nbh, 32 * kCombineWarps, 0, ctx.stream>>>(a);
   return cudaGetLastError();
 }
 

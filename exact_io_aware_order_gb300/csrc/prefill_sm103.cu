@@ -287,9 +287,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int c = 0; c < kBN; ++c)
           if (c > lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // Row max: eight independent chains of 3-input max, then a small tree.
+      float mxa[8];
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+      for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mxa[k] = fmax3(mxa[k], s[c + k], s[c + 8 + k]);
+      const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
+                             fmaxf(mxa[6], mxa[7]));
       const float m_new = fmaxf(m, mx * sl2);
       // Rescale only when some row of the warp gained more than 2^8; otherwise
       // keep the stale max for both l and O (exact either way).
@@ -303,30 +310,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         l *= corr;
         rescale_o = true;
       }
-      const float neg_m = -m;
-      float rs0 = 0.f, rs1 = 0.f;
+      // P = exp2(s * scale * log2e - m): packed FMA for the argument, MUFU ex2,
+      // packed into bf16 pairs for TMEM; the row sum uses four packed chains.
+      const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m, -m);
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, neg_m));
-          const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, neg_m));
-          rs0 += p0;
-          rs1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2v, nmv);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          rs[i & 3] = add2(rs[i & 3], pp);
+          pk[i] = pack_bf16x2(pp.x, pp.y);
         }
         tmem_st16(tSm + c * 16, pk);
       }
-      l += rs0 + rs1;
+      const float2 rsum = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
+      l += rsum.x + rsum.y;
       if (rescale_o) {  // O holds every P V product up to tile j-1 (in-order tensor core)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tOm + c * 32, r);
           tmem_wait_ld();
+          const float2 cv = make_float2(corr, corr);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+          for (int i = 0; i < 16; ++i) {
+            const float2 v = mul2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), cv);
+            r[2 * i] = __float_as_uint(v.x);
+            r[2 * i + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(tOm + c * 32, r);
         }
       }
