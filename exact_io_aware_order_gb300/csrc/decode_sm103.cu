@@ -63,11 +63,15 @@ struct DecodeSmem {
   static constexpr int kBarOff = kQOff + 16 * kQRowBytes;      // 2*kStages barriers
   static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;
   static constexpr int kTotal = kMiscOff + 16 + 1024;          // + alignment slack
-  // Merge scratch reuses the ring once the stream is done.
-  static constexpr int kMergeO = 0;                                  // [warps][16][D] f32
-  static constexpr int kMergeM = kConsumerWarps * 16 * D * 4;        // [warps][16]
-  static constexpr int kMergeL = kMergeM + kConsumerWarps * 16 * 4;  // [warps][16]
-  static_assert(kMergeL + kConsumerWarps * 16 * 4 <= kQOff, "merge scratch fits in the ring");
+  // Merge scratch reuses the ring once the stream is done: per warp 16 rows of
+  // D floats at a padded pitch (64-bit stores from a quad land in distinct
+  // bank pairs), then per warp and row m and l, then per row the warps' weights.
+  static constexpr int kMergePitch = D + 8;                            // floats
+  static constexpr int kMergeO = 0;                                    // [warps][16][pitch]
+  static constexpr int kMergeM = kConsumerWarps * 16 * kMergePitch * 4;  // [warps][16]
+  static constexpr int kMergeL = kMergeM + kConsumerWarps * 16 * 4;      // [warps][16]
+  static constexpr int kMergeF = kMergeL + kConsumerWarps * 16 * 4;      // [warps][16]
+  static_assert(kMergeF + kConsumerWarps * 16 * 4 <= kQOff, "merge scratch fits in the ring");
 };
 
 // Byte offset of (row, 16-byte chunk c) inside one 128-byte-swizzled span.
@@ -394,9 +398,10 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
 
     // ================= merge the consumer warps' states =================
     consumer_sync();  // every warp is done reading the ring
-    float* mo = reinterpret_cast<float*>(smem + L::kMergeO) + (size_t)cw * 16 * D;
+    float* mo = reinterpret_cast<float*>(smem + L::kMergeO);
     float* mm = reinterpret_cast<float*>(smem + L::kMergeM);
     float* ml = reinterpret_cast<float*>(smem + L::kMergeL);
+    float* mf = reinterpret_cast<float*>(smem + L::kMergeF);
     const int gid = lane >> 2;
     if (quad == 0) {
       mm[cw * 16 + gid] = m_r[0];
@@ -404,39 +409,61 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
       ml[cw * 16 + gid] = l_r[0];
       ml[cw * 16 + gid + 8] = l_r[1];
     }
+    float* mow = mo + (size_t)cw * 16 * L::kMergePitch;
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) {
       const int col = j * 8 + quad * 2;
-      *reinterpret_cast<float2*>(&mo[gid * D + col]) = make_float2(acc[j][0], acc[j][1]);
-      *reinterpret_cast<float2*>(&mo[(gid + 8) * D + col]) = make_float2(acc[j][2], acc[j][3]);
+      *reinterpret_cast<float2*>(&mow[gid * L::kMergePitch + col]) = make_float2(acc[j][0], acc[j][1]);
+      *reinterpret_cast<float2*>(&mow[(gid + 8) * L::kMergePitch + col]) =
+          make_float2(acc[j][2], acc[j][3]);
+    }
+    consumer_sync();
+    // Per row: the common max, each warp's weight e^(m_w - m) / l, and the LSE.
+    if (ctid < g && !*abort_flag) {
+      const int r = ctid;
+      float m = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, mm[w * 16 + r]);
+      float f[kConsumerWarps], lsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        f[w] = ex2_approx(mm[w * 16 + r] - m);  // 0 for a warp that saw no token
+        lsum += f[w] * ml[w * 16 + r];
+      }
+      const float inv = 1.f / lsum;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) mf[w * 16 + r] = f[w] * inv;
+      lse_out[r] = (m + __log2f(lsum)) * kLn2;
     }
     consumer_sync();
     if (!*abort_flag) {
-      for (int i = ctid; i < g * D; i += 32 * kConsumerWarps) {
-        const int r = i / D, c = i % D;
-        float m = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, mm[w * 16 + r]);
-        float lsum = 0.f, osum = 0.f;
+      for (int e = ctid; e < g * (D / 4); e += 32 * kConsumerWarps) {
+        const int r = e / (D / 4), c = (e % (D / 4)) * 4;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-          const float f = ex2_approx(mm[w * 16 + r] - m);  // 0 for a warp that saw no token
-          lsum += f * ml[w * 16 + r];
-          osum += f * reinterpret_cast<float*>(smem + L::kMergeO)[((size_t)w * 16 + r) * D + c];
+          const float fw = mf[w * 16 + r];
+          const float4 v = *reinterpret_cast<const float4*>(
+              &mo[((size_t)w * 16 + r) * L::kMergePitch + c]);
+          o.x = fmaf(fw, v.x, o.x);
+          o.y = fmaf(fw, v.y, o.y);
+          o.z = fmaf(fw, v.z, o.z);
+          o.w = fmaf(fw, v.w, o.w);
         }
-        o_out[(size_t)r * D + c] = osum / lsum;
-        if (c == 0) lse_out[r] = (m + __log2f(lsum)) * kLn2;
+        *reinterpret_cast<float4*>(o_out + (size_t)r * D + c) = o;
       }
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Combine: one 256-thread block per (sequence, query head).  Each warp takes
-// every 8th split (four loads in flight per lane); lanes own 4 consecutive
-// head-dim elements.
+// Combine: one 512-thread block per (sequence, query head).  Every thread
+// loads its share of the splits (eight at a time, all in flight together),
+// merges them with a running max, then the block merges the threads'
+// states: one memory round trip for up to 8 * 16 splits.
 // ---------------------------------------------------------------------------
-constexpr int kCombineWarps = 8;
+constexpr int kCombineWarps = 16;
+constexpr int kCombineBatch = 8;
 
 template <int D>
 __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const CombineArgs a) {
@@ -447,13 +474,47 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.num_splits;
   const size_t stride_s = (size_t)a.batch * a.n_q_heads;
+  const int sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
   __shared__ float s_max[kCombineWarps], s_sum[kCombineWarps];
   __shared__ float4 s_o[kCombineWarps][kRowsPerWarp][kLanesPerRow];
 
-  // 1) max over splits
-  float mx = -INFINITY;
-  for (int s = threadIdx.x; s < S; s += 32 * kCombineWarps)
-    mx = fmaxf(mx, a.lse_partial[(size_t)s * stride_s + bh]);
+  float m = -INFINITY, wsum = 0.f;  // running max / weight sum (natural-log domain)
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = warp * kRowsPerWarp + sub; s0 < S; s0 += kCombineBatch * kStep) {
+    float w[kCombineBatch];
+    float4 v[kCombineBatch];
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      const int s = s0 + u * kStep;
+      w[u] = -INFINITY;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s < S) {
+        const size_t idx = (size_t)s * stride_s + bh;
+        w[u] = a.lse_partial[idx];
+        v[u] = reinterpret_cast<const float4*>(a.o_partial + idx * D)[li];
+      }
+    }
+    float mb = m;
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) mb = fmaxf(mb, w[u]);
+    if (mb != -INFINITY) {
+      const float c = ex2_approx((m - mb) * kLog2e);  // 0 while m is -inf
+      acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
+      wsum *= c;
+#pragma unroll
+      for (int u = 0; u < kCombineBatch; ++u) {
+        const float e = ex2_approx((w[u] - mb) * kLog2e);  // 0 for an empty split
+        acc.x = fmaf(e, v[u].x, acc.x);
+        acc.y = fmaf(e, v[u].y, acc.y);
+        acc.z = fmaf(e, v[u].z, acc.z);
+        acc.w = fmaf(e, v[u].w, acc.w);
+        wsum += e;
+      }
+      m = mb;
+    }
+  }
+  // Block merge: the common max, then every thread's state rescaled to it.
+  float mx = m;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane == 0) s_max[warp] = mx;
@@ -467,44 +528,13 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
     if (threadIdx.x == 0) a.lse[bh] = -INFINITY;
     return;
   }
-  // 2) weighted sum of partial outputs, four splits in flight per lane
-  const int sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  int s = warp * kRowsPerWarp + sub;
-  for (; s + 3 * kStep < S; s += 4 * kStep) {
-    float w[4];
-    float4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const size_t idx = (size_t)(s + u * kStep) * stride_s + bh;
-      w[u] = a.lse_partial[idx];
-      v[u] = reinterpret_cast<const float4*>(a.o_partial + idx * D)[li];
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float e = ex2_approx((w[u] - mx) * kLog2e);
-      acc.x = fmaf(e, v[u].x, acc.x);
-      acc.y = fmaf(e, v[u].y, acc.y);
-      acc.z = fmaf(e, v[u].z, acc.z);
-      acc.w = fmaf(e, v[u].w, acc.w);
-      if (li == 0) wsum += e;
-    }
-  }
-  for (; s < S; s += kStep) {
-    const size_t idx = (size_t)s * stride_s + bh;
-    const float e = ex2_approx((a.lse_partial[idx] - mx) * kLog2e);
-    const float4 v = reinterpret_cast<const float4*>(a.o_partial + idx * D)[li];
-    acc.x = fmaf(e, v.x, acc.x);
-    acc.y = fmaf(e, v.y, acc.y);
-    acc.z = fmaf(e, v.z, acc.z);
-    acc.w = fmaf(e, v.w, acc.w);
-    if (li == 0) wsum += e;
-  }
+  const float f = ex2_approx((m - mx) * kLog2e);  // 0 for a thread that saw only empty splits
+  acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+  float ws = li == 0 ? wsum * f : 0.f;  // each split's weight counted once per sub-row
   s_o[warp][sub][li] = acc;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-  if (lane == 0) s_sum[warp] = wsum;
+  for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+  if (lane == 0) s_sum[warp] = ws;
   __syncthreads();
   float W = 0.f;
 #pragma unroll
