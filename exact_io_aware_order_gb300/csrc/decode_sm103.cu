@@ -135,6 +135,11 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
   const int g = a.n_q_heads / a.n_kv_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Inputs may come from the previous kernel on the stream: wait for it before
+  // the first global read; then let the next kernel (the combine) begin its
+  // launch while this grid streams.
+  grid_dep_wait();
+  grid_dep_launch();
   // ---- this split's token range (split rule: see the C header) ----
   const bool paged = a.block_table != nullptr;
   const long long capacity =
@@ -477,6 +482,8 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
   const int sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
   __shared__ float s_max[kCombineWarps], s_sum[kCombineWarps];
   __shared__ float4 s_o[kCombineWarps][kRowsPerWarp][kLanesPerRow];
+  grid_dep_wait();    // the partials come from the decode kernel before us
+  grid_dep_launch();
 
   float m = -INFINITY, wsum = 0.f;  // running max / weight sum (natural-log domain)
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -636,9 +643,17 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const LaunchCtx& ctx) {
   } else {
     kp.mode = kLoadPlain;
   }
-  dim3 grid(a.num_splits, a.n_kv_heads, a.batch);
-  decode_splitkv_kernel<D><<<grid, kThreads, L::kTotal, ctx.stream>>>(mk, mv, kp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_splits, a.n_kv_heads, a.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kTotal;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D>, mk, mv, kp);
 }
 
 }  // namespace
@@ -648,12 +663,18 @@ cudaError_t launch_decode(const DecodeArgs& a, const LaunchCtx& ctx) {
 }
 
 cudaError_t launch_combine(const CombineArgs& a, const LaunchCtx& ctx) {
-  const unsigned nbh = (unsigned)a.batch * (unsigned)a.n_q_heads;
-  if (a.head_dim == 128)
-    combine_kernel<128><<<nbh, 32 * kCombineWarps, 0, ctx.stream>>>(a);
-  else
-    combine_kernel<64><<<nbh, 32 * kCombineWarps, 0, ctx.stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.batch * (unsigned)a.n_q_heads);
+  cfg.blockDim = dim3(32 * kCombineWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, a)
+                           : cudaLaunchKernelEx(&cfg, combine_kernel<64>, a);
 }
 
 cudaError_t launch_wait_selftest(const LaunchCtx& ctx) {

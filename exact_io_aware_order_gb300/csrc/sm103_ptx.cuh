@@ -251,6 +251,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  wait: block until the grids this one
+// depends on have completed and their memory is visible (a no-op when the
+// launch did not allow programmatic overlap).  launch_dependents: allow the
+// next grid on the stream to begin launching once every CTA of this grid has
+// signalled (or exited).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Misc.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {
