@@ -12,23 +12,29 @@
 // strictly above the diagonal are never visited.
 //
 // GB300 design (the pages' A100/H100 kernels are prior art only):
-//   * one CTA owns two 128-row query tiles (Q0, Q1) of one head; K/V tiles are
-//     128 keys; K and V each have a 2-stage shared-memory ring fed by TMA
-//     (128-byte swizzle, 3-D tensor maps so rows past the end read as zero);
-//   * warp 8 is the TMA producer, warp 9 issues tcgen05.mma from one thread;
-//     warps 0-3 / 4-7 run the softmax of Q0 / Q1, one query row per thread
-//     (TMEM lane = row), so row max and row sum need no shuffles;
-//   * TMEM (512 columns): S0 | S1 | O0 | O1.  P is written as bf16 over the
-//     first half of its S columns and fed to the P V product straight from
-//     TMEM (A operand in tensor memory), V from shared memory (MN-major);
-//   * issue order S0(0), S1(0), then per key tile PV0(j), S0(j+1), PV1(j),
-//     S1(j+1): the tensor core computes one tile's products while the other
-//     tile's softmax runs (the overlap idea of FlashAttention-3, rebuilt
-//     around tcgen05's single-thread issue and commit-to-mbarrier);
+//   * one CTA owns one 128-row query tile of one head; key/value tiles are 128
+//     keys, streamed by TMA (128-byte swizzle, 3-D tensor maps so rows past the
+//     end read as zero) into a K ring and a V ring in shared memory;
+//   * TMEM (512 columns): three S buffers (128 columns each) and O.  S is
+//     triple-buffered, so the tensor core computes S(j+1), S(j+2) while the
+//     softmax works on S(j).  P(j) is written as bf16 over the first half of
+//     S(j)'s buffer and feeds O += P V straight from TMEM (A operand in tensor
+//     memory), V from shared memory (MN-major);
+//   * two threads issue tcgen05.mma: warp 9 the S products (S(j) as soon as
+//     K_j is in and PV(j-3) has freed the buffer), warp 10 the P V products
+//     (as soon as P(j) and V_j are ready).  Every wait or commit stalls its
+//     issuing thread for longer than one 128x128x16 MMA runs, so one thread
+//     alone leaves the tensor core idle between groups; with two, one
+//     thread's synchronisation overlaps the other's MMAs.  Warp 8 is the TMA
+//     producer;
+//   * warps 0-3 and 4-7 are two softmax warpgroups on the same 128 rows (TMEM
+//     lane = row), each owning 64 of the 128 key columns: they exchange the
+//     partial row max through shared memory (a bounded mbarrier, not an
+//     unbounded named barrier), so each thread exponentiates 64 scores;
 //   * base-2 exponentials with scale*log2(e) folded in; O is rescaled only
 //     when a row max grows by more than 2^8 (the same stale max is used for
-//     l and O, so the result is exact); the LSE is converted back to natural
-//     log at the end.
+//     l and O, so the result is exact), and only after the previous P V
+//     product has completed; the LSE is converted back to natural log;
 //   * every wait is bounded; on a timeout all roles leave their loops, the
 //     CTA waits for in-flight copies and MMAs, frees TMEM and exits.
 #include <cstdint>
@@ -45,9 +51,12 @@ namespace {
 
 constexpr int kBM = 128;                 // rows per query tile
 constexpr int kBN = 128;                 // keys per key/value tile
-constexpr int kThreads = 320;            // 10 warps
+constexpr int kThreads = 352;            // 11 warps
+constexpr int kSoftmaxThreads = 256;     // warps 0-7
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kSWarp = 9;                // issues S = Q K^T
+constexpr int kPVWarp = 10;              // issues O += P V
+constexpr int kSBuf = 3;                 // S buffers in TMEM
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -57,24 +66,21 @@ template <int D>
 struct PrefillSmem {
   static constexpr int kTileBytes = 128 * D * 2;       // one Q, K or V tile
   static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 64 bf16 (one swizzle span)
-  static constexpr int kQ0 = 0;
-  static constexpr int kQ1 = kTileBytes;
-  static constexpr int kK = 2 * kTileBytes;            // 2 stages
-  static constexpr int kV = 4 * kTileBytes;            // 2 stages
-  static constexpr int kBar = 6 * kTileBytes;
-  // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2],
-  // o_full[2], drain
-  static constexpr int kNumBars = 16;
-  static constexpr int kMisc = kBar + kNumBars * 8;    // tmem base, abort flag
+  static constexpr int kKSlots = D == 128 ? 2 : 4;
+  static constexpr int kVSlots = D == 128 ? 3 : 6;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kTileBytes;
+  static constexpr int kV = kK + kKSlots * kTileBytes;
+  static constexpr int kBar = kV + kVSlots * kTileBytes;
+  // barriers: q_full, k_full/k_empty[K slots], v_full/v_empty[V slots], s_full[3],
+  // p_full[3], pv_done[3], o_full, xmax[2], xsum, drain_s, drain_pv
+  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 3 * kSBuf + 1 + 2 + 1 + 2;
+  static constexpr int kXMax = kBar + kNumBars * 8;            // float [2][2][128]
+  static constexpr int kXSum = kXMax + 2 * 2 * 128 * 4;        // float [2][128]
+  static constexpr int kMisc = kXSum + 2 * 128 * 4;            // tmem base, abort flag
   static constexpr int kUsed = kMisc + 16;
-  // Ask for enough shared memory that two CTAs never share an SM (each
-  // allocates all 512 TMEM columns).
-  static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
-};
-
-enum BarId {
-  kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9, kPFull = 11, kOFull = 13,
-  kDrain = 15
+  static constexpr int kAlloc = kUsed + 1024;                  // + alignment slack
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
 struct PrefillParams {
@@ -83,7 +89,7 @@ struct PrefillParams {
   int batch, n_q_heads, n_kv_heads, seqlen;
   float sl2;  // scale * log2(e)
   int causal;
-  int n_row_blocks;  // ceil(seqlen / 256)
+  int n_q_tiles;  // ceil(seqlen / 128)
   uint32_t* err_word;
   uint64_t timeout_ns;
 };
@@ -93,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = PrefillSmem<D>;
+  constexpr int RK = L::kKSlots, RV = L::kVSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -100,39 +107,48 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   // ---- work item: longest causal rows first; adjacent CTAs share kv heads ----
   const int BH = p.batch * p.n_q_heads;
-  const int rb = p.n_row_blocks - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int qt = p.n_q_tiles - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int bidx = bh / p.n_q_heads, h = bh % p.n_q_heads;
   const int kvh = h / (p.n_q_heads / p.n_kv_heads);
   const int N = p.seqlen;
-  const int n_kv_tiles_all = (N + kBN - 1) / kBN;
-  // Query tile t covers rows [qa + t*128, +128) and visits nt_t key tiles.
-  const int qa = rb * 2 * kBM, qb = qa + kBM;
-  const int nt0 = p.causal ? (qa / kBN + 1) : n_kv_tiles_all;
-  const int nt1 = qb >= N ? 0 : (p.causal ? (qb / kBN + 1) : n_kv_tiles_all);
-  const int J = max(nt0, nt1);
+  const int q0 = qt * kBM;
+  const int n = p.causal ? (qt + 1) : (N + kBN - 1) / kBN;  // key tiles visited (>= 1)
 
+  // Barrier layout.
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const int kQFull = 0, kKFull = 1, kKEmpty = kKFull + RK, kVFull = kKEmpty + RK,
+            kVEmpty = kVFull + RV, kSFull = kVEmpty + RV, kPFull = kSFull + kSBuf,
+            kPVDone = kPFull + kSBuf, kOFull = kPVDone + kSBuf, kXMaxB = kOFull + 1,
+            kXSumB = kXMaxB + 2, kDrainS = kXSumB + 1, kDrainPV = kDrainS + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc + 4);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     mbar_init(bar(kQFull), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < RK; ++i) {
       mbar_init(bar(kKFull + i), 1);
       mbar_init(bar(kKEmpty + i), 1);
+    }
+    for (int i = 0; i < RV; ++i) {
       mbar_init(bar(kVFull + i), 1);
       mbar_init(bar(kVEmpty + i), 1);
-      mbar_init(bar(kSFull + i), 1);
-      mbar_init(bar(kPFull + i), 4 * 32);
-      mbar_init(bar(kOFull + i), 1);
     }
-    mbar_init(bar(kDrain), 1);
+    for (int i = 0; i < kSBuf; ++i) {
+      mbar_init(bar(kSFull + i), 1);
+      mbar_init(bar(kPFull + i), kSoftmaxThreads);
+      mbar_init(bar(kPVDone + i), 1);
+    }
+    mbar_init(bar(kOFull), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(bar(kXMaxB + i), kSoftmaxThreads);
+    mbar_init(bar(kXSumB), kSoftmaxThreads);
+    mbar_init(bar(kDrainS), 1);
+    mbar_init(bar(kDrainPV), 1);
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -145,161 +161,166 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S0 [0,128) | S1 [128,256) | O0 [256,256+D) | O1 [256+D, 256+2D)
-  auto tS = [tmem](int t) { return tmem + (t ? 128u : 0u); };
-  auto tO = [tmem](int t) { return tmem + 256u + (t ? (uint32_t)D : 0u); };
+  // TMEM columns: S buffers [0,128), [128,256), [256,384) | O [384, 384+D)
+  const uint32_t tO = tmem + 384u;
   const WaitCtl ctl{abort_flag, p.err_word, p.timeout_ns};
   const int zq = bidx * p.n_q_heads + h;      // Q / O tensor-map "plane"
   const int zk = bidx * p.n_kv_heads + kvh;   // K / V tensor-map plane
+  const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
+  const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);    // V is MN-major
+  const uint32_t dhi = sw128_desc_hi(1024);
 
   if (warp == kProducerWarp) {
     // ============================ TMA producer ============================
+    // Load order K0, K1, V0, K2, V1, K3, ...: the order the two issuing
+    // threads need the tiles.  K_j's slot is reused once S(j - RK) is done,
+    // V_j's once PV(j - RV) is done.
     if (lane == 0) {
-      const uint32_t qbytes = (nt1 > 0 ? 2u : 1u) * (uint32_t)L::kTileBytes;
-      mbar_arrive_expect_tx(bar(kQFull), qbytes);
+      mbar_arrive_expect_tx(bar(kQFull), (uint32_t)L::kTileBytes);
       for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(smem_u32(smem + L::kQ0 + c * L::kChunkBytes), &tm_q, bar(kQFull), c * 64, qa, zq);
-      if (nt1 > 0)
+        tma_load_3d(smem_u32(smem + L::kQ + c * L::kChunkBytes), &tm_q, bar(kQFull), c * 64, q0, zq);
+      int nk = 0, nv = 0;  // tiles issued
+      auto load = [&](bool is_k, int j) -> bool {
+        const int R = is_k ? RK : RV, slot = j % R;
+        const int full = (is_k ? kKFull : kVFull) + slot, empty = (is_k ? kKEmpty : kVEmpty) + slot;
+        if (j >= R && !mbar_wait(bar(empty), ((j / R) - 1) & 1, ctl)) return false;
+        mbar_arrive_expect_tx(bar(full), (uint32_t)L::kTileBytes);
+        const int base = is_k ? L::kK : L::kV;
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem_u32(smem + L::kQ1 + c * L::kChunkBytes), &tm_q, bar(kQFull), c * 64, qb, zq);
-      int nk = 0, nv = 0;  // K / V tiles issued
-      for (int j = 0; j < J; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(bar(kKEmpty + st), ((j >> 1) - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(bar(kKFull + st), L::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem_u32(smem + L::kK + st * L::kTileBytes + c * L::kChunkBytes), &tm_k,
-                      bar(kKFull + st), c * 64, j * kBN, zk);
-        ++nk;
-        if (j >= 2 && !mbar_wait(bar(kVEmpty + st), ((j >> 1) - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(bar(kVFull + st), L::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem_u32(smem + L::kV + st * L::kTileBytes + c * L::kChunkBytes), &tm_v,
-                      bar(kVFull + st), c * 64, j * kBN, zk);
-        ++nv;
+          tma_load_3d(smem_u32(smem + base + slot * L::kTileBytes + c * L::kChunkBytes),
+                      is_k ? &tm_k : &tm_v, bar(full), c * 64, j * kBN, zk);
+        if (is_k) ++nk; else ++nv;
+        return true;
+      };
+      bool ok = true;
+      for (int j = 0; ok && j < min(n, 2); ++j) ok = load(true, j);
+      for (int j = 0; ok && j < n; ++j) {
+        ok = load(false, j);
+        if (ok && j + 2 < n) ok = load(true, j + 2);
       }
       if (*abort_flag) {
         // Let copies already in flight land before the CTA's memory is released.
         volatile uint32_t no_abort = 0u;
         WaitCtl drain{&no_abort, p.err_word, p.timeout_ns};
         mbar_wait(bar(kQFull), 0, drain);
-        for (int j = max(0, nk - 2); j < nk; ++j) mbar_wait(bar(kKFull + (j & 1)), (j >> 1) & 1, drain);
-        for (int j = max(0, nv - 2); j < nv; ++j) mbar_wait(bar(kVFull + (j & 1)), (j >> 1) & 1, drain);
+        for (int j = max(0, nk - RK); j < nk; ++j) mbar_wait(bar(kKFull + j % RK), (j / RK) & 1, drain);
+        for (int j = max(0, nv - RV); j < nv; ++j) mbar_wait(bar(kVFull + j % RV), (j / RV) & 1, drain);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ============================ MMA issuer ============================
+  } else if (warp == kSWarp) {
+    // ============================ S = Q K^T issuer ============================
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
-      const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);    // V is MN-major
-      const uint32_t sQ0 = smem_u32(smem + L::kQ0), sQ1 = smem_u32(smem + L::kQ1);
-      const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+      const uint32_t q_lo = sw128_desc_lo(smem_u32(smem + L::kQ), 16);
+      const uint32_t k_lo0 = sw128_desc_lo(smem_u32(smem + L::kK), 16);
       bool ok = mbar_wait(bar(kQFull), 0, ctl);
-      tc_fence_after();
-      auto first_user = [&](int j) { return j < nt0 ? 0 : 1; };
-      auto last_user = [&](int j) { return j < nt1 ? 1 : 0; };
-      auto issue_s = [&](int t, int j) -> bool {
-        const int st = j & 1;
-        if (first_user(j) == t) {
-          if (!mbar_wait(bar(kKFull + st), (j >> 1) & 1, ctl)) return false;
-          tc_fence_after();
-        }
+      for (int j = 0; ok && j < n; ++j) {
+        const int b = j % kSBuf, slot = j % RK;
+        // Buffer b last held P(j-3): PV(j-3) must have read it.
+        if (j >= kSBuf && !mbar_wait(bar(kPVDone + b), ((j / kSBuf) - 1) & 1, ctl)) { ok = false; break; }
+        if (!mbar_wait(bar(kKFull + slot), (j / RK) & 1, ctl)) { ok = false; break; }
+        const uint32_t kb = k_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
+        const uint32_t dS = tmem + (uint32_t)(b * 128);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tS(t), smem_desc_sw128((t ? sQ1 : sQ0) + off, 16, 1024),
-                 smem_desc_sw128(sK + st * L::kTileBytes + off, 16, 1024), id_s, kk > 0);
+          const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss_lo(dS, q_lo + off, kb + off, dhi, id_s, kk > 0);
         }
-        mma_commit(bar(kSFull + t));
-        if (last_user(j) == t) mma_commit(bar(kKEmpty + st));
-        return true;
-      };
-      auto issue_pv = [&](int t, int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(bar(kPFull + t), j & 1, ctl)) return false;
-        tc_fence_after();
-        if (first_user(j) == t) {
-          if (!mbar_wait(bar(kVFull + st), (j >> 1) & 1, ctl)) return false;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // B = V tile rows [16kk, 16kk+16): 16 rows x 128 B per k step; the
-          // 64-column halves of the head dimension are one chunk apart.
-          const uint64_t bdesc =
-              smem_desc_sw128(sV + st * L::kTileBytes + kk * 16 * 128, L::kChunkBytes, 1024);
-          mma_ts(tO(t), tS(t) + kk * 8, bdesc, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (last_user(j) == t) mma_commit(bar(kVEmpty + st));
-        if (j == (t ? nt1 : nt0) - 1) mma_commit(bar(kOFull + t));
-        return true;
-      };
-      if (ok) ok = issue_s(0, 0);
-      if (ok && nt1 > 0) ok = issue_s(1, 0);
-      for (int j = 0; ok && j < J; ++j) {
-        if (j < nt0) {
-          ok = issue_pv(0, j);
-          if (ok && j + 1 < nt0) ok = issue_s(0, j + 1);
-        }
-        if (ok && j < nt1) {
-          ok = issue_pv(1, j);
-          if (ok && j + 1 < nt1) ok = issue_s(1, j + 1);
-        }
+        mma_commit(bar(kSFull + b));
+        mma_commit(bar(kKEmpty + slot));
       }
-      // Before TMEM can be freed every issued MMA must have finished (also on
-      // the abort path): one more commit on a barrier of its own, then wait.
-      mma_commit(bar(kDrain));
+      // Before TMEM can be freed every issued MMA must have finished.
+      mma_commit(bar(kDrainS));
       volatile uint32_t no_abort = 0u;
       WaitCtl drain{&no_abort, p.err_word, p.timeout_ns};
-      mbar_wait(bar(kDrain), 0, drain);
+      mbar_wait(bar(kDrainS), 0, drain);
+    }
+    __syncwarp();
+  } else if (warp == kPVWarp) {
+    // ============================ O += P V issuer ============================
+    if (lane == 0) {
+      const uint32_t v_lo0 = sw128_desc_lo(smem_u32(smem + L::kV), L::kChunkBytes);
+      bool ok = true;
+      for (int j = 0; ok && j < n; ++j) {
+        const int b = j % kSBuf, slot = j % RV;
+        if (!mbar_wait(bar(kPFull + b), (j / kSBuf) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();  // P(j) was written to TMEM by the softmax threads
+        if (!mbar_wait(bar(kVFull + slot), (j / RV) & 1, ctl)) { ok = false; break; }
+        // B = V tile rows [16kk, 16kk+16): 16 rows x 128 B per k step; the
+        // 64-column halves of the head dimension are one chunk apart (LBO).
+        const uint32_t vb = v_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
+        const uint32_t aP = tmem + (uint32_t)(b * 128);
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts_lo(tO, aP + kk * 8, vb + ((kk * 16 * 128) >> 4), dhi, id_pv, kk > 0 ? 1u : acc0);
+        mma_commit(bar(kVEmpty + slot));
+        mma_commit(bar(kPVDone + b));
+        if (j == n - 1) mma_commit(bar(kOFull));
+      }
+      mma_commit(bar(kDrainPV));
+      volatile uint32_t no_abort = 0u;
+      WaitCtl drain{&no_abort, p.err_word, p.timeout_ns};
+      mbar_wait(bar(kDrainPV), 0, drain);
     }
     __syncwarp();
   } else {
     // ============================ softmax warps ============================
-    const int t = warp >> 2;                        // query tile of this warpgroup
+    const int wg = warp >> 2;                       // key columns [64 wg, 64 wg + 64)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int row = (warp & 3) * 32 + lane;         // row within the tile (= TMEM lane)
-    const int q0 = t ? qb : qa;
-    const int n_my = t ? nt1 : nt0;
-    const uint32_t tSm = tS(t) + lane_base, tOm = tO(t) + lane_base;
     const int q_row = q0 + row;
     const float sl2 = p.sl2;
-    float m = -INFINITY, l = 0.f;
-    bool ok = n_my > 0;
-    for (int j = 0; ok && j < n_my; ++j) {
-      if (!mbar_wait_warp(bar(kSFull + t), j & 1, ctl)) { ok = false; break; }
+    float* xmax = reinterpret_cast<float*>(smem + L::kXMax);  // [parity][wg][row]
+    float* xsum = reinterpret_cast<float*>(smem + L::kXSum);  // [wg][row]
+    const uint32_t tOm = tO + lane_base + (uint32_t)(wg * (D / 2));  // this group's O columns
+    float m = -INFINITY, l = 0.f;   // running max (log2 domain); this group's partial sum
+    bool ok = true;
+    for (int j = 0; ok && j < n; ++j) {
+      const int b = j % kSBuf;
+      if (!mbar_wait_warp(bar(kSFull + b), (j / kSBuf) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      float s[kBN];
+      const uint32_t tSm = tmem + (uint32_t)(b * 128) + lane_base;
+      // This group's 64 scores of the row: two 32-column loads, one wait.
+      float s[64];
       {
-        uint32_t r[32];
+        uint32_t r[2][32];
+        tmem_ld32(tSm + wg * 64, r[0]);
+        tmem_ld32(tSm + wg * 64 + 32, r[1]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          tmem_ld32(tSm + c * 32, r);
-          tmem_wait_ld();
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-        }
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
       }
-      const int kv0 = j * kBN;
-      if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > N)) {
+      const int kv0 = j * kBN + wg * 64;   // key index of s[0]
+      if (p.causal ? (j * kBN + kBN - 1 > q0) : (j * kBN + kBN > N)) {
         const int lim = p.causal ? (q_row - kv0) : (N - 1 - kv0);  // last allowed column
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c > lim) s[c] = -INFINITY;
       }
-      // Row max: eight independent chains of 3-input max, then a small tree.
+      // Partial row max over 64 scores (eight 3-input-max chains), exchanged
+      // with the other group through shared memory.
       float mxa[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(s[k], s[k + 8]);
 #pragma unroll
-      for (int c = 16; c < kBN; c += 16)
+      for (int c = 16; c < 64; c += 16)
 #pragma unroll
         for (int k = 0; k < 8; ++k) mxa[k] = fmax3(mxa[k], s[c + k], s[c + 8 + k]);
-      const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
+      const float pm = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
                              fmaxf(mxa[6], mxa[7]));
+      const int xb = j & 1;
+      xmax[(xb * 2 + wg) * 128 + row] = pm;
+      tc_fence_before();  // this group's S loads are complete before the other writes P
+      mbar_arrive(bar(kXMaxB + xb));
+      if (!mbar_wait_warp(bar(kXMaxB + xb), (j >> 1) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      const float mx = fmaxf(pm, xmax[(xb * 2 + (wg ^ 1)) * 128 + row]);
       const float m_new = fmaxf(m, mx * sl2);
       // Rescale only when some row of the warp gained more than 2^8; otherwise
-      // keep the stale max for both l and O (exact either way).
+      // keep the stale max for both l and O (exact either way).  Both groups
+      // see the same row maxima, so they take the same decision.
       float corr = 1.f;
       bool rescale_o = false;
       if (j == 0) {
@@ -311,12 +332,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         rescale_o = true;
       }
       // P = exp2(s * scale * log2e - m): packed FMA for the argument, MUFU ex2,
-      // packed into bf16 pairs for TMEM; the row sum uses four packed chains.
+      // packed into bf16 pairs; this group's keys land in P columns
+      // [32 wg, 32 wg + 32) of the buffer (both groups have read their scores).
       const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m, -m);
       float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                       make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -325,13 +347,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           rs[i & 3] = add2(rs[i & 3], pp);
           pk[i] = pack_bf16x2(pp.x, pp.y);
         }
-        tmem_st16(tSm + c * 16, pk);
+        tmem_st16(tSm + wg * 32 + c * 16, pk);
       }
       const float2 rsum = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
       l += rsum.x + rsum.y;
-      if (rescale_o) {  // O holds every P V product up to tile j-1 (in-order tensor core)
+      if (rescale_o) {
+        // O must hold every P V product up to tile j-1 before it is rescaled.
+        const int bp = (j - 1) % kSBuf;
+        if (!mbar_wait_warp(bar(kPVDone + bp), ((j - 1) / kSBuf) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t r[32];
           tmem_ld32(tOm + c * 32, r);
           tmem_wait_ld();
@@ -347,17 +373,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(kPFull + t));
+      mbar_arrive(bar(kPFull + b));
     }
-    // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2 ----
-    if (ok) ok = mbar_wait_warp(bar(kOFull + t), 0, ctl);
+    // ---- epilogue: l = both groups' sums; O = acc / l; LSE = (m + log2 l) ln 2 ----
+    if (ok) {
+      xsum[wg * 128 + row] = l;
+      mbar_arrive(bar(kXSumB));
+      ok = mbar_wait_warp(bar(kXSumB), 0, ctl);
+    }
+    if (ok) ok = mbar_wait_warp(bar(kOFull), 0, ctl);
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float lt = xsum[row] + xsum[128 + row];
+      const float inv_l = 1.f / lt;
       const bool row_ok = q_row < N;
-      float* orow = p.o + ((size_t)zq * N + (size_t)(row_ok ? q_row : 0)) * D;
+      float* orow = p.o + ((size_t)zq * N + (size_t)(row_ok ? q_row : 0)) * D + wg * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t r[32];
         tmem_ld32(tOm + c * 32, r);
         tmem_wait_ld();
@@ -370,14 +402,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
       }
-      if (row_ok) p.lse[(size_t)zq * N + q_row] = (m + __log2f(l)) * kLn2;
+      if (row_ok && wg == 0) p.lse[(size_t)zq * N + q_row] = (m + __log2f(lt)) * kLn2;
     }
   }
 
-  // ---- teardown: every TMEM reader and the MMA drain are done ----
+  // ---- teardown: every TMEM reader and both MMA drains are done ----
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -444,10 +476,10 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   pp.seqlen = a.seqlen;
   pp.sl2 = a.scale * kLog2e;
   pp.causal = a.causal;
-  pp.n_row_blocks = (a.seqlen + 2 * kBM - 1) / (2 * kBM);
+  pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM;
   pp.err_word = ctx.err_word;
   pp.timeout_ns = ctx.timeout_ns;
-  const unsigned grid = (unsigned)pp.n_row_blocks * (unsigned)(a.batch * a.n_q_heads);
+  const unsigned grid = (unsigned)pp.n_q_tiles * (unsigned)(a.batch * a.n_q_heads);
   prefill_kernel<D><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, pp);
   return cudaGetLastError();
 }
