@@ -20,17 +20,17 @@
 //     softmax works on S(j).  P(j) is written as bf16 over the first half of
 //     S(j)'s buffer and feeds O += P V straight from TMEM (A operand in tensor
 //     memory), V from shared memory (MN-major);
-//   * two threads issue tcgen05.mma: warp 9 the S products (S(j) as soon as
-//     K_j is in and PV(j-3) has freed the buffer), warp 10 the P V products
+//   * two threads issue tcgen05.mma: warp 5 the S products (S(j) as soon as
+//     K_j is in and PV(j-3) has freed the buffer), warp 6 the P V products
 //     (as soon as P(j) and V_j are ready).  Every wait or commit stalls its
 //     issuing thread for longer than one 128x128x16 MMA runs, so one thread
 //     alone leaves the tensor core idle between groups; with two, one
-//     thread's synchronisation overlaps the other's MMAs.  Warp 8 is the TMA
+//     thread's synchronisation overlaps the other's MMAs.  Warp 4 is the TMA
 //     producer;
-//   * warps 0-3 and 4-7 are two softmax warpgroups on the same 128 rows (TMEM
-//     lane = row), each owning 64 of the 128 key columns: they exchange the
-//     partial row max through shared memory (a bounded mbarrier, not an
-//     unbounded named barrier), so each thread exponentiates 64 scores;
+//   * warps 0-3 run the softmax, one query row per thread (TMEM lane = row),
+//     so row max and row sum need no shuffles and no cross-warp exchange;
+//     with one softmax warp per scheduler, its ALU work overlaps its own
+//     exponentials on the MUFU pipe;
 //   * base-2 exponentials with scale*log2(e) folded in; O is rescaled only
 //     when a row max grows by more than 2^8 (the same stale max is used for
 //     l and O, so the result is exact), and only after the previous P V
@@ -51,11 +51,11 @@ namespace {
 
 constexpr int kBM = 128;                 // rows per query tile
 constexpr int kBN = 128;                 // keys per key/value tile
-constexpr int kThreads = 352;            // 11 warps
-constexpr int kSoftmaxThreads = 256;     // warps 0-7
-constexpr int kProducerWarp = 8;
-constexpr int kSWarp = 9;                // issues S = Q K^T
-constexpr int kPVWarp = 10;              // issues O += P V
+constexpr int kThreads = 224;            // 7 warps
+constexpr int kSoftmaxThreads = 128;     // warps 0-3: one query row per thread
+constexpr int kProducerWarp = 4;
+constexpr int kSWarp = 5;                // issues S = Q K^T
+constexpr int kPVWarp = 6;               // issues O += P V
 constexpr int kSBuf = 3;                 // S buffers in TMEM
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -73,11 +73,9 @@ struct PrefillSmem {
   static constexpr int kV = kK + kKSlots * kTileBytes;
   static constexpr int kBar = kV + kVSlots * kTileBytes;
   // barriers: q_full, k_full/k_empty[K slots], v_full/v_empty[V slots], s_full[3],
-  // p_full[3], pv_done[3], o_full, xmax[2], xsum, drain_s, drain_pv
-  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 3 * kSBuf + 1 + 2 + 1 + 2;
-  static constexpr int kXMax = kBar + kNumBars * 8;            // float [2][2][128]
-  static constexpr int kXSum = kXMax + 2 * 2 * 128 * 4;        // float [2][128]
-  static constexpr int kMisc = kXSum + 2 * 128 * 4;            // tmem base, abort flag
+  // p_full[3], pv_done[3], o_full, drain_s, drain_pv
+  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 3 * kSBuf + 1 + 2;
+  static constexpr int kMisc = kBar + kNumBars * 8;            // tmem base, abort flag
   static constexpr int kUsed = kMisc + 16;
   static constexpr int kAlloc = kUsed + 1024;                  // + alignment slack
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -120,8 +118,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const int kQFull = 0, kKFull = 1, kKEmpty = kKFull + RK, kVFull = kKEmpty + RK,
             kVEmpty = kVFull + RV, kSFull = kVEmpty + RV, kPFull = kSFull + kSBuf,
-            kPVDone = kPFull + kSBuf, kOFull = kPVDone + kSBuf, kXMaxB = kOFull + 1,
-            kXSumB = kXMaxB + 2, kDrainS = kXSumB + 1, kDrainPV = kDrainS + 1;
+            kPVDone = kPFull + kSBuf, kOFull = kPVDone + kSBuf, kDrainS = kOFull + 1,
+            kDrainPV = kDrainS + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc + 4);
 
@@ -142,8 +140,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(bar(kPVDone + i), 1);
     }
     mbar_init(bar(kOFull), 1);
-    for (int i = 0; i < 2; ++i) mbar_init(bar(kXMaxB + i), kSoftmaxThreads);
-    mbar_init(bar(kXSumB), kSoftmaxThreads);
     mbar_init(bar(kDrainS), 1);
     mbar_init(bar(kDrainPV), 1);
     fence_mbar_init();
@@ -265,62 +261,50 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncwarp();
   } else {
     // ============================ softmax warps ============================
-    const int wg = warp >> 2;                       // key columns [64 wg, 64 wg + 64)
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int row = (warp & 3) * 32 + lane;         // row within the tile (= TMEM lane)
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int row = warp * 32 + lane;               // row within the tile (= TMEM lane)
     const int q_row = q0 + row;
     const float sl2 = p.sl2;
-    float* xmax = reinterpret_cast<float*>(smem + L::kXMax);  // [parity][wg][row]
-    float* xsum = reinterpret_cast<float*>(smem + L::kXSum);  // [wg][row]
-    const uint32_t tOm = tO + lane_base + (uint32_t)(wg * (D / 2));  // this group's O columns
-    float m = -INFINITY, l = 0.f;   // running max (log2 domain); this group's partial sum
+    const uint32_t tOm = tO + lane_base;
+    float m = -INFINITY, l = 0.f;   // running max (log2 domain) and sum of the row
     bool ok = true;
     for (int j = 0; ok && j < n; ++j) {
       const int b = j % kSBuf;
       if (!mbar_wait_warp(bar(kSFull + b), (j / kSBuf) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tSm = tmem + (uint32_t)(b * 128) + lane_base;
-      // This group's 64 scores of the row: two 32-column loads, one wait.
-      float s[64];
+      // The whole S row: four 32-column loads in flight, one wait.
+      float s[kBN];
       {
-        uint32_t r[2][32];
-        tmem_ld32(tSm + wg * 64, r[0]);
-        tmem_ld32(tSm + wg * 64 + 32, r[1]);
+        uint32_t r[kBN / 32][32];
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tSm + c * 32, r[c]);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < kBN / 32; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
       }
-      const int kv0 = j * kBN + wg * 64;   // key index of s[0]
-      if (p.causal ? (j * kBN + kBN - 1 > q0) : (j * kBN + kBN > N)) {
+      const int kv0 = j * kBN;
+      if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > N)) {
         const int lim = p.causal ? (q_row - kv0) : (N - 1 - kv0);  // last allowed column
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kBN; ++c)
           if (c > lim) s[c] = -INFINITY;
       }
-      // Partial row max over 64 scores (eight 3-input-max chains), exchanged
-      // with the other group through shared memory.
+      // Row max: eight independent chains of 3-input max, then a small tree.
       float mxa[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(s[k], s[k + 8]);
 #pragma unroll
-      for (int c = 16; c < 64; c += 16)
+      for (int c = 16; c < kBN; c += 16)
 #pragma unroll
         for (int k = 0; k < 8; ++k) mxa[k] = fmax3(mxa[k], s[c + k], s[c + 8 + k]);
-      const float pm = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
+      const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
                              fmaxf(mxa[6], mxa[7]));
-      const int xb = j & 1;
-      xmax[(xb * 2 + wg) * 128 + row] = pm;
-      tc_fence_before();  // this group's S loads are complete before the other writes P
-      mbar_arrive(bar(kXMaxB + xb));
-      if (!mbar_wait_warp(bar(kXMaxB + xb), (j >> 1) & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      const float mx = fmaxf(pm, xmax[(xb * 2 + (wg ^ 1)) * 128 + row]);
       const float m_new = fmaxf(m, mx * sl2);
       // Rescale only when some row of the warp gained more than 2^8; otherwise
-      // keep the stale max for both l and O (exact either way).  Both groups
-      // see the same row maxima, so they take the same decision.
+      // keep the stale max for both l and O (exact either way).
       float corr = 1.f;
       bool rescale_o = false;
       if (j == 0) {
@@ -332,13 +316,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         rescale_o = true;
       }
       // P = exp2(s * scale * log2e - m): packed FMA for the argument, MUFU ex2,
-      // packed into bf16 pairs; this group's keys land in P columns
-      // [32 wg, 32 wg + 32) of the buffer (both groups have read their scores).
+      // packed into bf16 pairs over the first 64 columns of the buffer; the row
+      // sum uses four packed chains.
       const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m, -m);
       float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                       make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < kBN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -347,7 +331,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           rs[i & 3] = add2(rs[i & 3], pp);
           pk[i] = pack_bf16x2(pp.x, pp.y);
         }
-        tmem_st16(tSm + wg * 32 + c * 16, pk);
+        tmem_st16(tSm + c * 16, pk);
       }
       const float2 rsum = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
       l += rsum.x + rsum.y;
@@ -357,7 +341,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!mbar_wait_warp(bar(kPVDone + bp), ((j - 1) / kSBuf) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tOm + c * 32, r);
           tmem_wait_ld();
@@ -375,21 +359,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tc_fence_before();
       mbar_arrive(bar(kPFull + b));
     }
-    // ---- epilogue: l = both groups' sums; O = acc / l; LSE = (m + log2 l) ln 2 ----
-    if (ok) {
-      xsum[wg * 128 + row] = l;
-      mbar_arrive(bar(kXSumB));
-      ok = mbar_wait_warp(bar(kXSumB), 0, ctl);
-    }
+    // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2 ----
     if (ok) ok = mbar_wait_warp(bar(kOFull), 0, ctl);
     if (ok) {
       tc_fence_after();
-      const float lt = xsum[row] + xsum[128 + row];
-      const float inv_l = 1.f / lt;
+      const float inv_l = 1.f / l;
       const bool row_ok = q_row < N;
-      float* orow = p.o + ((size_t)zq * N + (size_t)(row_ok ? q_row : 0)) * D + wg * (D / 2);
+      float* orow = p.o + ((size_t)zq * N + (size_t)(row_ok ? q_row : 0)) * D;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tOm + c * 32, r);
         tmem_wait_ld();
@@ -402,7 +380,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
       }
-      if (row_ok && wg == 0) p.lse[(size_t)zq * N + q_row] = (m + __log2f(lt)) * kLn2;
+      if (row_ok) p.lse[(size_t)zq * N + q_row] = (m + __log2f(l)) * kLn2;
     }
   }
 
