@@ -38,6 +38,7 @@
 //   * every wait is bounded; on a timeout all roles leave their loops, the
 //     CTA waits for in-flight copies and MMAs, frees TMEM and exits.
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <cuda.h>
@@ -51,11 +52,13 @@ namespace {
 
 constexpr int kBM = 128;                 // rows per query tile
 constexpr int kBN = 128;                 // keys per key/value tile
-constexpr int kThreads = 224;            // 7 warps
+constexpr int kThreads = 352;            // 11 warps
 constexpr int kSoftmaxThreads = 128;     // warps 0-3: one query row per thread
 constexpr int kProducerWarp = 4;
 constexpr int kSWarp = 5;                // issues S = Q K^T
 constexpr int kPVWarp = 6;               // issues O += P V
+constexpr int kEpiWarp0 = 7;             // warps 7-10: O / LSE epilogue
+constexpr int kEpiThreads = 128;
 constexpr int kSBuf = 3;                 // S buffers in TMEM
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -66,16 +69,20 @@ template <int D>
 struct PrefillSmem {
   static constexpr int kTileBytes = 128 * D * 2;       // one Q, K or V tile
   static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 64 bf16 (one swizzle span)
+  static constexpr int kQSlots = 2;
   static constexpr int kKSlots = D == 128 ? 2 : 4;
-  static constexpr int kVSlots = D == 128 ? 3 : 6;
+  static constexpr int kVSlots = D == 128 ? 2 : 6;
   static constexpr int kQ = 0;
-  static constexpr int kK = kTileBytes;
+  static constexpr int kK = kQ + kQSlots * kTileBytes;
   static constexpr int kV = kK + kKSlots * kTileBytes;
   static constexpr int kBar = kV + kVSlots * kTileBytes;
-  // barriers: q_full, k_full/k_empty[K slots], v_full/v_empty[V slots], s_full[3],
-  // p_full[3], pv_done[3], o_full, drain_s, drain_pv
-  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 3 * kSBuf + 1 + 2;
-  static constexpr int kMisc = kBar + kNumBars * 8;            // tmem base, abort flag
+  // barriers: q_full/q_empty, k_full/k_empty, v_full/v_empty (one pair per
+  // slot), s_full/p_full/pv_done [3], o_full, o_empty, stats_full/stats_empty [2],
+  // drain_s, drain_pv
+  static constexpr int kNumBars =
+      2 * kQSlots + 2 * kKSlots + 2 * kVSlots + 3 * kSBuf + 2 + 4 + 2;
+  static constexpr int kStats = kBar + kNumBars * 8;           // float2 (m, l) [2][128]
+  static constexpr int kMisc = kStats + 2 * 128 * 8;           // tmem base, abort flag
   static constexpr int kUsed = kMisc + 16;
   static constexpr int kAlloc = kUsed + 1024;                  // + alignment slack
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -87,45 +94,76 @@ struct PrefillParams {
   int batch, n_q_heads, n_kv_heads, seqlen;
   float sl2;  // scale * log2(e)
   int causal;
-  int n_q_tiles;  // ceil(seqlen / 128)
+  int n_q_tiles;    // ceil(seqlen / 128)
+  int total_tiles;  // n_q_tiles * batch * n_q_heads
   uint32_t* err_word;
   uint64_t timeout_ns;
 };
+
+// One query tile of one (sequence, head).
+struct Tile {
+  int q0;  // first query row
+  int zq;  // Q / O tensor-map plane (sequence * n_q_heads + head)
+  int zk;  // K / V tensor-map plane
+  int n;   // key tiles visited (>= 1)
+};
+
+// Work list, longest causal rows first: item w is query tile
+// n_q_tiles - 1 - w / (batch * n_q_heads) of (sequence, head) w % (batch * n_q_heads),
+// so consecutive items share kv heads while their K/V tiles are hot in L2.
+__device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p) {
+  const int BH = p.batch * p.n_q_heads;
+  const int qt = p.n_q_tiles - 1 - w / BH;
+  const int bh = w % BH;
+  const int bidx = bh / p.n_q_heads, h = bh % p.n_q_heads;
+  const int kvh = h / (p.n_q_heads / p.n_kv_heads);
+  Tile t;
+  t.q0 = qt * kBM;
+  t.zq = bidx * p.n_q_heads + h;
+  t.zk = bidx * p.n_kv_heads + kvh;
+  t.n = p.causal ? (qt + 1) : (p.seqlen + kBN - 1) / kBN;
+  return t;
+}
+
+// The r-th item of this CTA, or -1: rounds of gridDim.x items, taken in
+// alternating (snake) order so that, over two rounds, every CTA gets about
+// the same number of key tiles.
+__device__ __forceinline__ int item_of(int r, int total) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int w = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return w < total ? w : -1;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = PrefillSmem<D>;
-  constexpr int RK = L::kKSlots, RV = L::kVSlots;
+  constexpr int RQ = L::kQSlots, RK = L::kKSlots, RV = L::kVSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- work item: longest causal rows first; adjacent CTAs share kv heads ----
-  const int BH = p.batch * p.n_q_heads;
-  const int qt = p.n_q_tiles - 1 - static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int bidx = bh / p.n_q_heads, h = bh % p.n_q_heads;
-  const int kvh = h / (p.n_q_heads / p.n_kv_heads);
   const int N = p.seqlen;
-  const int q0 = qt * kBM;
-  const int n = p.causal ? (qt + 1) : (N + kBN - 1) / kBN;  // key tiles visited (>= 1)
 
   // Barrier layout.
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const int kQFull = 0, kKFull = 1, kKEmpty = kKFull + RK, kVFull = kKEmpty + RK,
-            kVEmpty = kVFull + RV, kSFull = kVEmpty + RV, kPFull = kSFull + kSBuf,
-            kPVDone = kPFull + kSBuf, kOFull = kPVDone + kSBuf, kDrainS = kOFull + 1,
-            kDrainPV = kDrainS + 1;
+  const int kQFull = 0, kQEmpty = kQFull + RQ, kKFull = kQEmpty + RQ, kKEmpty = kKFull + RK,
+            kVFull = kKEmpty + RK, kVEmpty = kVFull + RV, kSFull = kVEmpty + RV,
+            kPFull = kSFull + kSBuf, kPVDone = kPFull + kSBuf, kOFull = kPVDone + kSBuf,
+            kOEmpty = kOFull + 1, kStFull = kOEmpty + 1, kStEmpty = kStFull + 2,
+            kDrainS = kStEmpty + 2, kDrainPV = kDrainS + 1;
+  float2* stats = reinterpret_cast<float2*>(smem + L::kStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc + 4);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
-    mbar_init(bar(kQFull), 1);
+    for (int i = 0; i < RQ; ++i) {
+      mbar_init(bar(kQFull + i), 1);
+      mbar_init(bar(kQEmpty + i), 1);
+    }
     for (int i = 0; i < RK; ++i) {
       mbar_init(bar(kKFull + i), 1);
       mbar_init(bar(kKEmpty + i), 1);
@@ -140,6 +178,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(bar(kPVDone + i), 1);
     }
     mbar_init(bar(kOFull), 1);
+    mbar_init(bar(kOEmpty), kEpiThreads);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kStFull + i), kSoftmaxThreads);
+      mbar_init(bar(kStEmpty + i), kEpiThreads);
+    }
     mbar_init(bar(kDrainS), 1);
     mbar_init(bar(kDrainPV), 1);
     fence_mbar_init();
@@ -160,69 +203,112 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   // TMEM columns: S buffers [0,128), [128,256), [256,384) | O [384, 384+D)
   const uint32_t tO = tmem + 384u;
   const WaitCtl ctl{abort_flag, p.err_word, p.timeout_ns};
-  const int zq = bidx * p.n_q_heads + h;      // Q / O tensor-map "plane"
-  const int zk = bidx * p.n_kv_heads + kvh;   // K / V tensor-map plane
+  const int total = p.total_tiles;
+
+  // Every role walks the same sequence: the CTA's items r = 0, 1, ... and,
+  // within item r, key tiles j = 0 .. n-1.  Ring slots and barrier phases
+  // follow the running count over all items (g for key tiles), so the
+  // pipeline does not drain between items.
   const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
   const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);    // V is MN-major
   const uint32_t dhi = sw128_desc_hi(1024);
 
   if (warp == kProducerWarp) {
     // ============================ TMA producer ============================
-    // Load order K0, K1, V0, K2, V1, K3, ...: the order the two issuing
-    // threads need the tiles.  K_j's slot is reused once S(j - RK) is done,
-    // V_j's once PV(j - RV) is done.
+    // Two cursors over the flattened (item, key tile) sequence: K runs two
+    // key tiles ahead of V, and Q of an item is loaded just before its first
+    // K, so the tiles arrive in the order the issuing threads consume them,
+    // across item boundaries too.  A slot is reused once the MMAs that read
+    // its previous tile have completed.
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(kQFull), (uint32_t)L::kTileBytes);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(smem_u32(smem + L::kQ + c * L::kChunkBytes), &tm_q, bar(kQFull), c * 64, q0, zq);
-      int nk = 0, nv = 0;  // tiles issued
-      auto load = [&](bool is_k, int j) -> bool {
-        const int R = is_k ? RK : RV, slot = j % R;
-        const int full = (is_k ? kKFull : kVFull) + slot, empty = (is_k ? kKEmpty : kVEmpty) + slot;
-        if (j >= R && !mbar_wait(bar(empty), ((j / R) - 1) & 1, ctl)) return false;
-        mbar_arrive_expect_tx(bar(full), (uint32_t)L::kTileBytes);
-        const int base = is_k ? L::kK : L::kV;
+      struct Cursor {
+        int r, j, w;
+        Tile t;
+      };
+      auto start = [&](Cursor& c) {
+        c.r = 0;
+        c.j = 0;
+        c.w = item_of(0, total);
+        if (c.w >= 0) c.t = tile_of(c.w, p);
+      };
+      auto advance = [&](Cursor& c) {
+        if (++c.j == c.t.n) {
+          c.j = 0;
+          c.w = item_of(++c.r, total);
+          if (c.w >= 0) c.t = tile_of(c.w, p);
+        }
+      };
+      int nq = 0, nk = 0, nv = 0;  // tiles issued
+      auto load_tile = [&](const CUtensorMap* map, int base, int full, int empty, int R, int cnt,
+                           int y, int z) -> bool {
+        const int slot = cnt % R;
+        if (cnt >= R && !mbar_wait(bar(empty + slot), ((cnt / R) - 1) & 1, ctl)) return false;
+        mbar_arrive_expect_tx(bar(full + slot), (uint32_t)L::kTileBytes);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem_u32(smem + base + slot * L::kTileBytes + c * L::kChunkBytes),
-                      is_k ? &tm_k : &tm_v, bar(full), c * 64, j * kBN, zk);
-        if (is_k) ++nk; else ++nv;
+          tma_load_3d(smem_u32(smem + base + slot * L::kTileBytes + c * L::kChunkBytes), map,
+                      bar(full + slot), c * 64, y, z);
         return true;
       };
-      bool ok = true;
-      for (int j = 0; ok && j < min(n, 2); ++j) ok = load(true, j);
-      for (int j = 0; ok && j < n; ++j) {
-        ok = load(false, j);
-        if (ok && j + 2 < n) ok = load(true, j + 2);
+      Cursor kc, vc;
+      start(kc);
+      start(vc);
+      auto load_k = [&]() -> bool {
+        if (kc.w < 0) return true;
+        if (kc.j == 0) {
+          if (!load_tile(&tm_q, L::kQ, kQFull, kQEmpty, RQ, nq, kc.t.q0, kc.t.zq)) return false;
+          ++nq;
+        }
+        if (!load_tile(&tm_k, L::kK, kKFull, kKEmpty, RK, nk, kc.j * kBN, kc.t.zk)) return false;
+        ++nk;
+        advance(kc);
+        return true;
+      };
+      bool ok = load_k() && load_k();
+      while (ok && vc.w >= 0) {
+        ok = load_tile(&tm_v, L::kV, kVFull, kVEmpty, RV, nv, vc.j * kBN, vc.t.zk);
+        if (!ok) break;
+        ++nv;
+        advance(vc);
+        ok = load_k();
       }
       if (*abort_flag) {
         // Let copies already in flight land before the CTA's memory is released.
         volatile uint32_t no_abort = 0u;
         WaitCtl drain{&no_abort, p.err_word, p.timeout_ns};
-        mbar_wait(bar(kQFull), 0, drain);
-        for (int j = max(0, nk - RK); j < nk; ++j) mbar_wait(bar(kKFull + j % RK), (j / RK) & 1, drain);
-        for (int j = max(0, nv - RV); j < nv; ++j) mbar_wait(bar(kVFull + j % RV), (j / RV) & 1, drain);
+        for (int i = max(0, nq - RQ); i < nq; ++i) mbar_wait(bar(kQFull + i % RQ), (i / RQ) & 1, drain);
+        for (int i = max(0, nk - RK); i < nk; ++i) mbar_wait(bar(kKFull + i % RK), (i / RK) & 1, drain);
+        for (int i = max(0, nv - RV); i < nv; ++i) mbar_wait(bar(kVFull + i % RV), (i / RV) & 1, drain);
       }
     }
   } else if (warp == kSWarp) {
     // ============================ S = Q K^T issuer ============================
     if (lane == 0) {
-      const uint32_t q_lo = sw128_desc_lo(smem_u32(smem + L::kQ), 16);
       const uint32_t k_lo0 = sw128_desc_lo(smem_u32(smem + L::kK), 16);
-      bool ok = mbar_wait(bar(kQFull), 0, ctl);
-      for (int j = 0; ok && j < n; ++j) {
-        const int b = j % kSBuf, slot = j % RK;
-        // Buffer b last held P(j-3): PV(j-3) must have read it.
-        if (j >= kSBuf && !mbar_wait(bar(kPVDone + b), ((j / kSBuf) - 1) & 1, ctl)) { ok = false; break; }
-        if (!mbar_wait(bar(kKFull + slot), (j / RK) & 1, ctl)) { ok = false; break; }
-        const uint32_t kb = k_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
-        const uint32_t dS = tmem + (uint32_t)(b * 128);
+      bool ok = true;
+      int g = 0;
+      for (int r = 0; ok; ++r) {
+        const int w = item_of(r, total);
+        if (w < 0) break;
+        const Tile t = tile_of(w, p);
+        const int qs = r % RQ;
+        if (!mbar_wait(bar(kQFull + qs), (r / RQ) & 1, ctl)) { ok = false; break; }
+        const uint32_t q_lo = sw128_desc_lo(smem_u32(smem + L::kQ + qs * L::kTileBytes), 16);
+        for (int j = 0; j < t.n; ++j, ++g) {
+          const int b = g % kSBuf, slot = g % RK;
+          // Buffer b last held P(g-3): PV(g-3) must have read it.
+          if (g >= kSBuf && !mbar_wait(bar(kPVDone + b), ((g / kSBuf) - 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(bar(kKFull + slot), (g / RK) & 1, ctl)) { ok = false; break; }
+          const uint32_t kb = k_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
+          const uint32_t dS = tmem + (uint32_t)(b * 128);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lo(dS, q_lo + off, kb + off, dhi, id_s, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+            mma_ss_lo(dS, q_lo + off, kb + off, dhi, id_s, kk > 0);
+          }
+          mma_commit(bar(kSFull + b));
+          mma_commit(bar(kKEmpty + slot));
         }
-        mma_commit(bar(kSFull + b));
-        mma_commit(bar(kKEmpty + slot));
+        if (ok) mma_commit(bar(kQEmpty + qs));  // every S product of this item has read Q
       }
       // Before TMEM can be freed every issued MMA must have finished.
       mma_commit(bar(kDrainS));
@@ -236,22 +322,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (lane == 0) {
       const uint32_t v_lo0 = sw128_desc_lo(smem_u32(smem + L::kV), L::kChunkBytes);
       bool ok = true;
-      for (int j = 0; ok && j < n; ++j) {
-        const int b = j % kSBuf, slot = j % RV;
-        if (!mbar_wait(bar(kPFull + b), (j / kSBuf) & 1, ctl)) { ok = false; break; }
-        tc_fence_after();  // P(j) was written to TMEM by the softmax threads
-        if (!mbar_wait(bar(kVFull + slot), (j / RV) & 1, ctl)) { ok = false; break; }
-        // B = V tile rows [16kk, 16kk+16): 16 rows x 128 B per k step; the
-        // 64-column halves of the head dimension are one chunk apart (LBO).
-        const uint32_t vb = v_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
-        const uint32_t aP = tmem + (uint32_t)(b * 128);
-        const uint32_t acc0 = j > 0 ? 1u : 0u;
+      int g = 0;
+      for (int r = 0; ok; ++r) {
+        const int w = item_of(r, total);
+        if (w < 0) break;
+        const int n = tile_of(w, p).n;
+        for (int j = 0; j < n; ++j, ++g) {
+          const int b = g % kSBuf, slot = g % RV;
+          if (!mbar_wait(bar(kPFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
+          // The first product of an item overwrites O: the epilogue must have
+          // read the previous item's O out of TMEM.
+          if (j == 0 && r > 0 && !mbar_wait(bar(kOEmpty), (r - 1) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();  // P(g) was written to TMEM by the softmax threads
+          if (!mbar_wait(bar(kVFull + slot), (g / RV) & 1, ctl)) { ok = false; break; }
+          // B = V tile rows [16kk, 16kk+16): 16 rows x 128 B per k step; the
+          // 64-column halves of the head dimension are one chunk apart (LBO).
+          const uint32_t vb = v_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
+          const uint32_t aP = tmem + (uint32_t)(b * 128);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_lo(tO, aP + kk * 8, vb + ((kk * 16 * 128) >> 4), dhi, id_pv, kk > 0 ? 1u : acc0);
-        mma_commit(bar(kVEmpty + slot));
-        mma_commit(bar(kPVDone + b));
-        if (j == n - 1) mma_commit(bar(kOFull));
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts_lo(tO, aP + kk * 8, vb + ((kk * 16 * 128) >> 4), dhi, id_pv, kk > 0 ? 1u : acc0);
+          mma_commit(bar(kVEmpty + slot));
+          mma_commit(bar(kPVDone + b));
+          if (j == n - 1) mma_commit(bar(kOFull));
+        }
       }
       mma_commit(bar(kDrainPV));
       volatile uint32_t no_abort = 0u;
@@ -259,128 +354,156 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_wait(bar(kDrainPV), 0, drain);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kProducerWarp) {
     // ============================ softmax warps ============================
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int row = warp * 32 + lane;               // row within the tile (= TMEM lane)
-    const int q_row = q0 + row;
     const float sl2 = p.sl2;
     const uint32_t tOm = tO + lane_base;
-    float m = -INFINITY, l = 0.f;   // running max (log2 domain) and sum of the row
     bool ok = true;
-    for (int j = 0; ok && j < n; ++j) {
-      const int b = j % kSBuf;
-      if (!mbar_wait_warp(bar(kSFull + b), (j / kSBuf) & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t tSm = tmem + (uint32_t)(b * 128) + lane_base;
-      // The whole S row: four 32-column loads in flight, one wait.
-      float s[kBN];
-      {
-        uint32_t r[kBN / 32][32];
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tSm + c * 32, r[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
-      }
-      const int kv0 = j * kBN;
-      if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > N)) {
-        const int lim = p.causal ? (q_row - kv0) : (N - 1 - kv0);  // last allowed column
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c > lim) s[c] = -INFINITY;
-      }
-      // Row max: eight independent chains of 3-input max, then a small tree.
-      float mxa[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(s[k], s[k + 8]);
-#pragma unroll
-      for (int c = 16; c < kBN; c += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mxa[k] = fmax3(mxa[k], s[c + k], s[c + 8 + k]);
-      const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
-                             fmaxf(mxa[6], mxa[7]));
-      const float m_new = fmaxf(m, mx * sl2);
-      // Rescale only when some row of the warp gained more than 2^8; otherwise
-      // keep the stale max for both l and O (exact either way).
-      float corr = 1.f;
-      bool rescale_o = false;
-      if (j == 0) {
-        m = m_new;  // O is written fresh by the first P V product
-      } else if (__any_sync(0xffffffffu, m_new - m > kRescaleThreshold)) {
-        corr = ex2_approx(m - m_new);
-        m = m_new;
-        l *= corr;
-        rescale_o = true;
-      }
-      // P = exp2(s * scale * log2e - m): packed FMA for the argument, MUFU ex2,
-      // packed into bf16 pairs over the first 64 columns of the buffer; the row
-      // sum uses four packed chains.
-      const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m, -m);
-      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2v, nmv);
-          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          rs[i & 3] = add2(rs[i & 3], pp);
-          pk[i] = pack_bf16x2(pp.x, pp.y);
-        }
-        tmem_st16(tSm + c * 16, pk);
-      }
-      const float2 rsum = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
-      l += rsum.x + rsum.y;
-      if (rescale_o) {
-        // O must hold every P V product up to tile j-1 before it is rescaled.
-        const int bp = (j - 1) % kSBuf;
-        if (!mbar_wait_warp(bar(kPVDone + bp), ((j - 1) / kSBuf) & 1, ctl)) { ok = false; break; }
+    int g = 0;
+    for (int r = 0; ok; ++r) {
+      const int w = item_of(r, total);
+      if (w < 0) break;
+      const Tile t = tile_of(w, p);
+      const int q0 = t.q0, q_row = q0 + row;
+      float m = -INFINITY, l = 0.f;   // running max (log2 domain) and sum of the row
+      for (int j = 0; j < t.n; ++j, ++g) {
+        const int b = g % kSBuf;
+        if (!mbar_wait_warp(bar(kSFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t tSm = tmem + (uint32_t)(b * 128) + lane_base;
+        // The whole S row: four 32-column loads in flight, one wait.
+        float s[kBN];
+        {
+          uint32_t rr[kBN / 32][32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tOm + c * 32, r);
+          for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tSm + c * 32, rr[c]);
           tmem_wait_ld();
-          const float2 cv = make_float2(corr, corr);
+#pragma unroll
+          for (int c = 0; c < kBN / 32; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[c][i]);
+        }
+        const int kv0 = j * kBN;
+        if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > N)) {
+          const int lim = p.causal ? (q_row - kv0) : (N - 1 - kv0);  // last allowed column
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c > lim) s[c] = -INFINITY;
+        }
+        // Row max: eight independent chains of 3-input max, then a small tree.
+        float mxa[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+        for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mxa[k] = fmax3(mxa[k], s[c + k], s[c + 8 + k]);
+        const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
+                               fmaxf(mxa[6], mxa[7]));
+        const float m_new = fmaxf(m, mx * sl2);
+        // Rescale only when some row of the warp gained more than 2^8; otherwise
+        // keep the stale max for both l and O (exact either way).
+        float corr = 1.f;
+        bool rescale_o = false;
+        if (j == 0) {
+          m = m_new;  // O is written fresh by the item's first P V product
+        } else if (__any_sync(0xffffffffu, m_new - m > kRescaleThreshold)) {
+          corr = ex2_approx(m - m_new);
+          m = m_new;
+          l *= corr;
+          rescale_o = true;
+        }
+        // P = exp2(s * scale * log2e - m): packed FMA for the argument, MUFU ex2,
+        // packed into bf16 pairs over the first 64 columns of the buffer; the row
+        // sum uses four packed chains.
+        const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m, -m);
+        float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float2 v = mul2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), cv);
-            r[2 * i] = __float_as_uint(v.x);
-            r[2 * i + 1] = __float_as_uint(v.y);
+            const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2v, nmv);
+            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            rs[i & 3] = add2(rs[i & 3], pp);
+            pk[i] = pack_bf16x2(pp.x, pp.y);
           }
-          tmem_st32(tOm + c * 32, r);
+          tmem_st16(tSm + c * 16, pk);
         }
+        const float2 rsum = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
+        l += rsum.x + rsum.y;
+        if (rescale_o) {
+          // O must hold every P V product up to key tile j-1 before it is rescaled.
+          const int bp = (g - 1) % kSBuf;
+          if (!mbar_wait_warp(bar(kPVDone + bp), ((g - 1) / kSBuf) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(tOm + c * 32, rr);
+            tmem_wait_ld();
+            const float2 cv = make_float2(corr, corr);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 v =
+                  mul2(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), cv);
+              rr[2 * i] = __float_as_uint(v.x);
+              rr[2 * i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tOm + c * 32, rr);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kPFull + b));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kPFull + b));
+      if (!ok) break;
+      // Row statistics to the epilogue warps (two slots, alternating items).
+      const int ss = r & 1;
+      if (r >= 2 && !mbar_wait_warp(bar(kStEmpty + ss), ((r >> 1) - 1) & 1, ctl)) { ok = false; break; }
+      stats[ss * 128 + row] = make_float2(m, l);
+      mbar_arrive(bar(kStFull + ss));
     }
-    // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2 ----
-    if (ok) ok = mbar_wait_warp(bar(kOFull), 0, ctl);
-    if (ok) {
+  } else if (warp >= kEpiWarp0) {
+    // ======================= epilogue: O = acc / l, LSE =======================
+    // Warp w may access TMEM lanes [32 (w % 4), 32 (w % 4) + 32).
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t tOm = tO + ((uint32_t)(quarter * 32) << 16);
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int w = item_of(r, total);
+      if (w < 0) break;
+      const Tile t = tile_of(w, p);
+      if (!mbar_wait_warp(bar(kOFull), r & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      const float inv_l = 1.f / l;
-      const bool row_ok = q_row < N;
-      float* orow = p.o + ((size_t)zq * N + (size_t)(row_ok ? q_row : 0)) * D;
+      uint32_t acc[D / 32][32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tOm + c * 32, r);
-        tmem_wait_ld();
-        if (row_ok) {
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tOm + c * 32, acc[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(kOEmpty));  // O may now be overwritten by the next item
+      const int ss = r & 1;
+      if (!mbar_wait_warp(bar(kStFull + ss), (r >> 1) & 1, ctl)) { ok = false; break; }
+      const float2 ml = stats[ss * 128 + row];
+      mbar_arrive(bar(kStEmpty + ss));
+      const int q_row = t.q0 + row;
+      if (q_row < N) {
+        const float inv_l = 1.f / ml.y;
+        float* orow = p.o + ((size_t)t.zq * N + (size_t)q_row) * D;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float4 v = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
-                                   __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
-            reinterpret_cast<float4*>(orow + c * 32)[i] = v;
-          }
-        }
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(orow + c * 32)[i] =
+                make_float4(__uint_as_float(acc[c][4 * i]) * inv_l, __uint_as_float(acc[c][4 * i + 1]) * inv_l,
+                            __uint_as_float(acc[c][4 * i + 2]) * inv_l,
+                            __uint_as_float(acc[c][4 * i + 3]) * inv_l);
+        p.lse[(size_t)t.zq * N + q_row] = (ml.x + __log2f(ml.y)) * kLn2;
       }
-      if (row_ok) p.lse[(size_t)zq * N + q_row] = (m + __log2f(l)) * kLn2;
     }
   }
 
@@ -455,9 +578,12 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   pp.sl2 = a.scale * kLog2e;
   pp.causal = a.causal;
   pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM;
+  pp.total_tiles = pp.n_q_tiles * a.batch * a.n_q_heads;
   pp.err_word = ctx.err_word;
   pp.timeout_ns = ctx.timeout_ns;
-  const unsigned grid = (unsigned)pp.n_q_tiles * (unsigned)(a.batch * a.n_q_heads);
+  // Persistent: one CTA per SM (shared memory and TMEM admit one), each
+  // walking its share of the work list.
+  const unsigned grid = (unsigned)std::min(pp.total_tiles, std::max(ctx.num_sms, 1));
   prefill_kernel<D><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, pp);
   return cudaGetLastError();
 }
