@@ -75,7 +75,8 @@ struct PrefillSmem {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQSlots * kTileBytes;
   static constexpr int kV = kK + kKSlots * kTileBytes;
-  static constexpr int kBar = kV + kVSlots * kTileBytes;
+  static constexpr int kStage = kV + kVSlots * kTileBytes;     // O staging: 4 warps x 32 rows x 128 B
+  static constexpr int kBar = kStage + 4 * 4096;
   // barriers: q_full/q_empty, k_full/k_empty, v_full/v_empty (one pair per
   // slot), s_full/p_full/pv_done [3], o_full, o_empty, stats_full/stats_empty [2],
   // drain_s, drain_pv
@@ -137,7 +138,8 @@ __device__ __forceinline__ int item_of(int r, int total) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const PrefillParams p) {
   using L = PrefillSmem<D>;
   constexpr int RQ = L::kQSlots, RK = L::kKSlots, RV = L::kVSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -195,6 +197,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -470,9 +473,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   } else if (warp >= kEpiWarp0) {
     // ======================= epilogue: O = acc / l, LSE =======================
     // Warp w may access TMEM lanes [32 (w % 4), 32 (w % 4) + 32).
+    // Each warp writes its 32 rows of O through a 4 KB staging box in shared
+    // memory (32 rows x 32 floats, 128-byte swizzle: conflict-free row-wise
+    // writes) and one TMA store per 32 columns, so the global writes are
+    // whole lines and the load/store unit stays free for the softmax warps.
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tOm = tO + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t stage = smem_u32(smem + L::kStage + quarter * 4096);
     bool ok = true;
     for (int r = 0; ok; ++r) {
       const int w = item_of(r, total);
@@ -490,21 +498,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (!mbar_wait_warp(bar(kStFull + ss), (r >> 1) & 1, ctl)) { ok = false; break; }
       const float2 ml = stats[ss * 128 + row];
       mbar_arrive(bar(kStEmpty + ss));
-      const int q_row = t.q0 + row;
-      if (q_row < N) {
-        const float inv_l = 1.f / ml.y;
-        float* orow = p.o + ((size_t)t.zq * N + (size_t)q_row) * D;
+      const float inv_l = 1.f / ml.y;
+      const int row0 = t.q0 + quarter * 32;  // first row of this warp's box
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c)
+      for (int c = 0; c < D / 32; ++c) {
+        if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
+        __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            reinterpret_cast<float4*>(orow + c * 32)[i] =
-                make_float4(__uint_as_float(acc[c][4 * i]) * inv_l, __uint_as_float(acc[c][4 * i + 1]) * inv_l,
-                            __uint_as_float(acc[c][4 * i + 2]) * inv_l,
-                            __uint_as_float(acc[c][4 * i + 3]) * inv_l);
-        p.lse[(size_t)t.zq * N + q_row] = (ml.x + __log2f(ml.y)) * kLn2;
+        for (int i = 0; i < 8; ++i)
+          st_shared_v4(stage + lane * 128 + ((i ^ (lane & 7)) << 4),
+                       make_float4(__uint_as_float(acc[c][4 * i]) * inv_l,
+                                   __uint_as_float(acc[c][4 * i + 1]) * inv_l,
+                                   __uint_as_float(acc[c][4 * i + 2]) * inv_l,
+                                   __uint_as_float(acc[c][4 * i + 3]) * inv_l));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < N) {  // rows past the end are clipped by the copy
+          tma_store_3d(&tm_o, stage, c * 32, row0, t.zq);
+          bulk_commit_group();
+        }
       }
+      const int q_row = t.q0 + row;
+      if (q_row < N) p.lse[(size_t)t.zq * N + q_row] = (ml.x + __log2f(ml.y)) * kLn2;
     }
+    if (lane == 0) bulk_wait_all();  // O is in global memory before the CTA exits
+    __syncwarp();
   }
 
   // ---- teardown: every TMEM reader and both MMA drains are done ----
@@ -551,6 +569,19 @@ bool make_map(CUtensorMap* m, const void* base, int D, int rows, int planes) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 output (planes, rows, D): box = 32 x 32 x 1 (128-byte rows), 128-byte swizzle.
+bool make_out_map(CUtensorMap* m, void* base, int D, int rows, int planes) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * 4 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   using L = PrefillSmem<D>;
@@ -563,10 +594,11 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, a.q, D, a.seqlen, a.batch * a.n_q_heads) ||
       !make_map(&mk, a.k, D, a.seqlen, a.batch * a.n_kv_heads) ||
-      !make_map(&mv, a.v, D, a.seqlen, a.batch * a.n_kv_heads))
+      !make_map(&mv, a.v, D, a.seqlen, a.batch * a.n_kv_heads) ||
+      !make_out_map(&mo, a.o, D, a.seqlen, a.batch * a.n_q_heads))
     return cudaErrorInvalidValue;
   PrefillParams pp;
   pp.o = a.o;
@@ -584,7 +616,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   // Persistent: one CTA per SM (shared memory and TMEM admit one), each
   // walking its share of the work list.
   const unsigned grid = (unsigned)std::min(pp.total_tiles, std::max(ctx.num_sms, 1));
-  prefill_kernel<D><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, pp);
+  prefill_kernel<D><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, mo, pp);
   return cudaGetLastError();
 }
 
