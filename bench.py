@@ -50,6 +50,29 @@ WORKLOADS = {
 }
 
 
+def rank_env() -> tuple:
+    """(rank, world size) from the launcher's environment; (0, 1) without one."""
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def rank_max(dist, vals, device=None) -> list:
+    """Max over ranks of each timed quantity (identity in a single process).
+    Every rank gets the same list back."""
+    if dist is None:
+        return [float(v) for v in vals]
+    import torch
+
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_rate(units_per_step: float, steps: int, world: int, slowest_ms: float) -> float:
+    """Whole-job throughput of replicas: every rank processes units_per_step
+    each step (weak scaling), over the slowest rank's time."""
+    return world * units_per_step * steps / (slowest_ms * 1e-3)
+
+
 def prefill_flops(n_q: int, seqlen: int, d: int, batch: int = 1) -> float:
     return 4.0 * batch * n_q * float(seqlen) ** 2 * d / 2.0
 
@@ -223,19 +246,11 @@ def run_gb300(args, rank: int, world: int, dist):
     pre_total = sum(pre_ms)
     dec_total = sum(dec_ms) + sum(cmb_ms)
 
-    # max over ranks of each timed quantity
-    def rmax(val: float) -> float:
-        if dist is None:
-            return val
-        t = torch.tensor([val], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    total_ms, pre_total, dec_total = rmax(total_ms), rmax(pre_total), rmax(dec_total)
+    total_ms, pre_total, dec_total = rank_max(dist, [total_ms, pre_total, dec_total], dev)
     avg_pre = statistics.mean(pre_ms)
     avg_dec = statistics.mean(dec_ms)
-    prefill_tflops = world * flops * args.steps / (pre_total * 1e-3) / 1e12
-    decode_gbs = world * dec_bytes * args.steps / (dec_total * 1e-3) / 1e9
+    prefill_tflops = job_rate(flops, args.steps, world, pre_total) / 1e12
+    decode_gbs = job_rate(dec_bytes, args.steps, world, dec_total) / 1e9
     achieved = flops / (avg_pre * 1e-3) / 1e12
     dec_achieved = dec_bytes / (avg_dec * 1e-3) / 1e9
     traffic = profiled_traffic() if args.workload == "qwen" else None
@@ -341,13 +356,10 @@ def run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist):
     torch.cuda.synchronize()
     pre = sum(e[0].elapsed_time(e[1]) for e in evs)
     dcd = sum(e[1].elapsed_time(e[2]) for e in evs)
-    if dist is not None:
-        t = torch.tensor([pre, dcd], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        pre, dcd = float(t[0]), float(t[1])
-    return {"value": round(world * flops * n / (pre * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    pre, dcd = rank_max(dist, [pre, dcd], dev)
+    return {"value": round(job_rate(flops, n, world, pre) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "decode_value": round(world * dec_bytes * n / (dcd * 1e-3) / 1e9, 1),
+            "decode_value": round(job_rate(dec_bytes, n, world, dcd) / 1e9, 1),
             "decode_unit": "GB/s (end to end, cache copied from host each step)"}
 
 
@@ -467,8 +479,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    rank, world = rank_env()
     if args.impl == "reference":
         res = run_reference(args, rank, world)
         if res is not None:
