@@ -14,4 +14,6 @@ from .attention_ref import (  # noqa: F401
     decode,
     decode_partials,
     combine,
+    append_token,
+    decode_append,
 )

@@ -33,6 +33,10 @@ reason in the design notes of the repository):
   (batch, max_kv_len, n_kv, d).
 * An empty key set (a zero-length sequence or an empty split) has LSE = -inf
   and O = 0: the plain value of an empty sum.
+* Decode with append (§"Minimal implementation", the decode call against a
+  paged cache): the per-sequence length counts the tokens already cached; the
+  call writes the new token's key and value at that position, attends over
+  length + 1 tokens, and leaves the length to the caller to increment.
 """
 
 from __future__ import annotations
@@ -49,6 +53,8 @@ __all__ = [
     "decode",
     "decode_partials",
     "combine",
+    "append_token",
+    "decode_append",
 ]
 
 _ROW_BLOCK = 256
@@ -277,3 +283,55 @@ def combine(o_parts, lse_parts):
     o = (w[..., None] * o_parts).sum(axis=0)
     o[empty] = 0.0
     return o, lse
+
+
+def _append_position(kv_len: int) -> int:
+    """Where the new token goes: right after the kv_len cached tokens."""
+    return kv_len
+
+
+def append_token(k_cache, v_cache, block_table, kv_lens: Sequence[int], k_new, v_new,
+                 block_size: int = 0):
+    """Writes each sequence's new key and value row into the cache.
+
+    Page §"Minimal implementation": the decode call takes the cache, the
+    block table and the per-sequence count of tokens already cached, and
+    appends the new keys and values in place; the caller then increments the
+    counts.  k_new, v_new: (B, n_kv, d).  Sequence b's new row goes to token
+    position kv_lens[b] (a paged cache maps it through the block table as in
+    :func:`gather_sequence`).  Returns copies of the two caches with the rows
+    written; raises ValueError when a sequence has no free slot.
+    """
+    def _copy(c):
+        return c.clone() if hasattr(c, "clone") else np.array(c, copy=True)
+
+    kc, vc = _copy(k_cache), _copy(v_cache)
+    for b in range(len(kv_lens)):
+        t = _append_position(int(kv_lens[b]))
+        if block_table is None:
+            if not 0 <= t < kc.shape[1]:
+                raise ValueError(f"sequence {b}: no free slot at position {t}")
+            kc[b, t] = k_new[b]
+            vc[b, t] = v_new[b]
+        else:
+            bt = np.asarray(block_table)
+            if not 0 <= t < bt.shape[1] * block_size:
+                raise ValueError(f"sequence {b}: no free slot at position {t}")
+            blk, slot = int(bt[b, t // block_size]), t % block_size
+            kc[blk, slot] = k_new[b]
+            vc[blk, slot] = v_new[b]
+    return kc, vc
+
+
+def decode_append(q, k_new, v_new, k_cache, v_cache, block_table, kv_lens: Sequence[int],
+                  scale: float, block_size: int = 0):
+    """Single-token decode that first appends the token's own key and value
+    (page §"Minimal implementation"): the query of sequence b attends over its
+    kv_lens[b] cached tokens plus the new one.
+
+    Returns (O (B, n_q, d), LSE (B, n_q), k_cache', v_cache'), the caches as
+    :func:`append_token` leaves them.
+    """
+    kc, vc = append_token(k_cache, v_cache, block_table, kv_lens, k_new, v_new, block_size)
+    o, lse = decode(q, kc, vc, block_table, [int(n) + 1 for n in kv_lens], scale, block_size)
+    return o, lse, kc, vc

@@ -263,6 +263,73 @@ def test_empty_sequence_and_empty_split():
 
 
 # ---------------------------------------------------------------------------
+# Decode with append (page §"Minimal implementation": the decode call writes
+# the new token's key and value at position cache_seqlens[b], attends over
+# cache_seqlens[b] + 1 tokens; the caller increments the lengths).
+# ---------------------------------------------------------------------------
+
+def _paged_empty_cache(n_blocks_used, extra, bs, nkv, d, seed):
+    perm = torch.randperm(n_blocks_used + extra, generator=torch.Generator().manual_seed(seed))
+    table = perm[:n_blocks_used].to(torch.int32).reshape(1, -1)
+    kc = torch.full((n_blocks_used + extra, bs, nkv, d), float("nan"), dtype=torch.float64)
+    return table, kc, kc.clone()
+
+
+def _pin_append():
+    """Token-by-token decode with append, starting from an empty cache full
+    of NaN, reproduces every row of causal prefill (an independently pinned
+    definition): paged with a permuted block table, and contiguous."""
+    N, nq, nkv, d, bs = 37, 4, 2, 8, 8
+    x = W.make_prefill(1, nq, nkv, N, d, seed=5)
+    op, lp = oracle.prefill(x.q, x.k, x.v, x.scale, True)
+    table, kc, vc = _paged_empty_cache((N + bs - 1) // bs, 2, bs, nkv, d, seed=3)
+    kk = torch.full((1, N, nkv, d), float("nan"), dtype=torch.float64)
+    vv = kk.clone()
+    err = 0.0
+    for t in range(N):
+        q, kn, vn = x.q[:, :, t], x.k[:, :, t], x.v[:, :, t]
+        o, lse, kc, vc = oracle.decode_append(q, kn, vn, kc, vc, table, [t], x.scale, bs)
+        o2, lse2, kk, vv = oracle.decode_append(q, kn, vn, kk, vv, None, [t], x.scale)
+        for oo, ll in ((o, lse), (o2, lse2)):
+            err = max(err, float(np.abs(oo - op[:, :, t]).max()), float(np.abs(ll - lp[:, :, t]).max()))
+    return err
+
+
+def test_decode_append_reproduces_prefill_rows():
+    assert _pin_append() <= TOL
+
+
+def test_decode_append_closed_form_and_written_slot():
+    """kv_len = 0: the query sees only its own token, so O = v_new of its kv
+    head and LSE = scale * q . k_new.  Exactly one slot per sequence changes."""
+    B, nq, nkv, d, bs = 2, 6, 3, 16, 4
+    g = nq // nkv
+    gen = torch.Generator().manual_seed(9)
+    q = torch.randn(B, nq, d, generator=gen, dtype=torch.float64)
+    kn = torch.randn(B, nkv, d, generator=gen, dtype=torch.float64)
+    vn = torch.randn(B, nkv, d, generator=gen, dtype=torch.float64)
+    table = torch.tensor([[3, 1], [0, 2]], dtype=torch.int32)
+    kc = torch.randn(4, bs, nkv, d, generator=gen, dtype=torch.float64)
+    vc = torch.randn(4, bs, nkv, d, generator=gen, dtype=torch.float64)
+    o, lse, kc2, vc2 = oracle.decode_append(q, kn, vn, kc, vc, table, [0, 5], 0.3, bs)
+    for h in range(nq):
+        assert np.abs(o[0, h] - vn[0, h // g].numpy()).max() <= TOL
+        assert abs(lse[0, h] - 0.3 * float(q[0, h] @ kn[0, h // g])) <= TOL
+    changed = (kc2 != kc).any(dim=(2, 3)) | (vc2 != vc).any(dim=(2, 3))
+    assert changed.sum() == 2 and changed[3, 0] and changed[2, 1]   # seq 0 -> block 3 slot 0,
+    assert torch.equal(kc2[2, 1], kn[1]) and torch.equal(vc2[3, 0], vn[0])  # seq 1 -> pos 5
+    # the caller's caches are not modified
+    assert not torch.equal(kc2, kc)
+
+
+def test_decode_append_full_cache_raises():
+    x = W.make_decode_contiguous(1, 2, 1, 8, 16, seed=1, max_kv_len=16)
+    with pytest.raises(ValueError):
+        oracle.decode_append(x.q, x.k_cache[:, 0], x.v_cache[:, 0], x.k_cache, x.v_cache, None,
+                             [16], x.scale)
+
+
+# ---------------------------------------------------------------------------
 # Chunk-combine identity.
 # ---------------------------------------------------------------------------
 
@@ -372,7 +439,7 @@ def test_toy_run_split_decode(golden):
 def _pins():
     return {"bruteforce": (_pin_bruteforce, TOL), "sdpa": (_pin_sdpa, 1e-12),
             "closed": (_pin_closed_forms, TOL), "gqa": (_pin_gqa, TOL),
-            "combine": (_pin_combine, TOL)}
+            "combine": (_pin_combine, TOL), "append": (_pin_append, TOL)}
 
 
 def _any_pin_fails():
@@ -392,7 +459,8 @@ def test_pins_pass_unmutated():
 
 
 @pytest.mark.parametrize("mutation", ["gqa_modulo", "strict_mask", "no_scale", "lse_no_max",
-                                      "combine_unweighted", "gqa_off_by_one"])
+                                      "combine_unweighted", "gqa_off_by_one",
+                                      "append_off_by_one", "append_not_attended"])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     orig_ma = ref.masked_attention
     orig_comb = ref.combine
@@ -417,6 +485,12 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
                 lse = lse - s.max(axis=1)     # dropped the max term
             return o, lse
         monkeypatch.setattr(ref, "masked_attention", bad)
+    elif mutation == "append_off_by_one":
+        monkeypatch.setattr(ref, "_append_position", lambda n: n + 1)
+    elif mutation == "append_not_attended":
+        orig_dec = ref.decode
+        monkeypatch.setattr(ref, "decode", lambda q, kc, vc, bt, lens, scale, bs=0:
+                            orig_dec(q, kc, vc, bt, [n - 1 for n in lens], scale, bs))
     elif mutation == "combine_unweighted":
         monkeypatch.setattr(ref, "combine", lambda o, l: (ref._f64(o).mean(0), ref._f64(l).max(0)))
         monkeypatch.setattr(oracle, "combine", ref.combine)
