@@ -16,5 +16,7 @@ from .api import (  # noqa: F401
     selftest_bounded_wait,
     split_ranges,
     decode_noalloc,
+    decode_append_splitkv,
+    decode_append,
 )
 from ._lib import AttnError, lib  # noqa: F401

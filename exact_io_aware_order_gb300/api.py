@@ -82,18 +82,9 @@ def split_ranges(kv_len: int, num_splits: int):
     return [(min(s * c, kv_len), min(s * c + c, kv_len)) for s in range(num_splits)]
 
 
-def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                   kv_lens: torch.Tensor, block_table: Optional[torch.Tensor] = None,
-                   num_splits: int = 0, max_kv_len: Optional[int] = None,
-                   scale: Optional[float] = None, o_partial: Optional[torch.Tensor] = None,
-                   lse_partial: Optional[torch.Tensor] = None, stream=None):
-    """Split-KV single-token decode (``attn_decode_splitkv``).
-
-    q: (B, n_q, d) bf16.  Paged: k_cache, v_cache (num_blocks, block_size,
-    n_kv, d) with block_table (B, max_blocks) int32; contiguous (block_table
-    None): (B, L, n_kv, d).  kv_lens: (B,) int32 on the device.
-    Returns (o_partial (S, B, n_q, d), lse_partial (S, B, n_q)), fp32.
-    """
+def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
+                 o_partial, lse_partial, stream, new_kv=None):
+    """Shape checks and marshalling shared by the plain and appending decode."""
     _need(q, "q", _BF16, 3)
     _need(k_cache, "k_cache", _BF16, 4)
     _need(v_cache, "v_cache", _BF16, 4)
@@ -104,6 +95,11 @@ def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     n_kv = k_cache.shape[2]
     if k_cache.shape[3] != d or kv_lens.shape[0] != B:
         raise ValueError("cache head_dim or kv_lens length does not match q")
+    if new_kv is not None:
+        for t, name in zip(new_kv, ("k_new", "v_new")):
+            _need(t, name, _BF16, 3)
+            if tuple(t.shape) != (B, n_kv, d):
+                raise ValueError(f"{name} must be (batch, n_kv_heads, head_dim)")
     if block_table is not None:
         _need(block_table, "block_table", torch.int32, 2)
         if block_table.shape[0] != B:
@@ -131,13 +127,51 @@ def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     _need(lse_partial, "lse_partial", torch.float32, 3)
     if o_partial.shape[0] != num_splits or lse_partial.shape[0] != num_splits:
         raise ValueError("partial buffers must have num_splits rows")
-    st = lib().attn_decode_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), bt_ptr,
-                                   kv_lens.data_ptr(), int(num_splits), o_partial.data_ptr(),
-                                   lse_partial.data_ptr(), B, n_q, n_kv, d, block_size,
-                                   max_blocks, num_blocks, int(max_kv_len), float(scale),
-                                   _stream(stream))
-    check("attn_decode_splitkv", st)
+    tail = (kv_lens.data_ptr(), int(num_splits), o_partial.data_ptr(), lse_partial.data_ptr(), B,
+            n_q, n_kv, d, block_size, max_blocks, num_blocks, int(max_kv_len), float(scale),
+            _stream(stream))
+    if new_kv is None:
+        name = "attn_decode_splitkv"
+        st = lib().attn_decode_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), bt_ptr,
+                                       *tail)
+    else:
+        name = "attn_decode_append_splitkv"
+        st = lib().attn_decode_append_splitkv(q.data_ptr(), new_kv[0].data_ptr(),
+                                              new_kv[1].data_ptr(), k_cache.data_ptr(),
+                                              v_cache.data_ptr(), bt_ptr, *tail)
+    check(name, st)
     return o_partial, lse_partial
+
+
+def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   kv_lens: torch.Tensor, block_table: Optional[torch.Tensor] = None,
+                   num_splits: int = 0, max_kv_len: Optional[int] = None,
+                   scale: Optional[float] = None, o_partial: Optional[torch.Tensor] = None,
+                   lse_partial: Optional[torch.Tensor] = None, stream=None):
+    """Split-KV single-token decode (``attn_decode_splitkv``).
+
+    q: (B, n_q, d) bf16.  Paged: k_cache, v_cache (num_blocks, block_size,
+    n_kv, d) with block_table (B, max_blocks) int32; contiguous (block_table
+    None): (B, L, n_kv, d).  kv_lens: (B,) int32 on the device.
+    Returns (o_partial (S, B, n_q, d), lse_partial (S, B, n_q)), fp32.
+    """
+    return _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
+                        o_partial, lse_partial, stream)
+
+
+def decode_append_splitkv(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                          k_cache: torch.Tensor, v_cache: torch.Tensor, kv_lens: torch.Tensor,
+                          block_table: Optional[torch.Tensor] = None, num_splits: int = 0,
+                          max_kv_len: Optional[int] = None, scale: Optional[float] = None,
+                          o_partial: Optional[torch.Tensor] = None,
+                          lse_partial: Optional[torch.Tensor] = None, stream=None):
+    """Split-KV decode that first writes each sequence's new key and value
+    (k_new, v_new: (B, n_kv, d) bf16) into the cache at position kv_lens[b]
+    and attends over kv_lens[b] + 1 tokens (``attn_decode_append_splitkv``).
+    kv_lens is not modified: the caller increments it afterwards.
+    """
+    return _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
+                        o_partial, lse_partial, stream, new_kv=(k_new, v_new))
 
 
 def combine(o_partial: torch.Tensor, lse_partial: torch.Tensor,
@@ -169,6 +203,16 @@ def decode(q, k_cache, v_cache, kv_lens, block_table=None, num_splits: int = 0,
     """Split-KV decode followed by the combine: returns (O (B, n_q, d), LSE (B, n_q))."""
     op, lp = decode_splitkv(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len,
                             scale, stream=stream)
+    return combine(op, lp, stream=stream)
+
+
+def decode_append(q, k_new, v_new, k_cache, v_cache, kv_lens, block_table=None,
+                  num_splits: int = 0, max_kv_len: Optional[int] = None,
+                  scale: Optional[float] = None, stream=None):
+    """Decode with append followed by the combine: returns (O, LSE); the new
+    rows are in the caches afterwards, kv_lens is left to the caller."""
+    op, lp = decode_append_splitkv(q, k_new, v_new, k_cache, v_cache, kv_lens, block_table,
+                                   num_splits, max_kv_len, scale, stream=stream)
     return combine(op, lp, stream=stream)
 
 

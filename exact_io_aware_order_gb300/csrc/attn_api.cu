@@ -166,12 +166,18 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
   return ATTN_OK;
 }
 
-int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
-                        const int32_t* block_table, const int32_t* kv_lens, int num_splits,
-                        float* o_partial, float* lse_partial, int batch, int n_q_heads,
-                        int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
-                        int num_blocks, int max_kv_len, float scale, void* stream) {
+namespace {
+
+// Validation and launch shared by the plain and the appending decode.
+int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,
+                const attn_bf16* k_cache, const attn_bf16* v_cache, const int32_t* block_table,
+                const int32_t* kv_lens, int num_splits, float* o_partial, float* lse_partial,
+                int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                int max_blocks_per_seq, int num_blocks, int max_kv_len, float scale,
+                void* stream, bool append) {
   if (!q || !k_cache || !v_cache || !kv_lens || !o_partial || !lse_partial) return ATTN_ERR_NULL;
+  if (append && (!k_new || !v_new)) return ATTN_ERR_NULL;
+  if (append && (!aligned(k_new, 16) || !aligned(v_new, 16))) return ATTN_ERR_ALIGN;
   const bool paged = block_table != nullptr;
   if (batch < 1 || batch > 65535 || n_q_heads < 1 || n_kv_heads < 1 || n_kv_heads > 65535 ||
       max_kv_len < 0 || !valid_scale(scale))
@@ -194,8 +200,35 @@ int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn
   attn::DecodeArgs a{q, k_cache, v_cache, block_table, kv_lens, num_splits, o_partial, lse_partial,
                      batch, n_q_heads, n_kv_heads, head_dim, paged ? block_size : 0,
                      paged ? max_blocks_per_seq : 0, paged ? num_blocks : 0, max_kv_len, scale};
+  if (append) {
+    a.k_new = k_new;
+    a.v_new = v_new;
+  }
   if (attn::launch_decode(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
+}
+
+}  // namespace
+
+int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                        const int32_t* block_table, const int32_t* kv_lens, int num_splits,
+                        float* o_partial, float* lse_partial, int batch, int n_q_heads,
+                        int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                        int num_blocks, int max_kv_len, float scale, void* stream) {
+  return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_table, kv_lens, num_splits,
+                     o_partial, lse_partial, batch, n_q_heads, n_kv_heads, head_dim, block_size,
+                     max_blocks_per_seq, num_blocks, max_kv_len, scale, stream, false);
+}
+
+int attn_decode_append_splitkv(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,
+                               attn_bf16* k_cache, attn_bf16* v_cache, const int32_t* block_table,
+                               const int32_t* kv_lens, int num_splits, float* o_partial,
+                               float* lse_partial, int batch, int n_q_heads, int n_kv_heads,
+                               int head_dim, int block_size, int max_blocks_per_seq,
+                               int num_blocks, int max_kv_len, float scale, void* stream) {
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, block_table, kv_lens, num_splits,
+                     o_partial, lse_partial, batch, n_q_heads, n_kv_heads, head_dim, block_size,
+                     max_blocks_per_seq, num_blocks, max_kv_len, scale, stream, true);
 }
 
 int attn_combine(const float* o_partial, const float* lse_partial, int num_splits, int batch,

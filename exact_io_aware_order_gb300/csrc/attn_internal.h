@@ -41,6 +41,13 @@ struct DecodeArgs {
   int batch, n_q_heads, n_kv_heads, head_dim;
   int block_size, max_blocks_per_seq, num_blocks, max_kv_len;
   float scale;
+  // Decode with append: when set, each sequence's new key / value row
+  // ((batch, n_kv_heads, head_dim) bf16) is written into the cache at
+  // position kv_lens[b] and attended together with the cached tokens.  The
+  // caches are then written, so the entry point that sets these takes
+  // writable cache pointers.
+  const uint16_t* k_new = nullptr;
+  const uint16_t* v_new = nullptr;
 };
 
 struct CombineArgs {

@@ -142,13 +142,18 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
   grid_dep_launch();
   // ---- this split's token range (split rule: see the C header) ----
   const bool paged = a.block_table != nullptr;
+  const bool append = a.k_new != nullptr;
   const long long capacity =
       paged ? (long long)a.max_blocks_per_seq * a.block_size : (long long)a.max_kv_len;
-  int len = a.kv_lens[b];
-  if (len < 0 || (long long)len > capacity) {
+  int len = a.kv_lens[b];  // tokens already cached
+  bool len_ok = true;
+  if (len < 0 || (long long)len + (append ? 1 : 0) > capacity) {
     if (threadIdx.x == 0 && split == 0) atomicOr(kp.err_word, kErrKvLen);
-    len = len < 0 ? 0 : (int)capacity;
+    len = len < 0 ? 0 : (int)capacity - (append ? 1 : 0);
+    len_ok = false;  // attend over the clamped length, write nothing
   }
+  const int pos_new = len;  // the appended token's position
+  if (append) len += 1;     // the new token attends to itself too
   const int per = (len + S - 1) / S;
   const int chunk = (per + kSplitGranule - 1) / kSplitGranule * kSplitGranule;
   const int t0 = min(split * chunk, len);
@@ -163,6 +168,35 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
     return;
   }
   const int n_stage_iters = (n_tok + kStageTokens - 1) / kStageTokens;
+
+  // ---- decode with append: the split that holds the new position writes
+  // the new key / value row of this kv head into the cache (page "FlashAttention
+  // for inference", section "Minimal implementation": the decode call appends
+  // the new keys and values in place).  The write is fenced against the async
+  // proxy and the block synchronises below before the producer's first copy,
+  // so the copies that cover the position read the new row.  No other block
+  // reads that position.
+  if (append && len_ok && pos_new >= t0 && pos_new < t1 && threadIdx.x < 2 * (D / 8)) {
+    const bool is_v = threadIdx.x >= D / 8;
+    const int c = threadIdx.x % (D / 8);  // 16-byte chunk of the row
+    long long row = -1;                   // (token, kv head) row index in the cache
+    if (paged) {
+      const int blk = a.block_table[(size_t)b * a.max_blocks_per_seq + pos_new / a.block_size];
+      if (blk >= 0 && blk < a.num_blocks)
+        row = ((long long)blk * a.block_size + pos_new % a.block_size) * a.n_kv_heads + kvh;
+      else if (c == 0 && !is_v)
+        atomicOr(kp.err_word, kErrBlockIndex);
+    } else {
+      row = ((long long)b * a.max_kv_len + pos_new) * a.n_kv_heads + kvh;
+    }
+    if (row >= 0) {
+      const uint4 val = reinterpret_cast<const uint4*>(
+          (is_v ? a.v_new : a.k_new) + ((size_t)b * a.n_kv_heads + kvh) * D)[c];
+      uint16_t* dst = const_cast<uint16_t*>(is_v ? a.v_cache : a.k_cache) + (size_t)row * D;
+      reinterpret_cast<uint4*>(dst)[c] = val;
+      fence_proxy_async_global();
+    }
+  }
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff);

@@ -136,6 +136,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, float4 v) {
                : "memory");
 }
 
+// Orders this thread's generic-proxy global writes before later async-proxy
+// (TMA) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Untiled copy global -> shared; dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {

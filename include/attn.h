@@ -138,6 +138,39 @@ int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn
                         int num_blocks, int max_kv_len, float scale, void* stream);
 
 /*
+ * attn_decode_append_splitkv -- split-KV single-token decode that first
+ * appends each sequence's new key and value to its cache.
+ *
+ * Page: same, section "Minimal implementation": the decode call against a
+ * paged cache takes the cache, the block table and the per-sequence count of
+ * tokens already cached, appends the new keys and values in place, and the
+ * caller increments the counts afterwards.
+ *
+ *   k_new, v_new: (batch, n_kv_heads, head_dim) bf16, the new token's key and
+ *                value per sequence, 16-byte aligned
+ *   k_cache,
+ *   v_cache    : as for attn_decode_splitkv, but WRITTEN: the row of token
+ *                kv_lens[b] (all kv heads) receives k_new[b] / v_new[b]; no
+ *                other byte of either cache changes
+ *   kv_lens    : (batch,) int32 tokens already cached (read, not modified); the
+ *                query of sequence b attends over kv_lens[b] + 1 tokens, the
+ *                new one last; kv_lens[b] + 1 must not exceed the capacity --
+ *                a larger value is flagged, clamped and nothing is written
+ *   other arguments, the split rule (applied to kv_lens[b] + 1 tokens), the
+ *   partial outputs and the errors are those of attn_decode_splitkv.
+ * A block-table entry outside [0, num_blocks) for the new position is flagged
+ * and that row is not written.  The call must not overlap, on the device,
+ * another call that reads or writes the same cache rows.
+ */
+int attn_decode_append_splitkv(const attn_bf16* q, const attn_bf16* k_new,
+                               const attn_bf16* v_new, attn_bf16* k_cache, attn_bf16* v_cache,
+                               const int32_t* block_table, const int32_t* kv_lens,
+                               int num_splits, float* o_partial, float* lse_partial, int batch,
+                               int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                               int max_blocks_per_seq, int num_blocks, int max_kv_len,
+                               float scale, void* stream);
+
+/*
  * attn_combine -- merge per-split partial results by their LSE weights.
  *
  * Page: same, section "The online softmax, with every symbol defined" (the

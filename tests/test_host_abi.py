@@ -99,6 +99,30 @@ def test_decode_validation(L):
     assert _decode(L, bt=P + 2) == c["ATTN_ERR_ALIGN"]
 
 
+def _append(L, **kw):
+    a = dict(q=P, kn=P, vn=P, k=P, v=P, bt=P, lens=P, S=4, op=P, lp=P, B=2, hq=8, hkv=2, d=128,
+             bs=16, mb=8, nb=16, maxlen=128, scale=0.1)
+    a.update(kw)
+    return L.attn_decode_append_splitkv(a["q"], a["kn"], a["vn"], a["k"], a["v"], a["bt"],
+                                        a["lens"], a["S"], a["op"], a["lp"], a["B"], a["hq"],
+                                        a["hkv"], a["d"], a["bs"], a["mb"], a["nb"], a["maxlen"],
+                                        a["scale"], None)
+
+
+def test_decode_append_validation(L):
+    c = _lib.status_codes()
+    assert _append(L, kn=None) == c["ATTN_ERR_NULL"]
+    assert _append(L, vn=None) == c["ATTN_ERR_NULL"]
+    assert _append(L, kn=P + 8) == c["ATTN_ERR_ALIGN"]
+    assert _append(L, vn=P + 2) == c["ATTN_ERR_ALIGN"]
+    # the rest is the plain decode's validation
+    assert _append(L, k=None) == c["ATTN_ERR_NULL"]
+    assert _append(L, d=80) == c["ATTN_ERR_HEADDIM"]
+    assert _append(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
+    assert _append(L, S=-1) == c["ATTN_ERR_SPLITS"]
+    assert _append(L, bs=0) == c["ATTN_ERR_SHAPE"]
+
+
 def test_combine_validation(L):
     c = _lib.status_codes()
     f = L.attn_combine
@@ -152,7 +176,8 @@ def test_split_rule(kv_len, S):
 
 def test_header_documents_each_entry_point():
     text = open(os.path.join(ROOT, "include", "attn.h")).read()
-    for name in ["attn_prefill", "attn_decode_splitkv", "attn_combine", "attn_decode_num_splits"]:
+    for name in ["attn_prefill", "attn_decode_splitkv", "attn_combine", "attn_decode_num_splits",
+                 "attn_decode_append_splitkv"]:
         block = text[:text.index(name + "(")]
         doc = block[block.rindex("/*"):]
         assert "Page:" in doc or "section" in doc, f"{name} lacks its citation"
