@@ -239,6 +239,7 @@ def run_gb300(args, rank: int, world: int, dist):
         dist.barrier()
     clocks = sampler.stop()
     attn.check_device_status()
+    app = time_decode_append(args, attn, dq, caches, dec, S, op, lp, sweep, sweep_out, dist, dev)
     total_ms = t_start.elapsed_time(t_end)
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[4].elapsed_time(e[2]) for e in evs]
@@ -285,9 +286,64 @@ def run_gb300(args, rank: int, world: int, dist):
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
+    if app is not None:
+        app["roofline"]["peak"] = peaks["hbm_gbs"]
+        app["roofline"]["frac"] = round(app["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
+        app["roofline"]["peak_source"] = peak_src + " hbm copy"
+        result["decode_append"] = app
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist)
     return result
+
+
+def time_decode_append(args, attn, dq, caches, dec, S, op, lp, sweep, sweep_out, dist, dev):
+    """Decode with in-place append on the decode workload's shape: kv_len - 1
+    cached tokens plus the appended one, so the same number of tokens is
+    attended.  Timed like the step's decode (a read-only L2 sweep before each
+    launch, outside its events; the cache copies rotate)."""
+    import torch
+
+    if dec.block_table is not None:
+        return None  # measured on the contiguous single-sequence workload only
+    n = max(3, min(args.steps, 200))
+    B, Hq, D = dq.shape
+    lens = (dec.kv_lens - 1).clamp(min=0).to(dev)
+    g = torch.Generator().manual_seed(1)
+    kn = torch.randn(B, dec.n_kv, D, generator=g).to(torch.bfloat16).to(dev)
+    vn = torch.randn(B, dec.n_kv, D, generator=g).to(torch.bfloat16).to(dev)
+
+    def launch(i):
+        kc, vc = caches[i % len(caches)]
+        attn.decode_append_splitkv(dq, kn, vn, kc, vc, lens, None, num_splits=S,
+                                   scale=dec.scale, o_partial=op, lse_partial=lp)
+
+    for i in range(3):
+        launch(i)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    for i in range(n):
+        torch.sum(sweep, dim=0, out=sweep_out)
+        evs[i][0].record()
+        launch(i)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    attn.check_device_status()
+    (tot,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
+    tokens = int(dec.kv_lens.sum())
+    # K and V of every attended token (the appended one is read back from the
+    # cache), q, the new rows read and written, the final O and LSE.
+    nbytes = tokens * dec.n_kv * D * 2 * 2 + dq.numel() * 2 + 2 * 2 * kn.numel() * 2 + \
+        B * Hq * (D + 1) * 4
+    avg_us = tot / n * 1e3
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": round(job_rate(nbytes, n, world, tot) / 1e9, 1), "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / (avg_us * 1e-6) / 1e9, 1),
+                         "unit": "GB/s", "kernel": "decode_splitkv_kernel<128> (append)",
+                         "bytes_per_launch": nbytes, "avg_launch_us": round(avg_us, 2)},
+            "tokens_attended": tokens, "launches": n}
 
 
 def run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist):
