@@ -16,4 +16,6 @@ from .attention_ref import (  # noqa: F401
     combine,
     append_token,
     decode_append,
+    prefill_varlen,
+    prefill_varlen_rows,
 )

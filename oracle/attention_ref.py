@@ -33,6 +33,11 @@ reason in the design notes of the repository):
   (batch, max_kv_len, n_kv, d).
 * An empty key set (a zero-length sequence or an empty split) has LSE = -inf
   and O = 0: the plain value of an empty sum.
+* Variable-length prefill (§"Interaction with post-trained models", the
+  paragraph on packed data and variable-length batches): several sequences
+  are packed end to end without padding and none attends to another; the
+  packed layout is head-major, q (n_q, total, d), k / v (n_kv, total, d), with
+  cu_seqlens (num_seqs + 1) marking where each sequence starts.
 * Decode with append (§"Minimal implementation", the decode call against a
   paged cache): the per-sequence length counts the tokens already cached; the
   call writes the new token's key and value at that position, attends over
@@ -55,6 +60,8 @@ __all__ = [
     "combine",
     "append_token",
     "decode_append",
+    "prefill_varlen",
+    "prefill_varlen_rows",
 ]
 
 _ROW_BLOCK = 256
@@ -335,3 +342,58 @@ def decode_append(q, k_new, v_new, k_cache, v_cache, block_table, kv_lens: Seque
     kc, vc = append_token(k_cache, v_cache, block_table, kv_lens, k_new, v_new, block_size)
     o, lse = decode(q, kc, vc, block_table, [int(n) + 1 for n in kv_lens], scale, block_size)
     return o, lse, kc, vc
+
+
+def _seq_bounds(cu_seqlens) -> list:
+    """(start, end) of each packed sequence from the cumulative lengths."""
+    cu = [int(x) for x in np.asarray(cu_seqlens).reshape(-1)]
+    if cu[0] != 0 or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must start at 0 and not decrease")
+    return list(zip(cu[:-1], cu[1:]))
+
+
+def prefill_varlen(q, k, v, cu_seqlens, scale: float, causal: bool = True):
+    """Prefill of sequences packed end to end (page §"Interaction with
+    post-trained models", packed data and variable-length batches: examples
+    packed into one sequence must not attend to each other).
+
+    q: (n_q, total, d); k, v: (n_kv, total, d); cu_seqlens: (num_seqs + 1,)
+    with sequence s occupying rows [cu[s], cu[s+1]).  Each sequence is the
+    plain prefill of :func:`prefill` on its own rows.  Rows past cu[-1] are
+    not part of any sequence and come back as O = 0, LSE = -inf.
+    Returns O (n_q, total, d) and LSE (n_q, total), float64.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n_q, total, d = q.shape
+    o = np.zeros((n_q, total, v.shape[2]))
+    lse = np.full((n_q, total), -np.inf)
+    for a, b in _seq_bounds(cu_seqlens):
+        if b == a:
+            continue
+        os_, ls_ = prefill(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], scale, causal)
+        o[:, a:b] = os_[0]
+        lse[:, a:b] = ls_[0]
+    return o, lse
+
+
+def prefill_varlen_rows(q, k, v, cu_seqlens, scale: float, causal: bool,
+                        rows: Iterable[tuple[int, int]]):
+    """:func:`prefill_varlen` for a sample of (head, packed row) pairs, at
+    sizes where every row is too slow.  Returns O (len(rows), d), LSE (len(rows),)."""
+    bounds = _seq_bounds(cu_seqlens)
+    starts = [a for a, _ in bounds]
+    n_q, n_kv = q.shape[0], k.shape[0]
+    rows = list(rows)
+    o = np.zeros((len(rows), v.shape[2]))
+    lse = np.full((len(rows),), -np.inf)
+    for idx, (h, i) in enumerate(rows):
+        s = int(np.searchsorted(starts, i, side="right")) - 1
+        a, b = bounds[s]
+        if not a <= i < b:
+            continue
+        kh = _kv_head(h, n_q, n_kv)
+        hi = i + 1 if causal else b
+        ob, lb = masked_attention(_f64(q[h, i:i + 1]), _f64(k[kh, a:hi]), _f64(v[kh, a:hi]),
+                                  scale, None)
+        o[idx], lse[idx] = ob[0], lb[0]
+    return o, lse

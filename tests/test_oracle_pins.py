@@ -330,6 +330,73 @@ def test_decode_append_full_cache_raises():
 
 
 # ---------------------------------------------------------------------------
+# Variable-length (packed) prefill (page §"Interaction with post-trained
+# models": packed examples must not attend to each other).
+# ---------------------------------------------------------------------------
+
+def _pin_varlen():
+    """Packed prefill against an independent formulation: ONE masked
+    attention over the whole packed sequence with the block-diagonal causal
+    mask (same sequence and j <= i), and against brute force on a tiny case."""
+    lens = [5, 1, 0, 17, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, nq, nkv, d = int(cu[-1]) + 3, 4, 2, 8          # 3 rows past the last sequence
+    g = torch.Generator().manual_seed(13)
+    q = torch.randn(nq, T, d, generator=g, dtype=torch.float64)
+    k = torch.randn(nkv, T, d, generator=g, dtype=torch.float64)
+    v = torch.randn(nkv, T, d, generator=g, dtype=torch.float64)
+    seq = np.full(T, -1)
+    for s_, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        seq[a:b] = s_
+    err = 0.0
+    for causal in (True, False):
+        o, lse = oracle.prefill_varlen(q, k, v, cu, 0.37, causal)
+        allowed = (seq[:, None] == seq[None, :]) & (seq[:, None] >= 0)
+        if causal:
+            allowed &= np.arange(T)[None, :] <= np.arange(T)[:, None]
+        for h in range(nq):
+            ob, lb = ref.masked_attention(q[h].numpy(), k[h // (nq // nkv)].numpy(),
+                                          v[h // (nq // nkv)].numpy(), 0.37, allowed)
+            fin = np.isfinite(lb)
+            assert np.array_equal(fin, np.isfinite(lse[h]))
+            err = max(err, float(np.abs(ob - o[h]).max()), float(np.abs(lb[fin] - lse[h][fin]).max()))
+        # brute force on one row of each non-empty sequence
+        for a, b in zip(cu[:-1], cu[1:]):
+            if b == a:
+                continue
+            i = b - 1
+            for h in (0, nq - 1):
+                kh = h // (nq // nkv)
+                hi = i + 1 if causal else b
+                sc = [0.37 * math.fsum(float(q[h, i, t]) * float(k[kh, j, t]) for t in range(d))
+                      for j in range(a, hi)]
+                mx = max(sc)
+                w = [math.exp(x - mx) for x in sc]
+                z = math.fsum(w)
+                bo = [math.fsum(w[jj] * float(v[kh, a + jj, t]) for jj in range(len(w))) / z
+                      for t in range(d)]
+                err = max(err, max(abs(bo[t] - o[h, i, t]) for t in range(d)),
+                          abs(mx + math.log(z) - lse[h, i]))
+    return err
+
+
+def test_varlen_prefill_matches_block_diagonal_mask_and_brute_force():
+    assert _pin_varlen() <= TOL
+
+
+def test_varlen_sampled_rows_match_full():
+    lens = [130, 7, 300]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    x = W.make_prefill(1, 4, 2, int(cu[-1]), 16, seed=4)
+    q, k, v = x.q[0], x.k[0], x.v[0]
+    o, lse = oracle.prefill_varlen(q, k, v, cu, x.scale, True)
+    rows = [(0, 0), (3, 129), (1, 130), (2, 136), (0, 137), (3, 436)]
+    orow, lrow = oracle.prefill_varlen_rows(q, k, v, cu, x.scale, True, rows)
+    for idx, (h, i) in enumerate(rows):
+        assert np.abs(orow[idx] - o[h, i]).max() <= TOL and abs(lrow[idx] - lse[h, i]) <= TOL
+
+
+# ---------------------------------------------------------------------------
 # Chunk-combine identity.
 # ---------------------------------------------------------------------------
 
@@ -439,7 +506,8 @@ def test_toy_run_split_decode(golden):
 def _pins():
     return {"bruteforce": (_pin_bruteforce, TOL), "sdpa": (_pin_sdpa, 1e-12),
             "closed": (_pin_closed_forms, TOL), "gqa": (_pin_gqa, TOL),
-            "combine": (_pin_combine, TOL), "append": (_pin_append, TOL)}
+            "combine": (_pin_combine, TOL), "append": (_pin_append, TOL),
+            "varlen": (_pin_varlen, TOL)}
 
 
 def _any_pin_fails():
@@ -460,7 +528,8 @@ def test_pins_pass_unmutated():
 
 @pytest.mark.parametrize("mutation", ["gqa_modulo", "strict_mask", "no_scale", "lse_no_max",
                                       "combine_unweighted", "gqa_off_by_one",
-                                      "append_off_by_one", "append_not_attended"])
+                                      "append_off_by_one", "append_not_attended",
+                                      "varlen_cross_sequence"])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     orig_ma = ref.masked_attention
     orig_comb = ref.combine
@@ -485,6 +554,10 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
                 lse = lse - s.max(axis=1)     # dropped the max term
             return o, lse
         monkeypatch.setattr(ref, "masked_attention", bad)
+    elif mutation == "varlen_cross_sequence":
+        # sequences attend to the previous one's rows too (no per-example masking)
+        monkeypatch.setattr(ref, "_seq_bounds", lambda cu: [(0, int(b)) for b in
+                                                            np.asarray(cu).reshape(-1)[1:]])
     elif mutation == "append_off_by_one":
         monkeypatch.setattr(ref, "_append_position", lambda n: n + 1)
     elif mutation == "append_not_attended":
