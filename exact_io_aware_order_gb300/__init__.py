@@ -7,6 +7,7 @@ the computation runs in the library's CUDA kernels.
 
 from .api import (  # noqa: F401
     prefill,
+    prefill_varlen,
     decode_splitkv,
     combine,
     decode,

@@ -68,6 +68,41 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[f
     return out, lse
 
 
+def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                   scale: Optional[float] = None, causal: bool = True,
+                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   stream=None):
+    """Prefill of sequences packed end to end (``attn_prefill_varlen``).
+
+    q: (n_q, total, d) bf16; k, v: (n_kv, total, d) bf16; cu_seqlens:
+    (num_seqs + 1,) int32 on the device.  Returns (O (n_q, total, d) fp32,
+    LSE (n_q, total) fp32); rows outside every sequence are left as they were
+    in ``out`` / ``lse``.
+    """
+    _need(q, "q", _BF16, 3)
+    _need(k, "k", _BF16, 3)
+    _need(v, "v", _BF16, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    n_q, T, d = q.shape
+    n_kv = k.shape[0]
+    if k.shape != (n_kv, T, d) or v.shape != k.shape:
+        raise ValueError("k and v must be (n_kv, total, d) matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((n_q, T, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((n_q, T), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, 3)
+    _need(lse, "lse", torch.float32, 2)
+    st = lib().attn_prefill_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr(), cu_seqlens.data_ptr(), cu_seqlens.numel() - 1,
+                                   T, n_q, n_kv, d, float(scale), int(bool(causal)),
+                                   _stream(stream))
+    check("attn_prefill_varlen", st)
+    return out, lse
+
+
 def decode_num_splits(batch: int, n_kv_heads: int, max_kv_len: int, num_sms: int = 0) -> int:
     """The split-count policy (``attn_decode_num_splits``)."""
     return int(lib().attn_decode_num_splits(int(batch), int(n_kv_heads), int(max_kv_len),

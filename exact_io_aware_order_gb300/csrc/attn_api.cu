@@ -166,6 +166,31 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
   return ATTN_OK;
 }
 
+int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+                        float* lse, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                        int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
+                        void* stream) {
+  if (!q || !k || !v || !o || !lse || !cu_seqlens) return ATTN_ERR_NULL;
+  if (num_seqs < 1 || num_seqs > attn::kMaxVarlenSeqs || n_q_heads < 1 || n_kv_heads < 1 ||
+      n_q_heads > (1 << 20) || total_tokens < 1 || total_tokens > (1 << 24) ||
+      !valid_scale(scale))
+    return ATTN_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(cu_seqlens, 4))
+    return ATTN_ERR_ALIGN;
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  attn::PrefillArgs a{q, k, v, o, lse, 1, n_q_heads, n_kv_heads, total_tokens, head_dim, scale,
+                      causal ? 1 : 0};
+  a.cu_seqlens = cu_seqlens;
+  a.num_seqs = num_seqs;
+  if (attn::launch_prefill(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
 namespace {
 
 // Validation and launch shared by the plain and the appending decode.

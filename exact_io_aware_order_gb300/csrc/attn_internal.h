@@ -10,6 +10,7 @@ namespace attn {
 constexpr uint32_t kErrTimeout = 1u;     // a bounded wait gave up
 constexpr uint32_t kErrBlockIndex = 2u;  // a block-table entry outside [0, num_blocks)
 constexpr uint32_t kErrKvLen = 4u;       // a kv_len outside [0, capacity]
+constexpr uint32_t kErrSeqLens = 8u;     // cu_seqlens not increasing within [0, total]
 
 struct LaunchCtx {
   cudaStream_t stream;
@@ -27,7 +28,14 @@ struct PrefillArgs {
   int batch, n_q_heads, n_kv_heads, seqlen, head_dim;
   float scale;
   int causal;
+  // Packed variable-length mode: when set, batch is 1, seqlen is the total
+  // of packed rows and sequence s occupies rows [cu_seqlens[s], cu_seqlens[s+1]).
+  const int32_t* cu_seqlens = nullptr;
+  int num_seqs = 0;
 };
+
+// Largest number of packed sequences per variable-length prefill call.
+constexpr int kMaxVarlenSeqs = 1024;
 
 struct DecodeArgs {
   const uint16_t* q;

@@ -65,7 +65,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max grows > 2^8
 
-template <int D>
+template <int D, bool VARLEN>
 struct PrefillSmem {
   static constexpr int kTileBytes = 128 * D * 2;       // one Q, K or V tile
   static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 64 bf16 (one swizzle span)
@@ -84,7 +84,12 @@ struct PrefillSmem {
       2 * kQSlots + 2 * kKSlots + 2 * kVSlots + 3 * kSBuf + 2 + 4 + 2;
   static constexpr int kStats = kBar + kNumBars * 8;           // float2 (m, l) [2][128]
   static constexpr int kMisc = kStats + 2 * 128 * 8;           // tmem base, abort flag
-  static constexpr int kUsed = kMisc + 16;
+  // Packed variable-length mode: per sequence its first row, its length and
+  // the running count of work items before it (one more entry: the total).
+  static constexpr int kSeqStart = kMisc + 16;
+  static constexpr int kSeqLen = kSeqStart + (VARLEN ? kMaxVarlenSeqs * 4 : 0);
+  static constexpr int kItemPrefix = kSeqLen + (VARLEN ? kMaxVarlenSeqs * 4 : 0);
+  static constexpr int kUsed = kItemPrefix + (VARLEN ? (kMaxVarlenSeqs + 1) * 4 : 0);
   static constexpr int kAlloc = kUsed + 1024;                  // + alignment slack
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -96,33 +101,71 @@ struct PrefillParams {
   float sl2;  // scale * log2(e)
   int causal;
   int n_q_tiles;    // ceil(seqlen / 128)
-  int total_tiles;  // n_q_tiles * batch * n_q_heads
+  int total_tiles;  // n_q_tiles * batch * n_q_heads (padded mode)
+  const int32_t* cu_seqlens;  // packed mode: (num_seqs + 1) row offsets
+  int num_seqs;
   uint32_t* err_word;
   uint64_t timeout_ns;
 };
 
 // One query tile of one (sequence, head).
 struct Tile {
-  int q0;  // first query row
-  int zq;  // Q / O tensor-map plane (sequence * n_q_heads + head)
-  int zk;  // K / V tensor-map plane
-  int n;   // key tiles visited (>= 1)
+  int row0;  // tensor-map row of the tile's first query
+  int qrel;  // index of that query within its sequence
+  int kv0;   // tensor-map row of the sequence's first key
+  int len;   // sequence length (keys and queries)
+  int zq;    // Q / O tensor-map plane (sequence * n_q_heads + head)
+  int zk;    // K / V tensor-map plane
+  int n;     // key tiles visited (>= 1)
 };
 
-// Work list, longest causal rows first: item w is query tile
+// Shared-memory tables of the packed variable-length mode.
+struct SeqTables {
+  const int* start;   // first row of each sequence
+  const int* len;     // length of each sequence
+  const int* prefix;  // work items before each sequence; prefix[num_seqs] = all items
+};
+
+// Work list, longest causal rows first.  Padded batch: item w is query tile
 // n_q_tiles - 1 - w / (batch * n_q_heads) of (sequence, head) w % (batch * n_q_heads),
 // so consecutive items share kv heads while their K/V tiles are hot in L2.
-__device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p) {
-  const int BH = p.batch * p.n_q_heads;
-  const int qt = p.n_q_tiles - 1 - w / BH;
-  const int bh = w % BH;
-  const int bidx = bh / p.n_q_heads, h = bh % p.n_q_heads;
-  const int kvh = h / (p.n_q_heads / p.n_kv_heads);
+// Packed sequences: the items of sequence s are prefix[s] .. prefix[s+1]-1,
+// again longest tile first and heads fastest.
+template <bool VARLEN>
+__device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const SeqTables& st) {
   Tile t;
-  t.q0 = qt * kBM;
-  t.zq = bidx * p.n_q_heads + h;
-  t.zk = bidx * p.n_kv_heads + kvh;
-  t.n = p.causal ? (qt + 1) : (p.seqlen + kBN - 1) / kBN;
+  if constexpr (!VARLEN) {
+    const int BH = p.batch * p.n_q_heads;
+    const int qt = p.n_q_tiles - 1 - w / BH;
+    const int bh = w % BH;
+    const int bidx = bh / p.n_q_heads, h = bh % p.n_q_heads;
+    const int kvh = h / (p.n_q_heads / p.n_kv_heads);
+    t.row0 = t.qrel = qt * kBM;
+    t.kv0 = 0;
+    t.len = p.seqlen;
+    t.zq = bidx * p.n_q_heads + h;
+    t.zk = bidx * p.n_kv_heads + kvh;
+    t.n = p.causal ? (qt + 1) : (p.seqlen + kBN - 1) / kBN;
+  } else {
+    // The sequence: the last one whose first item is at or before w (a
+    // sequence without items shares its prefix with the next one).
+    int lo = 0, hi = p.num_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (st.prefix[mid] <= w) lo = mid; else hi = mid - 1;
+    }
+    const int local = w - st.prefix[lo];
+    const int h = local % p.n_q_heads;
+    const int tiles = (st.len[lo] + kBM - 1) / kBM;
+    const int qt = tiles - 1 - local / p.n_q_heads;
+    t.qrel = qt * kBM;
+    t.row0 = st.start[lo] + t.qrel;
+    t.kv0 = st.start[lo];
+    t.len = st.len[lo];
+    t.zq = h;
+    t.zk = h / (p.n_q_heads / p.n_kv_heads);
+    t.n = p.causal ? (qt + 1) : tiles;
+  }
   return t;
 }
 
@@ -135,12 +178,12 @@ __device__ __forceinline__ int item_of(int r, int total) {
   return w < total ? w : -1;
 }
 
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const PrefillParams p) {
-  using L = PrefillSmem<D>;
+  using L = PrefillSmem<D, VARLEN>;
   constexpr int RQ = L::kQSlots, RK = L::kKSlots, RV = L::kVSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -199,6 +242,48 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_o);
   }
+  int* seq_start = reinterpret_cast<int*>(smem + L::kSeqStart);
+  int* seq_len = reinterpret_cast<int*>(smem + L::kSeqLen);
+  int* item_prefix = reinterpret_cast<int*>(smem + L::kItemPrefix);
+  if constexpr (VARLEN) {
+    // Packed sequences: one warp reads cu_seqlens, clamps each sequence to
+    // [previous end, total] (flagging any that had to be), and scans the
+    // per-sequence item counts (n_q_heads x query tiles).
+    if (warp == kEpiWarp0) {
+      int carry = 0, prev_end = 0;
+      bool bad = false;
+      for (int base = 0; base < p.num_seqs; base += 32) {
+        const int s = base + lane;
+        int a = 0, e = 0;
+        if (s < p.num_seqs) {
+          a = p.cu_seqlens[s];
+          e = p.cu_seqlens[s + 1];
+        }
+        const int a_prev = __shfl_up_sync(0xffffffffu, e, 1);
+        const int lower = lane == 0 ? prev_end : a_prev;  // the previous sequence's end
+        int a_c = min(max(a, 0), N), e_c = min(max(e, a_c), N);
+        if (s < p.num_seqs && (a != a_c || e != e_c || a < lower || (s == 0 && a != 0))) bad = true;
+        if (s >= p.num_seqs) a_c = e_c = 0;
+        const int items = ((e_c - a_c + kBM - 1) / kBM) * p.n_q_heads;
+        int incl = items;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (s < p.num_seqs) {
+          seq_start[s] = a_c;
+          seq_len[s] = e_c - a_c;
+          item_prefix[s + 1] = carry + incl;
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+        prev_end = __shfl_sync(0xffffffffu, e, 31);
+      }
+      if (lane == 0) item_prefix[0] = 0;
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err_word, kErrSeqLens);
+    }
+  }
+  const SeqTables seqt{seq_start, seq_len, item_prefix};
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -206,7 +291,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   // TMEM columns: S buffers [0,128), [128,256), [256,384) | O [384, 384+D)
   const uint32_t tO = tmem + 384u;
   const WaitCtl ctl{abort_flag, p.err_word, p.timeout_ns};
-  const int total = p.total_tiles;
+  const int total = VARLEN ? item_prefix[p.num_seqs] : p.total_tiles;
 
   // Every role walks the same sequence: the CTA's items r = 0, 1, ... and,
   // within item r, key tiles j = 0 .. n-1.  Ring slots and barrier phases
@@ -232,13 +317,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         c.r = 0;
         c.j = 0;
         c.w = item_of(0, total);
-        if (c.w >= 0) c.t = tile_of(c.w, p);
+        if (c.w >= 0) c.t = tile_of<VARLEN>(c.w, p, seqt);
       };
       auto advance = [&](Cursor& c) {
         if (++c.j == c.t.n) {
           c.j = 0;
           c.w = item_of(++c.r, total);
-          if (c.w >= 0) c.t = tile_of(c.w, p);
+          if (c.w >= 0) c.t = tile_of<VARLEN>(c.w, p, seqt);
         }
       };
       int nq = 0, nk = 0, nv = 0;  // tiles issued
@@ -258,17 +343,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       auto load_k = [&]() -> bool {
         if (kc.w < 0) return true;
         if (kc.j == 0) {
-          if (!load_tile(&tm_q, L::kQ, kQFull, kQEmpty, RQ, nq, kc.t.q0, kc.t.zq)) return false;
+          if (!load_tile(&tm_q, L::kQ, kQFull, kQEmpty, RQ, nq, kc.t.row0, kc.t.zq)) return false;
           ++nq;
         }
-        if (!load_tile(&tm_k, L::kK, kKFull, kKEmpty, RK, nk, kc.j * kBN, kc.t.zk)) return false;
+        if (!load_tile(&tm_k, L::kK, kKFull, kKEmpty, RK, nk, kc.t.kv0 + kc.j * kBN, kc.t.zk))
+          return false;
         ++nk;
         advance(kc);
         return true;
       };
       bool ok = load_k() && load_k();
       while (ok && vc.w >= 0) {
-        ok = load_tile(&tm_v, L::kV, kVFull, kVEmpty, RV, nv, vc.j * kBN, vc.t.zk);
+        ok = load_tile(&tm_v, L::kV, kVFull, kVEmpty, RV, nv, vc.t.kv0 + vc.j * kBN, vc.t.zk);
         if (!ok) break;
         ++nv;
         advance(vc);
@@ -292,7 +378,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int r = 0; ok; ++r) {
         const int w = item_of(r, total);
         if (w < 0) break;
-        const Tile t = tile_of(w, p);
+        const Tile t = tile_of<VARLEN>(w, p, seqt);
         const int qs = r % RQ;
         if (!mbar_wait(bar(kQFull + qs), (r / RQ) & 1, ctl)) { ok = false; break; }
         const uint32_t q_lo = sw128_desc_lo(smem_u32(smem + L::kQ + qs * L::kTileBytes), 16);
@@ -329,7 +415,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int r = 0; ok; ++r) {
         const int w = item_of(r, total);
         if (w < 0) break;
-        const int n = tile_of(w, p).n;
+        const int n = tile_of<VARLEN>(w, p, seqt).n;
         for (int j = 0; j < n; ++j, ++g) {
           const int b = g % kSBuf, slot = g % RV;
           if (!mbar_wait(bar(kPFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
@@ -368,8 +454,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int r = 0; ok; ++r) {
       const int w = item_of(r, total);
       if (w < 0) break;
-      const Tile t = tile_of(w, p);
-      const int q0 = t.q0, q_row = q0 + row;
+      const Tile t = tile_of<VARLEN>(w, p, seqt);
+      const int q0 = t.qrel, q_row = q0 + row;  // indices within the sequence
       float m = -INFINITY, l = 0.f;   // running max (log2 domain) and sum of the row
       for (int j = 0; j < t.n; ++j, ++g) {
         const int b = g % kSBuf;
@@ -389,8 +475,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[c][i]);
         }
         const int kv0 = j * kBN;
-        if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > N)) {
-          const int lim = p.causal ? (q_row - kv0) : (N - 1 - kv0);  // last allowed column
+        if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > t.len)) {
+          const int lim = p.causal ? (q_row - kv0) : (t.len - 1 - kv0);  // last allowed column
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
             if (c > lim) s[c] = -INFINITY;
@@ -485,7 +571,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int r = 0; ok; ++r) {
       const int w = item_of(r, total);
       if (w < 0) break;
-      const Tile t = tile_of(w, p);
+      const Tile t = tile_of<VARLEN>(w, p, seqt);
       if (!mbar_wait_warp(bar(kOFull), r & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       uint32_t acc[D / 32][32];
@@ -499,27 +585,44 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const float2 ml = stats[ss * 128 + row];
       mbar_arrive(bar(kStEmpty + ss));
       const float inv_l = 1.f / ml.y;
-      const int row0 = t.q0 + quarter * 32;  // first row of this warp's box
+      const int row0 = t.row0 + quarter * 32;  // tensor row of this warp's box
+      // Rows of the box inside the sequence.  A padded batch's boxes end at
+      // the tensor's end, where the copy clips; a packed sequence's last box
+      // may reach into the next sequence, so it is written row by row.
+      const int in_seq = t.len - (t.qrel + quarter * 32);
+      if (!VARLEN || in_seq >= 32) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
-        __syncwarp();
+        for (int c = 0; c < D / 32; ++c) {
+          if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
+          __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          st_shared_v4(stage + lane * 128 + ((i ^ (lane & 7)) << 4),
-                       make_float4(__uint_as_float(acc[c][4 * i]) * inv_l,
-                                   __uint_as_float(acc[c][4 * i + 1]) * inv_l,
-                                   __uint_as_float(acc[c][4 * i + 2]) * inv_l,
-                                   __uint_as_float(acc[c][4 * i + 3]) * inv_l));
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && row0 < N) {  // rows past the end are clipped by the copy
-          tma_store_3d(&tm_o, stage, c * 32, row0, t.zq);
-          bulk_commit_group();
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(stage + lane * 128 + ((i ^ (lane & 7)) << 4),
+                         make_float4(__uint_as_float(acc[c][4 * i]) * inv_l,
+                                     __uint_as_float(acc[c][4 * i + 1]) * inv_l,
+                                     __uint_as_float(acc[c][4 * i + 2]) * inv_l,
+                                     __uint_as_float(acc[c][4 * i + 3]) * inv_l));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < N) {  // rows past the tensor's end are clipped by the copy
+            tma_store_3d(&tm_o, stage, c * 32, row0, t.zq);
+            bulk_commit_group();
+          }
         }
+      } else if (lane < in_seq) {
+        float* orow = p.o + ((size_t)t.zq * N + (size_t)(row0 + lane)) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(orow + c * 32)[i] =
+                make_float4(__uint_as_float(acc[c][4 * i]) * inv_l,
+                            __uint_as_float(acc[c][4 * i + 1]) * inv_l,
+                            __uint_as_float(acc[c][4 * i + 2]) * inv_l,
+                            __uint_as_float(acc[c][4 * i + 3]) * inv_l);
       }
-      const int q_row = t.q0 + row;
-      if (q_row < N) p.lse[(size_t)t.zq * N + q_row] = (ml.x + __log2f(ml.y)) * kLn2;
+      if (t.qrel + row < t.len && t.row0 + row < N)
+        p.lse[(size_t)t.zq * N + t.row0 + row] = (ml.x + __log2f(ml.y)) * kLn2;
     }
     if (lane == 0) bulk_wait_all();  // O is in global memory before the CTA exits
     __syncwarp();
@@ -582,15 +685,15 @@ bool make_out_map(CUtensorMap* m, void* base, int D, int rows, int planes) {
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool VARLEN>
 cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
-  using L = PrefillSmem<D>;
+  using L = PrefillSmem<D, VARLEN>;
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kAlloc);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VARLEN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
@@ -611,19 +714,26 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   pp.causal = a.causal;
   pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM;
   pp.total_tiles = pp.n_q_tiles * a.batch * a.n_q_heads;
+  pp.cu_seqlens = a.cu_seqlens;
+  pp.num_seqs = a.num_seqs;
   pp.err_word = ctx.err_word;
   pp.timeout_ns = ctx.timeout_ns;
   // Persistent: one CTA per SM (shared memory and TMEM admit one), each
-  // walking its share of the work list.
-  const unsigned grid = (unsigned)std::min(pp.total_tiles, std::max(ctx.num_sms, 1));
-  prefill_kernel<D><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, mo, pp);
+  // walking its share of the work list.  Packed sequences: the item count is
+  // on the device, so every SM gets a CTA (those without items exit at once).
+  const int sms = std::max(ctx.num_sms, 1);
+  const unsigned grid = (unsigned)(VARLEN ? sms : std::min(pp.total_tiles, sms));
+  prefill_kernel<D, VARLEN><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, mo, pp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx) {
-  return a.head_dim == 128 ? launch_prefill_t<128>(a, ctx) : launch_prefill_t<64>(a, ctx);
+  const bool varlen = a.cu_seqlens != nullptr;
+  if (a.head_dim == 128)
+    return varlen ? launch_prefill_t<128, true>(a, ctx) : launch_prefill_t<128, false>(a, ctx);
+  return varlen ? launch_prefill_t<64, true>(a, ctx) : launch_prefill_t<64, false>(a, ctx);
 }
 
 }  // namespace attn

@@ -125,6 +125,31 @@ def make_decode_paged(batch: int, n_q: int, n_kv: int, head_dim: int,
                         1.0 / math.sqrt(head_dim), max_len)
 
 
+@dataclass
+class VarlenInputs:
+    q: torch.Tensor            # (n_q, total, d) bf16, sequences packed end to end
+    k: torch.Tensor            # (n_kv, total, d) bf16
+    v: torch.Tensor
+    cu_seqlens: torch.Tensor   # (num_seqs + 1,) int32
+    scale: float
+    causal: bool = True
+
+
+def make_prefill_varlen(lens, n_q: int, n_kv: int, head_dim: int, seed: int = 0,
+                        extra_rows: int = 0, causal: bool = True) -> VarlenInputs:
+    """Sequences of the given lengths packed end to end (head-major), plus
+    ``extra_rows`` rows that belong to no sequence.  Draw order: Q, K, V."""
+    lens = [int(n) for n in lens]
+    T = sum(lens) + extra_rows
+    gen = torch.Generator().manual_seed(seed)
+    q = _randn_bf16(gen, (n_q, T, head_dim))
+    k = _randn_bf16(gen, (n_kv, T, head_dim))
+    v = _randn_bf16(gen, (n_kv, T, head_dim))
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.as_tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    return VarlenInputs(q, k, v, cu, 1.0 / math.sqrt(head_dim), causal)
+
+
 def paged_lens_uniform(batch: int, lo: int, hi: int, seed: int = 0):
     """Integer-uniform sequence lengths in [lo, hi] inclusive (seeded)."""
     gen = torch.Generator().manual_seed(seed + 1)
@@ -153,6 +178,14 @@ def llama_long_prefill(seqlen: int = 32768, seed: int = 0) -> PrefillInputs:
 def qwen_decode(kv_len: int = 30720, seed: int = 0) -> DecodeInputs:
     """Single-token decode, 28 / 4 heads, head_dim 128, contiguous cache."""
     return make_decode_contiguous(1, 28, 4, 128, kv_len, seed=seed)
+
+
+def qwen_varlen_prefill(seed: int = 0, num_seqs: int = 16, lo: int = 256,
+                        hi: int = 4096) -> VarlenInputs:
+    """A prefill batch of prompts of different lengths (integer-uniform in
+    [lo, hi], seeded) packed without padding, 28 / 4 heads, head_dim 128."""
+    lens = paged_lens_uniform(num_seqs, lo, hi, seed + 7)
+    return make_prefill_varlen(lens, 28, 4, 128, seed=seed)
 
 
 def llama_paged_decode(seed: int = 0, batch: int = 16) -> DecodeInputs:

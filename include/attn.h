@@ -88,6 +88,36 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
                  int head_dim, float scale, int causal, void* stream);
 
 /*
+ * attn_prefill_varlen -- prefill of several sequences packed end to end
+ * without padding (variable-length batch).
+ *
+ * Page: same, section "Interaction with post-trained models" (packed data and
+ * variable-length batches: examples packed into one sequence do not attend to
+ * each other; engines batch prompts of different lengths this way), with the
+ * per-sequence computation of attn_prefill.
+ *
+ *   q   : (n_q_heads,  total_tokens, head_dim) bf16, 16-byte aligned
+ *   k, v: (n_kv_heads, total_tokens, head_dim) bf16, 16-byte aligned
+ *   o   : (n_q_heads,  total_tokens, head_dim) fp32 output, 16-byte aligned
+ *   lse : (n_q_heads,  total_tokens) fp32 output (natural log), 4-byte aligned
+ *   cu_seqlens: (num_seqs + 1,) int32 on the device, 0 = cu[0] <= cu[1] <= ...
+ *         <= cu[num_seqs] <= total_tokens; sequence s is rows [cu[s], cu[s+1])
+ *         (empty sequences allowed)
+ *   causal: nonzero -> row i of a sequence attends to its keys j <= i; zero ->
+ *         to every key of its own sequence.
+ * Rows outside every sequence are not written.  A cu_seqlens that breaks the
+ * rule above is clamped into it and flagged (ATTN_ERR_DEVICE from
+ * attn_check_device_status).
+ * Limits: 1 <= num_seqs <= 1024; head_dim in {64, 128}; 1 <= total_tokens <= 2^24;
+ *   n_q_heads % n_kv_heads == 0.
+ * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
+ */
+int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+                        float* lse, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                        int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
+                        void* stream);
+
+/*
  * attn_decode_num_splits -- the split-count policy for single-token decode.
  *
  * Page: same, section "Decode: a different bottleneck": splitting the key/value

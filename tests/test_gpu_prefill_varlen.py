@@ -1,0 +1,82 @@
+"""Parity of the packed variable-length prefill (attn_prefill_varlen), through
+the C ABI, against the float64 oracle's prefill_varlen: whole outputs at small
+sizes, sampled rows at a 16-prompt batch, rows outside every sequence left
+untouched, one packed sequence equal to the padded prefill bit for bit, and
+bad cu_seqlens reported."""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_order_gb300 as attn
+from exact_io_aware_order_gb300 import workloads as W
+from exact_io_aware_order_gb300._lib import AttnError, status_codes
+import oracle
+from gpu_util import compare, nan_like
+
+pytestmark = pytest.mark.gpu
+
+
+def run(x, dev):
+    n_q, T, d = x.q.shape
+    o, lse = nan_like((n_q, T, d), dev), nan_like((n_q, T), dev)
+    attn.prefill_varlen(x.q.to(dev), x.k.to(dev), x.v.to(dev), x.cu_seqlens.to(dev), x.scale,
+                        x.causal, out=o, lse=lse)
+    attn.check_device_status()
+    return o, lse
+
+
+@pytest.mark.parametrize("lens,hq,hkv,d,causal,extra", [
+    ([1, 127, 128, 129, 300], 8, 2, 128, True, 0),      # tile edges around 128
+    ([1000, 7, 256, 0, 513], 28, 4, 128, True, 5),      # an empty sequence, rows past the end
+    ([200, 1, 64, 129], 4, 4, 64, True, 3),             # head_dim 64, MHA
+    ([130, 300, 5], 8, 1, 128, False, 2),               # full (non-causal) attention per sequence
+    ([77], 6, 3, 128, True, 0),                         # a single short sequence
+])
+def test_varlen_full(dev, lens, hq, hkv, d, causal, extra):
+    x = W.make_prefill_varlen(lens, hq, hkv, d, seed=sum(lens), extra_rows=extra, causal=causal)
+    o, lse = run(x, dev)
+    o_ref, lse_ref = oracle.prefill_varlen(x.q, x.k, x.v, x.cu_seqlens, x.scale, causal)
+    T0 = int(x.cu_seqlens[-1])
+    compare(o[:, :T0], lse[:, :T0], o_ref[:, :T0], lse_ref[:, :T0], f"varlen {lens}")
+    assert torch.isnan(o[:, T0:]).all() and torch.isnan(lse[:, T0:]).all(), \
+        "rows outside every sequence were written"
+
+
+def test_varlen_sixteen_prompts_sampled(dev):
+    """16 prompts, lengths uniform in [256, 4096], 28 / 4 heads: every
+    sequence's first, last and boundary-adjacent rows plus random rows."""
+    x = W.qwen_varlen_prefill()
+    o, lse = run(x, dev)
+    cu = x.cu_seqlens.tolist()
+    rng = np.random.default_rng(0)
+    rows = []
+    for a, b in zip(cu[:-1], cu[1:]):
+        for i in {a, a + 1, a + 127, a + 128, b - 1, b - 2} | set(rng.integers(a, b, 4).tolist()):
+            if a <= i < b:
+                rows.append((int(rng.integers(0, 28)), int(i)))
+    o_ref, lse_ref = oracle.prefill_varlen_rows(x.q, x.k, x.v, cu, x.scale, True, rows)
+    hs = torch.tensor([h for h, _ in rows])
+    ix = torch.tensor([i for _, i in rows])
+    compare(o[hs, ix], lse[hs, ix], o_ref, lse_ref, "16 prompts sampled")
+
+
+def test_one_sequence_equals_padded_prefill_bitwise(dev):
+    """One packed sequence is exactly the padded batch-1 prefill: same tiles,
+    same arithmetic, so the same bits."""
+    x = W.make_prefill(1, 28, 4, 1500, 128, seed=3)
+    o_p, l_p = attn.prefill(x.q.to(dev), x.k.to(dev), x.v.to(dev), x.scale, True)
+    cu = torch.tensor([0, 1500], dtype=torch.int32, device=dev)
+    o_v, l_v = attn.prefill_varlen(x.q[0].to(dev), x.k[0].to(dev), x.v[0].to(dev), cu, x.scale, True)
+    attn.check_device_status()
+    assert torch.equal(o_v, o_p[0]) and torch.equal(l_v, l_p[0])
+
+
+def test_bad_cu_seqlens_is_reported(dev):
+    x = W.make_prefill_varlen([100, 100], 4, 2, 64, seed=1)
+    cu = torch.tensor([0, 150, 120], dtype=torch.int32, device=dev)   # decreasing
+    with pytest.raises(AttnError) as e:
+        attn.prefill_varlen(x.q.to(dev), x.k.to(dev), x.v.to(dev), cu, x.scale, True)
+        attn.check_device_status()
+    assert e.value.status == status_codes()["ATTN_ERR_DEVICE"]
+    attn.check_device_status()                                          # cleared

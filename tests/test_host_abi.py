@@ -71,6 +71,26 @@ def test_prefill_validation(L):
     assert _prefill(L, lse=P + 2) == c["ATTN_ERR_ALIGN"]
 
 
+def _varlen(L, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, cu=P, S=3, T=500, hq=4, hkv=2, d=128, scale=0.1, causal=1)
+    a.update(kw)
+    return L.attn_prefill_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu"], a["S"], a["T"],
+                                 a["hq"], a["hkv"], a["d"], a["scale"], a["causal"], None)
+
+
+def test_prefill_varlen_validation(L):
+    c = _lib.status_codes()
+    assert _varlen(L, cu=None) == c["ATTN_ERR_NULL"]
+    assert _varlen(L, S=0) == c["ATTN_ERR_SHAPE"]
+    assert _varlen(L, S=1025) == c["ATTN_ERR_SHAPE"]
+    assert _varlen(L, T=0) == c["ATTN_ERR_SHAPE"]
+    assert _varlen(L, T=(1 << 24) + 1) == c["ATTN_ERR_SHAPE"]
+    assert _varlen(L, d=96) == c["ATTN_ERR_HEADDIM"]
+    assert _varlen(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
+    assert _varlen(L, cu=P + 2) == c["ATTN_ERR_ALIGN"]
+    assert _varlen(L, q=P + 8) == c["ATTN_ERR_ALIGN"]
+
+
 def _decode(L, **kw):
     a = dict(q=P, k=P, v=P, bt=P, lens=P, S=4, op=P, lp=P, B=2, hq=8, hkv=2, d=128, bs=16,
              mb=8, nb=16, maxlen=128, scale=0.1)
@@ -177,7 +197,7 @@ def test_split_rule(kv_len, S):
 def test_header_documents_each_entry_point():
     text = open(os.path.join(ROOT, "include", "attn.h")).read()
     for name in ["attn_prefill", "attn_decode_splitkv", "attn_combine", "attn_decode_num_splits",
-                 "attn_decode_append_splitkv"]:
+                 "attn_decode_append_splitkv", "attn_prefill_varlen"]:
         block = text[:text.index(name + "(")]
         doc = block[block.rindex("/*"):]
         assert "Page:" in doc or "section" in doc, f"{name} lacks its citation"
