@@ -153,6 +153,8 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
   if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || seqlen < 1 || seqlen > (1 << 24) ||
       (long long)batch * n_q_heads > (1LL << 20) || !valid_scale(scale))
     return ATTN_ERR_SHAPE;
+  // work items (query tiles x heads x sequences) are counted in 32 bits
+  if ((long long)batch * n_q_heads * ((seqlen + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
@@ -174,6 +176,9 @@ int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16*
   if (num_seqs < 1 || num_seqs > attn::kMaxVarlenSeqs || n_q_heads < 1 || n_kv_heads < 1 ||
       n_q_heads > (1 << 20) || total_tokens < 1 || total_tokens > (1 << 24) ||
       !valid_scale(scale))
+    return ATTN_ERR_SHAPE;
+  // work items (at most total/128 + num_seqs query tiles per head) are counted in 32 bits
+  if ((long long)n_q_heads * ((total_tokens + 127) / 128 + num_seqs) > 0x7fffffffLL)
     return ATTN_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;

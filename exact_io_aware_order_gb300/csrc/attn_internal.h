@@ -35,7 +35,7 @@ struct PrefillArgs {
 };
 
 // Largest number of packed sequences per variable-length prefill call.
-constexpr int kMaxVarlenSeqs = 1024;
+constexpr int kMaxVarlenSeqs = 512;
 
 struct DecodeArgs {
   const uint16_t* q;

@@ -130,7 +130,11 @@ struct SeqTables {
 // n_q_tiles - 1 - w / (batch * n_q_heads) of (sequence, head) w % (batch * n_q_heads),
 // so consecutive items share kv heads while their K/V tiles are hot in L2.
 // Packed sequences: the items of sequence s are prefix[s] .. prefix[s+1]-1,
-// again longest tile first and heads fastest.
+// again longest tile first and heads fastest, taken in the same snake order,
+// so the CTAs work on one or two sequences at a time and their K/V stay in
+// L2.  (A globally longest-first order balances better but spreads the work
+// over every sequence at once; claiming items dynamically balances too but
+// costs more per tile; both measured slower.)
 template <bool VARLEN>
 __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const SeqTables& st) {
   Tile t;

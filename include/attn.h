@@ -79,7 +79,7 @@ const char* attn_status_string(int status);
  *   scale: multiplies q.k (pass 1/sqrt(head_dim) for standard attention)
  *   causal: nonzero -> row i attends to keys j <= i; zero -> to every key.
  * Limits: head_dim in {64, 128}; 1 <= seqlen <= 2^24; batch*n_q_heads <= 2^20;
- *   n_q_heads % n_kv_heads == 0.  bf16 inputs, fp32 accumulation, P rounded
+ *   batch*n_q_heads*ceil(seqlen/128) < 2^31; n_q_heads % n_kv_heads == 0.  bf16 inputs, fp32 accumulation, P rounded
  *   to bf16 before the P*V product.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
  */
@@ -108,8 +108,8 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
  * Rows outside every sequence are not written.  A cu_seqlens that breaks the
  * rule above is clamped into it and flagged (ATTN_ERR_DEVICE from
  * attn_check_device_status).
- * Limits: 1 <= num_seqs <= 1024; head_dim in {64, 128}; 1 <= total_tokens <= 2^24;
- *   n_q_heads % n_kv_heads == 0.
+ * Limits: 1 <= num_seqs <= 512; head_dim in {64, 128}; 1 <= total_tokens <= 2^24;
+ *   n_q_heads % n_kv_heads == 0; n_q_heads * (ceil(total_tokens/128) + num_seqs) < 2^31.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
  */
 int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,

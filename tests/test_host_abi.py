@@ -61,6 +61,7 @@ def test_prefill_validation(L):
     assert _prefill(L, n=0) == c["ATTN_ERR_SHAPE"]
     assert _prefill(L, batch=0) == c["ATTN_ERR_SHAPE"]
     assert _prefill(L, n=(1 << 24) + 1) == c["ATTN_ERR_SHAPE"]
+    assert _prefill(L, batch=1, hq=1 << 20, hkv=1, n=1 << 24) == c["ATTN_ERR_SHAPE"]  # items > 2^31
     assert _prefill(L, scale=0.0) == c["ATTN_ERR_SHAPE"]
     assert _prefill(L, scale=float("nan")) == c["ATTN_ERR_SHAPE"]
     assert _prefill(L, d=96) == c["ATTN_ERR_HEADDIM"]
@@ -82,7 +83,8 @@ def test_prefill_varlen_validation(L):
     c = _lib.status_codes()
     assert _varlen(L, cu=None) == c["ATTN_ERR_NULL"]
     assert _varlen(L, S=0) == c["ATTN_ERR_SHAPE"]
-    assert _varlen(L, S=1025) == c["ATTN_ERR_SHAPE"]
+    assert _varlen(L, S=513) == c["ATTN_ERR_SHAPE"]
+    assert _varlen(L, hq=1 << 20, hkv=1, T=1 << 24) == c["ATTN_ERR_SHAPE"]   # item count > 2^31
     assert _varlen(L, T=0) == c["ATTN_ERR_SHAPE"]
     assert _varlen(L, T=(1 << 24) + 1) == c["ATTN_ERR_SHAPE"]
     assert _varlen(L, d=96) == c["ATTN_ERR_HEADDIM"]
