@@ -78,7 +78,7 @@ def _f64(x) -> np.ndarray:
 
 
 def masked_attention(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray,
-                     scale: float, allowed: np.ndarray | None = None):
+                     scale: float, allowed: np.ndarray | None = None, softcap: float = 0.0):
     """Plain attention of some query rows against a key/value set.
 
     s_ij = scale * q_i . k_j   (page §"The bottleneck it attacks": S = QK^T/sqrt d)
@@ -86,7 +86,10 @@ def masked_attention(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray,
     O_i   = sum_{j allowed} exp(s_ij - LSE_i) v_j   (= softmax(s_i)^T V)
 
     ``allowed`` is a boolean (rows, keys) matrix; None means every key.
-    A row with no allowed key gets LSE = -inf and O = 0.
+    A row with no allowed key gets LSE = -inf and O = 0.  With softcap > 0
+    the scores are first soft-capped, s -> softcap * tanh(s / softcap) (page
+    §"Interaction with post-trained models": logit soft-capping is one of the
+    attention variants kernels support).
     Returns (O (rows, dv), LSE (rows,)), float64.
     """
     q_rows = _f64(q_rows)
@@ -99,6 +102,8 @@ def masked_attention(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray,
     if k.shape[0] == 0:
         return np.zeros((r, dv)), np.full((r,), -np.inf)
     s = scale * (q_rows @ k.T)                      # S, materialised
+    if softcap > 0:
+        s = softcap * np.tanh(s / softcap)
     if allowed is not None:
         s = np.where(allowed, s, -np.inf)
     m = s.max(axis=1)                               # row max (only for stability)
@@ -127,12 +132,32 @@ def _causal_allowed(r0: int, r1: int, ncols: int) -> np.ndarray:
     return cols <= rows
 
 
-def prefill(q, k, v, scale: float, causal: bool = True):
+def _window_allowed(r0: int, r1: int, ncols: int, causal: bool, window_left: int):
+    """Rows r0..r1-1 over keys 0..ncols-1: key j <= row i when causal, and
+    j >= i - window_left when a sliding window is set (window_left >= 0);
+    None when every key is allowed."""
+    if not causal and window_left < 0:
+        return None
+    rows = np.arange(r0, r1)[:, None]
+    cols = np.arange(ncols)[None, :]
+    ok = np.ones((r1 - r0, ncols), dtype=bool)
+    if causal:
+        ok &= cols <= rows
+    if window_left >= 0:
+        ok &= cols >= rows - window_left
+    return ok
+
+
+def prefill(q, k, v, scale: float, causal: bool = True, window_left: int = -1,
+            softcap: float = 0.0):
     """Attention forward over whole sequences (the prefill case).
 
     q: (B, n_q, N, d); k, v: (B, n_kv, N, d).  Returns O (B, n_q, N, d) and
     LSE (B, n_q, N), float64.  Causal: row i sees keys j <= i (page
-    §"Prefill: tiles, loop order and the tensor cores").
+    §"Prefill: tiles, loop order and the tensor cores").  Sliding window
+    (window_left >= 0): row i sees only keys j >= i - window_left; softcap > 0
+    soft-caps the scores (page §"Interaction with post-trained models", the
+    variants kernels support).
     """
     q = _f64(q)
     k = _f64(k)
@@ -149,16 +174,20 @@ def prefill(q, k, v, scale: float, causal: bool = True):
             for r0 in range(0, N, _ROW_BLOCK):
                 r1 = min(N, r0 + _ROW_BLOCK)
                 ncols = r1 if causal else N
-                allowed = _causal_allowed(r0, r1, ncols) if causal else None
+                if window_left < 0:
+                    allowed = _causal_allowed(r0, r1, ncols) if causal else None
+                else:
+                    allowed = _window_allowed(r0, r1, ncols, causal, window_left)
                 ob, lb = masked_attention(q[b, h, r0:r1], k[b, kh, :ncols],
-                                          v[b, kh, :ncols], scale, allowed)
+                                          v[b, kh, :ncols], scale, allowed, softcap)
                 o[b, h, r0:r1] = ob
                 lse[b, h, r0:r1] = lb
     return o, lse
 
 
 def prefill_rows(q, k, v, scale: float, causal: bool,
-                 rows: Iterable[tuple[int, int, int]]):
+                 rows: Iterable[tuple[int, int, int]], window_left: int = -1,
+                 softcap: float = 0.0):
     """The same definition as :func:`prefill`, for a sample of (b, h, i) rows.
 
     Used at sizes where every row would take too long on the CPU.  Returns
@@ -178,7 +207,9 @@ def prefill_rows(q, k, v, scale: float, causal: bool,
         kb, vb = _f64(k[b, kh]), _f64(v[b, kh])      # upcast once per (sequence, kv head)
         for idx, h, i in members:
             ncols = i + 1 if causal else N
-            ob, lb = masked_attention(_f64(q[b, h, i:i + 1]), kb[:ncols], vb[:ncols], scale, None)
+            lo = max(0, i - window_left) if window_left >= 0 else 0
+            ob, lb = masked_attention(_f64(q[b, h, i:i + 1]), kb[lo:ncols], vb[lo:ncols], scale,
+                                      None, softcap)
             o[idx] = ob[0]
             lse[idx] = lb[0]
     return o, lse
@@ -211,9 +242,12 @@ def gather_sequence(cache, block_table, b: int, kv_len: int, kv_head: int,
 
 
 def decode(q, k_cache, v_cache, block_table, kv_lens: Sequence[int],
-           scale: float, block_size: int = 0):
+           scale: float, block_size: int = 0, window_left: int = -1, softcap: float = 0.0):
     """Single-token decode: one query row per (sequence, query head) attends
-    to every cached token 0..kv_len-1 of its sequence.
+    to every cached token 0..kv_len-1 of its sequence.  The query is the
+    sequence's last token, position kv_len - 1, so a sliding window
+    (window_left >= 0) keeps tokens kv_len - 1 - window_left .. kv_len - 1;
+    softcap > 0 soft-caps the scores.
 
     q: (B, n_q, d).  Returns O (B, n_q, d) and LSE (B, n_q), float64.
     """
@@ -224,11 +258,12 @@ def decode(q, k_cache, v_cache, block_table, kv_lens: Sequence[int],
     lse = np.zeros((B, n_q))
     for b in range(B):
         L = int(kv_lens[b])
+        lo = max(0, L - 1 - window_left) if window_left >= 0 else 0
         for kh in range(n_kv):
-            kb = gather_sequence(k_cache, block_table, b, L, kh, block_size)
-            vb = gather_sequence(v_cache, block_table, b, L, kh, block_size)
+            kb = gather_sequence(k_cache, block_table, b, L, kh, block_size)[lo:]
+            vb = gather_sequence(v_cache, block_table, b, L, kh, block_size)[lo:]
             heads = [h for h in range(n_q) if _kv_head(h, n_q, n_kv) == kh]
-            ob, lb = masked_attention(q[b, heads], kb, vb, scale, None)
+            ob, lb = masked_attention(q[b, heads], kb, vb, scale, None, softcap)
             o[b, heads] = ob
             lse[b, heads] = lb
     return o, lse
@@ -236,7 +271,7 @@ def decode(q, k_cache, v_cache, block_table, kv_lens: Sequence[int],
 
 def decode_partials(q, k_cache, v_cache, block_table, kv_lens: Sequence[int],
                     scale: float, block_size: int,
-                    ranges: Sequence[Sequence[tuple[int, int]]]):
+                    ranges: Sequence[Sequence[tuple[int, int]]], softcap: float = 0.0):
     """Per-split partial results: the plain definition restricted to each
     split's token range (page §"Decode: a different bottleneck", split-KV).
 
@@ -258,7 +293,7 @@ def decode_partials(q, k_cache, v_cache, block_table, kv_lens: Sequence[int],
             heads = [h for h in range(n_q) if _kv_head(h, n_q, n_kv) == kh]
             for s, (t0, t1) in enumerate(ranges[b]):
                 ob, lb = masked_attention(q[b, heads], kb[t0:t1], vb[t0:t1],
-                                          scale, None)
+                                          scale, None, softcap)
                 o[s, b, heads] = ob
                 lse[s, b, heads] = lb
     return o, lse

@@ -101,7 +101,7 @@ def test_worked_example_blocks_and_combine(golden):
 # Brute force: scalar loops with math.exp / math.fsum.
 # ---------------------------------------------------------------------------
 
-def _brute_prefill(q, k, v, scale, causal):
+def _brute_prefill(q, k, v, scale, causal, window_left=-1, softcap=0.0):
     B, nq, N, d = q.shape
     nkv = k.shape[1]
     g = nq // nkv
@@ -112,7 +112,11 @@ def _brute_prefill(q, k, v, scale, causal):
             kh = h // g
             for i in range(N):
                 js = range(i + 1) if causal else range(N)
+                if window_left >= 0:
+                    js = [j for j in js if j >= i - window_left]
                 sc = [scale * math.fsum(q[b, h, i, t] * k[b, kh, j, t] for t in range(d)) for j in js]
+                if softcap > 0:
+                    sc = [softcap * math.tanh(x / softcap) for x in sc]
                 m = max(sc)
                 z = math.fsum(math.exp(x - m) for x in sc)
                 lse[b, h, i] = m + math.log(z)
@@ -260,6 +264,70 @@ def test_empty_sequence_and_empty_split():
     assert np.all(np.isneginf(lp[1, 1])) and np.all(op[1, 1] == 0)
     oc, lc = oracle.combine(op, lp)
     assert np.all(oc[0] == 0.0) and np.all(np.isneginf(lc[0]))
+
+
+# ---------------------------------------------------------------------------
+# Attention variants (page §"Interaction with post-trained models": sliding
+# windows and logit soft-capping are among the variants kernels support).
+# ---------------------------------------------------------------------------
+
+def _pin_variants():
+    """Sliding window and soft-capping against scalar brute force (math.tanh,
+    math.fsum), causal and not, GQA."""
+    rng = np.random.default_rng(17)
+    worst = 0.0
+    for N, nq, nkv, d, causal, W, cap in [(19, 2, 1, 4, True, 3, 0.0), (23, 4, 2, 8, True, 0, 0.0),
+                                          (17, 2, 2, 4, False, 5, 0.0), (21, 4, 1, 8, True, -1, 1.5),
+                                          (16, 2, 1, 4, True, 6, 2.0), (13, 2, 2, 8, False, -1, 0.7)]:
+        q = rng.standard_normal((1, nq, N, d)) * 2
+        k = rng.standard_normal((1, nkv, N, d))
+        v = rng.standard_normal((1, nkv, N, d))
+        ob, lb = _brute_prefill(q, k, v, 0.9, causal, W, cap)
+        oo, lo = oracle.prefill(q, k, v, 0.9, causal, window_left=W, softcap=cap)
+        worst = max(worst, float(np.abs(ob - oo).max()), float(np.abs(lb - lo).max()))
+    return worst
+
+
+def test_variants_brute_force():
+    assert _pin_variants() <= TOL
+
+
+def test_variant_closed_forms_and_limits():
+    x = W.make_prefill(1, 4, 2, 300, 16, seed=2)
+    q, k, v = x.q, x.k, x.v
+    # window 0: every row sees only itself -> O_i = v_i, LSE_i = s_ii
+    o, lse = oracle.prefill(q, k, v, x.scale, True, window_left=0)
+    qd, kd, vd = _f64(q), _f64(k), _f64(v)
+    for h in range(4):
+        assert np.abs(o[0, h] - vd[0, h // 2]).max() <= TOL
+        sii = x.scale * np.einsum("nd,nd->n", qd[0, h], kd[0, h // 2])
+        assert np.abs(lse[0, h] - sii).max() <= TOL
+    # a window covering the whole sequence changes nothing
+    o_full, l_full = oracle.prefill(q, k, v, x.scale, True)
+    o_w, l_w = oracle.prefill(q, k, v, x.scale, True, window_left=299)
+    assert np.abs(o_w - o_full).max() <= TOL and np.abs(l_w - l_full).max() <= TOL
+    # soft-capping with a huge cap is the identity on the scores (tanh(u) = u - u^3/3 + ...)
+    o_c, l_c = oracle.prefill(q, k, v, x.scale, True, softcap=1e7)
+    assert np.abs(o_c - o_full).max() <= 1e-10 and np.abs(l_c - l_full).max() <= 1e-10
+    # rows sampled one by one agree with whole prefill, window + cap
+    o_v, l_v = oracle.prefill(q, k, v, x.scale, True, window_left=40, softcap=3.0)
+    rows = [(0, 0, 0), (0, 3, 41), (0, 1, 299), (0, 2, 120)]
+    orow, lrow = oracle.prefill_rows(q, k, v, x.scale, True, rows, window_left=40, softcap=3.0)
+    for idx, (b, h, i) in enumerate(rows):
+        assert np.abs(orow[idx] - o_v[b, h, i]).max() <= TOL and abs(lrow[idx] - l_v[b, h, i]) <= TOL
+
+
+def test_decode_variants_equal_last_prefill_row():
+    N = 211
+    x = W.make_prefill(1, 6, 2, N, 16, seed=8)
+    kc = x.k[0].permute(1, 0, 2).unsqueeze(0).contiguous()
+    vc = x.v[0].permute(1, 0, 2).unsqueeze(0).contiguous()
+    for Wl, cap in [(50, 0.0), (-1, 2.5), (7, 1.0), (0, 0.0)]:
+        op, lp = oracle.prefill(x.q, x.k, x.v, x.scale, True, window_left=Wl, softcap=cap)
+        od, ld = oracle.decode(x.q[:, :, N - 1], kc, vc, None, [N], x.scale, window_left=Wl,
+                               softcap=cap)
+        assert np.abs(od - op[:, :, N - 1]).max() <= TOL
+        assert np.abs(ld - lp[:, :, N - 1]).max() <= TOL
 
 
 # ---------------------------------------------------------------------------
@@ -507,7 +575,7 @@ def _pins():
     return {"bruteforce": (_pin_bruteforce, TOL), "sdpa": (_pin_sdpa, 1e-12),
             "closed": (_pin_closed_forms, TOL), "gqa": (_pin_gqa, TOL),
             "combine": (_pin_combine, TOL), "append": (_pin_append, TOL),
-            "varlen": (_pin_varlen, TOL)}
+            "varlen": (_pin_varlen, TOL), "variants": (_pin_variants, TOL)}
 
 
 def _any_pin_fails():
@@ -529,7 +597,8 @@ def test_pins_pass_unmutated():
 @pytest.mark.parametrize("mutation", ["gqa_modulo", "strict_mask", "no_scale", "lse_no_max",
                                       "combine_unweighted", "gqa_off_by_one",
                                       "append_off_by_one", "append_not_attended",
-                                      "varlen_cross_sequence"])
+                                      "varlen_cross_sequence", "window_off_by_one",
+                                      "softcap_unscaled"])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     orig_ma = ref.masked_attention
     orig_comb = ref.combine
@@ -554,6 +623,16 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
                 lse = lse - s.max(axis=1)     # dropped the max term
             return o, lse
         monkeypatch.setattr(ref, "masked_attention", bad)
+    elif mutation == "window_off_by_one":
+        orig_wa = ref._window_allowed
+        monkeypatch.setattr(ref, "_window_allowed",
+                            lambda r0, r1, n, c, w: orig_wa(r0, r1, n, c, w - 1 if w > 0 else w))
+    elif mutation == "softcap_unscaled":
+        def bad_cap(q, k, v, scale, allowed=None, softcap=0.0):
+            # cap * tanh(s) instead of cap * tanh(s / cap): the same as the
+            # right formula applied to scores scaled by cap
+            return orig_ma(q, k, v, scale * softcap if softcap > 0 else scale, allowed, softcap)
+        monkeypatch.setattr(ref, "masked_attention", bad_cap)
     elif mutation == "varlen_cross_sequence":
         # sequences attend to the previous one's rows too (no per-example masking)
         monkeypatch.setattr(ref, "_seq_bounds", lambda cu: [(0, int(b)) for b in
