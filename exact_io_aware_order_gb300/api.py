@@ -40,8 +40,10 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
 
 def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
             causal: bool = True, out: Optional[torch.Tensor] = None,
-            lse: Optional[torch.Tensor] = None, stream=None):
-    """Attention forward over whole sequences (``attn_prefill``).
+            lse: Optional[torch.Tensor] = None, stream=None, window_left: int = -1,
+            softcap: float = 0.0):
+    """Attention forward over whole sequences (``attn_prefill``; with a
+    sliding window or soft-capping, ``attn_prefill_ex``).
 
     q: (B, n_q, N, d) bf16; k, v: (B, n_kv, N, d) bf16.  Returns
     (O (B, n_q, N, d) fp32, LSE (B, n_q, N) fp32, natural log).
@@ -61,10 +63,13 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[f
         lse = torch.empty((B, n_q, N), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32, 4)
     _need(lse, "lse", torch.float32, 3)
-    st = lib().attn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                            lse.data_ptr(), B, n_q, n_kv, N, d, float(scale), int(bool(causal)),
-                            _stream(stream))
-    check("attn_prefill", st)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, n_q, n_kv,
+            N, d, float(scale), int(bool(causal)))
+    if window_left == -1 and softcap == 0.0:
+        check("attn_prefill", lib().attn_prefill(*args, _stream(stream)))
+    else:
+        check("attn_prefill_ex", lib().attn_prefill_ex(*args, int(window_left), float(softcap),
+                                                       _stream(stream)))
     return out, lse
 
 
@@ -109,16 +114,25 @@ def decode_num_splits(batch: int, n_kv_heads: int, max_kv_len: int, num_sms: int
                                             int(num_sms)))
 
 
-def split_ranges(kv_len: int, num_splits: int):
-    """Token range of every split under the library's split rule:
-    c = roundup(ceil(len / S), 16); split s covers [s*c, min((s+1)*c, len))."""
-    per = -(-kv_len // num_splits)
+def split_ranges(kv_len: int, num_splits: int, window_left: int = -1):
+    """Tokens attended by every split under the library's split rule:
+    c = roundup(ceil(len / S), 16); split s covers [s*c, min((s+1)*c, len)).
+    With a sliding window the rule applies from lo16 (the window's first
+    token lo rounded down to a multiple of 16) and tokens below lo are dropped."""
+    lo = max(0, kv_len - 1 - window_left) if window_left >= 0 else 0
+    lo16 = lo // 16 * 16
+    n = kv_len - lo16
+    per = -(-n // num_splits)
     c = -(-per // 16) * 16
-    return [(min(s * c, kv_len), min(s * c + c, kv_len)) for s in range(num_splits)]
+    out = []
+    for s in range(num_splits):
+        a, b = lo16 + min(s * c, n), lo16 + min(min(s * c, n) + c, n)
+        out.append((min(max(a, lo), b), b))
+    return out
 
 
 def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
-                 o_partial, lse_partial, stream, new_kv=None):
+                 o_partial, lse_partial, stream, new_kv=None, window_left=-1, softcap=0.0):
     """Shape checks and marshalling shared by the plain and appending decode."""
     _need(q, "q", _BF16, 3)
     _need(k_cache, "k_cache", _BF16, 4)
@@ -165,7 +179,12 @@ def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_l
     tail = (kv_lens.data_ptr(), int(num_splits), o_partial.data_ptr(), lse_partial.data_ptr(), B,
             n_q, n_kv, d, block_size, max_blocks, num_blocks, int(max_kv_len), float(scale),
             _stream(stream))
-    if new_kv is None:
+    if new_kv is None and (window_left != -1 or softcap != 0.0):
+        name = "attn_decode_splitkv_ex"
+        st = lib().attn_decode_splitkv_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                          bt_ptr, *tail[:-1], int(window_left), float(softcap),
+                                          tail[-1])
+    elif new_kv is None:
         name = "attn_decode_splitkv"
         st = lib().attn_decode_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), bt_ptr,
                                        *tail)
@@ -182,8 +201,10 @@ def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                    kv_lens: torch.Tensor, block_table: Optional[torch.Tensor] = None,
                    num_splits: int = 0, max_kv_len: Optional[int] = None,
                    scale: Optional[float] = None, o_partial: Optional[torch.Tensor] = None,
-                   lse_partial: Optional[torch.Tensor] = None, stream=None):
-    """Split-KV single-token decode (``attn_decode_splitkv``).
+                   lse_partial: Optional[torch.Tensor] = None, stream=None, window_left: int = -1,
+                   softcap: float = 0.0):
+    """Split-KV single-token decode (``attn_decode_splitkv``; with a sliding
+    window or soft-capping, ``attn_decode_splitkv_ex``).
 
     q: (B, n_q, d) bf16.  Paged: k_cache, v_cache (num_blocks, block_size,
     n_kv, d) with block_table (B, max_blocks) int32; contiguous (block_table
@@ -191,7 +212,7 @@ def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     Returns (o_partial (S, B, n_q, d), lse_partial (S, B, n_q)), fp32.
     """
     return _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
-                        o_partial, lse_partial, stream)
+                        o_partial, lse_partial, stream, window_left=window_left, softcap=softcap)
 
 
 def decode_append_splitkv(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,

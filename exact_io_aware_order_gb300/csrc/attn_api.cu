@@ -146,12 +146,19 @@ int attn_decode_num_splits(int batch, int n_kv_heads, int max_kv_len, int num_sm
   return split_policy(batch, n_kv_heads, max_kv_len, num_sms);
 }
 
-int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o, float* lse,
+namespace {
+
+bool valid_variant(int window_left, float softcap) {
+  return window_left >= -1 && softcap >= 0.f && softcap < 3.0e38f;
+}
+
+int prefill_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o, float* lse,
                  int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim, float scale,
-                 int causal, void* stream) {
+                 int causal, int window_left, float softcap, void* stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || seqlen < 1 || seqlen > (1 << 24) ||
-      (long long)batch * n_q_heads > (1LL << 20) || !valid_scale(scale))
+      (long long)batch * n_q_heads > (1LL << 20) || !valid_scale(scale) ||
+      !valid_variant(window_left, softcap))
     return ATTN_ERR_SHAPE;
   // work items (query tiles x heads x sequences) are counted in 32 bits
   if ((long long)batch * n_q_heads * ((seqlen + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_SHAPE;
@@ -164,8 +171,26 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
   if (!ds) return st;
   attn::PrefillArgs a{q, k, v, o, lse, batch, n_q_heads, n_kv_heads, seqlen, head_dim, scale,
                       causal ? 1 : 0};
+  a.window_left = window_left;
+  a.softcap = softcap;
   if (attn::launch_prefill(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
+}
+
+}  // namespace
+
+int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o, float* lse,
+                 int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim, float scale,
+                 int causal, void* stream) {
+  return prefill_impl(q, k, v, o, lse, batch, n_q_heads, n_kv_heads, seqlen, head_dim, scale,
+                      causal, -1, 0.f, stream);
+}
+
+int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+                    float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim,
+                    float scale, int causal, int window_left, float softcap, void* stream) {
+  return prefill_impl(q, k, v, o, lse, batch, n_q_heads, n_kv_heads, seqlen, head_dim, scale,
+                      causal, window_left, softcap, stream);
 }
 
 int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
@@ -204,9 +229,10 @@ int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_n
                 const int32_t* kv_lens, int num_splits, float* o_partial, float* lse_partial,
                 int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                 int max_blocks_per_seq, int num_blocks, int max_kv_len, float scale,
-                void* stream, bool append) {
+                void* stream, bool append, int window_left = -1, float softcap = 0.f) {
   if (!q || !k_cache || !v_cache || !kv_lens || !o_partial || !lse_partial) return ATTN_ERR_NULL;
   if (append && (!k_new || !v_new)) return ATTN_ERR_NULL;
+  if (!valid_variant(window_left, softcap)) return ATTN_ERR_SHAPE;
   if (append && (!aligned(k_new, 16) || !aligned(v_new, 16))) return ATTN_ERR_ALIGN;
   const bool paged = block_table != nullptr;
   if (batch < 1 || batch > 65535 || n_q_heads < 1 || n_kv_heads < 1 || n_kv_heads > 65535 ||
@@ -234,6 +260,8 @@ int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_n
     a.k_new = k_new;
     a.v_new = v_new;
   }
+  a.window_left = window_left;
+  a.softcap = softcap;
   if (attn::launch_decode(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
@@ -248,6 +276,18 @@ int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn
   return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_table, kv_lens, num_splits,
                      o_partial, lse_partial, batch, n_q_heads, n_kv_heads, head_dim, block_size,
                      max_blocks_per_seq, num_blocks, max_kv_len, scale, stream, false);
+}
+
+int attn_decode_splitkv_ex(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                           const int32_t* block_table, const int32_t* kv_lens, int num_splits,
+                           float* o_partial, float* lse_partial, int batch, int n_q_heads,
+                           int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                           int num_blocks, int max_kv_len, float scale, int window_left,
+                           float softcap, void* stream) {
+  return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_table, kv_lens, num_splits,
+                     o_partial, lse_partial, batch, n_q_heads, n_kv_heads, head_dim, block_size,
+                     max_blocks_per_seq, num_blocks, max_kv_len, scale, stream, false, window_left,
+                     softcap);
 }
 
 int attn_decode_append_splitkv(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,

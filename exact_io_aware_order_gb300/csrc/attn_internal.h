@@ -32,6 +32,10 @@ struct PrefillArgs {
   // of packed rows and sequence s occupies rows [cu_seqlens[s], cu_seqlens[s+1]).
   const int32_t* cu_seqlens = nullptr;
   int num_seqs = 0;
+  // Variants: a sliding window (row i sees keys j >= i - window_left; -1 =
+  // none) and logit soft-capping (s -> softcap * tanh(s / softcap); 0 = off).
+  int window_left = -1;
+  float softcap = 0.f;
 };
 
 // Largest number of packed sequences per variable-length prefill call.
@@ -56,6 +60,10 @@ struct DecodeArgs {
   // writable cache pointers.
   const uint16_t* k_new = nullptr;
   const uint16_t* v_new = nullptr;
+  // Variants, as for prefill; the query is the sequence's last token, so the
+  // window keeps tokens kv_len - 1 - window_left .. kv_len - 1.
+  int window_left = -1;
+  float softcap = 0.f;
 };
 
 struct CombineArgs {

@@ -154,10 +154,16 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
   const int pos_new = len;  // the appended token's position
   if (append) len += 1;     // the new token attends to itself too
-  const int per = (len + S - 1) / S;
+  // A sliding window keeps tokens lo_tok .. len-1; the splits cover
+  // [lo16, len) with lo16 = lo_tok rounded down to the split granule, and
+  // tokens below lo_tok are masked.
+  const int lo_tok = a.window_left >= 0 ? max(0, len - 1 - a.window_left) : 0;
+  const int lo16 = lo_tok / kSplitGranule * kSplitGranule;
+  const int n_att = len - lo16;
+  const int per = (n_att + S - 1) / S;
   const int chunk = (per + kSplitGranule - 1) / kSplitGranule * kSplitGranule;
-  const int t0 = min(split * chunk, len);
-  const int t1 = min(t0 + chunk, len);
+  const int t0 = lo16 + min(split * chunk, n_att);
+  const int t1 = lo16 + min(min(split * chunk, n_att) + chunk, n_att);
   const int n_tok = t1 - t0;
 
   float* o_out = a.o_partial + (((size_t)split * a.batch + b) * a.n_q_heads + (size_t)kvh * g) * D;
@@ -319,7 +325,11 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
       const int c = kk * 16 + (lane >> 4) * 8;
       ldsm_x4(smem_u32(sq + r * L::kQRowBytes + c * 2), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
     }
-    const float sl2 = a.scale * kLog2e;
+    // With soft-capping the scores become tanh(s * scale / softcap) and the
+    // factor softcap (times log2 e) moves into sl2.
+    const bool capped = a.softcap > 0.f;
+    const float sl2 = capped ? a.softcap * kLog2e : a.scale * kLog2e;
+    const float cap_in2 = capped ? 2.f * kLog2e * a.scale / a.softcap : 0.f;
     float m_r[2] = {-INFINITY, -INFINITY};  // running max (log2 domain) of rows gid, gid+8
     float l_r[2] = {0.f, 0.f};
     float acc[D / 8][4];
@@ -359,14 +369,21 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
           mma16816(s[0], qa[kk], b0, b1);
           mma16816(s[1], qa[kk], b2, b3);
         }
-        // ---- mask tokens past the end, online softmax update ----
+        if (capped) {
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[n][e] = tanh_from_exp2(s[n][e] * cap_in2);
+        }
+        // ---- mask tokens past the end or left of the window, online softmax update ----
+        const int lo_rel = lo_tok - (base + r0);  // first token of the warp's 16 in the window
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int tok = n * 8 + quad * 2 + (e & 1);
-            if (tok >= vc) s[n][e] = -INFINITY;
+            if (tok >= vc || tok < lo_rel) s[n][e] = -INFINITY;
             mx[e >> 1] = fmaxf(mx[e >> 1], s[n][e]);
           }
         bool grow = false;
@@ -375,8 +392,8 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int r = 0; r < 2; ++r) {
           mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
           mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-          m_new[r] = fmaxf(m_r[r], mx[r] * sl2);  // finite: token 0 of the warp is valid
-          grow |= m_new[r] - m_r[r] > kRescaleThreshold;  // always true on the first stage
+          m_new[r] = fmaxf(m_r[r], mx[r] * sl2);  // -inf only while every token was masked
+          grow |= m_new[r] - m_r[r] > kRescaleThreshold;  // true at the first unmasked token
         }
         // Keep the stale max unless some row of the warp grew by more than 2^8.
         const bool rescale = __any_sync(0xffffffffu, grow);
@@ -390,12 +407,15 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         float rs[2] = {0.f, 0.f};
         uint32_t pa[4];
+        // Rows that have seen only masked tokens keep m = -inf: reference 0.
+        const float mr0 = m_r[0] == -INFINITY ? 0.f : m_r[0];
+        const float mr1 = m_r[1] == -INFINITY ? 0.f : m_r[1];
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
-          const float p0 = ex2_approx(fmaf(s[n][0], sl2, -m_r[0]));
-          const float p1 = ex2_approx(fmaf(s[n][1], sl2, -m_r[0]));
-          const float p2 = ex2_approx(fmaf(s[n][2], sl2, -m_r[1]));
-          const float p3 = ex2_approx(fmaf(s[n][3], sl2, -m_r[1]));
+          const float p0 = ex2_approx(fmaf(s[n][0], sl2, -mr0));
+          const float p1 = ex2_approx(fmaf(s[n][1], sl2, -mr0));
+          const float p2 = ex2_approx(fmaf(s[n][2], sl2, -mr1));
+          const float p3 = ex2_approx(fmaf(s[n][3], sl2, -mr1));
           rs[0] += p0 + p1;
           rs[1] += p2 + p3;
           pa[2 * n + 0] = pack_bf16x2(p0, p1);  // row gid,   tokens 8n + 2q, +1

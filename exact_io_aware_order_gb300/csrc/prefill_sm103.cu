@@ -98,8 +98,10 @@ struct PrefillParams {
   float* o;
   float* lse;
   int batch, n_q_heads, n_kv_heads, seqlen;
-  float sl2;  // scale * log2(e)
+  float sl2;  // scale * log2(e); with soft-capping, softcap * log2(e)
   int causal;
+  int window_left;  // sliding window: row i sees keys j >= i - window_left (-1: none)
+  float cap_in2;    // soft-capping: 2 log2(e) scale / softcap (the tanh argument's factor)
   int n_q_tiles;    // ceil(seqlen / 128)
   int total_tiles;  // n_q_tiles * batch * n_q_heads (padded mode)
   const int32_t* cu_seqlens;  // packed mode: (num_seqs + 1) row offsets
@@ -116,6 +118,7 @@ struct Tile {
   int len;   // sequence length (keys and queries)
   int zq;    // Q / O tensor-map plane (sequence * n_q_heads + head)
   int zk;    // K / V tensor-map plane
+  int j0;    // first key tile visited (> 0 only with a sliding window)
   int n;     // key tiles visited (>= 1)
 };
 
@@ -135,7 +138,7 @@ struct SeqTables {
 // L2.  (A globally longest-first order balances better but spreads the work
 // over every sequence at once; claiming items dynamically balances too but
 // costs more per tile; both measured slower.)
-template <bool VARLEN>
+template <bool VARLEN, bool VARIANT>
 __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const SeqTables& st) {
   Tile t;
   if constexpr (!VARLEN) {
@@ -170,6 +173,13 @@ __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const Seq
     t.zk = h / (p.n_q_heads / p.n_kv_heads);
     t.n = p.causal ? (qt + 1) : tiles;
   }
+  // A sliding window skips the key tiles left of every row's window: the
+  // tile's first row sees keys from qrel - window_left on.
+  t.j0 = 0;
+  if constexpr (VARIANT) {
+    if (p.window_left >= 0 && t.qrel > p.window_left) t.j0 = (t.qrel - p.window_left) / kBN;
+    t.n -= t.j0;
+  }
   return t;
 }
 
@@ -182,7 +192,9 @@ __device__ __forceinline__ int item_of(int r, int total) {
   return w < total ? w : -1;
 }
 
-template <int D, bool VARLEN>
+// VARIANT: the kernel built for a sliding window and / or soft-capping (both
+// set at run time); the plain kernel has neither in its code.
+template <int D, bool VARLEN, bool VARIANT>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -321,13 +333,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         c.r = 0;
         c.j = 0;
         c.w = item_of(0, total);
-        if (c.w >= 0) c.t = tile_of<VARLEN>(c.w, p, seqt);
+        if (c.w >= 0) c.t = tile_of<VARLEN, VARIANT>(c.w, p, seqt);
       };
       auto advance = [&](Cursor& c) {
         if (++c.j == c.t.n) {
           c.j = 0;
           c.w = item_of(++c.r, total);
-          if (c.w >= 0) c.t = tile_of<VARLEN>(c.w, p, seqt);
+          if (c.w >= 0) c.t = tile_of<VARLEN, VARIANT>(c.w, p, seqt);
         }
       };
       int nq = 0, nk = 0, nv = 0;  // tiles issued
@@ -350,7 +362,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           if (!load_tile(&tm_q, L::kQ, kQFull, kQEmpty, RQ, nq, kc.t.row0, kc.t.zq)) return false;
           ++nq;
         }
-        if (!load_tile(&tm_k, L::kK, kKFull, kKEmpty, RK, nk, kc.t.kv0 + kc.j * kBN, kc.t.zk))
+        if (!load_tile(&tm_k, L::kK, kKFull, kKEmpty, RK, nk, kc.t.kv0 + (kc.t.j0 + kc.j) * kBN,
+                       kc.t.zk))
           return false;
         ++nk;
         advance(kc);
@@ -358,7 +371,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       };
       bool ok = load_k() && load_k();
       while (ok && vc.w >= 0) {
-        ok = load_tile(&tm_v, L::kV, kVFull, kVEmpty, RV, nv, vc.t.kv0 + vc.j * kBN, vc.t.zk);
+        ok = load_tile(&tm_v, L::kV, kVFull, kVEmpty, RV, nv, vc.t.kv0 + (vc.t.j0 + vc.j) * kBN,
+                       vc.t.zk);
         if (!ok) break;
         ++nv;
         advance(vc);
@@ -382,7 +396,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int r = 0; ok; ++r) {
         const int w = item_of(r, total);
         if (w < 0) break;
-        const Tile t = tile_of<VARLEN>(w, p, seqt);
+        const Tile t = tile_of<VARLEN, VARIANT>(w, p, seqt);
         const int qs = r % RQ;
         if (!mbar_wait(bar(kQFull + qs), (r / RQ) & 1, ctl)) { ok = false; break; }
         const uint32_t q_lo = sw128_desc_lo(smem_u32(smem + L::kQ + qs * L::kTileBytes), 16);
@@ -419,7 +433,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int r = 0; ok; ++r) {
         const int w = item_of(r, total);
         if (w < 0) break;
-        const int n = tile_of<VARLEN>(w, p, seqt).n;
+        const int n = tile_of<VARLEN, VARIANT>(w, p, seqt).n;
         for (int j = 0; j < n; ++j, ++g) {
           const int b = g % kSBuf, slot = g % RV;
           if (!mbar_wait(bar(kPFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
@@ -458,7 +472,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int r = 0; ok; ++r) {
       const int w = item_of(r, total);
       if (w < 0) break;
-      const Tile t = tile_of<VARLEN>(w, p, seqt);
+      const Tile t = tile_of<VARLEN, VARIANT>(w, p, seqt);
       const int q0 = t.qrel, q_row = q0 + row;  // indices within the sequence
       float m = -INFINITY, l = 0.f;   // running max (log2 domain) and sum of the row
       for (int j = 0; j < t.n; ++j, ++g) {
@@ -478,8 +492,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
             for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[c][i]);
         }
-        const int kv0 = j * kBN;
-        if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > t.len)) {
+        const int kv0 = (t.j0 + j) * kBN;  // first key of the tile, within the sequence
+        if constexpr (VARIANT) {
+          if (p.cap_in2 != 0.f) {
+            // s -> softcap * tanh(s * scale / softcap); the factor softcap
+            // (and log2 e) is in sl2, so s becomes the tanh.
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) s[c] = tanh_from_exp2(s[c] * p.cap_in2);
+          }
+          const bool hi_edge = p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > t.len);
+          const bool lo_edge = p.window_left >= 0 && kv0 < q0 + kBM - 1 - p.window_left;
+          if (hi_edge || lo_edge) {
+            const int lim = !hi_edge ? kBN : p.causal ? (q_row - kv0) : (t.len - 1 - kv0);
+            const int lo = lo_edge ? (q_row - p.window_left - kv0) : -1;  // first allowed column
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+              if (c > lim || c < lo) s[c] = -INFINITY;
+          }
+        } else if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > t.len)) {
           const int lim = p.causal ? (q_row - kv0) : (t.len - 1 - kv0);  // last allowed column
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
@@ -511,7 +541,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // P = exp2(s * scale * log2e - m): packed FMA for the argument, MUFU ex2,
         // packed into bf16 pairs over the first 64 columns of the buffer; the row
         // sum uses four packed chains.
-        const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m, -m);
+        // A row whose keys in this item's tiles so far were all outside its
+        // window has m = -inf (all its P are 0): take 0 as its reference.
+        const float m_ref = (VARIANT && m == -INFINITY) ? 0.f : m;
+        const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m_ref, -m_ref);
         float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
 #pragma unroll
@@ -575,7 +608,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int r = 0; ok; ++r) {
       const int w = item_of(r, total);
       if (w < 0) break;
-      const Tile t = tile_of<VARLEN>(w, p, seqt);
+      const Tile t = tile_of<VARLEN, VARIANT>(w, p, seqt);
       if (!mbar_wait_warp(bar(kOFull), r & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       uint32_t acc[D / 32][32];
@@ -689,14 +722,14 @@ bool make_out_map(CUtensorMap* m, void* base, int D, int rows, int planes) {
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool VARLEN>
+template <int D, bool VARLEN, bool VARIANT>
 cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   using L = PrefillSmem<D, VARLEN>;
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VARLEN>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VARLEN, VARIANT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
@@ -714,8 +747,10 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   pp.n_q_heads = a.n_q_heads;
   pp.n_kv_heads = a.n_kv_heads;
   pp.seqlen = a.seqlen;
-  pp.sl2 = a.scale * kLog2e;
+  pp.sl2 = a.softcap > 0.f ? a.softcap * kLog2e : a.scale * kLog2e;
   pp.causal = a.causal;
+  pp.window_left = a.window_left;
+  pp.cap_in2 = a.softcap > 0.f ? 2.f * kLog2e * a.scale / a.softcap : 0.f;
   pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM;
   pp.total_tiles = pp.n_q_tiles * a.batch * a.n_q_heads;
   pp.cu_seqlens = a.cu_seqlens;
@@ -727,17 +762,24 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   // on the device, so every SM gets a CTA (those without items exit at once).
   const int sms = std::max(ctx.num_sms, 1);
   const unsigned grid = (unsigned)(VARLEN ? sms : std::min(pp.total_tiles, sms));
-  prefill_kernel<D, VARLEN><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, mo, pp);
+  prefill_kernel<D, VARLEN, VARIANT><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, mo, pp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+template <int D, bool VARLEN>
+cudaError_t launch_prefill_cap(const PrefillArgs& a, const LaunchCtx& ctx) {
+  const bool variant = a.softcap > 0.f || a.window_left >= 0;
+  return variant ? launch_prefill_t<D, VARLEN, true>(a, ctx)
+                 : launch_prefill_t<D, VARLEN, false>(a, ctx);
+}
+
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx) {
   const bool varlen = a.cu_seqlens != nullptr;
   if (a.head_dim == 128)
-    return varlen ? launch_prefill_t<128, true>(a, ctx) : launch_prefill_t<128, false>(a, ctx);
-  return varlen ? launch_prefill_t<64, true>(a, ctx) : launch_prefill_t<64, false>(a, ctx);
+    return varlen ? launch_prefill_cap<128, true>(a, ctx) : launch_prefill_cap<128, false>(a, ctx);
+  return varlen ? launch_prefill_cap<64, true>(a, ctx) : launch_prefill_cap<64, false>(a, ctx);
 }
 
 }  // namespace attn

@@ -346,6 +346,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // max of three (PTX max.f32 with three sources).
+// MUFU reciprocal (approximate).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh(u) from the identity tanh(u) = 1 - 2 / (exp(2u) + 1), with the
+// argument pre-multiplied: pass v = 2 * log2(e) * u.  Overflow of exp2 for
+// large u gives 1, underflow for very negative u gives -1; the absolute
+// error is a few 1e-7.
+__device__ __forceinline__ float tanh_from_exp2(float v) {
+  return fmaf(-2.f, rcp_approx(ex2_approx(v) + 1.f), 1.f);
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

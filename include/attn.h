@@ -88,6 +88,22 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
                  int head_dim, float scale, int causal, void* stream);
 
 /*
+ * attn_prefill_ex -- attn_prefill with the attention variants of the page's
+ * section "Interaction with post-trained models" (sliding windows and logit
+ * soft-capping are among the variants current kernels support).
+ *
+ *   window_left: -1 for none; otherwise row i attends only to keys
+ *                j >= i - window_left (with causal, i - window_left <= j <= i)
+ *   softcap    : 0 for none; otherwise each scaled score s = scale * q.k is
+ *                replaced by softcap * tanh(s / softcap) before the softmax
+ * Everything else, and the errors, as attn_prefill (a negative window_left
+ * other than -1, or a negative or non-finite softcap, is ATTN_ERR_SHAPE).
+ */
+int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+                    float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim,
+                    float scale, int causal, int window_left, float softcap, void* stream);
+
+/*
  * attn_prefill_varlen -- prefill of several sequences packed end to end
  * without padding (variable-length batch).
  *
@@ -166,6 +182,23 @@ int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn
                         float* o_partial, float* lse_partial, int batch, int n_q_heads,
                         int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
                         int num_blocks, int max_kv_len, float scale, void* stream);
+
+/*
+ * attn_decode_splitkv_ex -- attn_decode_splitkv with the variants of
+ * attn_prefill_ex.  The query is the sequence's last token (position
+ * kv_len - 1), so a window keeps tokens lo = max(0, kv_len - 1 - window_left)
+ * .. kv_len - 1.  With a window the split rule applies to tokens
+ * [lo16, kv_len), lo16 = lo rounded down to a multiple of 16: c =
+ * roundup(ceil((kv_len - lo16) / S), 16), split s covers [lo16 + s*c,
+ * min(lo16 + (s+1)*c, kv_len)), and tokens below lo carry no weight.
+ */
+int attn_decode_splitkv_ex(const attn_bf16* q, const attn_bf16* k_cache,
+                           const attn_bf16* v_cache, const int32_t* block_table,
+                           const int32_t* kv_lens, int num_splits, float* o_partial,
+                           float* lse_partial, int batch, int n_q_heads, int n_kv_heads,
+                           int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                           int max_kv_len, float scale, int window_left, float softcap,
+                           void* stream);
 
 /*
  * attn_decode_append_splitkv -- split-KV single-token decode that first

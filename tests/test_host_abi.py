@@ -72,6 +72,32 @@ def test_prefill_validation(L):
     assert _prefill(L, lse=P + 2) == c["ATTN_ERR_ALIGN"]
 
 
+def test_variant_validation(L):
+    c = _lib.status_codes()
+    ex = lambda w, cap: L.attn_prefill_ex(P, P, P, P, P, 1, 4, 2, 128, 128, 0.1, 1, w, cap, None)
+    assert ex(-2, 0.0) == c["ATTN_ERR_SHAPE"]
+    assert ex(0, -1.0) == c["ATTN_ERR_SHAPE"]
+    assert ex(0, float("nan")) == c["ATTN_ERR_SHAPE"]
+    assert ex(0, float("inf")) == c["ATTN_ERR_SHAPE"]
+    assert L.attn_prefill_ex(None, P, P, P, P, 1, 4, 2, 128, 128, 0.1, 1, 5, 1.0, None) == \
+        c["ATTN_ERR_NULL"]
+    dx = lambda w, cap: L.attn_decode_splitkv_ex(P, P, P, P, P, 4, P, P, 2, 8, 2, 128, 16, 8, 16,
+                                                 128, 0.1, w, cap, None)
+    assert dx(-3, 0.0) == c["ATTN_ERR_SHAPE"] and dx(4, -0.5) == c["ATTN_ERR_SHAPE"]
+
+
+@pytest.mark.parametrize("kv_len,S,W", [(100, 3, 10), (1000, 7, 0), (33, 2, 16), (5000, 9, 4095),
+                                        (17, 4, 100), (0, 3, 5), (64, 1, 15)])
+def test_split_rule_with_window(kv_len, S, W):
+    from exact_io_aware_order_gb300.api import split_ranges
+
+    r = split_ranges(kv_len, S, W)
+    lo = max(0, kv_len - 1 - W)
+    covered = [t for a, b in r for t in range(a, b)]
+    assert covered == list(range(lo, kv_len))          # exactly the window, in order
+    assert all(a % 16 == 0 or a == lo for a, b in r if a < b)
+
+
 def _varlen(L, **kw):
     a = dict(q=P, k=P, v=P, o=P, lse=P, cu=P, S=3, T=500, hq=4, hkv=2, d=128, scale=0.1, causal=1)
     a.update(kw)
