@@ -241,6 +241,8 @@ def run_gb300(args, rank: int, world: int, dist):
     attn.check_device_status()
     app = time_decode_append(args, attn, dq, caches, dec, S, op, lp, sweep, sweep_out, dist, dev)
     vl = time_prefill_varlen(args, attn, W, dist, dev) if args.workload == "qwen" else None
+    var = time_variants(args, attn, q, k, v, x.scale, o, lse, dq, caches, dec, S, op, lp, sweep,
+                        sweep_out, dist, dev) if args.workload == "qwen" else None
     total_ms = t_start.elapsed_time(t_end)
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[4].elapsed_time(e[2]) for e in evs]
@@ -287,6 +289,11 @@ def run_gb300(args, rank: int, world: int, dist):
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
+    if var is not None:
+        for v_ in var["prefill"].values():
+            v_["frac"] = round(v_["value"] / peaks["bf16_tflops"], 4)
+        var["decode"]["frac"] = round(var["decode"]["value"] / peaks["hbm_gbs"], 4)
+        result["variants"] = var
     if vl is not None:
         vl["roofline"]["peak"] = peaks["bf16_tflops"]
         vl["roofline"]["frac"] = round(vl["roofline"]["achieved"] / peaks["bf16_tflops"], 4)
@@ -300,6 +307,64 @@ def run_gb300(args, rank: int, world: int, dist):
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist)
     return result
+
+
+def time_variants(args, attn, q, k, v, scale, o, lse, dq, caches, dec, S, op, lp, sweep, sweep_out,
+                  dist, dev):
+    """The attention variants on the step's shapes: prefill with a 4096-token
+    sliding window and a soft cap of 50, and the decode with the same window.
+    FLOPs count the keys each row actually sees (4 d per query-key pair and
+    head); decode bytes count the K/V rows inside the window."""
+    import torch
+
+    Wl, cap = 4095, 50.0
+    B, Hq, N, D = q.shape
+    keys = sum(min(i + 1, Wl + 1) for i in range(N))
+    flops = 4.0 * D * Hq * B * keys
+    n = max(3, min(args.steps, 100))
+    world = dist.get_world_size() if dist is not None else 1
+
+    def timed(fn, before=None):
+        for i in range(3):
+            fn(i)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        for i in range(n):
+            if before is not None:
+                before()
+            evs[i][0].record()
+            fn(i)
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        attn.check_device_status()
+        (tot,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
+        return tot
+
+    full = 4.0 * D * Hq * B * sum(i + 1 for i in range(N))
+    pre = {}
+    for name, (w_, c_, fl) in {"window": (Wl, 0.0, flops), "softcap": (-1, cap, full),
+                               "window+softcap": (Wl, cap, flops)}.items():
+        t = timed(lambda i: attn.prefill(q, k, v, scale, True, out=o, lse=lse, window_left=w_,
+                                         softcap=c_))
+        pre[name] = {"value": round(job_rate(fl, n, world, t) / 1e12, 2), "unit": "TFLOP/s",
+                     "window_left": w_, "softcap": c_, "flops_per_launch": fl,
+                     "avg_launch_ms": round(t / n, 4)}
+    Bd, Hqd, Dd = dq.shape
+    lens = dec.kv_lens.to(dev)
+    att = sum(min(int(n_), Wl + 1) for n_ in dec.kv_lens.tolist())
+    dbytes = att * dec.n_kv * Dd * 2 * 2 + dq.numel() * 2 + Bd * Hqd * (Dd + 1) * 4
+    t_dec = timed(lambda i: attn.decode_splitkv(dq, caches[i % len(caches)][0],
+                                                caches[i % len(caches)][1], lens, None,
+                                                num_splits=S, scale=dec.scale, o_partial=op,
+                                                lse_partial=lp, window_left=Wl),
+                  before=lambda: torch.sum(sweep, dim=0, out=sweep_out))
+    return {"prefill": pre,
+            "decode": {"value": round(job_rate(dbytes, n, world, t_dec) / 1e9, 1), "unit": "GB/s",
+                       "window_left": Wl, "bytes_per_launch": dbytes,
+                       "avg_launch_us": round(t_dec / n * 1e3, 2)}}
 
 
 def time_prefill_varlen(args, attn, W, dist, dev):

@@ -138,7 +138,11 @@ struct SeqTables {
 // L2.  (A globally longest-first order balances better but spreads the work
 // over every sequence at once; claiming items dynamically balances too but
 // costs more per tile; both measured slower.)
-template <bool VARLEN, bool VARIANT>
+// Kernel flavours: the plain kernel, one with a sliding window, and one with
+// a window and / or soft-capping (both set at run time).
+enum Variant : int { kPlain = 0, kWindow = 1, kWindowCap = 2 };
+
+template <bool VARLEN, int VARIANT>
 __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const SeqTables& st) {
   Tile t;
   if constexpr (!VARLEN) {
@@ -176,7 +180,7 @@ __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const Seq
   // A sliding window skips the key tiles left of every row's window: the
   // tile's first row sees keys from qrel - window_left on.
   t.j0 = 0;
-  if constexpr (VARIANT) {
+  if constexpr (VARIANT != kPlain) {
     if (p.window_left >= 0 && t.qrel > p.window_left) t.j0 = (t.qrel - p.window_left) / kBN;
     t.n -= t.j0;
   }
@@ -192,9 +196,9 @@ __device__ __forceinline__ int item_of(int r, int total) {
   return w < total ? w : -1;
 }
 
-// VARIANT: the kernel built for a sliding window and / or soft-capping (both
-// set at run time); the plain kernel has neither in its code.
-template <int D, bool VARLEN, bool VARIANT>
+// VARIANT selects the flavour (see Variant): the plain kernel has neither a
+// window nor soft-capping in its code, the window kernel no soft-capping.
+template <int D, bool VARLEN, int VARIANT>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -493,8 +497,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[c][i]);
         }
         const int kv0 = (t.j0 + j) * kBN;  // first key of the tile, within the sequence
-        if constexpr (VARIANT) {
-          if (p.cap_in2 != 0.f) {
+        if constexpr (VARIANT != kPlain) {
+          if (VARIANT == kWindowCap && p.cap_in2 != 0.f) {
             // s -> softcap * tanh(s * scale / softcap); the factor softcap
             // (and log2 e) is in sl2, so s becomes the tanh.
 #pragma unroll
@@ -543,7 +547,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // sum uses four packed chains.
         // A row whose keys in this item's tiles so far were all outside its
         // window has m = -inf (all its P are 0): take 0 as its reference.
-        const float m_ref = (VARIANT && m == -INFINITY) ? 0.f : m;
+        const float m_ref = (VARIANT != kPlain && m == -INFINITY) ? 0.f : m;
         const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m_ref, -m_ref);
         float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
@@ -722,7 +726,7 @@ bool make_out_map(CUtensorMap* m, void* base, int D, int rows, int planes) {
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool VARLEN, bool VARIANT>
+template <int D, bool VARLEN, int VARIANT>
 cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   using L = PrefillSmem<D, VARLEN>;
   static bool configured[64] = {};
@@ -770,9 +774,9 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
 
 template <int D, bool VARLEN>
 cudaError_t launch_prefill_cap(const PrefillArgs& a, const LaunchCtx& ctx) {
-  const bool variant = a.softcap > 0.f || a.window_left >= 0;
-  return variant ? launch_prefill_t<D, VARLEN, true>(a, ctx)
-                 : launch_prefill_t<D, VARLEN, false>(a, ctx);
+  if (a.softcap > 0.f) return launch_prefill_t<D, VARLEN, kWindowCap>(a, ctx);
+  if (a.window_left >= 0) return launch_prefill_t<D, VARLEN, kWindow>(a, ctx);
+  return launch_prefill_t<D, VARLEN, kPlain>(a, ctx);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx) {
