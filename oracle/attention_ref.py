@@ -78,7 +78,8 @@ def _f64(x) -> np.ndarray:
 
 
 def masked_attention(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray,
-                     scale: float, allowed: np.ndarray | None = None, softcap: float = 0.0):
+                     scale: float, allowed: np.ndarray | None = None, softcap: float = 0.0,
+                     bias: np.ndarray | None = None):
     """Plain attention of some query rows against a key/value set.
 
     s_ij = scale * q_i . k_j   (page §"The bottleneck it attacks": S = QK^T/sqrt d)
@@ -89,7 +90,8 @@ def masked_attention(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray,
     A row with no allowed key gets LSE = -inf and O = 0.  With softcap > 0
     the scores are first soft-capped, s -> softcap * tanh(s / softcap) (page
     §"Interaction with post-trained models": logit soft-capping is one of the
-    attention variants kernels support).
+    attention variants kernels support).  ``bias`` (rows, keys), if given, is
+    added to the (capped) scores: the ALiBi bias of the same section.
     Returns (O (rows, dv), LSE (rows,)), float64.
     """
     q_rows = _f64(q_rows)
@@ -104,6 +106,8 @@ def masked_attention(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray,
     s = scale * (q_rows @ k.T)                      # S, materialised
     if softcap > 0:
         s = softcap * np.tanh(s / softcap)
+    if bias is not None:
+        s = s + bias
     if allowed is not None:
         s = np.where(allowed, s, -np.inf)
     m = s.max(axis=1)                               # row max (only for stability)
@@ -148,8 +152,14 @@ def _window_allowed(r0: int, r1: int, ncols: int, causal: bool, window_left: int
     return ok
 
 
+def _alibi(slope: float, rows: np.ndarray, cols: np.ndarray) -> np.ndarray:
+    """ALiBi bias: -slope * |i - j| for query position i and key position j
+    (for causal attention, j <= i, this is -slope * (i - j))."""
+    return -slope * np.abs(rows[:, None] - cols[None, :]).astype(np.float64)
+
+
 def prefill(q, k, v, scale: float, causal: bool = True, window_left: int = -1,
-            softcap: float = 0.0):
+            softcap: float = 0.0, alibi_slopes=None):
     """Attention forward over whole sequences (the prefill case).
 
     q: (B, n_q, N, d); k, v: (B, n_kv, N, d).  Returns O (B, n_q, N, d) and
@@ -157,7 +167,7 @@ def prefill(q, k, v, scale: float, causal: bool = True, window_left: int = -1,
     §"Prefill: tiles, loop order and the tensor cores").  Sliding window
     (window_left >= 0): row i sees only keys j >= i - window_left; softcap > 0
     soft-caps the scores (page §"Interaction with post-trained models", the
-    variants kernels support).
+    variants kernels support); alibi_slopes (n_q,) adds -slope_h * |i - j|.
     """
     q = _f64(q)
     k = _f64(k)
@@ -178,8 +188,11 @@ def prefill(q, k, v, scale: float, causal: bool = True, window_left: int = -1,
                     allowed = _causal_allowed(r0, r1, ncols) if causal else None
                 else:
                     allowed = _window_allowed(r0, r1, ncols, causal, window_left)
+                bias = None
+                if alibi_slopes is not None:
+                    bias = _alibi(float(alibi_slopes[h]), np.arange(r0, r1), np.arange(ncols))
                 ob, lb = masked_attention(q[b, h, r0:r1], k[b, kh, :ncols],
-                                          v[b, kh, :ncols], scale, allowed, softcap)
+                                          v[b, kh, :ncols], scale, allowed, softcap, bias)
                 o[b, h, r0:r1] = ob
                 lse[b, h, r0:r1] = lb
     return o, lse
@@ -187,7 +200,7 @@ def prefill(q, k, v, scale: float, causal: bool = True, window_left: int = -1,
 
 def prefill_rows(q, k, v, scale: float, causal: bool,
                  rows: Iterable[tuple[int, int, int]], window_left: int = -1,
-                 softcap: float = 0.0):
+                 softcap: float = 0.0, alibi_slopes=None):
     """The same definition as :func:`prefill`, for a sample of (b, h, i) rows.
 
     Used at sizes where every row would take too long on the CPU.  Returns
@@ -208,8 +221,11 @@ def prefill_rows(q, k, v, scale: float, causal: bool,
         for idx, h, i in members:
             ncols = i + 1 if causal else N
             lo = max(0, i - window_left) if window_left >= 0 else 0
+            bias = None
+            if alibi_slopes is not None:
+                bias = _alibi(float(alibi_slopes[h]), np.array([i]), np.arange(lo, ncols))
             ob, lb = masked_attention(_f64(q[b, h, i:i + 1]), kb[lo:ncols], vb[lo:ncols], scale,
-                                      None, softcap)
+                                      None, softcap, bias)
             o[idx] = ob[0]
             lse[idx] = lb[0]
     return o, lse
@@ -242,12 +258,14 @@ def gather_sequence(cache, block_table, b: int, kv_len: int, kv_head: int,
 
 
 def decode(q, k_cache, v_cache, block_table, kv_lens: Sequence[int],
-           scale: float, block_size: int = 0, window_left: int = -1, softcap: float = 0.0):
+           scale: float, block_size: int = 0, window_left: int = -1, softcap: float = 0.0,
+           alibi_slopes=None):
     """Single-token decode: one query row per (sequence, query head) attends
     to every cached token 0..kv_len-1 of its sequence.  The query is the
     sequence's last token, position kv_len - 1, so a sliding window
     (window_left >= 0) keeps tokens kv_len - 1 - window_left .. kv_len - 1;
-    softcap > 0 soft-caps the scores.
+    softcap > 0 soft-caps the scores; alibi_slopes (n_q,) adds
+    -slope_h * (kv_len - 1 - j).
 
     q: (B, n_q, d).  Returns O (B, n_q, d) and LSE (B, n_q), float64.
     """
@@ -263,15 +281,20 @@ def decode(q, k_cache, v_cache, block_table, kv_lens: Sequence[int],
             kb = gather_sequence(k_cache, block_table, b, L, kh, block_size)[lo:]
             vb = gather_sequence(v_cache, block_table, b, L, kh, block_size)[lo:]
             heads = [h for h in range(n_q) if _kv_head(h, n_q, n_kv) == kh]
-            ob, lb = masked_attention(q[b, heads], kb, vb, scale, None, softcap)
-            o[b, heads] = ob
-            lse[b, heads] = lb
+            for h in heads:
+                bias = None
+                if alibi_slopes is not None:
+                    bias = _alibi(float(alibi_slopes[h]), np.array([L - 1]), np.arange(lo, L))
+                ob, lb = masked_attention(q[b, h:h + 1], kb, vb, scale, None, softcap, bias)
+                o[b, h] = ob[0]
+                lse[b, h] = lb[0]
     return o, lse
 
 
 def decode_partials(q, k_cache, v_cache, block_table, kv_lens: Sequence[int],
                     scale: float, block_size: int,
-                    ranges: Sequence[Sequence[tuple[int, int]]], softcap: float = 0.0):
+                    ranges: Sequence[Sequence[tuple[int, int]]], softcap: float = 0.0,
+                    alibi_slopes=None):
     """Per-split partial results: the plain definition restricted to each
     split's token range (page §"Decode: a different bottleneck", split-KV).
 
@@ -292,10 +315,14 @@ def decode_partials(q, k_cache, v_cache, block_table, kv_lens: Sequence[int],
             vb = gather_sequence(v_cache, block_table, b, L, kh, block_size)
             heads = [h for h in range(n_q) if _kv_head(h, n_q, n_kv) == kh]
             for s, (t0, t1) in enumerate(ranges[b]):
-                ob, lb = masked_attention(q[b, heads], kb[t0:t1], vb[t0:t1],
-                                          scale, None, softcap)
-                o[s, b, heads] = ob
-                lse[s, b, heads] = lb
+                for h in heads:
+                    bias = None
+                    if alibi_slopes is not None:
+                        bias = _alibi(float(alibi_slopes[h]), np.array([L - 1]), np.arange(t0, t1))
+                    ob, lb = masked_attention(q[b, h:h + 1], kb[t0:t1], vb[t0:t1],
+                                              scale, None, softcap, bias)
+                    o[s, b, h] = ob[0]
+                    lse[s, b, h] = lb[0]
     return o, lse
 
 

@@ -101,7 +101,7 @@ def test_worked_example_blocks_and_combine(golden):
 # Brute force: scalar loops with math.exp / math.fsum.
 # ---------------------------------------------------------------------------
 
-def _brute_prefill(q, k, v, scale, causal, window_left=-1, softcap=0.0):
+def _brute_prefill(q, k, v, scale, causal, window_left=-1, softcap=0.0, slopes=None):
     B, nq, N, d = q.shape
     nkv = k.shape[1]
     g = nq // nkv
@@ -117,6 +117,8 @@ def _brute_prefill(q, k, v, scale, causal, window_left=-1, softcap=0.0):
                 sc = [scale * math.fsum(q[b, h, i, t] * k[b, kh, j, t] for t in range(d)) for j in js]
                 if softcap > 0:
                     sc = [softcap * math.tanh(x / softcap) for x in sc]
+                if slopes is not None:
+                    sc = [x - slopes[h] * abs(i - j) for x, j in zip(sc, js)]
                 m = max(sc)
                 z = math.fsum(math.exp(x - m) for x in sc)
                 lse[b, h, i] = m + math.log(z)
@@ -285,6 +287,16 @@ def _pin_variants():
         ob, lb = _brute_prefill(q, k, v, 0.9, causal, W, cap)
         oo, lo = oracle.prefill(q, k, v, 0.9, causal, window_left=W, softcap=cap)
         worst = max(worst, float(np.abs(ob - oo).max()), float(np.abs(lb - lo).max()))
+    # ALiBi, with and without a window, causal and not
+    for N, nq, nkv, d, causal, W in [(18, 4, 2, 4, True, -1), (15, 2, 1, 8, False, -1),
+                                     (20, 4, 4, 4, True, 5)]:
+        q = rng.standard_normal((1, nq, N, d))
+        k = rng.standard_normal((1, nkv, N, d))
+        v = rng.standard_normal((1, nkv, N, d))
+        slopes = [2.0 ** (-8.0 * (h + 1) / nq) for h in range(nq)]
+        ob, lb = _brute_prefill(q, k, v, 0.7, causal, W, 0.0, slopes)
+        oo, lo = oracle.prefill(q, k, v, 0.7, causal, window_left=W, alibi_slopes=slopes)
+        worst = max(worst, float(np.abs(ob - oo).max()), float(np.abs(lb - lo).max()))
     return worst
 
 
@@ -322,10 +334,13 @@ def test_decode_variants_equal_last_prefill_row():
     x = W.make_prefill(1, 6, 2, N, 16, seed=8)
     kc = x.k[0].permute(1, 0, 2).unsqueeze(0).contiguous()
     vc = x.v[0].permute(1, 0, 2).unsqueeze(0).contiguous()
-    for Wl, cap in [(50, 0.0), (-1, 2.5), (7, 1.0), (0, 0.0)]:
-        op, lp = oracle.prefill(x.q, x.k, x.v, x.scale, True, window_left=Wl, softcap=cap)
+    slopes = [0.5, 0.25, 0.125, 0.0625, 0.03125, 0.0]
+    for Wl, cap, al in [(50, 0.0, None), (-1, 2.5, None), (7, 1.0, None), (0, 0.0, None),
+                        (-1, 0.0, slopes), (30, 0.0, slopes)]:
+        op, lp = oracle.prefill(x.q, x.k, x.v, x.scale, True, window_left=Wl, softcap=cap,
+                                alibi_slopes=al)
         od, ld = oracle.decode(x.q[:, :, N - 1], kc, vc, None, [N], x.scale, window_left=Wl,
-                               softcap=cap)
+                               softcap=cap, alibi_slopes=al)
         assert np.abs(od - op[:, :, N - 1]).max() <= TOL
         assert np.abs(ld - lp[:, :, N - 1]).max() <= TOL
 
@@ -598,7 +613,7 @@ def test_pins_pass_unmutated():
                                       "combine_unweighted", "gqa_off_by_one",
                                       "append_off_by_one", "append_not_attended",
                                       "varlen_cross_sequence", "window_off_by_one",
-                                      "softcap_unscaled"])
+                                      "softcap_unscaled", "alibi_sign"])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     orig_ma = ref.masked_attention
     orig_comb = ref.combine
@@ -633,6 +648,8 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
             # right formula applied to scores scaled by cap
             return orig_ma(q, k, v, scale * softcap if softcap > 0 else scale, allowed, softcap)
         monkeypatch.setattr(ref, "masked_attention", bad_cap)
+    elif mutation == "alibi_sign":
+        monkeypatch.setattr(ref, "_alibi", lambda slope, r, c: slope * np.abs(r[:, None] - c[None, :]))
     elif mutation == "varlen_cross_sequence":
         # sequences attend to the previous one's rows too (no per-example masking)
         monkeypatch.setattr(ref, "_seq_bounds", lambda cu: [(0, int(b)) for b in
