@@ -345,12 +345,17 @@ def time_variants(args, attn, q, k, v, scale, o, lse, dq, caches, dec, S, op, lp
 
     full = 4.0 * D * Hq * B * sum(i + 1 for i in range(N))
     pre = {}
-    for name, (w_, c_, fl) in {"window": (Wl, 0.0, flops), "softcap": (-1, cap, full),
-                               "window+softcap": (Wl, cap, flops)}.items():
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)], dtype=torch.float32,
+                          device=dev)
+    for name, (w_, c_, al, fl) in {"window": (Wl, 0.0, None, flops),
+                                   "softcap": (-1, cap, None, full),
+                                   "window+softcap": (Wl, cap, None, flops),
+                                   "alibi": (-1, 0.0, slopes, full)}.items():
         t = timed(lambda i: attn.prefill(q, k, v, scale, True, out=o, lse=lse, window_left=w_,
-                                         softcap=c_))
+                                         softcap=c_, alibi_slopes=al))
         pre[name] = {"value": round(job_rate(fl, n, world, t) / 1e12, 2), "unit": "TFLOP/s",
-                     "window_left": w_, "softcap": c_, "flops_per_launch": fl,
+                     "window_left": w_, "softcap": c_, "alibi": al is not None,
+                     "flops_per_launch": fl,
                      "avg_launch_ms": round(t / n, 4)}
     Bd, Hqd, Dd = dq.shape
     lens = dec.kv_lens.to(dev)

@@ -41,9 +41,10 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
 def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
             causal: bool = True, out: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, stream=None, window_left: int = -1,
-            softcap: float = 0.0):
+            softcap: float = 0.0, alibi_slopes: Optional[torch.Tensor] = None):
     """Attention forward over whole sequences (``attn_prefill``; with a
-    sliding window or soft-capping, ``attn_prefill_ex``).
+    sliding window, soft-capping or ALiBi slopes ((n_q,) fp32 on the device),
+    ``attn_prefill_ex``).
 
     q: (B, n_q, N, d) bf16; k, v: (B, n_kv, N, d) bf16.  Returns
     (O (B, n_q, N, d) fp32, LSE (B, n_q, N) fp32, natural log).
@@ -65,11 +66,17 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[f
     _need(lse, "lse", torch.float32, 3)
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, n_q, n_kv,
             N, d, float(scale), int(bool(causal)))
-    if window_left == -1 and softcap == 0.0:
+    if window_left == -1 and softcap == 0.0 and alibi_slopes is None:
         check("attn_prefill", lib().attn_prefill(*args, _stream(stream)))
     else:
+        al = None
+        if alibi_slopes is not None:
+            _need(alibi_slopes, "alibi_slopes", torch.float32, 1)
+            if alibi_slopes.numel() != n_q:
+                raise ValueError("alibi_slopes must have one slope per query head")
+            al = alibi_slopes.data_ptr()
         check("attn_prefill_ex", lib().attn_prefill_ex(*args, int(window_left), float(softcap),
-                                                       _stream(stream)))
+                                                       al, _stream(stream)))
     return out, lse
 
 
@@ -132,7 +139,8 @@ def split_ranges(kv_len: int, num_splits: int, window_left: int = -1):
 
 
 def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
-                 o_partial, lse_partial, stream, new_kv=None, window_left=-1, softcap=0.0):
+                 o_partial, lse_partial, stream, new_kv=None, window_left=-1, softcap=0.0,
+                 alibi_slopes=None):
     """Shape checks and marshalling shared by the plain and appending decode."""
     _need(q, "q", _BF16, 3)
     _need(k_cache, "k_cache", _BF16, 4)
@@ -179,11 +187,17 @@ def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_l
     tail = (kv_lens.data_ptr(), int(num_splits), o_partial.data_ptr(), lse_partial.data_ptr(), B,
             n_q, n_kv, d, block_size, max_blocks, num_blocks, int(max_kv_len), float(scale),
             _stream(stream))
-    if new_kv is None and (window_left != -1 or softcap != 0.0):
+    if new_kv is None and (window_left != -1 or softcap != 0.0 or alibi_slopes is not None):
+        al = None
+        if alibi_slopes is not None:
+            _need(alibi_slopes, "alibi_slopes", torch.float32, 1)
+            if alibi_slopes.numel() != n_q:
+                raise ValueError("alibi_slopes must have one slope per query head")
+            al = alibi_slopes.data_ptr()
         name = "attn_decode_splitkv_ex"
         st = lib().attn_decode_splitkv_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                           bt_ptr, *tail[:-1], int(window_left), float(softcap),
-                                          tail[-1])
+                                          al, tail[-1])
     elif new_kv is None:
         name = "attn_decode_splitkv"
         st = lib().attn_decode_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), bt_ptr,
@@ -202,7 +216,7 @@ def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                    num_splits: int = 0, max_kv_len: Optional[int] = None,
                    scale: Optional[float] = None, o_partial: Optional[torch.Tensor] = None,
                    lse_partial: Optional[torch.Tensor] = None, stream=None, window_left: int = -1,
-                   softcap: float = 0.0):
+                   softcap: float = 0.0, alibi_slopes: Optional[torch.Tensor] = None):
     """Split-KV single-token decode (``attn_decode_splitkv``; with a sliding
     window or soft-capping, ``attn_decode_splitkv_ex``).
 
@@ -212,7 +226,8 @@ def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     Returns (o_partial (S, B, n_q, d), lse_partial (S, B, n_q)), fp32.
     """
     return _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
-                        o_partial, lse_partial, stream, window_left=window_left, softcap=softcap)
+                        o_partial, lse_partial, stream, window_left=window_left, softcap=softcap,
+                        alibi_slopes=alibi_slopes)
 
 
 def decode_append_splitkv(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,

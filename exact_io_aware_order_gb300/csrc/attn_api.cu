@@ -154,7 +154,8 @@ bool valid_variant(int window_left, float softcap) {
 
 int prefill_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o, float* lse,
                  int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim, float scale,
-                 int causal, int window_left, float softcap, void* stream) {
+                 int causal, int window_left, float softcap, const float* alibi_slopes,
+                 void* stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || seqlen < 1 || seqlen > (1 << 24) ||
       (long long)batch * n_q_heads > (1LL << 20) || !valid_scale(scale) ||
@@ -164,7 +165,9 @@ int prefill_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
   if ((long long)batch * n_q_heads * ((seqlen + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+  if (alibi_slopes && softcap > 0.f) return ATTN_ERR_SHAPE;  // not combined
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(alibi_slopes, 4))
     return ATTN_ERR_ALIGN;
   int st = ATTN_OK;
   DeviceState* ds = device_state(&st);
@@ -173,6 +176,7 @@ int prefill_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
                       causal ? 1 : 0};
   a.window_left = window_left;
   a.softcap = softcap;
+  a.alibi_slopes = alibi_slopes;
   if (attn::launch_prefill(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
@@ -183,14 +187,15 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
                  int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim, float scale,
                  int causal, void* stream) {
   return prefill_impl(q, k, v, o, lse, batch, n_q_heads, n_kv_heads, seqlen, head_dim, scale,
-                      causal, -1, 0.f, stream);
+                      causal, -1, 0.f, nullptr, stream);
 }
 
 int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
                     float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim,
-                    float scale, int causal, int window_left, float softcap, void* stream) {
+                    float scale, int causal, int window_left, float softcap,
+                    const float* alibi_slopes, void* stream) {
   return prefill_impl(q, k, v, o, lse, batch, n_q_heads, n_kv_heads, seqlen, head_dim, scale,
-                      causal, window_left, softcap, stream);
+                      causal, window_left, softcap, alibi_slopes, stream);
 }
 
 int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
@@ -229,10 +234,13 @@ int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_n
                 const int32_t* kv_lens, int num_splits, float* o_partial, float* lse_partial,
                 int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                 int max_blocks_per_seq, int num_blocks, int max_kv_len, float scale,
-                void* stream, bool append, int window_left = -1, float softcap = 0.f) {
+                void* stream, bool append, int window_left = -1, float softcap = 0.f,
+                const float* alibi_slopes = nullptr) {
   if (!q || !k_cache || !v_cache || !kv_lens || !o_partial || !lse_partial) return ATTN_ERR_NULL;
   if (append && (!k_new || !v_new)) return ATTN_ERR_NULL;
   if (!valid_variant(window_left, softcap)) return ATTN_ERR_SHAPE;
+  if (alibi_slopes && softcap > 0.f) return ATTN_ERR_SHAPE;  // not combined
+  if (!aligned(alibi_slopes, 4)) return ATTN_ERR_ALIGN;
   if (append && (!aligned(k_new, 16) || !aligned(v_new, 16))) return ATTN_ERR_ALIGN;
   const bool paged = block_table != nullptr;
   if (batch < 1 || batch > 65535 || n_q_heads < 1 || n_kv_heads < 1 || n_kv_heads > 65535 ||
@@ -262,6 +270,7 @@ int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_n
   }
   a.window_left = window_left;
   a.softcap = softcap;
+  a.alibi_slopes = alibi_slopes;
   if (attn::launch_decode(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
@@ -283,11 +292,11 @@ int attn_decode_splitkv_ex(const attn_bf16* q, const attn_bf16* k_cache, const a
                            float* o_partial, float* lse_partial, int batch, int n_q_heads,
                            int n_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
                            int num_blocks, int max_kv_len, float scale, int window_left,
-                           float softcap, void* stream) {
+                           float softcap, const float* alibi_slopes, void* stream) {
   return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_table, kv_lens, num_splits,
                      o_partial, lse_partial, batch, n_q_heads, n_kv_heads, head_dim, block_size,
                      max_blocks_per_seq, num_blocks, max_kv_len, scale, stream, false, window_left,
-                     softcap);
+                     softcap, alibi_slopes);
 }
 
 int attn_decode_append_splitkv(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,

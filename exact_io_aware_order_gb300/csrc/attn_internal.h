@@ -36,6 +36,7 @@ struct PrefillArgs {
   // none) and logit soft-capping (s -> softcap * tanh(s / softcap); 0 = off).
   int window_left = -1;
   float softcap = 0.f;
+  const float* alibi_slopes = nullptr;  // (n_q_heads,): adds -slope_h * |i - j|
 };
 
 // Largest number of packed sequences per variable-length prefill call.
@@ -64,6 +65,7 @@ struct DecodeArgs {
   // window keeps tokens kv_len - 1 - window_left .. kv_len - 1.
   int window_left = -1;
   float softcap = 0.f;
+  const float* alibi_slopes = nullptr;  // (n_q_heads,): adds -slope_h * (kv_len - 1 - j)
 };
 
 struct CombineArgs {

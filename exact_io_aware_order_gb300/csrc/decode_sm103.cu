@@ -330,6 +330,19 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
     const bool capped = a.softcap > 0.f;
     const float sl2 = capped ? a.softcap * kLog2e : a.scale * kLog2e;
     const float cap_in2 = capped ? 2.f * kLog2e * a.scale / a.softcap : 0.f;
+    // ALiBi: rows gid and gid + 8 are query heads kvh * g + row; their slopes
+    // in log2 units.  The scores are then biased and scaled in place, so the
+    // softmax below uses a unit scale (sl2x).
+    const bool alibi = a.alibi_slopes != nullptr;
+    float al2[2] = {0.f, 0.f};
+    if (alibi) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = (lane >> 2) + 8 * r;
+        if (row < g) al2[r] = a.alibi_slopes[kvh * g + row] * kLog2e;
+      }
+    }
+    const float sl2x = alibi ? 1.f : sl2;
     float m_r[2] = {-INFINITY, -INFINITY};  // running max (log2 domain) of rows gid, gid+8
     float l_r[2] = {0.f, 0.f};
     float acc[D / 8][4];
@@ -375,6 +388,16 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
             for (int e = 0; e < 4; ++e) s[n][e] = tanh_from_exp2(s[n][e] * cap_in2);
         }
+        if (alibi) {
+          // s -> s scale log2 e - slope log2 e (len - 1 - token)
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = base + r0 + n * 8 + quad * 2 + (e & 1);
+              s[n][e] = fmaf(s[n][e], sl2, -al2[e >> 1] * static_cast<float>(len - 1 - tok));
+            }
+        }
         // ---- mask tokens past the end or left of the window, online softmax update ----
         const int lo_rel = lo_tok - (base + r0);  // first token of the warp's 16 in the window
         float mx[2] = {-INFINITY, -INFINITY};
@@ -392,7 +415,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int r = 0; r < 2; ++r) {
           mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
           mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-          m_new[r] = fmaxf(m_r[r], mx[r] * sl2);  // -inf only while every token was masked
+          m_new[r] = fmaxf(m_r[r], mx[r] * sl2x);  // -inf only while every token was masked
           grow |= m_new[r] - m_r[r] > kRescaleThreshold;  // true at the first unmasked token
         }
         // Keep the stale max unless some row of the warp grew by more than 2^8.
@@ -412,10 +435,10 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
         const float mr1 = m_r[1] == -INFINITY ? 0.f : m_r[1];
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
-          const float p0 = ex2_approx(fmaf(s[n][0], sl2, -mr0));
-          const float p1 = ex2_approx(fmaf(s[n][1], sl2, -mr0));
-          const float p2 = ex2_approx(fmaf(s[n][2], sl2, -mr1));
-          const float p3 = ex2_approx(fmaf(s[n][3], sl2, -mr1));
+          const float p0 = ex2_approx(fmaf(s[n][0], sl2x, -mr0));
+          const float p1 = ex2_approx(fmaf(s[n][1], sl2x, -mr0));
+          const float p2 = ex2_approx(fmaf(s[n][2], sl2x, -mr1));
+          const float p3 = ex2_approx(fmaf(s[n][3], sl2x, -mr1));
           rs[0] += p0 + p1;
           rs[1] += p2 + p3;
           pa[2 * n + 0] = pack_bf16x2(p0, p1);  // row gid,   tokens 8n + 2q, +1

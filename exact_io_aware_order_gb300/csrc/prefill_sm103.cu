@@ -102,6 +102,7 @@ struct PrefillParams {
   int causal;
   int window_left;  // sliding window: row i sees keys j >= i - window_left (-1: none)
   float cap_in2;    // soft-capping: 2 log2(e) scale / softcap (the tanh argument's factor)
+  const float* alibi_slopes;  // ALiBi: per query head slope (natural-log units)
   int n_q_tiles;    // ceil(seqlen / 128)
   int total_tiles;  // n_q_tiles * batch * n_q_heads (padded mode)
   const int32_t* cu_seqlens;  // packed mode: (num_seqs + 1) row offsets
@@ -138,9 +139,10 @@ struct SeqTables {
 // L2.  (A globally longest-first order balances better but spreads the work
 // over every sequence at once; claiming items dynamically balances too but
 // costs more per tile; both measured slower.)
-// Kernel flavours: the plain kernel, one with a sliding window, and one with
-// a window and / or soft-capping (both set at run time).
-enum Variant : int { kPlain = 0, kWindow = 1, kWindowCap = 2 };
+// Kernel flavours: the plain kernel, one with a sliding window, one with a
+// window and / or soft-capping, one with ALiBi and an optional window (the
+// window and the cap are set at run time).
+enum Variant : int { kPlain = 0, kWindow = 1, kWindowCap = 2, kWindowAlibi = 3 };
 
 template <bool VARLEN, int VARIANT>
 __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const SeqTables& st) {
@@ -469,7 +471,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // ============================ softmax warps ============================
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int row = warp * 32 + lane;               // row within the tile (= TMEM lane)
-    const float sl2 = p.sl2;
     const uint32_t tOm = tO + lane_base;
     bool ok = true;
     int g = 0;
@@ -479,6 +480,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const Tile t = tile_of<VARLEN, VARIANT>(w, p, seqt);
       const int q0 = t.qrel, q_row = q0 + row;  // indices within the sequence
       float m = -INFINITY, l = 0.f;   // running max (log2 domain) and sum of the row
+      // ALiBi: this head's slope in log2 units; the scores are then biased
+      // and scaled in place, so the passes below use a unit scale.
+      float alibi_l2 = 0.f, sl2 = p.sl2;
+      if constexpr (VARIANT == kWindowAlibi) {
+        alibi_l2 = p.alibi_slopes[t.zq % p.n_q_heads] * kLog2e;
+        sl2 = 1.f;
+      }
       for (int j = 0; j < t.n; ++j, ++g) {
         const int b = g % kSBuf;
         if (!mbar_wait_warp(bar(kSFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
@@ -503,6 +511,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // (and log2 e) is in sl2, so s becomes the tanh.
 #pragma unroll
             for (int c = 0; c < kBN; ++c) s[c] = tanh_from_exp2(s[c] * p.cap_in2);
+          }
+          if constexpr (VARIANT == kWindowAlibi) {
+            // s -> s scale log2 e - slope log2 e |i - j|
+            const float dist0 = static_cast<float>(kv0 - q_row);  // key c is at j - i = dist0 + c
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+              s[c] = fmaf(s[c], p.sl2, -alibi_l2 * fabsf(dist0 + static_cast<float>(c)));
           }
           const bool hi_edge = p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > t.len);
           const bool lo_edge = p.window_left >= 0 && kv0 < q0 + kBM - 1 - p.window_left;
@@ -755,6 +770,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   pp.causal = a.causal;
   pp.window_left = a.window_left;
   pp.cap_in2 = a.softcap > 0.f ? 2.f * kLog2e * a.scale / a.softcap : 0.f;
+  pp.alibi_slopes = a.alibi_slopes;
   pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM;
   pp.total_tiles = pp.n_q_tiles * a.batch * a.n_q_heads;
   pp.cu_seqlens = a.cu_seqlens;
@@ -774,6 +790,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
 
 template <int D, bool VARLEN>
 cudaError_t launch_prefill_cap(const PrefillArgs& a, const LaunchCtx& ctx) {
+  if (a.alibi_slopes) return launch_prefill_t<D, VARLEN, kWindowAlibi>(a, ctx);
   if (a.softcap > 0.f) return launch_prefill_t<D, VARLEN, kWindowCap>(a, ctx);
   if (a.window_left >= 0) return launch_prefill_t<D, VARLEN, kWindow>(a, ctx);
   return launch_prefill_t<D, VARLEN, kPlain>(a, ctx);

@@ -89,19 +89,24 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
 
 /*
  * attn_prefill_ex -- attn_prefill with the attention variants of the page's
- * section "Interaction with post-trained models" (sliding windows and logit
- * soft-capping are among the variants current kernels support).
+ * section "Interaction with post-trained models" (sliding windows, ALiBi and
+ * logit soft-capping are among the variants current kernels support).
  *
  *   window_left: -1 for none; otherwise row i attends only to keys
  *                j >= i - window_left (with causal, i - window_left <= j <= i)
  *   softcap    : 0 for none; otherwise each scaled score s = scale * q.k is
  *                replaced by softcap * tanh(s / softcap) before the softmax
- * Everything else, and the errors, as attn_prefill (a negative window_left
- * other than -1, or a negative or non-finite softcap, is ATTN_ERR_SHAPE).
+ *   alibi_slopes: NULL for none; otherwise (n_q_heads,) fp32 on the device,
+ *                4-byte aligned: head h adds -alibi_slopes[h] * |i - j| to the
+ *                score of query i and key j (after soft-capping)
+ * ALiBi and soft-capping together are ATTN_ERR_SHAPE.  Everything else, and
+ * the errors, as attn_prefill (a negative window_left other than -1, or a
+ * negative or non-finite softcap, is ATTN_ERR_SHAPE).
  */
 int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
                     float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim,
-                    float scale, int causal, int window_left, float softcap, void* stream);
+                    float scale, int causal, int window_left, float softcap,
+                    const float* alibi_slopes, void* stream);
 
 /*
  * attn_prefill_varlen -- prefill of several sequences packed end to end
@@ -191,6 +196,7 @@ int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn
  * [lo16, kv_len), lo16 = lo rounded down to a multiple of 16: c =
  * roundup(ceil((kv_len - lo16) / S), 16), split s covers [lo16 + s*c,
  * min(lo16 + (s+1)*c, kv_len)), and tokens below lo carry no weight.
+ * ALiBi adds -alibi_slopes[h] * (kv_len - 1 - j) to the score of token j.
  */
 int attn_decode_splitkv_ex(const attn_bf16* q, const attn_bf16* k_cache,
                            const attn_bf16* v_cache, const int32_t* block_table,
@@ -198,7 +204,7 @@ int attn_decode_splitkv_ex(const attn_bf16* q, const attn_bf16* k_cache,
                            float* lse_partial, int batch, int n_q_heads, int n_kv_heads,
                            int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
                            int max_kv_len, float scale, int window_left, float softcap,
-                           void* stream);
+                           const float* alibi_slopes, void* stream);
 
 /*
  * attn_decode_append_splitkv -- split-KV single-token decode that first

@@ -12,8 +12,12 @@ def nan_like(shape, device):
     return torch.full(shape, float("nan"), dtype=torch.float32, device=device)
 
 
-def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
-    """Element-wise parity: returns (max|dO|, mean|dO|, max|dLSE|)."""
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what="", lse_rel=0.0):
+    """Element-wise parity: returns (max|dO|, mean|dO|, max|dLSE|).
+
+    lse_rel adds a tolerance proportional to |LSE| for values whose fp32
+    representation itself is coarser than LSE_MAX (ALiBi partials far from
+    the query reach |LSE| ~ 1e4, where one fp32 step is ~1e-3)."""
     o = o_gpu.detach().double().cpu().numpy() if isinstance(o_gpu, torch.Tensor) else o_gpu
     lse = lse_gpu.detach().double().cpu().numpy() if isinstance(lse_gpu, torch.Tensor) else lse_gpu
     assert o.shape == o_ref.shape, (what, o.shape, o_ref.shape)
@@ -23,7 +27,8 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     assert np.array_equal(np.isneginf(lse), inf_ref), f"{what}: -inf pattern of LSE differs"
     assert np.isfinite(lse[~inf_ref]).all(), f"{what}: non-finite LSE"
     err = np.abs(o - o_ref)
-    lerr = np.abs(lse[~inf_ref] - lse_ref[~inf_ref]).max() if (~inf_ref).any() else 0.0
+    fin = ~inf_ref
+    lerr = (np.abs(lse[fin] - lse_ref[fin]) - lse_rel * np.abs(lse_ref[fin])).max() if fin.any() else 0.0
     emax, emean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
     assert emax <= O_MAX and emean <= O_MEAN and lerr <= LSE_MAX, \
         f"{what}: max|dO|={emax:.3e} mean|dO|={emean:.3e} max|dLSE|={lerr:.3e}"

@@ -116,3 +116,69 @@ def test_decode_window_equals_last_prefill_row(dev):
     _, _, o_d, l_d = run_decode(d, dev, 4, 200, 25.0)
     assert (o_d - o_p[:, :, -1]).abs().max().item() <= 1e-2
     assert (l_d - l_p[:, :, -1]).abs().max().item() <= 1e-3
+
+
+def alibi_slopes(n_heads):
+    """The usual geometric ALiBi slopes 2^(-8 (h+1) / n_heads)."""
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / n_heads) for h in range(n_heads)],
+                        dtype=torch.float32)
+
+
+@pytest.mark.parametrize("N,Hq,Hkv,D,causal,Wl", [
+    (1000, 8, 2, 128, True, -1),
+    (777, 4, 4, 64, True, -1),
+    (600, 8, 2, 128, False, -1),
+    (1500, 8, 2, 128, True, 300),
+])
+def test_prefill_alibi_full(dev, N, Hq, Hkv, D, causal, Wl):
+    x = W.make_prefill(1, Hq, Hkv, N, D, seed=N + 7, causal=causal)
+    sl = alibi_slopes(Hq)
+    o, lse = run_prefill(x, dev, window_left=Wl, alibi_slopes=sl.to(dev))
+    o_ref, lse_ref = oracle.prefill(x.q, x.k, x.v, x.scale, causal, window_left=Wl,
+                                    alibi_slopes=sl.tolist())
+    compare(o, lse, o_ref, lse_ref, f"alibi prefill N={N} W={Wl}")
+
+
+def test_prefill_alibi_qwen_8192_sampled(dev):
+    x = W.qwen_prefill(8192)
+    sl = alibi_slopes(28)
+    o, lse = run_prefill(x, dev, alibi_slopes=sl.to(dev))
+    rng = np.random.default_rng(4)
+    rows = [(0, int(h), int(i)) for h, i in zip(rng.integers(0, 28, 400), rng.integers(0, 8192, 400))]
+    o_ref, lse_ref = oracle.prefill_rows(x.q, x.k, x.v, x.scale, True, rows,
+                                         alibi_slopes=sl.tolist())
+    idx = tuple(torch.tensor(c) for c in zip(*rows))
+    compare(o[idx], lse[idx], o_ref, lse_ref, "alibi qwen 8192")
+
+
+@pytest.mark.parametrize("paged,lens,S,Wl", [
+    (False, [3000], 7, -1), (False, [30720], 76, -1), (False, [2000], 5, 300),
+    (True, [1000, 17, 5000, 64], 6, -1), (True, [1000, 17, 5000, 64], 6, 40),
+])
+def test_decode_alibi(dev, paged, lens, S, Wl):
+    if paged:
+        d = W.make_decode_paged(len(lens), 16, 4, 128, lens, block_size=16, seed=sum(lens) + 1)
+        Hq = 16
+    else:
+        d = W.make_decode_contiguous(len(lens), 28, 4, 128, lens[0], seed=lens[0] + 2)
+        Hq = 28
+    sl = alibi_slopes(Hq)
+    q, kc, vc, lens_d = d.q.to(dev), d.k_cache.to(dev), d.v_cache.to(dev), d.kv_lens.to(dev)
+    bt = d.block_table.to(dev) if d.block_table is not None else None
+    B = q.shape[0]
+    op, lp = nan_like((S, B, Hq, 128), dev), nan_like((S, B, Hq), dev)
+    attn.decode_splitkv(q, kc, vc, lens_d, bt, num_splits=S, max_kv_len=d.max_kv_len or None,
+                        scale=d.scale, o_partial=op, lse_partial=lp, window_left=Wl,
+                        alibi_slopes=sl.to(dev))
+    o, lse = attn.combine(op, lp)
+    attn.check_device_status()
+    L = d.kv_lens.tolist()
+    o_ref, lse_ref = oracle.decode(d.q, d.k_cache, d.v_cache, d.block_table, L, d.scale,
+                                   d.block_size, window_left=Wl, alibi_slopes=sl.tolist())
+    compare(o, lse, o_ref, lse_ref, f"alibi decode W={Wl}")
+    ranges = [split_ranges(n, S, Wl) for n in L]
+    op_ref, lp_ref = oracle.decode_partials(d.q, d.k_cache, d.v_cache, d.block_table, L, d.scale,
+                                            d.block_size, ranges, alibi_slopes=sl.tolist())
+    # far splits carry biases of -slope * distance ~ -2.5e4: their fp32 LSE
+    # is only good to a few units in the last place of that magnitude
+    compare(op, lp, op_ref, lp_ref, f"alibi decode partials W={Wl}", lse_rel=2.0 ** -21)

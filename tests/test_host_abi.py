@@ -74,16 +74,20 @@ def test_prefill_validation(L):
 
 def test_variant_validation(L):
     c = _lib.status_codes()
-    ex = lambda w, cap: L.attn_prefill_ex(P, P, P, P, P, 1, 4, 2, 128, 128, 0.1, 1, w, cap, None)
+    ex = lambda w, cap, al=None: L.attn_prefill_ex(P, P, P, P, P, 1, 4, 2, 128, 128, 0.1, 1, w, cap,
+                                                   al, None)
     assert ex(-2, 0.0) == c["ATTN_ERR_SHAPE"]
     assert ex(0, -1.0) == c["ATTN_ERR_SHAPE"]
     assert ex(0, float("nan")) == c["ATTN_ERR_SHAPE"]
     assert ex(0, float("inf")) == c["ATTN_ERR_SHAPE"]
-    assert L.attn_prefill_ex(None, P, P, P, P, 1, 4, 2, 128, 128, 0.1, 1, 5, 1.0, None) == \
+    assert L.attn_prefill_ex(None, P, P, P, P, 1, 4, 2, 128, 128, 0.1, 1, 5, 1.0, None, None) == \
         c["ATTN_ERR_NULL"]
-    dx = lambda w, cap: L.attn_decode_splitkv_ex(P, P, P, P, P, 4, P, P, 2, 8, 2, 128, 16, 8, 16,
-                                                 128, 0.1, w, cap, None)
+    assert ex(-1, 2.0, P) == c["ATTN_ERR_SHAPE"]            # ALiBi with soft-capping
+    assert ex(-1, 0.0, P + 2) == c["ATTN_ERR_ALIGN"]        # misaligned slopes
+    dx = lambda w, cap, al=None: L.attn_decode_splitkv_ex(P, P, P, P, P, 4, P, P, 2, 8, 2, 128, 16,
+                                                          8, 16, 128, 0.1, w, cap, al, None)
     assert dx(-3, 0.0) == c["ATTN_ERR_SHAPE"] and dx(4, -0.5) == c["ATTN_ERR_SHAPE"]
+    assert dx(-1, 1.0, P) == c["ATTN_ERR_SHAPE"] and dx(-1, 0.0, P + 1) == c["ATTN_ERR_ALIGN"]
 
 
 @pytest.mark.parametrize("kv_len,S,W", [(100, 3, 10), (1000, 7, 0), (33, 2, 16), (5000, 9, 4095),
