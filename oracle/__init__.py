@@ -19,3 +19,4 @@ from .attention_ref import (  # noqa: F401
     prefill_varlen,
     prefill_varlen_rows,
 )
+from . import fp8_ref  # noqa: F401  (FP8 block quantisation and its attention)
