@@ -19,5 +19,6 @@ from .api import (  # noqa: F401
     decode_noalloc,
     decode_append_splitkv,
     decode_append,
+    quantize_fp8,
 )
 from ._lib import AttnError, lib  # noqa: F401

@@ -115,6 +115,34 @@ def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
     return out, lse
 
 
+def quantize_fp8(x: torch.Tensor, signs: Optional[torch.Tensor] = None, block_rows: int = 128,
+                 transpose: bool = False, stream=None):
+    """FP8 (e4m3) block quantisation with optional incoherent rotation
+    (``attn_quantize_fp8``).  x: (..., rows, d) bf16, the leading dimensions
+    being planes.  Returns (codes uint8 (planes..., rows, d) or, transposed,
+    (planes..., d, rows); scales fp32 (planes..., ceil(rows/128)) or
+    (planes...,) when block_rows == 0)."""
+    _need(x, "x", _BF16, x.dim())
+    lead, rows, d = tuple(x.shape[:-2]), x.shape[-2], x.shape[-1]
+    planes = 1
+    for n in lead:
+        planes *= n
+    shape = lead + ((d, rows) if transpose else (rows, d))
+    codes = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    nb = -(-rows // 128)
+    scales = torch.empty(lead + ((nb,) if block_rows else ()), dtype=torch.float32, device=x.device)
+    sp = None
+    if signs is not None:
+        _need(signs, "signs", torch.float32, 1)
+        if signs.numel() != d:
+            raise ValueError("signs must have head_dim entries")
+        sp = signs.data_ptr()
+    st = lib().attn_quantize_fp8(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), sp, planes,
+                                 rows, d, int(block_rows), int(bool(transpose)), _stream(stream))
+    check("attn_quantize_fp8", st)
+    return codes, scales
+
+
 def decode_num_splits(batch: int, n_kv_heads: int, max_kv_len: int, num_sms: int = 0) -> int:
     """The split-count policy (``attn_decode_num_splits``)."""
     return int(lib().attn_decode_num_splits(int(batch), int(n_kv_heads), int(max_kv_len),

@@ -327,6 +327,25 @@ int attn_combine(const float* o_partial, const float* lse_partial, int num_split
   return ATTN_OK;
 }
 
+int attn_quantize_fp8(const attn_bf16* x, uint8_t* codes, float* scales, const float* signs,
+                      int planes, int rows, int head_dim, int block_rows, int transpose,
+                      void* stream) {
+  if (!x || !codes || !scales) return ATTN_ERR_NULL;
+  if (planes < 1 || planes > 65535 || rows < 1 || rows > (1 << 24) ||
+      (block_rows != 0 && block_rows != 128) || (transpose != 0 && transpose != 1))
+    return ATTN_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4) || !aligned(signs, 4))
+    return ATTN_ERR_ALIGN;
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  attn::QuantArgs a{x, codes, scales, signs, planes, rows, head_dim, block_rows, transpose,
+                    static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim)))};
+  if (attn::launch_quantize(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
 int attn_check_device_status(void* stream) {
   int st = ATTN_OK;
   DeviceState* ds = device_state(&st);

@@ -76,12 +76,24 @@ struct CombineArgs {
   float* lse;
 };
 
+struct QuantArgs {
+  const uint16_t* x;    // (planes, rows, head_dim) bf16
+  uint8_t* codes;       // (planes, rows, head_dim) or, transposed, (planes, head_dim, rows) e4m3
+  float* scales;        // (planes, ceil(rows / 128)) or (planes,) when block_rows == 0
+  const float* signs;   // (head_dim,) +-1 for the rotation, or null
+  int planes, rows, head_dim;
+  int block_rows;       // 128: one scale per 128 rows; 0: one scale per plane
+  int transpose;
+  float inv_sqrt_d;     // float32 value of 1 / sqrt(head_dim)
+};
+
 // Each returns cudaSuccess or the launch error.  Arguments are already
 // validated by the caller.
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_decode(const DecodeArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_combine(const CombineArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_wait_selftest(const LaunchCtx& ctx);
+cudaError_t launch_quantize(const QuantArgs& a, const LaunchCtx& ctx);
 
 // Resolves the current device's launch context (architecture check, error
 // word, SM count) for a call on `stream`; returns an attn_status code.

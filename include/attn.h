@@ -240,6 +240,34 @@ int attn_decode_append_splitkv(const attn_bf16* q, const attn_bf16* k_new,
                                float scale, void* stream);
 
 /*
+ * attn_quantize_fp8 -- FP8 (e4m3) block quantisation with optional
+ * incoherent processing, the input preparation of attn_prefill_fp8.
+ *
+ * Page: same, section "Interaction with post-trained models" (FlashAttention-3's
+ * FP8 path lowers the error of naive FP8 attention by block quantisation and
+ * incoherent processing) and section "The line of work".
+ *
+ *   x         : (planes, rows, head_dim) bf16, 16-byte aligned
+ *   signs     : (head_dim,) fp32 +-1, or NULL.  When given, every row is first
+ *               multiplied by diag(signs) H / sqrt(head_dim), H the Sylvester
+ *               Hadamard matrix (pass the same signs for Q and K, none for V)
+ *   block_rows: 128 -> one scale per block of 128 rows of a plane;
+ *               0   -> one scale per plane
+ *   codes     : e4m3 output, (planes, rows, head_dim), or with transpose = 1
+ *               (planes, head_dim, rows); 16-byte aligned
+ *   scales    : fp32 output, (planes, ceil(rows / 128)) or (planes,): each
+ *               block's amax / 448; codes = e4m3(x * (448 / amax)), rounded to
+ *               nearest, ties to even, saturating (amax 0 counts as 1)
+ * Every step is float32 with round-to-nearest: the rotation's butterflies run
+ * with stride 1, 2, 4, ..., head_dim/2 and end with one multiply by the
+ * float32 value of 1/sqrt(head_dim).
+ * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _ALIGN, _ARCH, _LAUNCH.
+ */
+int attn_quantize_fp8(const attn_bf16* x, uint8_t* codes, float* scales, const float* signs,
+                      int planes, int rows, int head_dim, int block_rows, int transpose,
+                      void* stream);
+
+/*
  * attn_combine -- merge per-split partial results by their LSE weights.
  *
  * Page: same, section "The online softmax, with every symbol defined" (the
