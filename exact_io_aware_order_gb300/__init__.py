@@ -20,5 +20,6 @@ from .api import (  # noqa: F401
     decode_append_splitkv,
     decode_append,
     quantize_fp8,
+    prefill_fp8,
 )
 from ._lib import AttnError, lib  # noqa: F401

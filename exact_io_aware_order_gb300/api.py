@@ -115,6 +115,34 @@ def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
     return out, lse
 
 
+def prefill_fp8(q8: torch.Tensor, k8: torch.Tensor, v8t: torch.Tensor, q_scales: torch.Tensor,
+                k_scales: torch.Tensor, v_scales: torch.Tensor, scale: float, causal: bool = True,
+                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                stream=None):
+    """Prefill on FP8 inputs from :func:`quantize_fp8` (``attn_prefill_fp8``):
+    q8 (B, n_q, N, 128) and k8 (B, n_kv, N, 128) e4m3 codes (uint8), v8t
+    (B, n_kv, 128, N) transposed, their block / head scales.  Returns
+    (O (B, n_q, N, 128) fp32, LSE (B, n_q, N) fp32)."""
+    for t, name in ((q8, "q8"), (k8, "k8"), (v8t, "v8t")):
+        _need(t, name, torch.uint8, 4)
+    B, n_q, N, d = q8.shape
+    n_kv = k8.shape[1]
+    if k8.shape != (B, n_kv, N, d) or v8t.shape != (B, n_kv, d, N):
+        raise ValueError("k8 must be (B, n_kv, N, d) and v8t (B, n_kv, d, N)")
+    for t, name in ((q_scales, "q_scales"), (k_scales, "k_scales"), (v_scales, "v_scales")):
+        _need(t, name, torch.float32, t.dim())
+    if out is None:
+        out = torch.empty((B, n_q, N, d), dtype=torch.float32, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, n_q, N), dtype=torch.float32, device=q8.device)
+    st = lib().attn_prefill_fp8(q8.data_ptr(), k8.data_ptr(), v8t.data_ptr(), q_scales.data_ptr(),
+                                k_scales.data_ptr(), v_scales.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, n_q, n_kv, N, d, float(scale),
+                                int(bool(causal)), _stream(stream))
+    check("attn_prefill_fp8", st)
+    return out, lse
+
+
 def quantize_fp8(x: torch.Tensor, signs: Optional[torch.Tensor] = None, block_rows: int = 128,
                  transpose: bool = False, stream=None):
     """FP8 (e4m3) block quantisation with optional incoherent rotation

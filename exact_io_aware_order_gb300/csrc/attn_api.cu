@@ -327,6 +327,34 @@ int attn_combine(const float* o_partial, const float* lse_partial, int num_split
   return ATTN_OK;
 }
 
+int attn_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_t* v_t,
+                     const float* q_scales, const float* k_scales, const float* v_scales,
+                     float* o, float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen,
+                     int head_dim, float scale, int causal, void* stream) {
+  if (!q || !k || !v_t || !q_scales || !k_scales || !v_scales || !o || !lse) return ATTN_ERR_NULL;
+  if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || seqlen < 16 || seqlen > (1 << 24) ||
+      seqlen % 16 != 0 || (long long)batch * n_q_heads > (1LL << 20) || !valid_scale(scale))
+    return ATTN_ERR_SHAPE;  // v_t rows are seqlen bytes: a multiple of 16 for the copies
+  if ((long long)batch * n_q_heads * ((seqlen + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  if (head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v_t, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(q_scales, 4) || !aligned(k_scales, 4) || !aligned(v_scales, 4))
+    return ATTN_ERR_ALIGN;
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  attn::PrefillArgs a{reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint16_t*>(k),
+                      reinterpret_cast<const uint16_t*>(v_t), o, lse, batch, n_q_heads,
+                      n_kv_heads, seqlen, head_dim, scale, causal ? 1 : 0};
+  a.fp8 = 1;
+  a.q_scales = q_scales;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
+  if (attn::launch_prefill(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
 int attn_quantize_fp8(const attn_bf16* x, uint8_t* codes, float* scales, const float* signs,
                       int planes, int rows, int head_dim, int block_rows, int transpose,
                       void* stream) {

@@ -37,6 +37,13 @@ struct PrefillArgs {
   int window_left = -1;
   float softcap = 0.f;
   const float* alibi_slopes = nullptr;  // (n_q_heads,): adds -slope_h * |i - j|
+  // FP8 inputs: q, k are e4m3 (planes, seqlen, head_dim), v e4m3 transposed
+  // (planes, head_dim, seqlen); their dequantisation scales per 128-row block
+  // (q, k) and per head (v).
+  int fp8 = 0;
+  const float* q_scales = nullptr;
+  const float* k_scales = nullptr;
+  const float* v_scales = nullptr;
 };
 
 // Largest number of packed sequences per variable-length prefill call.

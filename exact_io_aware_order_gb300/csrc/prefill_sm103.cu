@@ -65,13 +65,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max grows > 2^8
 
-template <int D, bool VARLEN>
+// ESZ: bytes per element of Q, K and V (2: bf16; 1: e4m3).
+template <int D, bool VARLEN, int ESZ = 2>
 struct PrefillSmem {
-  static constexpr int kTileBytes = 128 * D * 2;       // one Q, K or V tile
-  static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 64 bf16 (one swizzle span)
+  static constexpr int kTileBytes = 128 * D * ESZ;     // one Q, K or V tile
+  static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 128 B (one swizzle span)
+  static constexpr int kChunks = D * ESZ / 128;        // swizzle spans per row
   static constexpr int kQSlots = 2;
-  static constexpr int kKSlots = D == 128 ? 2 : 4;
-  static constexpr int kVSlots = D == 128 ? 2 : 6;
+  static constexpr int kKSlots = kTileBytes == 32768 ? 2 : 4;
+  static constexpr int kVSlots = kTileBytes == 32768 ? 2 : 6;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQSlots * kTileBytes;
   static constexpr int kV = kK + kKSlots * kTileBytes;
@@ -107,6 +109,11 @@ struct PrefillParams {
   int total_tiles;  // n_q_tiles * batch * n_q_heads (padded mode)
   const int32_t* cu_seqlens;  // packed mode: (num_seqs + 1) row offsets
   int num_seqs;
+  // FP8: dequantisation scales of the e4m3 inputs, per 128-row block of Q and
+  // K ((plane, n_q_tiles)) and per head of V ((plane,)).
+  const float* q_scales;
+  const float* k_scales;
+  const float* v_scales;
   uint32_t* err_word;
   uint64_t timeout_ns;
 };
@@ -142,7 +149,7 @@ struct SeqTables {
 // Kernel flavours: the plain kernel, one with a sliding window, one with a
 // window and / or soft-capping, one with ALiBi and an optional window (the
 // window and the cap are set at run time).
-enum Variant : int { kPlain = 0, kWindow = 1, kWindowCap = 2, kWindowAlibi = 3 };
+enum Variant : int { kPlain = 0, kWindow = 1, kWindowCap = 2, kWindowAlibi = 3, kFp8 = 4 };
 
 template <bool VARLEN, int VARIANT>
 __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const SeqTables& st) {
@@ -205,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const PrefillParams p) {
-  using L = PrefillSmem<D, VARLEN>;
+  constexpr bool FP8 = VARIANT == kFp8;
+  using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2>;
   constexpr int RQ = L::kQSlots, RK = L::kKSlots, RV = L::kVSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -319,8 +327,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   // within item r, key tiles j = 0 .. n-1.  Ring slots and barrier phases
   // follow the running count over all items (g for key tiles), so the
   // pipeline does not drain between items.
-  const uint32_t id_s = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
-  const uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);    // V is MN-major
+  // bf16: Q, K K-major, V MN-major.  e4m3: all K-major (V arrives transposed).
+  const uint32_t id_s = FP8 ? idesc_e4m3_f32(kBM, kBN) : idesc_bf16_f32(kBM, kBN, false, false);
+  const uint32_t id_pv = FP8 ? idesc_e4m3_f32(kBM, D) : idesc_bf16_f32(kBM, D, false, true);
   const uint32_t dhi = sw128_desc_hi(1024);
 
   if (warp == kProducerWarp) {
@@ -349,14 +358,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
       };
       int nq = 0, nk = 0, nv = 0;  // tiles issued
+      // `row`: first row of the tile in the tensor; a transposed tile (FP8
+      // V, (plane, d, rows)) takes its rows along the innermost dimension.
       auto load_tile = [&](const CUtensorMap* map, int base, int full, int empty, int R, int cnt,
-                           int y, int z) -> bool {
+                           int row, int z, bool transposed) -> bool {
         const int slot = cnt % R;
         if (cnt >= R && !mbar_wait(bar(empty + slot), ((cnt / R) - 1) & 1, ctl)) return false;
         mbar_arrive_expect_tx(bar(full + slot), (uint32_t)L::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem_u32(smem + base + slot * L::kTileBytes + c * L::kChunkBytes), map,
-                      bar(full + slot), c * 64, y, z);
+        for (int c = 0; c < L::kChunks; ++c) {
+          const uint32_t dst = smem_u32(smem + base + slot * L::kTileBytes + c * L::kChunkBytes);
+          if (transposed)
+            tma_load_3d(dst, map, bar(full + slot), row, c * 128, z);
+          else
+            tma_load_3d(dst, map, bar(full + slot), c * (128 / (FP8 ? 1 : 2)), row, z);
+        }
         return true;
       };
       Cursor kc, vc;
@@ -365,11 +380,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       auto load_k = [&]() -> bool {
         if (kc.w < 0) return true;
         if (kc.j == 0) {
-          if (!load_tile(&tm_q, L::kQ, kQFull, kQEmpty, RQ, nq, kc.t.row0, kc.t.zq)) return false;
+          if (!load_tile(&tm_q, L::kQ, kQFull, kQEmpty, RQ, nq, kc.t.row0, kc.t.zq, false))
+            return false;
           ++nq;
         }
         if (!load_tile(&tm_k, L::kK, kKFull, kKEmpty, RK, nk, kc.t.kv0 + (kc.t.j0 + kc.j) * kBN,
-                       kc.t.zk))
+                       kc.t.zk, false))
           return false;
         ++nk;
         advance(kc);
@@ -378,7 +394,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       bool ok = load_k() && load_k();
       while (ok && vc.w >= 0) {
         ok = load_tile(&tm_v, L::kV, kVFull, kVEmpty, RV, nv, vc.t.kv0 + (vc.t.j0 + vc.j) * kBN,
-                       vc.t.zk);
+                       vc.t.zk, FP8);
         if (!ok) break;
         ++nv;
         advance(vc);
@@ -413,10 +429,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           if (!mbar_wait(bar(kKFull + slot), (g / RK) & 1, ctl)) { ok = false; break; }
           const uint32_t kb = k_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
           const uint32_t dS = tmem + (uint32_t)(b * 128);
+          // k steps of 32 bytes (16 bf16 or 32 e4m3) along each 128-byte span
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < D * (FP8 ? 1 : 2) / 32; ++kk) {
             const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
-            mma_ss_lo(dS, q_lo + off, kb + off, dhi, id_s, kk > 0);
+            if constexpr (FP8)
+              mma_ss_lo_f8(dS, q_lo + off, kb + off, dhi, id_s, kk > 0);
+            else
+              mma_ss_lo(dS, q_lo + off, kb + off, dhi, id_s, kk > 0);
           }
           mma_commit(bar(kSFull + b));
           mma_commit(bar(kKEmpty + slot));
@@ -433,7 +453,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   } else if (warp == kPVWarp) {
     // ============================ O += P V issuer ============================
     if (lane == 0) {
-      const uint32_t v_lo0 = sw128_desc_lo(smem_u32(smem + L::kV), L::kChunkBytes);
+      // bf16 V: MN-major, the head dimension's two 64-column halves one
+      // chunk apart (LBO); e4m3 V^T: K-major like K.
+      const uint32_t v_lo0 = sw128_desc_lo(smem_u32(smem + L::kV), FP8 ? 16 : L::kChunkBytes);
       bool ok = true;
       int g = 0;
       for (int r = 0; ok; ++r) {
@@ -453,9 +475,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const uint32_t vb = v_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
           const uint32_t aP = tmem + (uint32_t)(b * 128);
           const uint32_t acc0 = j > 0 ? 1u : 0u;
+          if constexpr (FP8) {
+            // 32 keys per step: 8 columns of P (four e4m3 per column), 32 bytes of each V^T row
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts_lo(tO, aP + kk * 8, vb + ((kk * 16 * 128) >> 4), dhi, id_pv, kk > 0 ? 1u : acc0);
+            for (int kk = 0; kk < kBN / 32; ++kk)
+              mma_ts_lo_f8(tO, aP + kk * 8, vb + ((kk * 32) >> 4), dhi, id_pv, kk > 0 ? 1u : acc0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts_lo(tO, aP + kk * 8, vb + ((kk * 16 * 128) >> 4), dhi, id_pv,
+                        kk > 0 ? 1u : acc0);
+          }
           mma_commit(bar(kVEmpty + slot));
           mma_commit(bar(kPVDone + b));
           if (j == n - 1) mma_commit(bar(kOFull));
@@ -487,8 +517,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         alibi_l2 = p.alibi_slopes[t.zq % p.n_q_heads] * kLog2e;
         sl2 = 1.f;
       }
+      // FP8: the scores carry the Q block's scale (here) and the K block's
+      // (per key tile, below).
+      float q_scale = 1.f;
+      if constexpr (FP8) q_scale = p.q_scales[(size_t)t.zq * p.n_q_tiles + t.qrel / kBM];
       for (int j = 0; j < t.n; ++j, ++g) {
         const int b = g % kSBuf;
+        if constexpr (FP8)
+          sl2 = p.sl2 * q_scale * p.k_scales[(size_t)t.zk * p.n_q_tiles + t.j0 + j];
         if (!mbar_wait_warp(bar(kSFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tSm = tmem + (uint32_t)(b * 128) + lane_base;
@@ -568,15 +604,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t pk[16];
+          if constexpr (FP8) {
+            // e4m3 P: four keys per 32-bit column, key k in byte k % 4
+            uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2v, nmv);
-            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            rs[i & 3] = add2(rs[i & 3], pp);
-            pk[i] = pack_bf16x2(pp.x, pp.y);
+            for (int i = 0; i < 8; ++i) {
+              const float2 x0 = fma2(make_float2(s[c * 32 + 4 * i], s[c * 32 + 4 * i + 1]), sl2v, nmv);
+              const float2 x1 =
+                  fma2(make_float2(s[c * 32 + 4 * i + 2], s[c * 32 + 4 * i + 3]), sl2v, nmv);
+              const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+              const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+              rs[(2 * i) & 3] = add2(rs[(2 * i) & 3], p0);
+              rs[(2 * i + 1) & 3] = add2(rs[(2 * i + 1) & 3], p1);
+              pk[i] = e4m3x2_pack(p0.y, p0.x) | (e4m3x2_pack(p1.y, p1.x) << 16);
+            }
+            tmem_st8(tSm + c * 8, pk);
+          } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2v, nmv);
+              const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              rs[i & 3] = add2(rs[i & 3], pp);
+              pk[i] = pack_bf16x2(pp.x, pp.y);
+            }
+            tmem_st16(tSm + c * 16, pk);
           }
-          tmem_st16(tSm + c * 16, pk);
         }
         const float2 rsum = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
         l += rsum.x + rsum.y;
@@ -640,7 +693,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (!mbar_wait_warp(bar(kStFull + ss), (r >> 1) & 1, ctl)) { ok = false; break; }
       const float2 ml = stats[ss * 128 + row];
       mbar_arrive(bar(kStEmpty + ss));
-      const float inv_l = 1.f / ml.y;
+      const float inv_l = (FP8 ? p.v_scales[t.zk] : 1.f) / ml.y;  // FP8: V's per-head scale
       const int row0 = t.row0 + quarter * 32;  // tensor row of this warp's box
       // Rows of the box inside the sequence.  A padded batch's boxes end at
       // the tensor's end, where the copy clips; a packed sequence's last box
@@ -728,6 +781,19 @@ bool make_map(CUtensorMap* m, const void* base, int D, int rows, int planes) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// e4m3 (planes, rows, inner): box = 128 x 128 x 1 (128-byte rows), 128-byte swizzle.
+bool make_map_u8(CUtensorMap* m, const void* base, int inner, int rows, int planes) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)inner, (cuuint64_t)inner * (cuuint64_t)rows};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 output (planes, rows, D): box = 32 x 32 x 1 (128-byte rows), 128-byte swizzle.
 bool make_out_map(CUtensorMap* m, void* base, int D, int rows, int planes) {
   EncodeTiledFn enc = get_encode_fn();
@@ -743,7 +809,8 @@ bool make_out_map(CUtensorMap* m, void* base, int D, int rows, int planes) {
 
 template <int D, bool VARLEN, int VARIANT>
 cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
-  using L = PrefillSmem<D, VARLEN>;
+  constexpr bool FP8 = VARIANT == kFp8;
+  using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2>;
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -754,11 +821,18 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
     if (dev < 64) configured[dev] = true;
   }
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, a.q, D, a.seqlen, a.batch * a.n_q_heads) ||
-      !make_map(&mk, a.k, D, a.seqlen, a.batch * a.n_kv_heads) ||
-      !make_map(&mv, a.v, D, a.seqlen, a.batch * a.n_kv_heads) ||
-      !make_out_map(&mo, a.o, D, a.seqlen, a.batch * a.n_q_heads))
+  if (FP8) {
+    // Q, K (planes, rows, D) and V transposed (planes, D, rows), e4m3
+    if (!make_map_u8(&mq, a.q, D, a.seqlen, a.batch * a.n_q_heads) ||
+        !make_map_u8(&mk, a.k, D, a.seqlen, a.batch * a.n_kv_heads) ||
+        !make_map_u8(&mv, a.v, a.seqlen, D, a.batch * a.n_kv_heads))
+      return cudaErrorInvalidValue;
+  } else if (!make_map(&mq, a.q, D, a.seqlen, a.batch * a.n_q_heads) ||
+             !make_map(&mk, a.k, D, a.seqlen, a.batch * a.n_kv_heads) ||
+             !make_map(&mv, a.v, D, a.seqlen, a.batch * a.n_kv_heads)) {
     return cudaErrorInvalidValue;
+  }
+  if (!make_out_map(&mo, a.o, D, a.seqlen, a.batch * a.n_q_heads)) return cudaErrorInvalidValue;
   PrefillParams pp;
   pp.o = a.o;
   pp.lse = a.lse;
@@ -771,6 +845,9 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   pp.window_left = a.window_left;
   pp.cap_in2 = a.softcap > 0.f ? 2.f * kLog2e * a.scale / a.softcap : 0.f;
   pp.alibi_slopes = a.alibi_slopes;
+  pp.q_scales = a.q_scales;
+  pp.k_scales = a.k_scales;
+  pp.v_scales = a.v_scales;
   pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM;
   pp.total_tiles = pp.n_q_tiles * a.batch * a.n_q_heads;
   pp.cu_seqlens = a.cu_seqlens;
@@ -797,6 +874,10 @@ cudaError_t launch_prefill_cap(const PrefillArgs& a, const LaunchCtx& ctx) {
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx) {
+  if (a.fp8) {
+    if (a.head_dim != 128 || a.cu_seqlens) return cudaErrorInvalidValue;
+    return launch_prefill_t<128, false, kFp8>(a, ctx);
+  }
   const bool varlen = a.cu_seqlens != nullptr;
   if (a.head_dim == 128)
     return varlen ? launch_prefill_cap<128, true>(a, ctx) : launch_prefill_cap<128, false>(a, ctx);

@@ -240,6 +240,32 @@ int attn_decode_append_splitkv(const attn_bf16* q, const attn_bf16* k_new,
                                float scale, void* stream);
 
 /*
+ * attn_prefill_fp8 -- causal (or full) prefill on FP8 inputs prepared by
+ * attn_quantize_fp8.
+ *
+ * Page: same, section "Interaction with post-trained models" (FlashAttention-3's
+ * FP8 path: block quantisation and incoherent processing) and section "Prefill:
+ * tiles, loop order and the tensor cores" for everything else.
+ *
+ *   q        : (batch, n_q_heads,  seqlen, 128) e4m3, 16-byte aligned (rotated if
+ *              k is: pass the same signs to attn_quantize_fp8 for both)
+ *   k        : (batch, n_kv_heads, seqlen, 128) e4m3
+ *   v_t      : (batch, n_kv_heads, 128, seqlen) e4m3 (transposed)
+ *   q_scales : (batch, n_q_heads,  ceil(seqlen/128)) fp32 block scales
+ *   k_scales : (batch, n_kv_heads, ceil(seqlen/128)) fp32 block scales
+ *   v_scales : (batch, n_kv_heads) fp32 per-head scales
+ *   o, lse, scale, causal: as attn_prefill (o is the attention of the
+ *              dequantised inputs).  P is rounded to e4m3 for the P V product.
+ * Limits: head_dim 128; seqlen a multiple of 16 (the rows of v_t are
+ *   seqlen bytes); the other limits of attn_prefill.
+ * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
+ */
+int attn_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_t* v_t,
+                     const float* q_scales, const float* k_scales, const float* v_scales,
+                     float* o, float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen,
+                     int head_dim, float scale, int causal, void* stream);
+
+/*
  * attn_quantize_fp8 -- FP8 (e4m3) block quantisation with optional
  * incoherent processing, the input preparation of attn_prefill_fp8.
  *

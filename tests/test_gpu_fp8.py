@@ -45,3 +45,79 @@ def test_quantizer_bit_exact(dev, planes, rows, d, rot, block, transpose):
         got = got.transpose(0, 2, 1)
     assert np.array_equal(got, ref_codes)
     assert np.array_equal(scales.cpu().numpy().reshape(ref_scales.shape), ref_scales)
+
+
+def fp8_inputs(x, dev, signs, block=128):
+    """GPU FP8 inputs of a prefill workload: rotated + block-quantised Q, K,
+    per-head V (transposed)."""
+    sg = torch.from_numpy(signs).to(dev) if signs is not None else None
+    q8, qs = attn.quantize_fp8(x.q.to(dev), sg, block_rows=block)
+    k8, ks = attn.quantize_fp8(x.k.to(dev), sg, block_rows=block)
+    v8t, vs = attn.quantize_fp8(x.v.to(dev), None, block_rows=0, transpose=True)
+    if block == 0:   # one scale per head for Q and K too: present it per block
+        nb = -(-x.q.shape[2] // 128)
+        qs = qs.unsqueeze(-1).expand(*qs.shape, nb).contiguous()
+        ks = ks.unsqueeze(-1).expand(*ks.shape, nb).contiguous()
+    return q8, k8, v8t, qs, ks, vs
+
+
+def p_rounding_sigma(qz, scale, causal):
+    """Predicted rms of the O error from rounding P to e4m3: each P is off by
+    a relative error uniform in +-2^-4 (rms 2^-4 / sqrt 3), so
+    sigma_ij = 0.036 sqrt(sum_k P_ik^2 v_kj^2) with P normalised."""
+    qd = F.dequantize(qz["qc"], qz["qs"], 128)
+    kd = F.dequantize(qz["kc"], qz["ks"], 128)
+    vd = qz["vc"] * np.asarray(qz["vs"], dtype=np.float64)[..., None, None]
+    B, nq, N, d = qd.shape
+    g = nq // kd.shape[1]
+    sig = np.zeros(qd.shape)
+    for b in range(B):
+        for h in range(nq):
+            s = scale * qd[b, h] @ kd[b, h // g].T
+            if causal:
+                s = np.where(np.tril(np.ones((N, N), dtype=bool)), s, -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            sig[b, h] = (2.0 ** -4 / np.sqrt(3.0)) * np.sqrt((p ** 2) @ (vd[b, h // g] ** 2))
+    return sig
+
+
+@pytest.mark.parametrize("N,Hq,Hkv,causal", [(1024, 8, 2, True), (768, 4, 4, False),
+                                             (2048, 4, 1, True)])
+def test_prefill_fp8_parity(dev, N, Hq, Hkv, causal):
+    from exact_io_aware_order_gb300 import workloads as W
+
+    x = W.make_prefill(1, Hq, Hkv, N, 128, seed=N + Hq, causal=causal)
+    signs = signs_for(128, 11)
+    q8, k8, v8t, qs, ks, vs = fp8_inputs(x, dev, signs)
+    o, lse = attn.prefill_fp8(q8, k8, v8t, qs, ks, vs, x.scale, causal)
+    attn.check_device_status()
+    qz = F.quantize_for_attention(x.q, x.k, x.v, signs)
+    # the GPU's codes are the oracle's (checked bit for bit above); the attention:
+    o_ref, lse_ref = F.prefill_fp8(qz, x.scale, causal)
+    lerr = np.abs(lse.double().cpu().numpy() - lse_ref).max()
+    assert lerr <= 1e-3, lerr
+    sig = p_rounding_sigma(qz, x.scale, causal)
+    err = np.abs(o.double().cpu().numpy() - o_ref)
+    z = err / (sig + 1e-6)
+    assert z.max() <= 6.0, (z.max(), err.max())
+    assert z.mean() <= 1.0, z.mean()                 # ~0.8 for normally distributed errors
+
+
+def test_fp8_block_quantisation_and_rotation_lower_the_error(dev):
+    """Against exact attention on the unquantised inputs, the GPU FP8 path
+    with block scales and the rotation errs much less than with one scale per
+    head and no rotation, on queries and keys with outlier channels."""
+    from exact_io_aware_order_gb300 import workloads as W
+    import oracle
+
+    x = W.make_prefill(1, 8, 2, 1024, 128, seed=3)
+    x.q[..., :4] *= 20.0
+    x.k[..., :4] *= 20.0
+    o_exact, _ = oracle.prefill(x.q, x.k, x.v, x.scale, True)
+    errs = {}
+    for name, signs, block in (("naive", None, 0), ("block+rotation", signs_for(128, 2), 128)):
+        o, _ = attn.prefill_fp8(*fp8_inputs(x, dev, signs, block), x.scale, True)
+        errs[name] = np.sqrt(np.mean((o.double().cpu().numpy() - o_exact) ** 2))
+    attn.check_device_status()
+    assert errs["naive"] / errs["block+rotation"] > 1.5, errs
