@@ -51,7 +51,10 @@ namespace attn {
 namespace {
 
 constexpr int kBM = 128;                 // rows per query tile
-constexpr int kBN = 128;                 // keys per key/value tile
+// Keys per key/value tile: 128, or 64 for head_dim 256 (three S buffers of
+// 64 columns and O's 256 columns then fit the 512 TMEM columns).
+template <int D>
+constexpr int key_tile() { return D == 256 ? 64 : 128; }
 constexpr int kThreads = 352;            // 11 warps
 constexpr int kSoftmaxThreads = 128;     // warps 0-3: one query row per thread
 constexpr int kProducerWarp = 4;
@@ -68,14 +71,17 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max gro
 // ESZ: bytes per element of Q, K and V (2: bf16; 1: e4m3).
 template <int D, bool VARLEN, int ESZ = 2>
 struct PrefillSmem {
-  static constexpr int kTileBytes = 128 * D * ESZ;     // one Q, K or V tile
-  static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 128 B (one swizzle span)
+  static constexpr int kBNt = key_tile<D>();
+  static constexpr int kQTileBytes = 128 * D * ESZ;    // one Q tile (128 rows)
+  static constexpr int kTileBytes = kBNt * D * ESZ;    // one K or V tile
+  static constexpr int kQChunkBytes = 128 * 128;       // 128 rows x 128 B (one swizzle span)
+  static constexpr int kChunkBytes = kBNt * 128;       // K / V: kBNt rows x 128 B
   static constexpr int kChunks = D * ESZ / 128;        // swizzle spans per row
-  static constexpr int kQSlots = 2;
+  static constexpr int kQSlots = D == 256 ? 1 : 2;     // a 64 KB Q tile leaves room for one
   static constexpr int kKSlots = kTileBytes == 32768 ? 2 : 4;
   static constexpr int kVSlots = kTileBytes == 32768 ? 2 : 6;
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQSlots * kTileBytes;
+  static constexpr int kK = kQ + kQSlots * kQTileBytes;
   static constexpr int kV = kK + kKSlots * kTileBytes;
   static constexpr int kStage = kV + kVSlots * kTileBytes;     // O staging: 4 warps x 32 rows x 128 B
   static constexpr int kBar = kStage + 4 * 4096;
@@ -151,7 +157,7 @@ struct SeqTables {
 // window and the cap are set at run time).
 enum Variant : int { kPlain = 0, kWindow = 1, kWindowCap = 2, kWindowAlibi = 3, kFp8 = 4 };
 
-template <bool VARLEN, int VARIANT>
+template <bool VARLEN, int VARIANT, int kBN>
 __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const SeqTables& st) {
   Tile t;
   if constexpr (!VARLEN) {
@@ -165,7 +171,7 @@ __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const Seq
     t.len = p.seqlen;
     t.zq = bidx * p.n_q_heads + h;
     t.zk = bidx * p.n_kv_heads + kvh;
-    t.n = p.causal ? (qt + 1) : (p.seqlen + kBN - 1) / kBN;
+    t.n = p.causal ? (qt + 1) * kBM / kBN : (p.seqlen + kBN - 1) / kBN;
   } else {
     // The sequence: the last one whose first item is at or before w (a
     // sequence without items shares its prefix with the next one).
@@ -184,7 +190,7 @@ __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const Seq
     t.len = st.len[lo];
     t.zq = h;
     t.zk = h / (p.n_q_heads / p.n_kv_heads);
-    t.n = p.causal ? (qt + 1) : tiles;
+    t.n = p.causal ? (qt + 1) * kBM / kBN : (t.len + kBN - 1) / kBN;
   }
   // A sliding window skips the key tiles left of every row's window: the
   // tile's first row sees keys from qrel - window_left on.
@@ -213,6 +219,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const PrefillParams p) {
   constexpr bool FP8 = VARIANT == kFp8;
+  constexpr int kBN = key_tile<D>();
   using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2>;
   constexpr int RQ = L::kQSlots, RK = L::kKSlots, RV = L::kVSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -318,8 +325,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S buffers [0,128), [128,256), [256,384) | O [384, 384+D)
-  const uint32_t tO = tmem + 384u;
+  // TMEM columns: S buffers [0, kBN), [kBN, 2 kBN), [2 kBN, 3 kBN) | O [3 kBN, 3 kBN + D)
+  const uint32_t tO = tmem + 3u * kBN;
   const WaitCtl ctl{abort_flag, p.err_word, p.timeout_ns};
   const int total = VARLEN ? item_prefix[p.num_seqs] : p.total_tiles;
 
@@ -348,13 +355,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         c.r = 0;
         c.j = 0;
         c.w = item_of(0, total);
-        if (c.w >= 0) c.t = tile_of<VARLEN, VARIANT>(c.w, p, seqt);
+        if (c.w >= 0) c.t = tile_of<VARLEN, VARIANT, kBN>(c.w, p, seqt);
       };
       auto advance = [&](Cursor& c) {
         if (++c.j == c.t.n) {
           c.j = 0;
           c.w = item_of(++c.r, total);
-          if (c.w >= 0) c.t = tile_of<VARLEN, VARIANT>(c.w, p, seqt);
+          if (c.w >= 0) c.t = tile_of<VARLEN, VARIANT, kBN>(c.w, p, seqt);
         }
       };
       int nq = 0, nk = 0, nv = 0;  // tiles issued
@@ -363,10 +370,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       auto load_tile = [&](const CUtensorMap* map, int base, int full, int empty, int R, int cnt,
                            int row, int z, bool transposed) -> bool {
         const int slot = cnt % R;
+        const bool is_q = base == L::kQ;
+        const int tile_bytes = is_q ? L::kQTileBytes : L::kTileBytes;
+        const int chunk_bytes = is_q ? L::kQChunkBytes : L::kChunkBytes;
         if (cnt >= R && !mbar_wait(bar(empty + slot), ((cnt / R) - 1) & 1, ctl)) return false;
-        mbar_arrive_expect_tx(bar(full + slot), (uint32_t)L::kTileBytes);
+        mbar_arrive_expect_tx(bar(full + slot), (uint32_t)tile_bytes);
         for (int c = 0; c < L::kChunks; ++c) {
-          const uint32_t dst = smem_u32(smem + base + slot * L::kTileBytes + c * L::kChunkBytes);
+          const uint32_t dst = smem_u32(smem + base + slot * tile_bytes + c * chunk_bytes);
           if (transposed)
             tma_load_3d(dst, map, bar(full + slot), row, c * 128, z);
           else
@@ -418,25 +428,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int r = 0; ok; ++r) {
         const int w = item_of(r, total);
         if (w < 0) break;
-        const Tile t = tile_of<VARLEN, VARIANT>(w, p, seqt);
+        const Tile t = tile_of<VARLEN, VARIANT, kBN>(w, p, seqt);
         const int qs = r % RQ;
         if (!mbar_wait(bar(kQFull + qs), (r / RQ) & 1, ctl)) { ok = false; break; }
-        const uint32_t q_lo = sw128_desc_lo(smem_u32(smem + L::kQ + qs * L::kTileBytes), 16);
+        const uint32_t q_lo = sw128_desc_lo(smem_u32(smem + L::kQ + qs * L::kQTileBytes), 16);
         for (int j = 0; j < t.n; ++j, ++g) {
           const int b = g % kSBuf, slot = g % RK;
           // Buffer b last held P(g-3): PV(g-3) must have read it.
           if (g >= kSBuf && !mbar_wait(bar(kPVDone + b), ((g / kSBuf) - 1) & 1, ctl)) { ok = false; break; }
           if (!mbar_wait(bar(kKFull + slot), (g / RK) & 1, ctl)) { ok = false; break; }
           const uint32_t kb = k_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
-          const uint32_t dS = tmem + (uint32_t)(b * 128);
+          const uint32_t dS = tmem + (uint32_t)(b * kBN);
           // k steps of 32 bytes (16 bf16 or 32 e4m3) along each 128-byte span
 #pragma unroll
           for (int kk = 0; kk < D * (FP8 ? 1 : 2) / 32; ++kk) {
-            const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+            const uint32_t qoff = ((kk >> 2) * L::kQChunkBytes + (kk & 3) * 32) >> 4;
+            const uint32_t koff = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
             if constexpr (FP8)
-              mma_ss_lo_f8(dS, q_lo + off, kb + off, dhi, id_s, kk > 0);
+              mma_ss_lo_f8(dS, q_lo + qoff, kb + koff, dhi, id_s, kk > 0);
             else
-              mma_ss_lo(dS, q_lo + off, kb + off, dhi, id_s, kk > 0);
+              mma_ss_lo(dS, q_lo + qoff, kb + koff, dhi, id_s, kk > 0);
           }
           mma_commit(bar(kSFull + b));
           mma_commit(bar(kKEmpty + slot));
@@ -461,7 +472,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int r = 0; ok; ++r) {
         const int w = item_of(r, total);
         if (w < 0) break;
-        const int n = tile_of<VARLEN, VARIANT>(w, p, seqt).n;
+        const int n = tile_of<VARLEN, VARIANT, kBN>(w, p, seqt).n;
         for (int j = 0; j < n; ++j, ++g) {
           const int b = g % kSBuf, slot = g % RV;
           if (!mbar_wait(bar(kPFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
@@ -473,7 +484,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           // B = V tile rows [16kk, 16kk+16): 16 rows x 128 B per k step; the
           // 64-column halves of the head dimension are one chunk apart (LBO).
           const uint32_t vb = v_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
-          const uint32_t aP = tmem + (uint32_t)(b * 128);
+          const uint32_t aP = tmem + (uint32_t)(b * kBN);
           const uint32_t acc0 = j > 0 ? 1u : 0u;
           if constexpr (FP8) {
             // 32 keys per step: 8 columns of P (four e4m3 per column), 32 bytes of each V^T row
@@ -507,7 +518,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int r = 0; ok; ++r) {
       const int w = item_of(r, total);
       if (w < 0) break;
-      const Tile t = tile_of<VARLEN, VARIANT>(w, p, seqt);
+      const Tile t = tile_of<VARLEN, VARIANT, kBN>(w, p, seqt);
       const int q0 = t.qrel, q_row = q0 + row;  // indices within the sequence
       float m = -INFINITY, l = 0.f;   // running max (log2 domain) and sum of the row
       // ALiBi: this head's slope in log2 units; the scores are then biased
@@ -527,7 +538,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           sl2 = p.sl2 * q_scale * p.k_scales[(size_t)t.zk * p.n_q_tiles + t.j0 + j];
         if (!mbar_wait_warp(bar(kSFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tSm = tmem + (uint32_t)(b * 128) + lane_base;
+        const uint32_t tSm = tmem + (uint32_t)(b * kBN) + lane_base;
         // The whole S row: four 32-column loads in flight, one wait.
         float s[kBN];
         {
@@ -680,55 +691,81 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int r = 0; ok; ++r) {
       const int w = item_of(r, total);
       if (w < 0) break;
-      const Tile t = tile_of<VARLEN, VARIANT>(w, p, seqt);
+      const Tile t = tile_of<VARLEN, VARIANT, kBN>(w, p, seqt);
       if (!mbar_wait_warp(bar(kOFull), r & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t acc[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tOm + c * 32, acc[c]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(kOEmpty));  // O may now be overwritten by the next item
       const int ss = r & 1;
-      if (!mbar_wait_warp(bar(kStFull + ss), (r >> 1) & 1, ctl)) { ok = false; break; }
-      const float2 ml = stats[ss * 128 + row];
-      mbar_arrive(bar(kStEmpty + ss));
-      const float inv_l = (FP8 ? p.v_scales[t.zk] : 1.f) / ml.y;  // FP8: V's per-head scale
       const int row0 = t.row0 + quarter * 32;  // tensor row of this warp's box
       // Rows of the box inside the sequence.  A padded batch's boxes end at
       // the tensor's end, where the copy clips; a packed sequence's last box
       // may reach into the next sequence, so it is written row by row.
       const int in_seq = t.len - (t.qrel + quarter * 32);
-      if (!VARLEN || in_seq >= 32) {
+      // O is read kEC columns at a time (all of it for head_dim <= 128).
+      constexpr int kEC = D > 128 ? 128 : D;
+      auto store_cols = [&](const uint32_t (&acc)[kEC / 32][32], int col0, float inv_l) {
+        if (!VARLEN || in_seq >= 32) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
-          __syncwarp();
+          for (int c = 0; c < kEC / 32; ++c) {
+            if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
+            __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            st_shared_v4(stage + lane * 128 + ((i ^ (lane & 7)) << 4),
-                         make_float4(__uint_as_float(acc[c][4 * i]) * inv_l,
-                                     __uint_as_float(acc[c][4 * i + 1]) * inv_l,
-                                     __uint_as_float(acc[c][4 * i + 2]) * inv_l,
-                                     __uint_as_float(acc[c][4 * i + 3]) * inv_l));
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && row0 < N) {  // rows past the tensor's end are clipped by the copy
-            tma_store_3d(&tm_o, stage, c * 32, row0, t.zq);
-            bulk_commit_group();
+            for (int i = 0; i < 8; ++i)
+              st_shared_v4(stage + lane * 128 + ((i ^ (lane & 7)) << 4),
+                           make_float4(__uint_as_float(acc[c][4 * i]) * inv_l,
+                                       __uint_as_float(acc[c][4 * i + 1]) * inv_l,
+                                       __uint_as_float(acc[c][4 * i + 2]) * inv_l,
+                                       __uint_as_float(acc[c][4 * i + 3]) * inv_l));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && row0 < N) {  // rows past the tensor's end are clipped by the copy
+              tma_store_3d(&tm_o, stage, col0 + c * 32, row0, t.zq);
+              bulk_commit_group();
+            }
           }
+        } else if (lane < in_seq) {
+          float* orow = p.o + ((size_t)t.zq * N + (size_t)(row0 + lane)) * D + col0;
+#pragma unroll
+          for (int c = 0; c < kEC / 32; ++c)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              reinterpret_cast<float4*>(orow + c * 32)[i] =
+                  make_float4(__uint_as_float(acc[c][4 * i]) * inv_l,
+                              __uint_as_float(acc[c][4 * i + 1]) * inv_l,
+                              __uint_as_float(acc[c][4 * i + 2]) * inv_l,
+                              __uint_as_float(acc[c][4 * i + 3]) * inv_l);
         }
-      } else if (lane < in_seq) {
-        float* orow = p.o + ((size_t)t.zq * N + (size_t)(row0 + lane)) * D;
+      };
+      float2 ml;
+      if constexpr (D <= 128) {
+        uint32_t acc[kEC / 32][32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c)
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tOm + c * 32, acc[c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(kOEmpty));  // O may now be overwritten by the next item
+        if (!mbar_wait_warp(bar(kStFull + ss), (r >> 1) & 1, ctl)) { ok = false; break; }
+        ml = stats[ss * 128 + row];
+        mbar_arrive(bar(kStEmpty + ss));
+        store_cols(acc, 0, (FP8 ? p.v_scales[t.zk] : 1.f) / ml.y);  // FP8: V's per-head scale
+      } else {
+        // head_dim 256: the row statistics first, then O in two halves; O is
+        // released once its last half has been read.
+        if (!mbar_wait_warp(bar(kStFull + ss), (r >> 1) & 1, ctl)) { ok = false; break; }
+        ml = stats[ss * 128 + row];
+        mbar_arrive(bar(kStEmpty + ss));
+        const float inv_l = 1.f / ml.y;
+#pragma unroll 1
+        for (int h = 0; h < D / kEC; ++h) {
+          uint32_t acc[kEC / 32][32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            reinterpret_cast<float4*>(orow + c * 32)[i] =
-                make_float4(__uint_as_float(acc[c][4 * i]) * inv_l,
-                            __uint_as_float(acc[c][4 * i + 1]) * inv_l,
-                            __uint_as_float(acc[c][4 * i + 2]) * inv_l,
-                            __uint_as_float(acc[c][4 * i + 3]) * inv_l);
+          for (int c = 0; c < kEC / 32; ++c) tmem_ld32(tOm + h * kEC + c * 32, acc[c]);
+          tmem_wait_ld();
+          if (h == D / kEC - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(kOEmpty));
+          }
+          store_cols(acc, h * kEC, inv_l);
+        }
       }
       if (t.qrel + row < t.len && t.row0 + row < N)
         p.lse[(size_t)t.zq * N + t.row0 + row] = (ml.x + __log2f(ml.y)) * kLn2;
@@ -768,13 +805,13 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// (rows, planes) bf16 tensor of shape (planes, rows, D): box = 64 x 128 x 1, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int D, int rows, int planes) {
+// (rows, planes) bf16 tensor of shape (planes, rows, D): box = 64 x box_rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int D, int rows, int planes, int box_rows = 128) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * (cuuint64_t)rows};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -828,8 +865,8 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
         !make_map_u8(&mv, a.v, a.seqlen, D, a.batch * a.n_kv_heads))
       return cudaErrorInvalidValue;
   } else if (!make_map(&mq, a.q, D, a.seqlen, a.batch * a.n_q_heads) ||
-             !make_map(&mk, a.k, D, a.seqlen, a.batch * a.n_kv_heads) ||
-             !make_map(&mv, a.v, D, a.seqlen, a.batch * a.n_kv_heads)) {
+             !make_map(&mk, a.k, D, a.seqlen, a.batch * a.n_kv_heads, key_tile<D>()) ||
+             !make_map(&mv, a.v, D, a.seqlen, a.batch * a.n_kv_heads, key_tile<D>())) {
     return cudaErrorInvalidValue;
   }
   if (!make_out_map(&mo, a.o, D, a.seqlen, a.batch * a.n_q_heads)) return cudaErrorInvalidValue;
@@ -879,6 +916,11 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx) {
     return launch_prefill_t<128, false, kFp8>(a, ctx);
   }
   const bool varlen = a.cu_seqlens != nullptr;
+  if (a.head_dim == 256) {  // the plain padded prefill only
+    if (varlen || a.softcap > 0.f || a.window_left >= 0 || a.alibi_slopes)
+      return cudaErrorInvalidValue;
+    return launch_prefill_t<256, false, kPlain>(a, ctx);
+  }
   if (a.head_dim == 128)
     return varlen ? launch_prefill_cap<128, true>(a, ctx) : launch_prefill_cap<128, false>(a, ctx);
   return varlen ? launch_prefill_cap<64, true>(a, ctx) : launch_prefill_cap<64, false>(a, ctx);

@@ -78,7 +78,8 @@ const char* attn_status_string(int status);
  *   lse : (batch, n_q_heads,  seqlen) fp32 output (natural log), 4-byte aligned
  *   scale: multiplies q.k (pass 1/sqrt(head_dim) for standard attention)
  *   causal: nonzero -> row i attends to keys j <= i; zero -> to every key.
- * Limits: head_dim in {64, 128}; 1 <= seqlen <= 2^24; batch*n_q_heads <= 2^20;
+ * Limits: head_dim in {64, 128, 256} (256: 64-key tiles; see attn_prefill_ex for the
+ *   variants, which take 64 and 128); 1 <= seqlen <= 2^24; batch*n_q_heads <= 2^20;
  *   batch*n_q_heads*ceil(seqlen/128) < 2^31; n_q_heads % n_kv_heads == 0.  bf16 inputs, fp32 accumulation, P rounded
  *   to bf16 before the P*V product.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
@@ -99,7 +100,8 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
  *   alibi_slopes: NULL for none; otherwise (n_q_heads,) fp32 on the device,
  *                4-byte aligned: head h adds -alibi_slopes[h] * |i - j| to the
  *                score of query i and key j (after soft-capping)
- * ALiBi and soft-capping together are ATTN_ERR_SHAPE.  Everything else, and
+ * ALiBi and soft-capping together are ATTN_ERR_SHAPE; any variant with
+ * head_dim 256 is ATTN_ERR_HEADDIM.  Everything else, and
  * the errors, as attn_prefill (a negative window_left other than -1, or a
  * negative or non-finite softcap, is ATTN_ERR_SHAPE).
  */

@@ -115,3 +115,19 @@ def test_repeated_launch_is_deterministic(dev):
     o1, l1 = run_prefill(x, dev)
     o2, l2 = run_prefill(x, dev)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,causal", [
+    (1, 4, 1, 1000, True),     # ragged tail, GQA 4:1
+    (2, 2, 2, 384, True),      # batch, MHA, whole tiles
+    (1, 8, 2, 777, False),     # full attention
+    (1, 2, 1, 64, True),       # one 64-key tile
+    (1, 16, 2, 2048, True),
+])
+def test_head_dim_256(dev, B, Hq, Hkv, N, causal):
+    """head_dim 256 (one of the variants the page lists): 64-key tiles, O in
+    256 TMEM columns, the epilogue in two halves."""
+    x = W.make_prefill(B, Hq, Hkv, N, 256, seed=N + Hq, causal=causal)
+    o, lse = run_prefill(x, dev)
+    o_ref, lse_ref = oracle.prefill(x.q, x.k, x.v, x.scale, causal)
+    compare(o, lse, o_ref, lse_ref, f"d=256 B={B} N={N}")

@@ -65,7 +65,8 @@ def test_prefill_validation(L):
     assert _prefill(L, scale=0.0) == c["ATTN_ERR_SHAPE"]
     assert _prefill(L, scale=float("nan")) == c["ATTN_ERR_SHAPE"]
     assert _prefill(L, d=96) == c["ATTN_ERR_HEADDIM"]
-    assert _prefill(L, d=256) == c["ATTN_ERR_HEADDIM"]
+    assert _prefill(L, d=192) == c["ATTN_ERR_HEADDIM"]
+    assert _prefill(L, d=512) == c["ATTN_ERR_HEADDIM"]
     assert _prefill(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
     assert _prefill(L, q=P + 8) == c["ATTN_ERR_ALIGN"]
     assert _prefill(L, o=P + 4) == c["ATTN_ERR_ALIGN"]
@@ -83,6 +84,8 @@ def test_variant_validation(L):
     assert L.attn_prefill_ex(None, P, P, P, P, 1, 4, 2, 128, 128, 0.1, 1, 5, 1.0, None, None) == \
         c["ATTN_ERR_NULL"]
     assert ex(-1, 2.0, P) == c["ATTN_ERR_SHAPE"]            # ALiBi with soft-capping
+    assert L.attn_prefill_ex(P, P, P, P, P, 1, 4, 2, 128, 256, 0.1, 1, 16, 0.0, None, None) == \
+        c["ATTN_ERR_HEADDIM"]                               # head_dim 256: plain prefill only
     assert ex(-1, 0.0, P + 2) == c["ATTN_ERR_ALIGN"]        # misaligned slopes
     dx = lambda w, cap, al=None: L.attn_decode_splitkv_ex(P, P, P, P, P, 4, P, P, 2, 8, 2, 128, 16,
                                                           8, 16, 128, 0.1, w, cap, al, None)
