@@ -242,6 +242,7 @@ def run_gb300(args, rank: int, world: int, dist):
     app = time_decode_append(args, attn, dq, caches, dec, S, op, lp, sweep, sweep_out, dist, dev)
     vl = time_prefill_varlen(args, attn, W, dist, dev) if args.workload == "qwen" else None
     f8 = time_fp8(args, attn, x, q, k, v, o, lse, dist, dev) if args.workload == "qwen" else None
+    d256 = time_d256(args, attn, W, dist, dev) if args.workload == "qwen" else None
     var = time_variants(args, attn, q, k, v, x.scale, o, lse, dq, caches, dec, S, op, lp, sweep,
                         sweep_out, dist, dev) if args.workload == "qwen" else None
     total_ms = t_start.elapsed_time(t_end)
@@ -295,6 +296,10 @@ def run_gb300(args, rank: int, world: int, dist):
             v_["frac"] = round(v_["value"] / peaks["bf16_tflops"], 4)
         var["decode"]["frac"] = round(var["decode"]["value"] / peaks["hbm_gbs"], 4)
         result["variants"] = var
+    if d256 is not None:
+        d256["roofline"]["peak"] = peaks["bf16_tflops"]
+        d256["roofline"]["frac"] = round(d256["roofline"]["achieved"] / peaks["bf16_tflops"], 4)
+        result["prefill_d256"] = d256
     if f8 is not None:
         f8_peak = peaks["bf16_tflops"] * 2.0   # nominal dense fp8 / bf16 ratio (4.5 / 2.25)
         f8["roofline"]["peak"] = round(f8_peak, 1)
@@ -377,6 +382,41 @@ def time_variants(args, attn, q, k, v, scale, o, lse, dq, caches, dec, S, op, lp
             "decode": {"value": round(job_rate(dbytes, n, world, t_dec) / 1e9, 1), "unit": "GB/s",
                        "window_left": Wl, "bytes_per_launch": dbytes,
                        "avg_launch_us": round(t_dec / n * 1e3, 2)}}
+
+
+def time_d256(args, attn, W, dist, dev):
+    """Causal prefill with head_dim 256 at a Gemma-2-9B-like attention shape
+    (N = 8192, 16 query / 8 kv heads); inputs and output exceed L2."""
+    import torch
+
+    Hq, Hkv, N, D = 16, 8, 8192, 256
+    x = W.make_prefill(1, Hq, Hkv, N, D, seed=0)
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    o = torch.empty((1, Hq, N, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((1, Hq, N), dtype=torch.float32, device=dev)
+    flops = prefill_flops(Hq, N, D)
+    n = max(3, min(args.steps, 100))
+    for _ in range(3):
+        attn.prefill(q, k, v, x.scale, True, out=o, lse=lse)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    for i in range(n):
+        evs[i][0].record()
+        attn.prefill(q, k, v, x.scale, True, out=o, lse=lse)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    attn.check_device_status()
+    (tot,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
+    world = dist.get_world_size() if dist is not None else 1
+    avg_ms = tot / n
+    return {"value": round(job_rate(flops, n, world, tot) / 1e12, 2), "unit": "TFLOP/s",
+            "shape": "N=8192, 16/8 heads, head_dim 256, causal",
+            "roofline": {"bound": "tensor", "achieved": round(flops / (avg_ms * 1e-3) / 1e12, 2),
+                         "unit": "TFLOP/s", "kernel": "prefill_kernel<256>",
+                         "flops_per_launch": flops, "avg_launch_ms": round(avg_ms, 4)}}
 
 
 def time_fp8(args, attn, x, q, k, v, o, lse, dist, dev):
