@@ -299,6 +299,9 @@ def run_gb300(args, rank: int, world: int, dist):
     if d256 is not None:
         d256["roofline"]["peak"] = peaks["bf16_tflops"]
         d256["roofline"]["frac"] = round(d256["roofline"]["achieved"] / peaks["bf16_tflops"], 4)
+        d256["decode"]["roofline"]["peak"] = peaks["hbm_gbs"]
+        d256["decode"]["roofline"]["frac"] = round(
+            d256["decode"]["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
         result["prefill_d256"] = d256
     if f8 is not None:
         f8_peak = peaks["bf16_tflops"] * 2.0   # nominal dense fp8 / bf16 ratio (4.5 / 2.25)
@@ -412,11 +415,61 @@ def time_d256(args, attn, W, dist, dev):
     (tot,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
     world = dist.get_world_size() if dist is not None else 1
     avg_ms = tot / n
-    return {"value": round(job_rate(flops, n, world, tot) / 1e12, 2), "unit": "TFLOP/s",
-            "shape": "N=8192, 16/8 heads, head_dim 256, causal",
-            "roofline": {"bound": "tensor", "achieved": round(flops / (avg_ms * 1e-3) / 1e12, 2),
-                         "unit": "TFLOP/s", "kernel": "prefill_kernel<256>",
-                         "flops_per_launch": flops, "avg_launch_ms": round(avg_ms, 4)}}
+    res = {"value": round(job_rate(flops, n, world, tot) / 1e12, 2), "unit": "TFLOP/s",
+           "shape": "N=8192, 16/8 heads, head_dim 256, causal",
+           "roofline": {"bound": "tensor", "achieved": round(flops / (avg_ms * 1e-3) / 1e12, 2),
+                        "unit": "TFLOP/s", "kernel": "prefill_kernel<256>",
+                        "flops_per_launch": flops, "avg_launch_ms": round(avg_ms, 4)}}
+    del q, k, v, o, lse, x
+
+    # Split-KV decode at the same head shape over a contiguous 30720-token
+    # cache (251 MB of K and V, two copies in rotation: every launch reads HBM).
+    L = 30720
+    dd = W.make_decode_contiguous(1, Hq, Hkv, D, L, seed=1, max_kv_len=L)
+    dq, dlens = dd.q.to(dev), dd.kv_lens.to(dev)
+    caches = [(dd.k_cache.to(dev), dd.v_cache.to(dev)) for _ in range(2)]
+    S = attn.decode_num_splits(1, Hkv, L)
+    op = torch.empty((S, 1, Hq, D), dtype=torch.float32, device=dev)
+    lp = torch.empty((S, 1, Hq), dtype=torch.float32, device=dev)
+    do = torch.empty((1, Hq, D), dtype=torch.float32, device=dev)
+    dl = torch.empty((1, Hq), dtype=torch.float32, device=dev)
+    dbytes = L * Hkv * D * 2 * 2 + dq.numel() * 2 + do.numel() * 4 + dl.numel() * 4
+
+    def dec(i, ev=None):
+        kc, vc = caches[i % 2]
+        if ev is not None:
+            ev[0].record()
+        attn.decode_splitkv(dq, kc, vc, dlens, None, num_splits=S, max_kv_len=L, scale=dd.scale,
+                            o_partial=op, lse_partial=lp)
+        if ev is not None:
+            ev[1].record()
+        attn.combine(op, lp, out=do, lse=dl)
+        if ev is not None:
+            ev[2].record()
+
+    for i in range(3):
+        dec(i)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    for i in range(n):
+        dec(i, evs[i])
+    torch.cuda.synchronize()
+    attn.check_device_status()
+    dec_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    both_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    (tot_d,) = rank_max(dist, [sum(both_ms)], dev)
+    avg_d = statistics.mean(dec_ms)
+    res["decode"] = {"value": round(job_rate(dbytes, n, world, tot_d) / 1e9, 1), "unit": "GB/s",
+                     "shape": f"1 x 30720 tokens, 16/8 heads, head_dim 256, {S} splits",
+                     "roofline": {"bound": "hbm", "achieved": round(dbytes / (avg_d * 1e-3) / 1e9, 1),
+                                  "unit": "GB/s", "kernel": "decode_splitkv_kernel<256>",
+                                  "bytes_per_launch": dbytes,
+                                  "avg_launch_us": round(avg_d * 1e3, 2),
+                                  "combine_avg_us": round(statistics.mean(
+                                      [b - a for a, b in zip(dec_ms, both_ms)]) * 1e3, 2)}}
+    return res
 
 
 def time_fp8(args, attn, x, q, k, v, o, lse, dist, dev):

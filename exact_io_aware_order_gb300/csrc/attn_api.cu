@@ -114,7 +114,7 @@ const char* attn_status_string(int status) {
     case ATTN_OK: return "ATTN_OK";
     case ATTN_ERR_NULL: return "ATTN_ERR_NULL: a required pointer is NULL";
     case ATTN_ERR_SHAPE: return "ATTN_ERR_SHAPE: a size or the scale is out of range";
-    case ATTN_ERR_HEADDIM: return "ATTN_ERR_HEADDIM: head_dim must be 64 or 128";
+    case ATTN_ERR_HEADDIM: return "ATTN_ERR_HEADDIM: head_dim not supported by this call (see its limits)";
     case ATTN_ERR_GQA: return "ATTN_ERR_GQA: n_q_heads must be a multiple of n_kv_heads (decode: ratio <= 16)";
     case ATTN_ERR_SPLITS: return "ATTN_ERR_SPLITS: num_splits out of range";
     case ATTN_ERR_ALIGN: return "ATTN_ERR_ALIGN: a pointer is misaligned";
@@ -252,7 +252,7 @@ int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_n
                 (long long)block_size * max_blocks_per_seq > (1LL << 30)))
     return ATTN_ERR_SHAPE;
   if (!paged && max_kv_len < 1) return ATTN_ERR_SHAPE;
-  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 16) return ATTN_ERR_GQA;
   if (num_splits < 0 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
@@ -317,7 +317,7 @@ int attn_combine(const float* o_partial, const float* lse_partial, int num_split
   if (!o_partial || !lse_partial || !o || !lse) return ATTN_ERR_NULL;
   if (batch < 1 || n_q_heads < 1 || (long long)batch * n_q_heads > (1LL << 31) - 1)
     return ATTN_ERR_SHAPE;
-  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
   if (num_splits < 1 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
   if (!aligned(o_partial, 16) || !aligned(lse_partial, 4) || !aligned(o, 16) || !aligned(lse, 4))
     return ATTN_ERR_ALIGN;

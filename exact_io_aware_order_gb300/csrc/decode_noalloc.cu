@@ -64,7 +64,7 @@ extern "C" int attn_decode_noalloc(const attn_bf16* q, const attn_bf16* k_cache,
                 (long long)block_size * max_blocks_per_seq > (1LL << 30)))
     return ATTN_ERR_SHAPE;
   if (!paged && max_kv_len < 1) return ATTN_ERR_SHAPE;
-  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 16) return ATTN_ERR_GQA;
   if (num_splits < 0 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||

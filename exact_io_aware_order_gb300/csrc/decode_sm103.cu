@@ -549,7 +549,9 @@ constexpr int kCombineBatch = 8;
 
 template <int D>
 __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const CombineArgs a) {
-  constexpr int kLanesPerRow = D / 4;               // float4 per lane
+  constexpr int kVec = D / 4;                       // float4 per partial row
+  constexpr int kLanesPerRow = kVec < 32 ? kVec : 32;
+  constexpr int kPerLane = kVec / kLanesPerRow;     // float4 per lane (2 for head_dim 256)
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;   // splits handled per warp step
   constexpr int kStep = kCombineWarps * kRowsPerWarp;
   const int bh = blockIdx.x;
@@ -558,24 +560,29 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
   const size_t stride_s = (size_t)a.batch * a.n_q_heads;
   const int sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
   __shared__ float s_max[kCombineWarps], s_sum[kCombineWarps];
-  __shared__ float4 s_o[kCombineWarps][kRowsPerWarp][kLanesPerRow];
+  __shared__ float4 s_o[kCombineWarps][kRowsPerWarp][kVec];
   grid_dep_wait();    // the partials come from the decode kernel before us
   grid_dep_launch();
 
   float m = -INFINITY, wsum = 0.f;  // running max / weight sum (natural-log domain)
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[kPerLane];
+#pragma unroll
+  for (int e = 0; e < kPerLane; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = warp * kRowsPerWarp + sub; s0 < S; s0 += kCombineBatch * kStep) {
     float w[kCombineBatch];
-    float4 v[kCombineBatch];
+    float4 v[kCombineBatch][kPerLane];
 #pragma unroll
     for (int u = 0; u < kCombineBatch; ++u) {
       const int s = s0 + u * kStep;
       w[u] = -INFINITY;
-      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < kPerLane; ++e) v[u][e] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (s < S) {
         const size_t idx = (size_t)s * stride_s + bh;
         w[u] = a.lse_partial[idx];
-        v[u] = reinterpret_cast<const float4*>(a.o_partial + idx * D)[li];
+#pragma unroll
+        for (int e = 0; e < kPerLane; ++e)
+          v[u][e] = reinterpret_cast<const float4*>(a.o_partial + idx * D)[li + e * kLanesPerRow];
       }
     }
     float mb = m;
@@ -583,16 +590,22 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
     for (int u = 0; u < kCombineBatch; ++u) mb = fmaxf(mb, w[u]);
     if (mb != -INFINITY) {
       const float c = ex2_approx((m - mb) * kLog2e);  // 0 while m is -inf
-      acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
+#pragma unroll
+      for (int e = 0; e < kPerLane; ++e) {
+        acc[e].x *= c; acc[e].y *= c; acc[e].z *= c; acc[e].w *= c;
+      }
       wsum *= c;
 #pragma unroll
       for (int u = 0; u < kCombineBatch; ++u) {
-        const float e = ex2_approx((w[u] - mb) * kLog2e);  // 0 for an empty split
-        acc.x = fmaf(e, v[u].x, acc.x);
-        acc.y = fmaf(e, v[u].y, acc.y);
-        acc.z = fmaf(e, v[u].z, acc.z);
-        acc.w = fmaf(e, v[u].w, acc.w);
-        wsum += e;
+        const float ew = ex2_approx((w[u] - mb) * kLog2e);  // 0 for an empty split
+#pragma unroll
+        for (int e = 0; e < kPerLane; ++e) {
+          acc[e].x = fmaf(ew, v[u][e].x, acc[e].x);
+          acc[e].y = fmaf(ew, v[u][e].y, acc[e].y);
+          acc[e].z = fmaf(ew, v[u][e].z, acc[e].z);
+          acc[e].w = fmaf(ew, v[u][e].w, acc[e].w);
+        }
+        wsum += ew;
       }
       m = mb;
     }
@@ -613,9 +626,12 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
     return;
   }
   const float f = ex2_approx((m - mx) * kLog2e);  // 0 for a thread that saw only empty splits
-  acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+#pragma unroll
+  for (int e = 0; e < kPerLane; ++e) {
+    acc[e].x *= f; acc[e].y *= f; acc[e].z *= f; acc[e].w *= f;
+    s_o[warp][sub][li + e * kLanesPerRow] = acc[e];
+  }
   float ws = li == 0 ? wsum * f : 0.f;  // each split's weight counted once per sub-row
-  s_o[warp][sub][li] = acc;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
   if (lane == 0) s_sum[warp] = ws;
@@ -623,7 +639,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
   float W = 0.f;
 #pragma unroll
   for (int w = 0; w < kCombineWarps; ++w) W += s_sum[w];
-  for (int i = threadIdx.x; i < kLanesPerRow; i += blockDim.x) {
+  for (int i = threadIdx.x; i < kVec; i += blockDim.x) {
     float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int w = 0; w < kCombineWarps; ++w)
       for (int r = 0; r < kRowsPerWarp; ++r) {
@@ -736,6 +752,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const LaunchCtx& ctx) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, const LaunchCtx& ctx) {
+  if (a.head_dim == 256) return launch_decode_t<256>(a, ctx);
   return a.head_dim == 128 ? launch_decode_t<128>(a, ctx) : launch_decode_t<64>(a, ctx);
 }
 
@@ -750,6 +767,7 @@ cudaError_t launch_combine(const CombineArgs& a, const LaunchCtx& ctx) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (a.head_dim == 256) return cudaLaunchKernelEx(&cfg, combine_kernel<256>, a);
   return a.head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, a)
                            : cudaLaunchKernelEx(&cfg, combine_kernel<64>, a);
 }

@@ -74,6 +74,8 @@ def test_paged_batched_decode_auto_splits(dev):
     ([1, 2, 3], 1, 1, 128, 2, 1),            # one-token blocks
     ([777, 1], 5, 7, 64, 6, 3),              # odd block size
     ([4096], 1, 64, 128, 28, 4),
+    ([0, 1, 15, 16, 17, 3000], 4, 16, 256, 16, 8),   # head_dim 256, 16-token boxes
+    ([777, 1], 5, 7, 256, 4, 2),                     # head_dim 256, plain loads
 ])
 def test_paged_edge_cases(dev, lens, S, bs, D, Hq, Hkv):
     d = W.make_decode_paged(len(lens), Hq, Hkv, D, lens, block_size=bs, seed=sum(lens) + S,
@@ -88,6 +90,14 @@ def test_contiguous_edge_cases(dev, kv_len, L, S):
     d = W.make_decode_contiguous(2, 8, 2, 128, kv_len, seed=kv_len, max_kv_len=L)
     op, lp, o, lse = run_decode(d, dev, S)
     check_all(d, op, lp, o, lse, S, f"contig len={kv_len} L={L} S={S}")
+
+
+@pytest.mark.parametrize("kv_len,L,S", [(1, 1, 1), (4100, 4200, 5), (30720, 30720, 60)])
+def test_contiguous_head_dim_256(dev, kv_len, L, S):
+    """head_dim 256 (four 128-byte swizzle spans per cached row), 16 / 8 heads."""
+    d = W.make_decode_contiguous(2, 16, 8, 256, kv_len, seed=kv_len + 256, max_kv_len=L)
+    op, lp, o, lse = run_decode(d, dev, S)
+    check_all(d, op, lp, o, lse, S, f"contig d256 len={kv_len} L={L} S={S}")
 
 
 def test_slots_past_the_end_are_never_read(dev):
@@ -115,8 +125,9 @@ def test_split_count_does_not_change_the_result(dev):
         assert (lse - outs[0][1]).abs().max().item() <= 1e-4
 
 
-def test_decode_matches_last_prefill_row(dev):
-    x = W.make_prefill(1, 28, 4, 1111, 128, seed=8)
+@pytest.mark.parametrize("Hq,Hkv,D", [(28, 4, 128), (16, 8, 256)])
+def test_decode_matches_last_prefill_row(dev, Hq, Hkv, D):
+    x = W.make_prefill(1, Hq, Hkv, 1111, D, seed=8)
     o_p, lse_p = attn.prefill(x.q.to(dev), x.k.to(dev), x.v.to(dev), x.scale, True)
     kc = x.k[0].permute(1, 0, 2).unsqueeze(0).contiguous()
     vc = x.v[0].permute(1, 0, 2).unsqueeze(0).contiguous()
@@ -130,7 +141,7 @@ def test_decode_matches_last_prefill_row(dev):
 def test_combine_kernel_on_arbitrary_partials(dev):
     rng = np.random.default_rng(0)
     for S, B, Hq, D in [(5, 2, 3, 128), (148, 1, 28, 128), (1, 4, 2, 64), (1024, 1, 2, 64),
-                        (1024, 1, 1, 64)]:
+                        (1024, 1, 1, 64), (7, 2, 3, 256), (300, 1, 16, 256)]:
         op = rng.standard_normal((S, B, Hq, D)).astype(np.float32)
         lp = (rng.standard_normal((S, B, Hq)) * 5).astype(np.float32)
         lp[rng.random((S, B, Hq)) < 0.2] = -np.inf            # empty splits

@@ -83,6 +83,8 @@ def paged_with_room(B, Hq, Hkv, D, lens, bs, seed):
     ([0, 2, 3], 1, 1, 128, 2, 1),               # one-token blocks
     ([776, 0], 5, 7, 64, 6, 3),                 # odd block size (plain-load path)
     ([4095], 7, 64, 128, 28, 4),
+    ([0, 31, 2000], 4, 16, 256, 16, 8),         # head_dim 256
+    ([40, 0], 3, 7, 256, 4, 2),                 # head_dim 256, plain loads
 ])
 def test_paged_append(dev, lens, S, bs, D, Hq, Hkv):
     d = paged_with_room(len(lens), Hq, Hkv, D, lens, bs, seed=sum(lens) + S)

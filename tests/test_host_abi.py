@@ -145,6 +145,7 @@ def test_decode_validation(L):
     assert _decode(L, bt=None, maxlen=0) == c["ATTN_ERR_SHAPE"]
     assert _decode(L, scale=-1.0) == c["ATTN_ERR_SHAPE"]
     assert _decode(L, d=80) == c["ATTN_ERR_HEADDIM"]
+    assert _decode(L, d=512) == c["ATTN_ERR_HEADDIM"]
     assert _decode(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
     assert _decode(L, hq=34, hkv=2) == c["ATTN_ERR_GQA"]       # g = 17 > 16
     assert _decode(L, S=-1) == c["ATTN_ERR_SPLITS"]
@@ -184,6 +185,7 @@ def test_combine_validation(L):
     assert f(None, P, 4, 1, 8, 128, P, P, None) == c["ATTN_ERR_NULL"]
     assert f(P, P, 4, 0, 8, 128, P, P, None) == c["ATTN_ERR_SHAPE"]
     assert f(P, P, 4, 1, 8, 32, P, P, None) == c["ATTN_ERR_HEADDIM"]
+    assert f(P, P, 4, 1, 8, 512, P, P, None) == c["ATTN_ERR_HEADDIM"]
     assert f(P, P, 0, 1, 8, 128, P, P, None) == c["ATTN_ERR_SPLITS"]
     assert f(P, P, 1025, 1, 8, 128, P, P, None) == c["ATTN_ERR_SPLITS"]
     assert f(P + 8, P, 4, 1, 8, 128, P, P, None) == c["ATTN_ERR_ALIGN"]

@@ -45,7 +45,8 @@ def _to_dev(d, dev):
     return d
 
 
-@pytest.mark.parametrize("case", ["qwen_auto", "qwen_16", "paged_4", "paged_empty_seq"])
+@pytest.mark.parametrize("case", ["qwen_auto", "qwen_16", "paged_4", "paged_empty_seq",
+                                  "d256"])
 def test_noalloc_matches_allocating_entry_points(dev, case):
     if case.startswith("qwen"):
         d = W.qwen_decode(30720)
@@ -53,6 +54,9 @@ def test_noalloc_matches_allocating_entry_points(dev, case):
     elif case == "paged_4":
         d = W.llama_paged_decode()
         S = 4
+    elif case == "d256":
+        d = W.make_decode_paged(2, 16, 8, 256, [5000, 17], block_size=16, seed=7)
+        S = 0
     else:
         d = W.make_decode_paged(3, 8, 2, 128, [0, 700, 33], block_size=16, seed=5)
         S = 3
