@@ -163,9 +163,7 @@ int prefill_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
     return ATTN_ERR_SHAPE;
   // work items (query tiles x heads x sequences) are counted in 32 bits
   if ((long long)batch * n_q_heads * ((seqlen + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-  // head_dim 256: the plain prefill only
-  const bool variant = window_left >= 0 || softcap > 0.f || alibi_slopes != nullptr;
-  if (head_dim != 64 && head_dim != 128 && !(head_dim == 256 && !variant)) return ATTN_ERR_HEADDIM;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
   if (alibi_slopes && softcap > 0.f) return ATTN_ERR_SHAPE;  // not combined
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
@@ -212,7 +210,7 @@ int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16*
   // work items (at most total/128 + num_seqs query tiles per head) are counted in 32 bits
   if ((long long)n_q_heads * ((total_tokens + 127) / 128 + num_seqs) > 0x7fffffffLL)
     return ATTN_ERR_SHAPE;
-  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4) || !aligned(cu_seqlens, 4))

@@ -599,7 +599,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (j == 0) {
           m = m_new;  // O is written fresh by the item's first P V product
         } else if (__any_sync(0xffffffffu, m_new - m > kRescaleThreshold)) {
-          corr = ex2_approx(m - m_new);
+          // The rescale is warp-wide: a row still without an allowed key
+          // (m = m_new = -inf, l = 0, O = 0) keeps corr = 1 rather than
+          // exp2(-inf + inf).
+          corr = (VARIANT != kPlain && m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
           m = m_new;
           l *= corr;
           rescale_o = true;
@@ -916,11 +919,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx) {
     return launch_prefill_t<128, false, kFp8>(a, ctx);
   }
   const bool varlen = a.cu_seqlens != nullptr;
-  if (a.head_dim == 256) {  // the plain padded prefill only
-    if (varlen || a.softcap > 0.f || a.window_left >= 0 || a.alibi_slopes)
-      return cudaErrorInvalidValue;
-    return launch_prefill_t<256, false, kPlain>(a, ctx);
-  }
+  if (a.head_dim == 256)
+    return varlen ? launch_prefill_cap<256, true>(a, ctx) : launch_prefill_cap<256, false>(a, ctx);
   if (a.head_dim == 128)
     return varlen ? launch_prefill_cap<128, true>(a, ctx) : launch_prefill_cap<128, false>(a, ctx);
   return varlen ? launch_prefill_cap<64, true>(a, ctx) : launch_prefill_cap<64, false>(a, ctx);

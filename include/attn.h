@@ -78,8 +78,8 @@ const char* attn_status_string(int status);
  *   lse : (batch, n_q_heads,  seqlen) fp32 output (natural log), 4-byte aligned
  *   scale: multiplies q.k (pass 1/sqrt(head_dim) for standard attention)
  *   causal: nonzero -> row i attends to keys j <= i; zero -> to every key.
- * Limits: head_dim in {64, 128, 256} (256: 64-key tiles; see attn_prefill_ex for the
- *   variants, which take 64 and 128); 1 <= seqlen <= 2^24; batch*n_q_heads <= 2^20;
+ * Limits: head_dim in {64, 128, 256} (256: 64-key tiles); 1 <= seqlen <= 2^24;
+ *   batch*n_q_heads <= 2^20;
  *   batch*n_q_heads*ceil(seqlen/128) < 2^31; n_q_heads % n_kv_heads == 0.  bf16 inputs, fp32 accumulation, P rounded
  *   to bf16 before the P*V product.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
@@ -100,10 +100,10 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
  *   alibi_slopes: NULL for none; otherwise (n_q_heads,) fp32 on the device,
  *                4-byte aligned: head h adds -alibi_slopes[h] * |i - j| to the
  *                score of query i and key j (after soft-capping)
- * ALiBi and soft-capping together are ATTN_ERR_SHAPE; any variant with
- * head_dim 256 is ATTN_ERR_HEADDIM.  Everything else, and
- * the errors, as attn_prefill (a negative window_left other than -1, or a
- * negative or non-finite softcap, is ATTN_ERR_SHAPE).
+ * ALiBi and soft-capping together are ATTN_ERR_SHAPE.  Everything else
+ * (head_dim 64, 128 or 256), and the errors, as attn_prefill (a negative
+ * window_left other than -1, or a negative or non-finite softcap, is
+ * ATTN_ERR_SHAPE).
  */
 int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
                     float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim,
@@ -131,7 +131,7 @@ int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, 
  * Rows outside every sequence are not written.  A cu_seqlens that breaks the
  * rule above is clamped into it and flagged (ATTN_ERR_DEVICE from
  * attn_check_device_status).
- * Limits: 1 <= num_seqs <= 512; head_dim in {64, 128}; 1 <= total_tokens <= 2^24;
+ * Limits: 1 <= num_seqs <= 512; head_dim in {64, 128, 256}; 1 <= total_tokens <= 2^24;
  *   n_q_heads % n_kv_heads == 0; n_q_heads * (ceil(total_tokens/128) + num_seqs) < 2^31.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
  */

@@ -32,6 +32,8 @@ def run(x, dev):
     ([200, 1, 64, 129], 4, 4, 64, True, 3),             # head_dim 64, MHA
     ([130, 300, 5], 8, 1, 128, False, 2),               # full (non-causal) attention per sequence
     ([77], 6, 3, 128, True, 0),                         # a single short sequence
+    ([1, 63, 64, 65, 700, 0, 129], 8, 4, 256, True, 4),  # head_dim 256: 64-key tiles
+    ([300, 90], 4, 2, 256, False, 0),
 ])
 def test_varlen_full(dev, lens, hq, hkv, d, causal, extra):
     x = W.make_prefill_varlen(lens, hq, hkv, d, seed=sum(lens), extra_rows=extra, causal=causal)

@@ -36,6 +36,11 @@ def run_prefill(x, dev, **kw):
     (700, 4, 2, 64, True, -1, 1.0),         # a tight cap
     (1500, 8, 2, 128, True, 300, 50.0),     # both
     (300, 4, 1, 128, False, -1, 20.0),
+    (1000, 8, 4, 256, True, 63, 0.0),        # head_dim 256: 64-key tiles, window edges
+    (1000, 8, 4, 256, True, 64, 0.0),
+    (700, 4, 2, 256, False, 150, 0.0),
+    (900, 8, 4, 256, True, -1, 30.0),
+    (1100, 8, 4, 256, True, 200, 50.0),
 ])
 def test_prefill_variants_full(dev, N, Hq, Hkv, D, causal, Wl, cap):
     x = W.make_prefill(1, Hq, Hkv, N, D, seed=N + Wl, causal=causal)
@@ -129,6 +134,8 @@ def alibi_slopes(n_heads):
     (777, 4, 4, 64, True, -1),
     (600, 8, 2, 128, False, -1),
     (1500, 8, 2, 128, True, 300),
+    (900, 8, 4, 256, True, -1),              # head_dim 256
+    (700, 4, 2, 256, False, 100),
 ])
 def test_prefill_alibi_full(dev, N, Hq, Hkv, D, causal, Wl):
     x = W.make_prefill(1, Hq, Hkv, N, D, seed=N + 7, causal=causal)

@@ -84,8 +84,8 @@ def test_variant_validation(L):
     assert L.attn_prefill_ex(None, P, P, P, P, 1, 4, 2, 128, 128, 0.1, 1, 5, 1.0, None, None) == \
         c["ATTN_ERR_NULL"]
     assert ex(-1, 2.0, P) == c["ATTN_ERR_SHAPE"]            # ALiBi with soft-capping
-    assert L.attn_prefill_ex(P, P, P, P, P, 1, 4, 2, 128, 256, 0.1, 1, 16, 0.0, None, None) == \
-        c["ATTN_ERR_HEADDIM"]                               # head_dim 256: plain prefill only
+    assert L.attn_prefill_ex(P, P, P, P, P, 1, 4, 2, 128, 512, 0.1, 1, 16, 0.0, None, None) == \
+        c["ATTN_ERR_HEADDIM"]
     assert ex(-1, 0.0, P + 2) == c["ATTN_ERR_ALIGN"]        # misaligned slopes
     dx = lambda w, cap, al=None: L.attn_decode_splitkv_ex(P, P, P, P, P, 4, P, P, 2, 8, 2, 128, 16,
                                                           8, 16, 128, 0.1, w, cap, al, None)
@@ -121,6 +121,7 @@ def test_prefill_varlen_validation(L):
     assert _varlen(L, T=0) == c["ATTN_ERR_SHAPE"]
     assert _varlen(L, T=(1 << 24) + 1) == c["ATTN_ERR_SHAPE"]
     assert _varlen(L, d=96) == c["ATTN_ERR_HEADDIM"]
+    assert _varlen(L, d=512) == c["ATTN_ERR_HEADDIM"]
     assert _varlen(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
     assert _varlen(L, cu=P + 2) == c["ATTN_ERR_ALIGN"]
     assert _varlen(L, q=P + 8) == c["ATTN_ERR_ALIGN"]
