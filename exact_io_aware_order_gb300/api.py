@@ -144,21 +144,34 @@ def prefill_fp8(q8: torch.Tensor, k8: torch.Tensor, v8t: torch.Tensor, q_scales:
 
 
 def quantize_fp8(x: torch.Tensor, signs: Optional[torch.Tensor] = None, block_rows: int = 128,
-                 transpose: bool = False, stream=None):
+                 transpose: bool = False, stream=None, codes: Optional[torch.Tensor] = None,
+                 scales: Optional[torch.Tensor] = None):
     """FP8 (e4m3) block quantisation with optional incoherent rotation
     (``attn_quantize_fp8``).  x: (..., rows, d) bf16, the leading dimensions
     being planes.  Returns (codes uint8 (planes..., rows, d) or, transposed,
     (planes..., d, rows); scales fp32 (planes..., ceil(rows/128)) or
-    (planes...,) when block_rows == 0)."""
+    (planes...,) when block_rows == 0), written into ``codes`` / ``scales``
+    when given (contiguous, of those shapes)."""
     _need(x, "x", _BF16, x.dim())
     lead, rows, d = tuple(x.shape[:-2]), x.shape[-2], x.shape[-1]
     planes = 1
     for n in lead:
         planes *= n
     shape = lead + ((d, rows) if transpose else (rows, d))
-    codes = torch.empty(shape, dtype=torch.uint8, device=x.device)
     nb = -(-rows // 128)
-    scales = torch.empty(lead + ((nb,) if block_rows else ()), dtype=torch.float32, device=x.device)
+    sshape = lead + ((nb,) if block_rows else ())
+    if codes is None:
+        codes = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    else:
+        _need(codes, "codes", torch.uint8, len(shape))
+        if tuple(codes.shape) != shape:
+            raise ValueError(f"codes must have shape {shape}")
+    if scales is None:
+        scales = torch.empty(sshape, dtype=torch.float32, device=x.device)
+    else:
+        _need(scales, "scales", torch.float32, len(sshape))
+        if tuple(scales.shape) != sshape:
+            raise ValueError(f"scales must have shape {sshape}")
     sp = None
     if signs is not None:
         _need(signs, "signs", torch.float32, 1)

@@ -3,28 +3,47 @@
 // Page "FlashAttention for inference: tiled prefill and split-KV decoding",
 // section "Interaction with post-trained models": FlashAttention-3's FP8
 // path lowers the error of naive FP8 attention by block quantisation and
-// incoherent processing.  This kernel prepares the inputs of the FP8
-// prefill: optionally rotates each row by diag(signs) H / sqrt(d) (H the
+// incoherent processing.  These kernels prepare the inputs of the FP8
+// prefill: optionally rotate each row by diag(signs) H / sqrt(d) (H the
 // Sylvester Hadamard matrix; the same rotation for Q and K leaves Q K^T
-// unchanged), then quantises blocks of rows to e4m3 with scale amax / 448.
+// unchanged), then quantise blocks of rows to e4m3 with scale amax / 448.
 //
-// One thread per row, one CTA per block of 128 rows (or per plane when the
-// whole plane shares one scale, looping over its rows twice: amax, codes).
-// The rotation runs as in-register butterflies, stride 1, 2, 4, ..., d/2,
-// then one multiply by the float32 value of 1/sqrt(d); the scale and its
-// inverse are IEEE-rounded float32 divisions; codes are rounded to nearest
-// e4m3, ties to even, saturating.  The transposed output (plane, d, rows)
-// is written by consecutive threads to consecutive bytes.
+// Layout of the work: one CTA per block of 128 rows of a plane, eight warps
+// of 16 rows each.  Within a warp, LPR consecutive lanes share a row: lane l
+// holds elements [E c, E c + E) (c = l % LPR, E = d / LPR) of the rows
+// l / LPR + k (32 / LPR), k = 0, 1, ...  Row-major output takes LPR = 4 (32
+// elements per lane at head_dim 128: 64-byte loads, five of the rotation's
+// seven butterfly stages inside the lane); the transposed output takes
+// LPR = 32, so that a lane holds 16 consecutive rows of each of its
+// elements and writes them as 16 consecutive bytes.  Butterflies with
+// stride h < E pair elements inside a lane; larger strides pair lane l with
+// lane l ^ (h / E) through a shuffle, the lower index taking u + v and the
+// upper u - v (u the lower element, v the upper), written as
+// fma(+-1, own, partner), which rounds exactly like that sum or difference.
+// Every step is the float32 operation, in the order, of the definition:
+// signs multiply, butterflies with stride 1, 2, 4, ..., d/2, one multiply
+// by the float32 value of 1/sqrt(d); the scale and its inverse are
+// IEEE-rounded float32 divisions; codes are rounded to nearest e4m3, ties to
+// even, saturating.
+//
+// One scale per plane: a first pass takes each block's amax and combines
+// them per plane with an integer atomic max on the float's bits (amax >= 0,
+// where the bit patterns order like the values); the second pass quantises;
+// a last, one-thread-per-plane pass turns the stored amax into the scale.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
 #include "attn_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace attn {
 namespace {
 
-constexpr int kQRows = 128;  // rows per CTA pass (one per thread)
+constexpr int kBlockRows = 128;                 // rows per CTA
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kWarpRows = kBlockRows / kWarps;  // 16 rows per warp
 constexpr float kE4M3Max = 448.f;
 
 __device__ __forceinline__ uint32_t e4m3x2(float hi, float lo) {
@@ -33,128 +52,275 @@ __device__ __forceinline__ uint32_t e4m3x2(float hi, float lo) {
   return r;
 }
 
-// Loads row `row` of the plane (zero past the end) as float32, optionally
-// rotated.
-template <int D>
-__device__ __forceinline__ void load_row(const QuantArgs& a, int plane, int row, float (&x)[D]) {
-  if (row < a.rows) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + ((size_t)plane * a.rows + row) * D);
+// Lane geometry: E elements per lane, RW rows per warp-wide step, RPL rows
+// per lane.
+template <int D, int LPR>
+struct Geom {
+  static constexpr int E = D / LPR;
+  static constexpr int RW = 32 / LPR;
+  static constexpr int RPL = kWarpRows / RW;
+  static_assert(E % 2 == 0 && RPL >= 1, "lane geometry");
+};
+
+// The lane's rows (row0w + k RW + lane / LPR, k < RPL; zero past the end),
+// rotated when signs are given: x[k][e] is element E (lane % LPR) + e.
+template <int D, int LPR>
+__device__ __forceinline__ void load_rows(const QuantArgs& a, int plane, int row0w, int lane,
+                                          float (&x)[Geom<D, LPR>::RPL][Geom<D, LPR>::E]) {
+  using G = Geom<D, LPR>;
+  constexpr int E = G::E;
+  const int c = lane % LPR;
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 u = src[c];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  for (int k = 0; k < G::RPL; ++k) {
+    const int row = row0w + k * G::RW + lane / LPR;
+    if (row < a.rows) {
+      const uint16_t* src = a.x + ((size_t)plane * a.rows + row) * D + c * E;
+      uint32_t w[E / 2];
+      if constexpr (E >= 8) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[c * 8 + 2 * i] = __uint_as_float(w[i] << 16);
-        x[c * 8 + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        for (int i = 0; i < E / 8; ++i) {
+          const uint4 u = reinterpret_cast<const uint4*>(src)[i];
+          w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+        }
+      } else if constexpr (E == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(src);
+        w[0] = u.x; w[1] = u.y;
+      } else {
+        w[0] = *reinterpret_cast<const uint32_t*>(src);
+      }
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) {
+        x[k][2 * i] = __uint_as_float(w[i] << 16);
+        x[k][2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[k][e] = 0.f;
+    }
+  }
+  if (a.signs == nullptr) return;
+  // Pairs of elements go through the packed two-lane float32 instructions
+  // (each half rounded on its own, as the scalar operation).
+  float2 sg[E / 2];
+#pragma unroll
+  for (int e = 0; e < E; e += 2) sg[e / 2] = make_float2(a.signs[c * E + e], a.signs[c * E + e + 1]);
+  const float2 neg1 = make_float2(-1.f, -1.f);
+  const float2 isd = make_float2(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+  for (int k = 0; k < G::RPL; ++k) {
+    float* xr = x[k];
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 t = mul2(make_float2(xr[e], xr[e + 1]), sg[e / 2]);
+      xr[e] = t.x;
+      xr[e + 1] = t.y;
+    }
+    // strides inside the lane: (u, v) -> (u + v, u - v), u - v as fma(-1, v, u)
+    if constexpr (E == 2) {
+      const float u = xr[0], v = xr[1];
+      xr[0] = __fadd_rn(u, v);
+      xr[1] = __fsub_rn(u, v);
+    } else {
+      // stride 1: butterflies (e, e + 1) and (e + 2, e + 3) side by side
+#pragma unroll
+      for (int e = 0; e < E; e += 4) {
+        const float2 u = make_float2(xr[e], xr[e + 2]), v = make_float2(xr[e + 1], xr[e + 3]);
+        const float2 sm = add2(u, v), df = fma2(neg1, v, u);
+        xr[e] = sm.x; xr[e + 1] = df.x; xr[e + 2] = sm.y; xr[e + 3] = df.y;
+      }
+      // stride h >= 2: butterflies (e, e + h) and (e + 1, e + 1 + h) side by side
+#pragma unroll
+      for (int h = 2; h < E; h <<= 1)
+#pragma unroll
+        for (int e = 0; e < E; e += 2)
+          if ((e & h) == 0) {
+            const float2 u = make_float2(xr[e], xr[e + 1]), v = make_float2(xr[e + h], xr[e + h + 1]);
+            const float2 sm = add2(u, v), df = fma2(neg1, v, u);
+            xr[e] = sm.x; xr[e + 1] = sm.y; xr[e + h] = df.x; xr[e + h + 1] = df.y;
+          }
+    }
+    // strides across the row's lanes: the lower element becomes own + partner,
+    // the upper partner - own, both as fma(+-1, own, partner)
+#pragma unroll
+    for (int hl = 1; hl < LPR; hl <<= 1) {
+      const float sgn = (lane & hl) ? -1.f : 1.f;
+      const float2 sgn2 = make_float2(sgn, sgn);
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        const float y0 = __shfl_xor_sync(0xffffffffu, xr[e], hl);
+        const float y1 = __shfl_xor_sync(0xffffffffu, xr[e + 1], hl);
+        const float2 t = fma2(sgn2, make_float2(xr[e], xr[e + 1]), make_float2(y0, y1));
+        xr[e] = t.x;
+        xr[e + 1] = t.y;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 t = mul2(make_float2(xr[e], xr[e + 1]), isd);
+      xr[e] = t.x;
+      xr[e + 1] = t.y;
+    }
+  }
+}
+
+// Largest |x| over the CTA's rows (every thread gets it).
+template <int D, int LPR>
+__device__ __forceinline__ float block_amax(const float (&x)[Geom<D, LPR>::RPL][Geom<D, LPR>::E],
+                                            float* red) {
+  using G = Geom<D, LPR>;
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < G::RPL; ++k)
+#pragma unroll
+    for (int e = 0; e < G::E; ++e) m = fmaxf(m, fabsf(x[k][e]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  float b = red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) b = fmaxf(b, red[w]);
+  return b;
+}
+
+// Codes of the lane's rows: row-major (row, d) with LPR = 4, or transposed
+// (d, row) with LPR = 32.
+template <int D, int LPR>
+__device__ __forceinline__ void store_codes(const QuantArgs& a, int plane, int row0w, int lane,
+                                            const float (&x)[Geom<D, LPR>::RPL][Geom<D, LPR>::E],
+                                            float inv) {
+  using G = Geom<D, LPR>;
+  constexpr int E = G::E;
+  const int c = lane % LPR;
+  const float2 inv2 = make_float2(inv, inv);
+  // codes of element pairs: bits 0-7 element e, bits 8-15 element e + 1
+  uint32_t pr[G::RPL][E / 2];
+#pragma unroll
+  for (int k = 0; k < G::RPL; ++k)
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 t = mul2(make_float2(x[k][e], x[k][e + 1]), inv2);
+      pr[k][e / 2] = e4m3x2(t.y, t.x);
+    }
+  if constexpr (LPR != 32) {
+#pragma unroll
+    for (int k = 0; k < G::RPL; ++k) {
+      const int row = row0w + k * G::RW + lane / LPR;
+      if (row >= a.rows) continue;
+      uint8_t* dst = a.codes + ((size_t)plane * a.rows + row) * D + c * E;
+      uint32_t wd[E / 4];
+#pragma unroll
+      for (int i = 0; i < E / 4; ++i) wd[i] = pr[k][2 * i] | (pr[k][2 * i + 1] << 16);
+      if constexpr (E >= 16) {
+#pragma unroll
+        for (int i = 0; i < E / 16; ++i)
+          reinterpret_cast<uint4*>(dst)[i] = make_uint4(wd[4 * i], wd[4 * i + 1], wd[4 * i + 2], wd[4 * i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < E / 4; ++i) reinterpret_cast<uint32_t*>(dst)[i] = wd[i];
       }
     }
   } else {
+    // (plane, d, rows): the lane's 16 rows (row0w ..) of element d are 16
+    // consecutive bytes.
 #pragma unroll
-    for (int i = 0; i < D; ++i) x[i] = 0.f;
-  }
-  if (a.signs) {
+    for (int e = 0; e < E; ++e) {
+      const int sh = (e & 1) * 8;
+      uint8_t* dst = a.codes + ((size_t)plane * D + (size_t)(c * E + e)) * a.rows + row0w;
+      if ((a.rows & 15) == 0 && row0w + kWarpRows <= a.rows) {
+        uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < D; ++i) x[i] = __fmul_rn(x[i], a.signs[i]);
+        for (int q = 0; q < 4; ++q) {
+          w[q] = 0;
 #pragma unroll
-    for (int h = 1; h < D; h <<= 1)
-#pragma unroll
-      for (int b = 0; b < D; b += 2 * h)
-#pragma unroll
-        for (int i = 0; i < h; ++i) {
-          const float u = x[b + i], v = x[b + i + h];
-          x[b + i] = __fadd_rn(u, v);
-          x[b + i + h] = __fsub_rn(u, v);
+          for (int b = 0; b < 4; ++b) w[q] |= ((pr[4 * q + b][e / 2] >> sh) & 0xffu) << (8 * b);
         }
-    // float32 value of 1/sqrt(d), rounded once from the exact value by the host
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
 #pragma unroll
-    for (int i = 0; i < D; ++i) x[i] = __fmul_rn(x[i], a.inv_sqrt_d);
+        for (int k = 0; k < G::RPL; ++k)
+          if (row0w + k < a.rows) dst[k] = (uint8_t)(pr[k][e / 2] >> sh);
+      }
+    }
   }
 }
 
-template <int D>
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float m = red[0];
-#pragma unroll
-  for (int w = 1; w < kQRows / 32; ++w) m = fmaxf(m, red[w]);
-  return m;
+// One scale per block of 128 rows: amax, scale and codes in one pass.
+template <int D, int LPR>
+__global__ void __launch_bounds__(kThreads) quantize_block_kernel(const QuantArgs a) {
+  using G = Geom<D, LPR>;
+  __shared__ float red[kWarps];
+  const int plane = blockIdx.y, lane = threadIdx.x & 31;
+  const int row0w = blockIdx.x * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
+  float x[G::RPL][G::E];
+  load_rows<D, LPR>(a, plane, row0w, lane, x);
+  float amax = block_amax<D, LPR>(x, red);
+  if (amax == 0.f) amax = 1.f;
+  if (threadIdx.x == 0) a.scales[(size_t)plane * gridDim.x + blockIdx.x] = __fdiv_rn(amax, kE4M3Max);
+  store_codes<D, LPR>(a, plane, row0w, lane, x, __fdiv_rn(kE4M3Max, amax));
 }
 
-template <int D>
-__device__ __forceinline__ void store_row(const QuantArgs& a, int plane, int row,
-                                          const float (&x)[D], float inv) {
-  if (row >= a.rows) return;
-  uint32_t wds[D / 4];
-#pragma unroll
-  for (int i = 0; i < D / 4; ++i) {
-    const uint32_t lo = e4m3x2(__fmul_rn(x[4 * i + 1], inv), __fmul_rn(x[4 * i], inv));
-    const uint32_t hi = e4m3x2(__fmul_rn(x[4 * i + 3], inv), __fmul_rn(x[4 * i + 2], inv));
-    wds[i] = lo | (hi << 16);  // element k of the row in byte k
-  }
-  if (!a.transpose) {
-    uint4* dst = reinterpret_cast<uint4*>(a.codes + ((size_t)plane * a.rows + row) * D);
-#pragma unroll
-    for (int c = 0; c < D / 16; ++c)
-      dst[c] = make_uint4(wds[4 * c], wds[4 * c + 1], wds[4 * c + 2], wds[4 * c + 3]);
-  } else {
-    // (plane, d, rows): column `row` of each d-row; a warp writes 32 bytes.
-    uint8_t* dst = a.codes + (size_t)plane * D * a.rows + row;
-#pragma unroll
-    for (int k = 0; k < D; ++k) dst[(size_t)k * a.rows] = (uint8_t)(wds[k >> 2] >> (8 * (k & 3)));
-  }
+// One scale per plane, pass 1: the plane's amax, as float bits in scales[plane]
+// (zeroed before the launch).
+template <int D, int LPR>
+__global__ void __launch_bounds__(kThreads) plane_amax_kernel(const QuantArgs a) {
+  using G = Geom<D, LPR>;
+  __shared__ float red[kWarps];
+  const int plane = blockIdx.y, lane = threadIdx.x & 31;
+  const int row0w = blockIdx.x * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
+  float x[G::RPL][G::E];
+  load_rows<D, LPR>(a, plane, row0w, lane, x);
+  const float amax = block_amax<D, LPR>(x, red);
+  if (threadIdx.x == 0)
+    atomicMax(reinterpret_cast<unsigned int*>(a.scales) + plane, __float_as_uint(amax));
 }
 
-template <int D>
-__global__ void __launch_bounds__(kQRows) quantize_kernel(const QuantArgs a) {
-  __shared__ float red[kQRows / 32];
-  const int plane = blockIdx.y;
-  float x[D];
+// Pass 2: the codes, from the plane's amax.
+template <int D, int LPR>
+__global__ void __launch_bounds__(kThreads) plane_codes_kernel(const QuantArgs a) {
+  using G = Geom<D, LPR>;
+  const int plane = blockIdx.y, lane = threadIdx.x & 31;
+  const int row0w = blockIdx.x * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
+  float x[G::RPL][G::E];
+  load_rows<D, LPR>(a, plane, row0w, lane, x);
+  float amax = __uint_as_float(reinterpret_cast<const unsigned int*>(a.scales)[plane]);
+  if (amax == 0.f) amax = 1.f;
+  store_codes<D, LPR>(a, plane, row0w, lane, x, __fdiv_rn(kE4M3Max, amax));
+}
+
+// Pass 3: amax -> scale, in place.
+__global__ void plane_scale_kernel(const QuantArgs a) {
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= a.planes) return;
+  float amax = __uint_as_float(reinterpret_cast<const unsigned int*>(a.scales)[p]);
+  if (amax == 0.f) amax = 1.f;
+  a.scales[p] = __fdiv_rn(amax, kE4M3Max);
+}
+
+template <int D, int LPR>
+cudaError_t launch_quantize_t(const QuantArgs& a, const LaunchCtx& ctx) {
+  const dim3 grid((unsigned)((a.rows + kBlockRows - 1) / kBlockRows), (unsigned)a.planes);
   if (a.block_rows > 0) {
-    // One scale per block of 128 rows: this CTA's block.
-    const int row = blockIdx.x * kQRows + threadIdx.x;
-    load_row<D>(a, plane, row, x);
-    float m = 0.f;
-#pragma unroll
-    for (int i = 0; i < D; ++i) m = fmaxf(m, fabsf(x[i]));
-    float amax = block_max<D>(m, red);
-    if (amax == 0.f) amax = 1.f;
-    const float inv = __fdiv_rn(kE4M3Max, amax);
-    if (threadIdx.x == 0) a.scales[(size_t)plane * gridDim.x + blockIdx.x] = __fdiv_rn(amax, kE4M3Max);
-    store_row<D>(a, plane, row, x, inv);
-  } else {
-    // One scale for the whole plane: amax over every row, then the codes.
-    float m = 0.f;
-    for (int r0 = 0; r0 < a.rows; r0 += kQRows) {
-      load_row<D>(a, plane, r0 + threadIdx.x, x);
-#pragma unroll
-      for (int i = 0; i < D; ++i) m = fmaxf(m, fabsf(x[i]));
-    }
-    float amax = block_max<D>(m, red);
-    if (amax == 0.f) amax = 1.f;
-    const float inv = __fdiv_rn(kE4M3Max, amax);
-    if (threadIdx.x == 0) a.scales[plane] = __fdiv_rn(amax, kE4M3Max);
-    for (int r0 = 0; r0 < a.rows; r0 += kQRows) {
-      load_row<D>(a, plane, r0 + threadIdx.x, x);
-      store_row<D>(a, plane, r0 + threadIdx.x, x, inv);
-    }
+    quantize_block_kernel<D, LPR><<<grid, kThreads, 0, ctx.stream>>>(a);
+    return cudaGetLastError();
   }
+  cudaError_t e = cudaMemsetAsync(a.scales, 0, (size_t)a.planes * sizeof(float), ctx.stream);
+  if (e != cudaSuccess) return e;
+  plane_amax_kernel<D, 4><<<grid, kThreads, 0, ctx.stream>>>(a);
+  plane_codes_kernel<D, LPR><<<grid, kThreads, 0, ctx.stream>>>(a);
+  plane_scale_kernel<<<(a.planes + 127) / 128, 128, 0, ctx.stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_quantize_d(const QuantArgs& a, const LaunchCtx& ctx) {
+  return a.transpose ? launch_quantize_t<D, 32>(a, ctx) : launch_quantize_t<D, 4>(a, ctx);
 }
 
 }  // namespace
 
 cudaError_t launch_quantize(const QuantArgs& a, const LaunchCtx& ctx) {
-  const unsigned nb = a.block_rows > 0 ? (unsigned)((a.rows + kQRows - 1) / kQRows) : 1u;
-  const dim3 grid(nb, (unsigned)a.planes);
-  if (a.head_dim == 128)
-    quantize_kernel<128><<<grid, kQRows, 0, ctx.stream>>>(a);
-  else
-    quantize_kernel<64><<<grid, kQRows, 0, ctx.stream>>>(a);
-  return cudaGetLastError();
+  return a.head_dim == 128 ? launch_quantize_d<128>(a, ctx) : launch_quantize_d<64>(a, ctx);
 }
 
 }  // namespace attn

@@ -26,6 +26,9 @@ def signs_for(d, seed):
     (4, 1000, 128, False, 0, True),
     (2, 129, 64, True, 128, False),
     (1, 4096, 128, True, 0, False),
+    (3, 4100, 64, True, 0, True),      # per-plane scale, transposed, rows not a multiple of 16
+    (2, 8192, 128, True, 0, True),
+    (5, 17, 128, True, 128, True),     # one partial block
 ])
 def test_quantizer_bit_exact(dev, planes, rows, d, rot, block, transpose):
     g = torch.Generator().manual_seed(rows + d)
@@ -45,6 +48,20 @@ def test_quantizer_bit_exact(dev, planes, rows, d, rot, block, transpose):
         got = got.transpose(0, 2, 1)
     assert np.array_equal(got, ref_codes)
     assert np.array_equal(scales.cpu().numpy().reshape(ref_scales.shape), ref_scales)
+
+
+@pytest.mark.parametrize("block", [128, 0])
+def test_quantizer_all_zero_plane(dev, block):
+    """A block (or plane) of zeros: amax 0 counts as 1, so its scale is 1/448
+    and its codes are 0."""
+    x = torch.zeros(3, 200, 128, dtype=torch.bfloat16)
+    x[1] = torch.randn(200, 128, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    codes, scales = attn.quantize_fp8(x.to(dev), None, block_rows=block)
+    attn.check_device_status()
+    ref_codes, ref_scales = F.quantize_blocks(x.float().numpy(), block if block else 200)
+    assert np.array_equal(e4m3_values(codes), ref_codes)
+    assert np.array_equal(scales.cpu().numpy().reshape(ref_scales.shape), ref_scales)
+    assert np.all(scales.cpu().numpy()[0] == np.float32(1.0) / np.float32(448.0))
 
 
 def fp8_inputs(x, dev, signs, block=128):
