@@ -87,14 +87,26 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_hash(path: str) -> str:
+    """First 16 hex digits of the SHA-256 of a C/CUDA source with its //
+    comments, surrounding whitespace and blank lines removed: a comment edit
+    keeps the hash, any change to the code changes it."""
+    lines = []
+    for line in open(path, encoding="utf-8").read().splitlines():
+        code = line.split("//", 1)[0].strip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def profiled_traffic():
     """Per-launch DRAM bytes of the prefill kernel from the committed ncu
-    summary, or None when the kernel source changed since the capture."""
+    summary, or None when the kernel's code changed since the capture."""
     try:
         text = open(PROFILE_SUMMARY).read()
-        sha = hashlib.sha256(open(PREFILL_SRC, "rb").read()).hexdigest()[:16]
+        sha = code_hash(PREFILL_SRC)
         vals = dict(line.split(":", 1) for line in text.splitlines() if ":" in line)
-        if vals.get("source_sha256_16", "").strip() != sha:
+        if vals.get("code_sha256_16", "").strip() != sha:
             return None
         return float(vals["dram_bytes_per_launch"].strip())
     except Exception:

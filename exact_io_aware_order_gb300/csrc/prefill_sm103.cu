@@ -12,29 +12,38 @@
 // strictly above the diagonal are never visited.
 //
 // GB300 design (the pages' A100/H100 kernels are prior art only):
-//   * one CTA owns one 128-row query tile of one head; key/value tiles are 128
-//     keys, streamed by TMA (128-byte swizzle, 3-D tensor maps so rows past the
-//     end read as zero) into a K ring and a V ring in shared memory;
-//   * TMEM (512 columns): three S buffers (128 columns each) and O.  S is
-//     triple-buffered, so the tensor core computes S(j+1), S(j+2) while the
-//     softmax works on S(j).  P(j) is written as bf16 over the first half of
-//     S(j)'s buffer and feeds O += P V straight from TMEM (A operand in tensor
-//     memory), V from shared memory (MN-major);
+//   * persistent CTAs, one per SM, each walking its share of a work list of
+//     128-row query tiles (longest causal rows first, snake order across
+//     CTAs); every role counts tiles over all items, so the pipeline does not
+//     drain between items;
+//   * key/value tiles of 128 keys (64 at head_dim 256), streamed by TMA
+//     (128-byte swizzle, 3-D tensor maps so rows past the end read as zero)
+//     into a K ring and a V ring in shared memory; Q tiles double-buffered;
+//   * TMEM (512 columns): three S buffers and O.  S is triple-buffered, so the
+//     tensor core computes S(j+1), S(j+2) while the softmax works on S(j).
+//     P(j) is written as bf16 over the first half of S(j)'s buffer and feeds
+//     O += P V straight from TMEM (A operand in tensor memory), V from shared
+//     memory (MN-major);
 //   * two threads issue tcgen05.mma: warp 5 the S products (S(j) as soon as
-//     K_j is in and PV(j-3) has freed the buffer), warp 6 the P V products
-//     (as soon as P(j) and V_j are ready).  Every wait or commit stalls its
-//     issuing thread for longer than one 128x128x16 MMA runs, so one thread
-//     alone leaves the tensor core idle between groups; with two, one
-//     thread's synchronisation overlaps the other's MMAs.  Warp 4 is the TMA
-//     producer;
+//     K_j is in and the P V product three tiles back has freed the buffer),
+//     warp 6 the P V products (as soon as P(j) and V_j are ready).  Every
+//     wait or commit stalls its issuing thread for longer than one
+//     128x128x16 MMA runs, so one thread alone leaves the tensor core idle
+//     between groups; with two, one thread's synchronisation overlaps the
+//     other's MMAs.  Warp 4 is the TMA producer;
 //   * warps 0-3 run the softmax, one query row per thread (TMEM lane = row),
 //     so row max and row sum need no shuffles and no cross-warp exchange;
-//     with one softmax warp per scheduler, its ALU work overlaps its own
-//     exponentials on the MUFU pipe;
+//   * warps 7-10 are the epilogue: O / l read from TMEM once the item's last
+//     product is done (O is released at once for the next item), written
+//     through swizzled shared-memory boxes by TMA stores, and the LSE;
 //   * base-2 exponentials with scale*log2(e) folded in; O is rescaled only
 //     when a row max grows by more than 2^8 (the same stale max is used for
 //     l and O, so the result is exact), and only after the previous P V
 //     product has completed; the LSE is converted back to natural log;
+//   * flavours compiled separately, so the plain kernel carries none of the
+//     others' code: sliding window, window and/or soft-capping, ALiBi (with
+//     an optional window), FP8 (e4m3 operands, kind::f8f6f4, per-block
+//     scales), each padded or packed (variable-length sequences);
 //   * every wait is bounded; on a timeout all roles leave their loops, the
 //     CTA waits for in-flight copies and MMAs, frees TMEM and exits.
 #include <cstdint>
