@@ -93,3 +93,16 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 1
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["unit"] == d["unit"]
+
+
+def test_profile_guard_hashes_code_not_comments(tmp_path):
+    """The bench reports profiled DRAM traffic only while the kernel's code
+    matches the capture: a comment or blank-line edit keeps the hash, a code
+    edit changes it."""
+    base = "int f(int x) {  // doubles x\n  return 2 * x;\n}\n"
+    a, b, c = tmp_path / "a.cu", tmp_path / "b.cu", tmp_path / "c.cu"
+    a.write_text(base)
+    b.write_text("// a header comment\n\n" + base.replace("// doubles x", "// twice x") + "\n\n")
+    c.write_text(base.replace("2 * x", "3 * x"))
+    assert bench.code_hash(str(a)) == bench.code_hash(str(b))
+    assert bench.code_hash(str(a)) != bench.code_hash(str(c))
