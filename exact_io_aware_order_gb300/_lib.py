@@ -33,6 +33,9 @@ SIGNATURES = {
                             + [c_float, c_void_p]),
     "attn_decode_append_splitkv": (c_int, [c_void_p] * 7 + [c_int] + [c_void_p] * 2
                                    + [c_int] * 8 + [c_float, c_void_p]),
+    "attn_decode_append_splitkv_ex": (c_int, [c_void_p] * 7 + [c_int] + [c_void_p] * 2
+                                      + [c_int] * 8 + [c_float, c_int, c_float, c_void_p,
+                                                       c_void_p]),
     "attn_prefill_fp8": (c_int, [c_void_p] * 8 + [c_int] * 5 + [c_float, c_int, c_void_p]),
     "attn_quantize_fp8": (c_int, [c_void_p] * 4 + [c_int] * 5 + [c_void_p]),
     "attn_combine": (c_int, [c_void_p, c_void_p] + [c_int] * 4 + [c_void_p, c_void_p, c_void_p]),

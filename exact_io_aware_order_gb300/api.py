@@ -256,13 +256,14 @@ def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_l
     tail = (kv_lens.data_ptr(), int(num_splits), o_partial.data_ptr(), lse_partial.data_ptr(), B,
             n_q, n_kv, d, block_size, max_blocks, num_blocks, int(max_kv_len), float(scale),
             _stream(stream))
-    if new_kv is None and (window_left != -1 or softcap != 0.0 or alibi_slopes is not None):
-        al = None
-        if alibi_slopes is not None:
-            _need(alibi_slopes, "alibi_slopes", torch.float32, 1)
-            if alibi_slopes.numel() != n_q:
-                raise ValueError("alibi_slopes must have one slope per query head")
-            al = alibi_slopes.data_ptr()
+    variant = window_left != -1 or softcap != 0.0 or alibi_slopes is not None
+    al = None
+    if alibi_slopes is not None:
+        _need(alibi_slopes, "alibi_slopes", torch.float32, 1)
+        if alibi_slopes.numel() != n_q:
+            raise ValueError("alibi_slopes must have one slope per query head")
+        al = alibi_slopes.data_ptr()
+    if new_kv is None and variant:
         name = "attn_decode_splitkv_ex"
         st = lib().attn_decode_splitkv_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                           bt_ptr, *tail[:-1], int(window_left), float(softcap),
@@ -271,6 +272,12 @@ def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_l
         name = "attn_decode_splitkv"
         st = lib().attn_decode_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), bt_ptr,
                                        *tail)
+    elif variant:
+        name = "attn_decode_append_splitkv_ex"
+        st = lib().attn_decode_append_splitkv_ex(q.data_ptr(), new_kv[0].data_ptr(),
+                                                 new_kv[1].data_ptr(), k_cache.data_ptr(),
+                                                 v_cache.data_ptr(), bt_ptr, *tail[:-1],
+                                                 int(window_left), float(softcap), al, tail[-1])
     else:
         name = "attn_decode_append_splitkv"
         st = lib().attn_decode_append_splitkv(q.data_ptr(), new_kv[0].data_ptr(),
@@ -304,14 +311,19 @@ def decode_append_splitkv(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
                           block_table: Optional[torch.Tensor] = None, num_splits: int = 0,
                           max_kv_len: Optional[int] = None, scale: Optional[float] = None,
                           o_partial: Optional[torch.Tensor] = None,
-                          lse_partial: Optional[torch.Tensor] = None, stream=None):
+                          lse_partial: Optional[torch.Tensor] = None, stream=None,
+                          window_left: int = -1, softcap: float = 0.0,
+                          alibi_slopes: Optional[torch.Tensor] = None):
     """Split-KV decode that first writes each sequence's new key and value
     (k_new, v_new: (B, n_kv, d) bf16) into the cache at position kv_lens[b]
-    and attends over kv_lens[b] + 1 tokens (``attn_decode_append_splitkv``).
-    kv_lens is not modified: the caller increments it afterwards.
+    and attends over kv_lens[b] + 1 tokens (``attn_decode_append_splitkv``;
+    with a sliding window, soft-capping or ALiBi slopes,
+    ``attn_decode_append_splitkv_ex``).  kv_lens is not modified: the caller
+    increments it afterwards.
     """
     return _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
-                        o_partial, lse_partial, stream, new_kv=(k_new, v_new))
+                        o_partial, lse_partial, stream, new_kv=(k_new, v_new),
+                        window_left=window_left, softcap=softcap, alibi_slopes=alibi_slopes)
 
 
 def combine(o_partial: torch.Tensor, lse_partial: torch.Tensor,
@@ -348,11 +360,14 @@ def decode(q, k_cache, v_cache, kv_lens, block_table=None, num_splits: int = 0,
 
 def decode_append(q, k_new, v_new, k_cache, v_cache, kv_lens, block_table=None,
                   num_splits: int = 0, max_kv_len: Optional[int] = None,
-                  scale: Optional[float] = None, stream=None):
+                  scale: Optional[float] = None, stream=None, window_left: int = -1,
+                  softcap: float = 0.0, alibi_slopes: Optional[torch.Tensor] = None):
     """Decode with append followed by the combine: returns (O, LSE); the new
     rows are in the caches afterwards, kv_lens is left to the caller."""
     op, lp = decode_append_splitkv(q, k_new, v_new, k_cache, v_cache, kv_lens, block_table,
-                                   num_splits, max_kv_len, scale, stream=stream)
+                                   num_splits, max_kv_len, scale, stream=stream,
+                                   window_left=window_left, softcap=softcap,
+                                   alibi_slopes=alibi_slopes)
     return combine(op, lp, stream=stream)
 
 

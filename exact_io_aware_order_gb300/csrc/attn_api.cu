@@ -310,6 +310,20 @@ int attn_decode_append_splitkv(const attn_bf16* q, const attn_bf16* k_new, const
                      max_blocks_per_seq, num_blocks, max_kv_len, scale, stream, true);
 }
 
+int attn_decode_append_splitkv_ex(const attn_bf16* q, const attn_bf16* k_new,
+                                  const attn_bf16* v_new, attn_bf16* k_cache, attn_bf16* v_cache,
+                                  const int32_t* block_table, const int32_t* kv_lens,
+                                  int num_splits, float* o_partial, float* lse_partial, int batch,
+                                  int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, int max_kv_len,
+                                  float scale, int window_left, float softcap,
+                                  const float* alibi_slopes, void* stream) {
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, block_table, kv_lens, num_splits,
+                     o_partial, lse_partial, batch, n_q_heads, n_kv_heads, head_dim, block_size,
+                     max_blocks_per_seq, num_blocks, max_kv_len, scale, stream, true, window_left,
+                     softcap, alibi_slopes);
+}
+
 int attn_combine(const float* o_partial, const float* lse_partial, int num_splits, int batch,
                  int n_q_heads, int head_dim, float* o, float* lse, void* stream) {
   if (!o_partial || !lse_partial || !o || !lse) return ATTN_ERR_NULL;

@@ -242,6 +242,28 @@ int attn_decode_append_splitkv(const attn_bf16* q, const attn_bf16* k_new,
                                float scale, void* stream);
 
 /*
+ * attn_decode_append_splitkv_ex -- attn_decode_append_splitkv with the
+ * attention variants of attn_decode_splitkv_ex (page: same, sections
+ * "Minimal implementation" and "Interaction with post-trained models").
+ *
+ *   window_left, softcap, alibi_slopes: as attn_decode_splitkv_ex, applied to
+ *                the kv_lens[b] + 1 tokens with the new token as the query's
+ *                own position kv_lens[b]: a window keeps tokens
+ *                kv_lens[b] - window_left .. kv_lens[b]; ALiBi adds
+ *                -alibi_slopes[h] * (kv_lens[b] - j).
+ * Everything else, the writes and the errors, as attn_decode_append_splitkv and
+ * attn_decode_splitkv_ex (ALiBi with soft-capping is ATTN_ERR_SHAPE).
+ */
+int attn_decode_append_splitkv_ex(const attn_bf16* q, const attn_bf16* k_new,
+                                  const attn_bf16* v_new, attn_bf16* k_cache, attn_bf16* v_cache,
+                                  const int32_t* block_table, const int32_t* kv_lens,
+                                  int num_splits, float* o_partial, float* lse_partial, int batch,
+                                  int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, int max_kv_len,
+                                  float scale, int window_left, float softcap,
+                                  const float* alibi_slopes, void* stream);
+
+/*
  * attn_prefill_fp8 -- causal (or full) prefill on FP8 inputs prepared by
  * attn_quantize_fp8.
  *

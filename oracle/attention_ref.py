@@ -393,16 +393,21 @@ def append_token(k_cache, v_cache, block_table, kv_lens: Sequence[int], k_new, v
 
 
 def decode_append(q, k_new, v_new, k_cache, v_cache, block_table, kv_lens: Sequence[int],
-                  scale: float, block_size: int = 0):
+                  scale: float, block_size: int = 0, window_left: int = -1,
+                  softcap: float = 0.0, alibi_slopes=None):
     """Single-token decode that first appends the token's own key and value
     (page §"Minimal implementation"): the query of sequence b attends over its
-    kv_lens[b] cached tokens plus the new one.
+    kv_lens[b] cached tokens plus the new one.  The variants (sliding window,
+    soft-capping, ALiBi; §"Interaction with post-trained models") are those
+    of :func:`decode` over the kv_lens[b] + 1 tokens, the new token being the
+    query's own position.
 
     Returns (O (B, n_q, d), LSE (B, n_q), k_cache', v_cache'), the caches as
     :func:`append_token` leaves them.
     """
     kc, vc = append_token(k_cache, v_cache, block_table, kv_lens, k_new, v_new, block_size)
-    o, lse = decode(q, kc, vc, block_table, [int(n) + 1 for n in kv_lens], scale, block_size)
+    o, lse = decode(q, kc, vc, block_table, [int(n) + 1 for n in kv_lens], scale, block_size,
+                    window_left=window_left, softcap=softcap, alibi_slopes=alibi_slopes)
     return o, lse, kc, vc
 
 

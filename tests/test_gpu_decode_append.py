@@ -159,3 +159,41 @@ def test_bad_block_for_new_position_is_reported_and_not_written(dev):
         attn.check_device_status()
     assert e.value.status == status_codes()["ATTN_ERR_DEVICE"]
     assert torch.equal(bits(kc), bits(k0)) and torch.equal(bits(vc), bits(v0))
+
+
+def _alibi(n_heads):
+    """The usual geometric ALiBi slopes 2^(-8 (h+1) / n_heads)."""
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / n_heads) for h in range(n_heads)],
+                        dtype=torch.float32)
+
+
+@pytest.mark.parametrize("paged,lens,S,bs,D,Hq,Hkv,Wl,cap,alibi", [
+    (True, [0, 31, 2000], 4, 16, 128, 16, 4, 100, 0.0, False),    # window inside the splits
+    (False, [30719], 76, 0, 128, 28, 4, 4095, 0.0, False),         # window, full cache
+    (True, [5, 1000], 3, 16, 128, 8, 2, -1, 30.0, False),          # soft-capping
+    (True, [77, 1500], 5, 7, 128, 8, 2, 64, 50.0, False),          # window + cap, plain loads
+    (False, [2048], 33, 0, 128, 8, 2, -1, 0.0, True),              # ALiBi
+    (True, [0, 700], 4, 16, 256, 16, 8, 255, 0.0, False),          # head_dim 256 with a window
+])
+def test_append_with_variants(dev, paged, lens, S, bs, D, Hq, Hkv, Wl, cap, alibi):
+    """Decode with append and a sliding window, soft-capping or ALiBi
+    (attn_decode_append_splitkv_ex): the combined result against the oracle's
+    decode with append under the same variant, and the caches bit for bit."""
+    if paged:
+        d = paged_with_room(len(lens), Hq, Hkv, D, lens, bs, seed=sum(lens) + S + 17)
+    else:
+        d = W.make_decode_contiguous(len(lens), Hq, Hkv, D, lens[0], seed=lens[0] + 23,
+                                     max_kv_len=lens[0] + 1)
+    kn, vn = new_rows(len(lens), Hkv, D, seed=S + 5)
+    sl = _alibi(Hq) if alibi else None
+    q, kc, vc, ln = d.q.to(dev), d.k_cache.to(dev), d.v_cache.to(dev), d.kv_lens.to(dev)
+    bt = d.block_table.to(dev) if d.block_table is not None else None
+    o, lse = attn.decode_append(q, kn.to(dev), vn.to(dev), kc, vc, ln, bt, num_splits=S,
+                                max_kv_len=d.max_kv_len or None, scale=d.scale, window_left=Wl,
+                                softcap=cap, alibi_slopes=sl.to(dev) if alibi else None)
+    attn.check_device_status()
+    o_ref, lse_ref, kc_ref, vc_ref = oracle.decode_append(
+        d.q, kn, vn, d.k_cache, d.v_cache, d.block_table, d.kv_lens.tolist(), d.scale,
+        d.block_size, window_left=Wl, softcap=cap, alibi_slopes=sl.tolist() if alibi else None)
+    compare(o, lse, o_ref, lse_ref, f"append lens={lens} W={Wl} cap={cap} alibi={alibi}")
+    assert torch.equal(bits(kc), bits(kc_ref)) and torch.equal(bits(vc), bits(vc_ref))

@@ -166,6 +166,28 @@ def _append(L, **kw):
                                         a["scale"], None)
 
 
+def _append_ex(L, w=-1, cap=0.0, al=None, **kw):
+    a = dict(q=P, kn=P, vn=P, k=P, v=P, bt=P, lens=P, S=4, op=P, lp=P, B=2, hq=8, hkv=2, d=128,
+             bs=16, mb=8, nb=16, maxlen=128, scale=0.1)
+    a.update(kw)
+    return L.attn_decode_append_splitkv_ex(a["q"], a["kn"], a["vn"], a["k"], a["v"], a["bt"],
+                                           a["lens"], a["S"], a["op"], a["lp"], a["B"], a["hq"],
+                                           a["hkv"], a["d"], a["bs"], a["mb"], a["nb"],
+                                           a["maxlen"], a["scale"], w, cap, al, None)
+
+
+def test_decode_append_ex_validation(L):
+    c = _lib.status_codes()
+    assert _append_ex(L, kn=None) == c["ATTN_ERR_NULL"]
+    assert _append_ex(L, w=-3) == c["ATTN_ERR_SHAPE"]                # window below -1
+    assert _append_ex(L, cap=-1.0) == c["ATTN_ERR_SHAPE"]
+    assert _append_ex(L, cap=float("nan")) == c["ATTN_ERR_SHAPE"]
+    assert _append_ex(L, cap=2.0, al=P) == c["ATTN_ERR_SHAPE"]       # ALiBi with soft-capping
+    assert _append_ex(L, w=10, al=P + 2) == c["ATTN_ERR_ALIGN"]      # misaligned slopes
+    assert _append_ex(L, w=10, vn=P + 2) == c["ATTN_ERR_ALIGN"]
+    assert _append_ex(L, w=10, d=96) == c["ATTN_ERR_HEADDIM"]
+
+
 def test_decode_append_validation(L):
     c = _lib.status_codes()
     assert _append(L, kn=None) == c["ATTN_ERR_NULL"]

@@ -382,6 +382,26 @@ def test_decode_append_reproduces_prefill_rows():
     assert _pin_append() <= TOL
 
 
+def test_decode_append_with_variants_reproduces_prefill_rows():
+    """Token-by-token decode with append under a sliding window, soft-capping
+    or ALiBi, from an empty paged cache, reproduces every row of causal
+    prefill under the same variant (the prefill being pinned on its own)."""
+    N, nq, nkv, d, bs = 29, 4, 2, 8, 8
+    x = W.make_prefill(1, nq, nkv, N, d, seed=6)
+    slopes = [0.5, 0.25, 0.125, 0.0625]
+    for Wl, cap, al in [(5, 0.0, None), (-1, 1.5, None), (3, 2.0, None), (-1, 0.0, slopes),
+                        (6, 0.0, slopes)]:
+        op, lp = oracle.prefill(x.q, x.k, x.v, x.scale, True, window_left=Wl, softcap=cap,
+                                alibi_slopes=al)
+        table, kc, vc = _paged_empty_cache((N + bs - 1) // bs, 1, bs, nkv, d, seed=4)
+        for t in range(N):
+            o, lse, kc, vc = oracle.decode_append(x.q[:, :, t], x.k[:, :, t], x.v[:, :, t], kc, vc,
+                                                  table, [t], x.scale, bs, window_left=Wl,
+                                                  softcap=cap, alibi_slopes=al)
+            assert np.abs(o - op[:, :, t]).max() <= TOL, (Wl, cap, al is not None, t)
+            assert np.abs(lse - lp[:, :, t]).max() <= TOL
+
+
 def test_decode_append_closed_form_and_written_slot():
     """kv_len = 0: the query sees only its own token, so O = v_new of its kv
     head and LSE = scale * q . k_new.  Exactly one slot per sequence changes."""
