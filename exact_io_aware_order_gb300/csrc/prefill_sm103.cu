@@ -211,6 +211,16 @@ __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const Seq
   return t;
 }
 
+// The key tile an item visits j-th: in order, or, for causal ALiBi, from the
+// diagonal backwards.  The ALiBi bias grows toward the diagonal, so in order
+// the running max would grow tile after tile and O would be rescaled nearly
+// every tile; backwards, the first tile holds the row's largest scores.  The
+// online softmax is exact in any order.
+template <int VARIANT>
+__device__ __forceinline__ int key_tile_at(const Tile& t, int j, int causal) {
+  return (VARIANT == kWindowAlibi && causal) ? t.j0 + t.n - 1 - j : t.j0 + j;
+}
+
 // The r-th item of this CTA, or -1: rounds of gridDim.x items, taken in
 // alternating (snake) order so that, over two rounds, every CTA gets about
 // the same number of key tiles.
@@ -403,7 +413,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             return false;
           ++nq;
         }
-        if (!load_tile(&tm_k, L::kK, kKFull, kKEmpty, RK, nk, kc.t.kv0 + (kc.t.j0 + kc.j) * kBN,
+        if (!load_tile(&tm_k, L::kK, kKFull, kKEmpty, RK, nk,
+                       kc.t.kv0 + key_tile_at<VARIANT>(kc.t, kc.j, p.causal) * kBN,
                        kc.t.zk, false))
           return false;
         ++nk;
@@ -412,7 +423,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       };
       bool ok = load_k() && load_k();
       while (ok && vc.w >= 0) {
-        ok = load_tile(&tm_v, L::kV, kVFull, kVEmpty, RV, nv, vc.t.kv0 + (vc.t.j0 + vc.j) * kBN,
+        ok = load_tile(&tm_v, L::kV, kVFull, kVEmpty, RV, nv,
+                       vc.t.kv0 + key_tile_at<VARIANT>(vc.t, vc.j, p.causal) * kBN,
                        vc.t.zk, FP8);
         if (!ok) break;
         ++nv;
@@ -560,7 +572,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
             for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[c][i]);
         }
-        const int kv0 = (t.j0 + j) * kBN;  // first key of the tile, within the sequence
+        const int kv0 = key_tile_at<VARIANT>(t, j, p.causal) * kBN;  // first key of the tile
         if constexpr (VARIANT != kPlain) {
           if (VARIANT == kWindowCap && p.cap_in2 != 0.f) {
             // s -> softcap * tanh(s * scale / softcap); the factor softcap
