@@ -189,3 +189,31 @@ def test_decode_alibi(dev, paged, lens, S, Wl):
     # far splits carry biases of -slope * distance ~ -2.5e4: their fp32 LSE
     # is only good to a few units in the last place of that magnitude
     compare(op, lp, op_ref, lp_ref, f"alibi decode partials W={Wl}", lse_rel=2.0 ** -21)
+
+
+@pytest.mark.parametrize("D,paged,lens,S,Wl,cap,alibi", [
+    (64, True, [1000, 17, 3000], 5, 100, 0.0, False),      # head_dim 64: window
+    (64, False, [2500], 6, -1, 30.0, False),                # soft-capping
+    (64, True, [700, 2000], 4, -1, 0.0, True),              # ALiBi
+    (256, True, [1000, 17, 3000], 5, 200, 0.0, False),     # head_dim 256: window
+    (256, False, [2500], 6, 64, 50.0, False),               # window + soft-capping
+    (256, True, [700, 2000], 4, 300, 0.0, True),            # ALiBi with a window
+])
+def test_decode_variants_other_head_dims(dev, D, paged, lens, S, Wl, cap, alibi):
+    """Decode variants at head_dim 64 and 256 (the combined result)."""
+    if paged:
+        d = W.make_decode_paged(len(lens), 8, 4, D, lens, block_size=16, seed=sum(lens) + D)
+    else:
+        d = W.make_decode_contiguous(len(lens), 8, 2, D, lens[0], seed=lens[0] + D)
+    sl = alibi_slopes(8) if alibi else None
+    q, kc, vc, ln = d.q.to(dev), d.k_cache.to(dev), d.v_cache.to(dev), d.kv_lens.to(dev)
+    bt = d.block_table.to(dev) if d.block_table is not None else None
+    op, lp = attn.decode_splitkv(q, kc, vc, ln, bt, num_splits=S, max_kv_len=d.max_kv_len or None,
+                                 scale=d.scale, window_left=Wl, softcap=cap,
+                                 alibi_slopes=sl.to(dev) if alibi else None)
+    o, lse = attn.combine(op, lp)
+    attn.check_device_status()
+    o_ref, lse_ref = oracle.decode(d.q, d.k_cache, d.v_cache, d.block_table, d.kv_lens.tolist(),
+                                   d.scale, d.block_size, window_left=Wl, softcap=cap,
+                                   alibi_slopes=sl.tolist() if alibi else None)
+    compare(o, lse, o_ref, lse_ref, f"decode d={D} W={Wl} cap={cap} alibi={alibi}")
