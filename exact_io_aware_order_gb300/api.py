@@ -351,10 +351,14 @@ def combine(o_partial: torch.Tensor, lse_partial: torch.Tensor,
 
 
 def decode(q, k_cache, v_cache, kv_lens, block_table=None, num_splits: int = 0,
-           max_kv_len: Optional[int] = None, scale: Optional[float] = None, stream=None):
-    """Split-KV decode followed by the combine: returns (O (B, n_q, d), LSE (B, n_q))."""
+           max_kv_len: Optional[int] = None, scale: Optional[float] = None, stream=None,
+           window_left: int = -1, softcap: float = 0.0,
+           alibi_slopes: Optional[torch.Tensor] = None):
+    """Split-KV decode followed by the combine: returns (O (B, n_q, d), LSE (B, n_q)).
+    The variants are those of :func:`decode_splitkv`."""
     op, lp = decode_splitkv(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len,
-                            scale, stream=stream)
+                            scale, stream=stream, window_left=window_left, softcap=softcap,
+                            alibi_slopes=alibi_slopes)
     return combine(op, lp, stream=stream)
 
 

@@ -208,10 +208,9 @@ def test_decode_variants_other_head_dims(dev, D, paged, lens, S, Wl, cap, alibi)
     sl = alibi_slopes(8) if alibi else None
     q, kc, vc, ln = d.q.to(dev), d.k_cache.to(dev), d.v_cache.to(dev), d.kv_lens.to(dev)
     bt = d.block_table.to(dev) if d.block_table is not None else None
-    op, lp = attn.decode_splitkv(q, kc, vc, ln, bt, num_splits=S, max_kv_len=d.max_kv_len or None,
-                                 scale=d.scale, window_left=Wl, softcap=cap,
-                                 alibi_slopes=sl.to(dev) if alibi else None)
-    o, lse = attn.combine(op, lp)
+    o, lse = attn.decode(q, kc, vc, ln, bt, num_splits=S, max_kv_len=d.max_kv_len or None,
+                         scale=d.scale, window_left=Wl, softcap=cap,
+                         alibi_slopes=sl.to(dev) if alibi else None)
     attn.check_device_status()
     o_ref, lse_ref = oracle.decode(d.q, d.k_cache, d.v_cache, d.block_table, d.kv_lens.tolist(),
                                    d.scale, d.block_size, window_left=Wl, softcap=cap,
