@@ -574,11 +574,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         const int kv0 = key_tile_at<VARIANT>(t, j, p.causal) * kBN;  // first key of the tile
         if constexpr (VARIANT != kPlain) {
-          if (VARIANT == kWindowCap && p.cap_in2 != 0.f) {
-            // s -> softcap * tanh(s * scale / softcap); the factor softcap
-            // (and log2 e) is in sl2, so s becomes the tanh.
+          if constexpr (VARIANT == kWindowCap) {
+            // s -> softcap * tanh(s * scale / softcap) with tanh = 1 - 2 r,
+            // r = 1 / (2^v + 1), v = s * cap_in2: s keeps r, the max below
+            // takes the smallest r and the exponent folds 1 - 2 r into its
+            // FMA (softcap and log2 e are in sl2).  Masked scores get r = +inf.
+            // (the multiply and the +1 on pairs: one instruction for two scores)
+            const float2 ci = make_float2(p.cap_in2, p.cap_in2), one = make_float2(1.f, 1.f);
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) s[c] = tanh_from_exp2(s[c] * p.cap_in2);
+            for (int c = 0; c < kBN; c += 2) {
+              const float2 v = mul2(make_float2(s[c], s[c + 1]), ci);
+              const float2 e1 = add2(make_float2(ex2_approx(v.x), ex2_approx(v.y)), one);
+              s[c] = rcp_approx(e1.x);
+              s[c + 1] = rcp_approx(e1.y);
+            }
           }
           if constexpr (VARIANT == kWindowAlibi) {
             // s -> s scale log2 e - slope log2 e |i - j|
@@ -594,7 +603,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const int lo = lo_edge ? (q_row - p.window_left - kv0) : -1;  // first allowed column
 #pragma unroll
             for (int c = 0; c < kBN; ++c)
-              if (c > lim || c < lo) s[c] = -INFINITY;
+              if (c > lim || c < lo) s[c] = VARIANT == kWindowCap ? INFINITY : -INFINITY;
           }
         } else if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > t.len)) {
           const int lim = p.causal ? (q_row - kv0) : (t.len - 1 - kv0);  // last allowed column
@@ -602,16 +611,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           for (int c = 0; c < kBN; ++c)
             if (c > lim) s[c] = -INFINITY;
         }
-        // Row max: eight independent chains of 3-input max, then a small tree.
-        float mxa[8];
+        // Row max: eight independent chains of 3-input max, then a small tree
+        // (soft-capping: the smallest r, the largest tanh = 1 - 2 r).
+        float mx;
+        if constexpr (VARIANT == kWindowCap) {
+          float mna[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(s[k], s[k + 8]);
+          for (int k = 0; k < 8; ++k) mna[k] = fminf(s[k], s[k + 8]);
 #pragma unroll
-        for (int c = 16; c < kBN; c += 16)
+          for (int c = 16; c < kBN; c += 16)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mxa[k] = fmax3(mxa[k], s[c + k], s[c + 8 + k]);
-        const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
-                               fmaxf(mxa[6], mxa[7]));
+            for (int k = 0; k < 8; ++k) mna[k] = fmin3(mna[k], s[c + k], s[c + 8 + k]);
+          const float mn = fmin3(fmin3(mna[0], mna[1], mna[2]), fmin3(mna[3], mna[4], mna[5]),
+                                 fminf(mna[6], mna[7]));
+          mx = fmaf(-2.f, mn, 1.f);  // -inf when every score of the row is masked
+        } else {
+          float mxa[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+          for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mxa[k] = fmax3(mxa[k], s[c + k], s[c + 8 + k]);
+          mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
+                     fmaxf(mxa[6], mxa[7]));
+        }
         const float m_new = fmaxf(m, mx * sl2);
         // Rescale only when some row of the warp gained more than 2^8; otherwise
         // keep the stale max for both l and O (exact either way).
@@ -635,6 +659,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // window has m = -inf (all its P are 0): take 0 as its reference.
         const float m_ref = (VARIANT != kPlain && m == -INFINITY) ? 0.f : m;
         const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m_ref, -m_ref);
+        // soft-capping: exponent sl2 (1 - 2 r) - m = -2 sl2 r + (sl2 - m)
+        const float2 cap_a = make_float2(-2.f * sl2, -2.f * sl2), cap_b = make_float2(sl2 - m_ref, sl2 - m_ref);
         float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
 #pragma unroll
@@ -665,7 +691,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
               for (int i = 0; i < kPiece; ++i) {
                 const int k2 = c * 32 + hh * 2 * kPiece + 2 * i;
-                const float2 x = fma2(make_float2(s[k2], s[k2 + 1]), sl2v, nmv);
+                const float2 x = VARIANT == kWindowCap
+                                     ? fma2(make_float2(s[k2], s[k2 + 1]), cap_a, cap_b)
+                                     : fma2(make_float2(s[k2], s[k2 + 1]), sl2v, nmv);
                 const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                 rs[i & 3] = add2(rs[i & 3], pp);
                 pk[i] = pack_bf16x2(pp.x, pp.y);

@@ -413,6 +413,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Packed two-lane fp32 arithmetic (one instruction for two values).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   float2 d;
