@@ -15,7 +15,6 @@ from .api import (  # noqa: F401
     check_device_status,
     set_wait_timeout_ns,
     selftest_bounded_wait,
-    split_ranges,
     decode_noalloc,
     decode_append_splitkv,
     decode_append,

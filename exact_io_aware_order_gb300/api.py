@@ -190,23 +190,6 @@ def decode_num_splits(batch: int, n_kv_heads: int, max_kv_len: int, num_sms: int
                                             int(num_sms)))
 
 
-def split_ranges(kv_len: int, num_splits: int, window_left: int = -1):
-    """Tokens attended by every split under the library's split rule:
-    c = roundup(ceil(len / S), 16); split s covers [s*c, min((s+1)*c, len)).
-    With a sliding window the rule applies from lo16 (the window's first
-    token lo rounded down to a multiple of 16) and tokens below lo are dropped."""
-    lo = max(0, kv_len - 1 - window_left) if window_left >= 0 else 0
-    lo16 = lo // 16 * 16
-    n = kv_len - lo16
-    per = -(-n // num_splits)
-    c = -(-per // 16) * 16
-    out = []
-    for s in range(num_splits):
-        a, b = lo16 + min(s * c, n), lo16 + min(min(s * c, n) + c, n)
-        out.append((min(max(a, lo), b), b))
-    return out
-
-
 def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
                  o_partial, lse_partial, stream, new_kv=None, window_left=-1, softcap=0.0,
                  alibi_slopes=None):

@@ -33,3 +33,21 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, what="", lse_rel=0.0):
     assert emax <= O_MAX and emean <= O_MEAN and lerr <= LSE_MAX, \
         f"{what}: max|dO|={emax:.3e} mean|dO|={emean:.3e} max|dLSE|={lerr:.3e}"
     return emax, emean, float(lerr)
+
+
+def split_ranges(kv_len: int, num_splits: int, window_left: int = -1):
+    """Tokens attended by every split under the split rule the C header states
+    for attn_decode_splitkv(_ex), restated here for the tests:
+    c = roundup(ceil(len / S), 16); split s covers [s*c, min((s+1)*c, len)).
+    With a sliding window the rule applies from lo16 (the window's first
+    token lo rounded down to a multiple of 16) and tokens below lo are dropped."""
+    lo = max(0, kv_len - 1 - window_left) if window_left >= 0 else 0
+    lo16 = lo // 16 * 16
+    n = kv_len - lo16
+    per = -(-n // num_splits)
+    c = -(-per // 16) * 16
+    out = []
+    for s in range(num_splits):
+        a, b = lo16 + min(s * c, n), lo16 + min(min(s * c, n) + c, n)
+        out.append((min(max(a, lo), b), b))
+    return out

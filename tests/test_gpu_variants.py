@@ -9,9 +9,8 @@ import torch
 
 import exact_io_aware_order_gb300 as attn
 from exact_io_aware_order_gb300 import workloads as W
-from exact_io_aware_order_gb300.api import split_ranges
 import oracle
-from gpu_util import compare, nan_like
+from gpu_util import compare, nan_like, split_ranges
 
 pytestmark = pytest.mark.gpu
 

@@ -96,7 +96,7 @@ def test_variant_validation(L):
 @pytest.mark.parametrize("kv_len,S,W", [(100, 3, 10), (1000, 7, 0), (33, 2, 16), (5000, 9, 4095),
                                         (17, 4, 100), (0, 3, 5), (64, 1, 15)])
 def test_split_rule_with_window(kv_len, S, W):
-    from exact_io_aware_order_gb300.api import split_ranges
+    from gpu_util import split_ranges
 
     r = split_ranges(kv_len, S, W)
     lo = max(0, kv_len - 1 - W)
@@ -246,7 +246,7 @@ def _rule(kv_len, S):
 @pytest.mark.parametrize("kv_len,S", [(30720, 1), (30720, 16), (30720, 148), (1, 4), (17, 2),
                                       (1000, 7), (0, 3), (15, 16)])
 def test_split_rule(kv_len, S):
-    from exact_io_aware_order_gb300.api import split_ranges
+    from gpu_util import split_ranges
 
     r = split_ranges(kv_len, S)
     assert r == _rule(kv_len, S)

@@ -366,7 +366,7 @@ def _pin_append():
     x = W.make_prefill(1, nq, nkv, N, d, seed=5)
     op, lp = oracle.prefill(x.q, x.k, x.v, x.scale, True)
     table, kc, vc = _paged_empty_cache((N + bs - 1) // bs, 2, bs, nkv, d, seed=3)
-    kk = torch.full((1, N, nkv, d), float("nan"), dtype=torch.float64)
+    kk = torch.full((1, N + 3, nkv, d), float("nan"), dtype=torch.float64)  # spare slots
     vv = kk.clone()
     err = 0.0
     for t in range(N):
@@ -461,7 +461,8 @@ def _pin_varlen():
             ob, lb = ref.masked_attention(q[h].numpy(), k[h // (nq // nkv)].numpy(),
                                           v[h // (nq // nkv)].numpy(), 0.37, allowed)
             fin = np.isfinite(lb)
-            assert np.array_equal(fin, np.isfinite(lse[h]))
+            if not np.array_equal(fin, np.isfinite(lse[h])):
+                return math.inf                       # an empty row where there is none, or back
             err = max(err, float(np.abs(ob - o[h]).max()), float(np.abs(lb[fin] - lse[h][fin]).max()))
         # brute force on one row of each non-empty sequence
         for a, b in zip(cu[:-1], cu[1:]):
@@ -504,21 +505,71 @@ def test_varlen_sampled_rows_match_full():
 # ---------------------------------------------------------------------------
 
 def _pin_combine():
+    """Combine identity (page "FlashAttention for inference", section "The online
+    softmax, with every symbol defined", combining partial results): merging the
+    per-chunk partials of any chunking, empty chunks included, gives the whole
+    row's output and LSE -- plain, soft-capped and with ALiBi (the partials of
+    a variant are that variant's definition restricted to the chunk)."""
     rng = np.random.default_rng(0)
     worst = 0.0
     x = W.make_decode_contiguous(1, 6, 2, 32, 300, seed=4)
-    o_full, l_full = oracle.decode(x.q, x.k_cache, x.v_cache, None, [300], x.scale)
-    for trial in range(6):
-        cuts = np.sort(rng.choice(np.arange(0, 301), size=rng.integers(1, 7), replace=True))
-        bounds = [0] + cuts.tolist() + [300]
-        ranges = [[(bounds[i], bounds[i + 1]) for i in range(len(bounds) - 1)] + [(0, 0)]]
-        op, lp = oracle.decode_partials(x.q, x.k_cache, x.v_cache, None, [300], x.scale, 0, ranges)
-        oc, lc = oracle.combine(op, lp)
-        worst = max(worst, np.abs(oc - o_full).max(), np.abs(lc - l_full).max())
-        perm = rng.permutation(op.shape[0])           # order of chunks is irrelevant
-        oc2, lc2 = oracle.combine(op[perm], lp[perm])
-        worst = max(worst, np.abs(oc2 - oc).max(), np.abs(lc2 - lc).max())
+    slopes = [2.0 ** (-8.0 * (h + 1) / 6) for h in range(6)]
+    cases = [{}, {"softcap": 0.8}, {"alibi_slopes": slopes}]
+    for kw in cases:
+        o_full, l_full = oracle.decode(x.q, x.k_cache, x.v_cache, None, [300], x.scale, **kw)
+        for trial in range(6):
+            cuts = np.sort(rng.choice(np.arange(0, 301), size=rng.integers(1, 7), replace=True))
+            bounds = [0] + cuts.tolist() + [300]
+            ranges = [[(bounds[i], bounds[i + 1]) for i in range(len(bounds) - 1)] + [(0, 0)]]
+            op, lp = oracle.decode_partials(x.q, x.k_cache, x.v_cache, None, [300], x.scale, 0,
+                                            ranges, **kw)
+            oc, lc = oracle.combine(op, lp)
+            worst = max(worst, np.abs(oc - o_full).max(), np.abs(lc - l_full).max())
+            perm = rng.permutation(op.shape[0])           # order of chunks is irrelevant
+            oc2, lc2 = oracle.combine(op[perm], lp[perm])
+            worst = max(worst, np.abs(oc2 - oc).max(), np.abs(lc2 - lc).max())
     return worst
+
+
+def _pin_partials_bruteforce():
+    """Each split's partial (o, lse), plain and with each variant, against
+    scalar brute force (math.exp, math.tanh, math.fsum) over that split's
+    tokens only: the query is at position kv_len - 1, so ALiBi's distance is
+    kv_len - 1 - j whatever split holds token j."""
+    rng = np.random.default_rng(23)
+    nq, nkv, d, L = 4, 2, 4, 29
+    q = rng.standard_normal((1, nq, d))
+    kc = rng.standard_normal((1, L, nkv, d))
+    vc = rng.standard_normal((1, L, nkv, d))
+    ranges = [[(0, 7), (7, 7), (7, 20), (20, 29)]]
+    slopes = [0.3, 0.05, 0.7, 0.11]
+    worst = 0.0
+    for cap, sl in ((0.0, None), (1.3, None), (0.0, slopes)):
+        op, lp = oracle.decode_partials(q, kc, vc, None, [L], 0.8, 0, ranges, softcap=cap,
+                                        alibi_slopes=sl)
+        for s, (t0, t1) in enumerate(ranges[0]):
+            for h in range(nq):
+                kh = h // (nq // nkv)
+                sc = [0.8 * math.fsum(q[0, h, t] * kc[0, j, kh, t] for t in range(d))
+                      for j in range(t0, t1)]
+                if cap > 0:
+                    sc = [cap * math.tanh(v_ / cap) for v_ in sc]
+                if sl is not None:
+                    sc = [v_ - sl[h] * (L - 1 - j) for v_, j in zip(sc, range(t0, t1))]
+                if not sc:
+                    worst = max(worst, float(np.abs(op[s, 0, h]).max()),
+                                0.0 if lp[s, 0, h] == -np.inf else math.inf)
+                    continue
+                m = max(sc)
+                lse = m + math.log(math.fsum(math.exp(v_ - m) for v_ in sc))
+                o = [math.fsum(math.exp(v_ - lse) * vc[0, j, kh, t]
+                               for v_, j in zip(sc, range(t0, t1))) for t in range(d)]
+                worst = max(worst, abs(lse - lp[s, 0, h]), float(np.abs(np.array(o) - op[s, 0, h]).max()))
+    return worst
+
+
+def test_partials_with_variants_brute_force():
+    assert _pin_partials_bruteforce() <= TOL
 
 
 def test_combine_identity_random_chunkings():
@@ -609,17 +660,19 @@ def test_toy_run_split_decode(golden):
 def _pins():
     return {"bruteforce": (_pin_bruteforce, TOL), "sdpa": (_pin_sdpa, 1e-12),
             "closed": (_pin_closed_forms, TOL), "gqa": (_pin_gqa, TOL),
-            "combine": (_pin_combine, TOL), "append": (_pin_append, TOL),
+            "combine": (_pin_combine, TOL), "partials": (_pin_partials_bruteforce, TOL),
+            "append": (_pin_append, TOL),
             "varlen": (_pin_varlen, TOL), "variants": (_pin_variants, TOL)}
 
 
 def _any_pin_fails():
+    """Names of the pins whose error exceeds their tolerance.  A pin that
+    raises is not a catch: the exception propagates and fails the test, so a
+    planted mistake counts as caught only when some pin computes and
+    disagrees."""
     failed = []
     for name, (fn, tol) in _pins().items():
-        try:
-            err = fn()
-        except Exception:  # a crash counts as a caught mistake
-            err = math.inf
+        err = fn()
         if not (err <= tol):
             failed.append(name)
     return failed
@@ -633,7 +686,8 @@ def test_pins_pass_unmutated():
                                       "combine_unweighted", "gqa_off_by_one",
                                       "append_off_by_one", "append_not_attended",
                                       "varlen_cross_sequence", "window_off_by_one",
-                                      "softcap_unscaled", "alibi_sign"])
+                                      "softcap_unscaled", "alibi_sign",
+                                      "partials_softcap_dropped", "partials_alibi_dropped"])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     orig_ma = ref.masked_attention
     orig_comb = ref.combine
@@ -647,15 +701,20 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
         monkeypatch.setattr(ref, "_causal_allowed", strict)
     elif mutation == "no_scale":
         monkeypatch.setattr(ref, "masked_attention",
-                            lambda q, k, v, scale, allowed=None: orig_ma(q, k, v, 1.0, allowed))
+                            lambda q, k, v, scale, *a, **kw: orig_ma(q, k, v, 1.0, *a, **kw))
     elif mutation == "lse_no_max":
-        def bad(q, k, v, scale, allowed=None):
-            o, lse = orig_ma(q, k, v, scale, allowed)
-            s = scale * (ref._f64(q) @ ref._f64(k).T) if len(k) else None
-            if s is not None:
+        def bad(q, k, v, scale, allowed=None, softcap=0.0, bias=None):
+            o, lse = orig_ma(q, k, v, scale, allowed, softcap, bias)
+            if len(k) and len(q):
+                s = scale * (ref._f64(q) @ ref._f64(k).T)
+                if softcap > 0:
+                    s = softcap * np.tanh(s / softcap)
+                if bias is not None:
+                    s = s + bias
                 if allowed is not None:
                     s = np.where(allowed, s, -np.inf)
-                lse = lse - s.max(axis=1)     # dropped the max term
+                m = s.max(axis=1)
+                lse = lse - np.where(np.isfinite(m), m, 0.0)   # dropped the max term
             return o, lse
         monkeypatch.setattr(ref, "masked_attention", bad)
     elif mutation == "window_off_by_one":
@@ -663,10 +722,11 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
         monkeypatch.setattr(ref, "_window_allowed",
                             lambda r0, r1, n, c, w: orig_wa(r0, r1, n, c, w - 1 if w > 0 else w))
     elif mutation == "softcap_unscaled":
-        def bad_cap(q, k, v, scale, allowed=None, softcap=0.0):
+        def bad_cap(q, k, v, scale, allowed=None, softcap=0.0, bias=None):
             # cap * tanh(s) instead of cap * tanh(s / cap): the same as the
             # right formula applied to scores scaled by cap
-            return orig_ma(q, k, v, scale * softcap if softcap > 0 else scale, allowed, softcap)
+            return orig_ma(q, k, v, scale * softcap if softcap > 0 else scale, allowed, softcap,
+                           bias)
         monkeypatch.setattr(ref, "masked_attention", bad_cap)
     elif mutation == "alibi_sign":
         monkeypatch.setattr(ref, "_alibi", lambda slope, r, c: slope * np.abs(r[:, None] - c[None, :]))
@@ -678,8 +738,18 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
         monkeypatch.setattr(ref, "_append_position", lambda n: n + 1)
     elif mutation == "append_not_attended":
         orig_dec = ref.decode
-        monkeypatch.setattr(ref, "decode", lambda q, kc, vc, bt, lens, scale, bs=0:
-                            orig_dec(q, kc, vc, bt, [n - 1 for n in lens], scale, bs))
+        monkeypatch.setattr(ref, "decode", lambda q, kc, vc, bt, lens, scale, bs=0, **kw:
+                            orig_dec(q, kc, vc, bt, [n - 1 for n in lens], scale, bs, **kw))
+    elif mutation in ("partials_softcap_dropped", "partials_alibi_dropped"):
+        # the per-split partials forget one variant (the whole-row decode keeps it)
+        orig_part = ref.decode_partials
+        drop = "softcap" if mutation == "partials_softcap_dropped" else "alibi_slopes"
+
+        def bad_part(*a, **kw):
+            kw.pop(drop, None)
+            return orig_part(*a, **kw)
+        monkeypatch.setattr(ref, "decode_partials", bad_part)
+        monkeypatch.setattr(oracle, "decode_partials", bad_part)
     elif mutation == "combine_unweighted":
         monkeypatch.setattr(ref, "combine", lambda o, l: (ref._f64(o).mean(0), ref._f64(l).max(0)))
         monkeypatch.setattr(oracle, "combine", ref.combine)
