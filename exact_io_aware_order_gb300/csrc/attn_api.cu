@@ -75,6 +75,10 @@ attn::LaunchCtx make_ctx(void* stream, const DeviceState* s) {
 
 bool valid_scale(float scale) { return std::isfinite(scale) && scale > 0.f; }
 
+bool valid_variant(int window_left, float softcap) {
+  return window_left >= -1 && softcap >= 0.f && softcap < 3.0e38f;
+}
+
 int split_policy(int batch, int n_kv_heads, int max_kv_len, int num_sms) {
   if (batch <= 0 || n_kv_heads <= 0 || max_kv_len <= 0 || num_sms <= 0) return 1;
   // Two decode CTAs are resident per SM.  One sequence: exactly one full wave
@@ -103,6 +107,37 @@ int resolve_launch_ctx(void* stream, LaunchCtx* out) {
   DeviceState* ds = device_state(&st);
   if (!ds) return st;
   *out = make_ctx(stream, ds);
+  return ATTN_OK;
+}
+
+int validate_decode(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                    const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* block_table,
+                    const int32_t* kv_lens, int num_splits, const float* o_partial,
+                    const float* lse_partial, int batch, int n_q_heads, int n_kv_heads,
+                    int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                    int max_kv_len, float scale, bool append, int window_left, float softcap,
+                    const float* alibi_slopes) {
+  if (!q || !k_cache || !v_cache || !kv_lens || !o_partial || !lse_partial) return ATTN_ERR_NULL;
+  if (append && (!k_new || !v_new)) return ATTN_ERR_NULL;
+  if (!valid_variant(window_left, softcap)) return ATTN_ERR_SHAPE;
+  if (alibi_slopes && softcap > 0.f) return ATTN_ERR_SHAPE;  // not combined
+  if (!aligned(alibi_slopes, 4)) return ATTN_ERR_ALIGN;
+  if (append && (!aligned(k_new, 16) || !aligned(v_new, 16))) return ATTN_ERR_ALIGN;
+  const bool paged = block_table != nullptr;
+  if (batch < 1 || batch > 65535 || n_q_heads < 1 || n_kv_heads < 1 || n_kv_heads > 65535 ||
+      max_kv_len < 0 || !valid_scale(scale))
+    return ATTN_ERR_SHAPE;
+  if (paged && (block_size < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+                (long long)block_size * max_blocks_per_seq > (1LL << 30)))
+    return ATTN_ERR_SHAPE;
+  if (!paged && max_kv_len < 1) return ATTN_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
+  if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 16) return ATTN_ERR_GQA;
+  if (num_splits < 0 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(o_partial, 16) || !aligned(lse_partial, 4) || !aligned(kv_lens, 4) ||
+      (paged && !aligned(block_table, 4)))
+    return ATTN_ERR_ALIGN;
   return ATTN_OK;
 }
 }  // namespace attn
@@ -147,10 +182,6 @@ int attn_decode_num_splits(int batch, int n_kv_heads, int max_kv_len, int num_sm
 }
 
 namespace {
-
-bool valid_variant(int window_left, float softcap) {
-  return window_left >= -1 && softcap >= 0.f && softcap < 3.0e38f;
-}
 
 int prefill_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o, float* lse,
                  int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim, float scale,
@@ -228,7 +259,8 @@ int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16*
 
 namespace {
 
-// Validation and launch shared by the plain and the appending decode.
+// Launch shared by the plain and the appending decode (validation in
+// attn::validate_decode, which attn_decode_noalloc calls too).
 int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,
                 const attn_bf16* k_cache, const attn_bf16* v_cache, const int32_t* block_table,
                 const int32_t* kv_lens, int num_splits, float* o_partial, float* lse_partial,
@@ -236,27 +268,13 @@ int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_n
                 int max_blocks_per_seq, int num_blocks, int max_kv_len, float scale,
                 void* stream, bool append, int window_left = -1, float softcap = 0.f,
                 const float* alibi_slopes = nullptr) {
-  if (!q || !k_cache || !v_cache || !kv_lens || !o_partial || !lse_partial) return ATTN_ERR_NULL;
-  if (append && (!k_new || !v_new)) return ATTN_ERR_NULL;
-  if (!valid_variant(window_left, softcap)) return ATTN_ERR_SHAPE;
-  if (alibi_slopes && softcap > 0.f) return ATTN_ERR_SHAPE;  // not combined
-  if (!aligned(alibi_slopes, 4)) return ATTN_ERR_ALIGN;
-  if (append && (!aligned(k_new, 16) || !aligned(v_new, 16))) return ATTN_ERR_ALIGN;
+  const int vst = attn::validate_decode(q, k_new, v_new, k_cache, v_cache, block_table, kv_lens,
+                                        num_splits, o_partial, lse_partial, batch, n_q_heads,
+                                        n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                        num_blocks, max_kv_len, scale, append, window_left,
+                                        softcap, alibi_slopes);
+  if (vst != ATTN_OK) return vst;
   const bool paged = block_table != nullptr;
-  if (batch < 1 || batch > 65535 || n_q_heads < 1 || n_kv_heads < 1 || n_kv_heads > 65535 ||
-      max_kv_len < 0 || !valid_scale(scale))
-    return ATTN_ERR_SHAPE;
-  if (paged && (block_size < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
-                (long long)block_size * max_blocks_per_seq > (1LL << 30)))
-    return ATTN_ERR_SHAPE;
-  if (!paged && max_kv_len < 1) return ATTN_ERR_SHAPE;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
-  if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 16) return ATTN_ERR_GQA;
-  if (num_splits < 0 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(o_partial, 16) || !aligned(lse_partial, 4) || !aligned(kv_lens, 4) ||
-      (paged && !aligned(block_table, 4)))
-    return ATTN_ERR_ALIGN;
   int st = ATTN_OK;
   DeviceState* ds = device_state(&st);
   if (!ds) return st;

@@ -106,6 +106,19 @@ cudaError_t launch_quantize(const QuantArgs& a, const LaunchCtx& ctx);
 // word, SM count) for a call on `stream`; returns an attn_status code.
 int resolve_launch_ctx(void* stream, LaunchCtx* out);
 
+// Validation of a split-KV decode request, shared by every decode entry
+// point: pointers (o_partial / lse_partial stand for whatever the entry
+// point writes its per-split or final results to), shapes, GQA ratio, split
+// count, variants and alignment.  Returns an attn_status code; launches
+// nothing and touches no device state.
+int validate_decode(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                    const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* block_table,
+                    const int32_t* kv_lens, int num_splits, const float* o_partial,
+                    const float* lse_partial, int batch, int n_q_heads, int n_kv_heads,
+                    int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                    int max_kv_len, float scale, bool append, int window_left, float softcap,
+                    const float* alibi_slopes);
+
 // Split rule shared by the decode kernel's documentation and the host:
 // c = roundup(ceil(len / S), 16); split s covers [s*c, min((s+1)*c, len)).
 constexpr int kSplitGranule = 16;

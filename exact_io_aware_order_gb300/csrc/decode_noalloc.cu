@@ -1,7 +1,6 @@
 // attn_decode_noalloc: split-KV decode + combine with the split partials kept
 // in a fixed device buffer, for callers that cannot allocate device memory
 // (see include/attn.h).  It reuses the decode and combine kernels unchanged.
-#include <cmath>
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -19,14 +18,17 @@ constexpr int kMaxDevices = 64;
 // the host it is only a stand-in); it uses the address looked up below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
+// Per device: the buffer's device address once a lookup has succeeded.  A
+// failed lookup (for example one made while a stream capture forbids it) is
+// not remembered: the next call on that device tries again.
 struct ScratchAddr {
-  std::once_flag once;
-  cudaError_t err = cudaErrorUnknown;
+  std::mutex mu;
   void* ptr = nullptr;
 };
 ScratchAddr g_addr[kMaxDevices];
 
-// Once per device, with that device current: the buffer's device address.
+// The buffer's device address on the current device, looked up with that
+// device current.
 void* scratch_address(int* status) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -34,18 +36,19 @@ void* scratch_address(int* status) {
     return nullptr;
   }
   ScratchAddr& a = g_addr[dev];
-  std::call_once(a.once, [&a] {
-    a.err = cudaGetSymbolAddress(&a.ptr, g_noalloc_scratch);
-  });
-  if (a.err != cudaSuccess || a.ptr == nullptr) {
-    *status = ATTN_ERR_LAUNCH;
-    return nullptr;
+  std::lock_guard<std::mutex> lock(a.mu);
+  if (a.ptr == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // clear the recorded error: it must not surface at a later CUDA call
+      *status = ATTN_ERR_LAUNCH;
+      return nullptr;
+    }
+    a.ptr = p;
   }
   *status = ATTN_OK;
   return a.ptr;
 }
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
 
@@ -55,21 +58,14 @@ extern "C" int attn_decode_noalloc(const attn_bf16* q, const attn_bf16* k_cache,
                                    int batch, int n_q_heads, int n_kv_heads, int head_dim,
                                    int block_size, int max_blocks_per_seq, int num_blocks,
                                    int max_kv_len, float scale, void* stream) {
-  if (!q || !k_cache || !v_cache || !kv_lens || !o || !lse) return ATTN_ERR_NULL;
+  // The same checks as every other decode entry point (o and lse stand in
+  // for the partial outputs they replace).
+  const int vst = attn::validate_decode(q, nullptr, nullptr, k_cache, v_cache, block_table,
+                                        kv_lens, num_splits, o, lse, batch, n_q_heads, n_kv_heads,
+                                        head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                        max_kv_len, scale, false, -1, 0.f, nullptr);
+  if (vst != ATTN_OK) return vst;
   const bool paged = block_table != nullptr;
-  if (batch < 1 || batch > 65535 || n_q_heads < 1 || n_kv_heads < 1 || n_kv_heads > 65535 ||
-      max_kv_len < 0 || !std::isfinite(scale) || !(scale > 0.f))
-    return ATTN_ERR_SHAPE;
-  if (paged && (block_size < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
-                (long long)block_size * max_blocks_per_seq > (1LL << 30)))
-    return ATTN_ERR_SHAPE;
-  if (!paged && max_kv_len < 1) return ATTN_ERR_SHAPE;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
-  if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 16) return ATTN_ERR_GQA;
-  if (num_splits < 0 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
-      !aligned(lse, 4) || !aligned(kv_lens, 4) || (paged && !aligned(block_table, 4)))
-    return ATTN_ERR_ALIGN;
 
   attn::LaunchCtx ctx;
   if (num_splits == 0) {

@@ -575,6 +575,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int kv0 = key_tile_at<VARIANT>(t, j, p.causal) * kBN;  // first key of the tile
         if constexpr (VARIANT != kPlain) {
           if constexpr (VARIANT == kWindowCap) {
+            // This flavour requires softcap > 0 (cap_in2 != 0): with a zero
+            // factor every r would be 1/2 and the softmax uniform.  The host
+            // launches it only then (launch_prefill_t refuses otherwise).
             // s -> softcap * tanh(s * scale / softcap) with tanh = 1 - 2 r,
             // r = 1 / (2^v + 1), v = s * cap_in2: s keeps r, the max below
             // takes the smallest r and the exponent folds 1 - 2 r into its
@@ -911,6 +914,8 @@ template <int D, bool VARLEN, int VARIANT>
 cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   constexpr bool FP8 = VARIANT == kFp8;
   using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2>;
+  // The soft-cap flavour drops the factor's zero test from its hot loop.
+  if (VARIANT == kWindowCap && !(a.softcap > 0.f)) return cudaErrorInvalidValue;
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);

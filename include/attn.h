@@ -387,8 +387,10 @@ int attn_selftest_bounded_wait(void* stream);
  *   output part rounded up to 256 bytes, must fit in ATTN_NOALLOC_SCRATCH_BYTES;
  *   larger requests return ATTN_ERR_SCRATCH and launch nothing.
  * Set-up: the first call on each device looks up the buffer's device address
- *   (cudaGetSymbolAddress, once per device, with that device current); make
- *   that first call before any stream capture begins.
+ *   (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *   process; make that first call before any stream capture begins.  A
+ *   lookup that fails returns ATTN_ERR_LAUNCH and is tried again by the next
+ *   call on that device.
  * Sharing: every call reuses the same buffer, which keeps the previous call's
  *   contents.  Each call overwrites every partial value it later reads, so
  *   nothing needs clearing; but two calls whose kernels overlap on the GPU
