@@ -1,16 +1,22 @@
 #!/usr/bin/env python
 """Benchmark of the exact-attention hot path on GB300.
 
-One step = the whole hot path over one batch of synthetic input:
-  * causal prefill of one Qwen2.5-7B-shaped attention layer (batch 1, 28 query
-    / 4 key-value heads, head_dim 128, N = 8192 tokens): attn_prefill;
-  * one split-KV single-token decode over a 30720-token contiguous cache of the
-    same layer shape (auto split count): attn_decode_splitkv + attn_combine.
+One step = the whole hot path over one batch of synthetic input, run as the
+layer stack of a model forward:
+  * causal prefill at the Llama-3-8B attention shape at long context (batch 1,
+    32 query / 8 key-value heads, head_dim 128, N = 32768, 1% of the keys
+    scaled by 8), once per layer of that model (32 launches): attn_prefill;
+  * single-token split-KV decode + LSE combine at the Qwen2.5-7B attention
+    shape (28 / 4 heads) over a 30720-token contiguous cache, once per layer
+    of that model (28 layers, each its own cache, launched back to back):
+    attn_decode_splitkv + attn_combine.
 The headline value is causal-prefill attention TFLOP/s (4 N^2 d heads, halved
-for causal); the decode HBM GB/s is reported beside it.  Inputs are resident
-in HBM when the timed region starts; the decode cache rotates over four copies
-(4 x 62.9 MB > L2) and the prefill writes a 117 MB output each step, so no
-step reads warm L2 data from the step before.
+for causal); the decode's HBM GB/s per layer is reported beside it.  Inputs
+are resident in HBM when the timed region starts and exceed L2.  After the
+timed region every other workload is measured once and reported under
+"configs" (Qwen prefill at N = 2048 and 8192, Llama prefill at N = 30720, the
+decode split sweep single and chained, the paged batch decode), followed by
+the next rows (append, packed, FP8, head_dim 256, variants).
 
 `--impl reference` times the float64 CPU oracle (the only other place this file
 runs anything under oracle/) on a bounded sample of the same workload.
@@ -36,17 +42,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "causal prefill attention TFLOP/s (% BF16 peak); split-KV decode HBM GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "prefill_sm103_qwen_n8192.txt")
+# Nominal GB300 figures, for the fractions quoted beside the measured ones.
+NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 7900.0}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "prefill_sm103_llama_n32768.txt")
 PREFILL_SRC = os.path.join(ROOT, "exact_io_aware_order_gb300", "csrc", "prefill_sm103.cu")
 
-WORKLOADS = {
-    # name: (prefill (n_q, n_kv, N, d, spike), decode kind)
-    "qwen": dict(n_q=28, n_kv=4, seqlen=8192, d=128, spike=0.0, decode="qwen30720",
-                 desc="Qwen2.5-7B attention layer: causal prefill N=8192 (28/4 heads, d=128) + "
-                      "split-KV decode over a 30720-token contiguous cache"),
-    "llama-long": dict(n_q=32, n_kv=8, seqlen=32768, d=128, spike=0.01, decode="paged16",
-                       desc="Llama-3-8B attention layer: causal prefill N=32768 (32/8 heads, "
-                            "1% keys x8) + paged decode of 16 sequences, lengths U[1024,32768]"),
+HEADLINE = {
+    "prefill": dict(n_q=32, n_kv=8, seqlen=32768, d=128, layers=32),
+    "decode": dict(n_q=28, n_kv=4, kv_len=30720, layers=28),
+    "desc": "Llama-3-8B attention, causal prefill N=32768 (32/8 heads, d=128, 1% keys x8) "
+            "x 32 layers + Qwen2.5-7B attention, split-KV decode + combine over a "
+            "30720-token cache (28/4 heads) x 28 layers",
 }
 
 
@@ -163,6 +169,27 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # The GB300 arm.
 # ---------------------------------------------------------------------------
+def _ev():
+    import torch
+
+    return torch.cuda.Event(enable_timing=True)
+
+
+def _host_ahead():
+    """Keeps the GPU busy for ~1 ms so that the launches queued next are
+    already waiting when it gets to them (launch latency off the clock)."""
+    import torch
+
+    torch.cuda._sleep(2_000_000)
+
+
+def _rooflines(achieved, peak, nominal, unit, bound, **extra):
+    d = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+         "frac": round(achieved / peak, 4), "frac_of_nominal": round(achieved / nominal, 4)}
+    d.update(extra)
+    return d
+
+
 def run_gb300(args, rank: int, world: int, dist):
     import torch
 
@@ -172,67 +199,64 @@ def run_gb300(args, rank: int, world: int, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     attn.lib()  # fail loudly if the library is missing
-    wl = WORKLOADS[args.workload]
     peaks, peak_src = load_peaks()
+    P = HEADLINE["prefill"]
+    Dc = HEADLINE["decode"]
+    LP, LD = P["layers"], Dc["layers"]
 
     # ---- inputs (seeded, synthetic), resident in HBM ----
-    x = W.make_prefill(1, wl["n_q"], wl["n_kv"], wl["seqlen"], wl["d"], seed=0,
-                       spike_frac=wl["spike"])
+    x = W.llama_long_prefill(P["seqlen"])
     q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
-    o = torch.empty((1, wl["n_q"], wl["seqlen"], wl["d"]), dtype=torch.float32, device=dev)
-    lse = torch.empty((1, wl["n_q"], wl["seqlen"]), dtype=torch.float32, device=dev)
-    if wl["decode"] == "qwen30720":
-        dec = W.qwen_decode(30720)
-    else:
-        dec = W.llama_paged_decode()
-    n_copies = 4
-    caches = []
-    for c in range(n_copies):  # rotate so no decode reads a cache left warm in L2
-        caches.append((dec.k_cache.to(dev), dec.v_cache.to(dev)))
-    dq = dec.q.to(dev)
-    dlens = dec.kv_lens.to(dev)
-    dbt = dec.block_table.to(dev) if dec.block_table is not None else None
+    o = [torch.empty(tuple(x.q.shape), dtype=torch.float32, device=dev) for _ in range(2)]
+    lse = [torch.empty(tuple(x.q.shape[:3]), dtype=torch.float32, device=dev) for _ in range(2)]
+    flops = prefill_flops(P["n_q"], P["seqlen"], P["d"])
+    dec = W.qwen_decode(Dc["kv_len"])
+    dq, dlens = dec.q.to(dev), dec.kv_lens.to(dev)
+    kc0, vc0 = dec.k_cache.to(dev), dec.v_cache.to(dev)
+    caches = [(kc0, vc0)] + [(kc0.clone(), vc0.clone()) for _ in range(LD - 1)]  # one per layer
     B, Hq, D = dq.shape
     S = attn.decode_num_splits(B, dec.n_kv, dec.max_kv_len)
     op = torch.empty((S, B, Hq, D), dtype=torch.float32, device=dev)
     lp = torch.empty((S, B, Hq), dtype=torch.float32, device=dev)
     do = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
     dl = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-    tokens = int(dec.kv_lens.sum())
-    dec_bytes = (tokens * dec.n_kv * D * 2 * 2) + dq.numel() * 2 + do.numel() * 4 + dl.numel() * 4
-    flops = prefill_flops(wl["n_q"], wl["seqlen"], wl["d"])
+    dec_bytes = decode_bytes(dec)
 
-    # A read-only sweep over a buffer twice the size of L2 between the prefill
-    # and the decode: the prefill leaves much of its 117 MB output dirty in L2,
-    # and without the sweep the decode's timing would include writing those
-    # lines back.  The sweep leaves only clean lines (none of the decode's
-    # inputs), so the decode still reads its cache from HBM.
-    sweep = torch.ones((2 * (int(torch.cuda.get_device_properties(dev).L2_cache_size) or (128 << 20))) // 4,
-                       dtype=torch.float32, device=dev)
+    # A read-only sweep over twice the L2 between the prefill chain and the
+    # decode chain: the prefill leaves much of its output dirty in L2, and
+    # without the sweep the first decodes would pay for those write-backs.
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size) or (128 << 20)
+    sweep = torch.ones((2 * l2) // 4, dtype=torch.float32, device=dev)
     sweep_out = torch.empty((), dtype=torch.float32, device=dev)
 
-    def step(i, ev=None):
-        kc, vc = caches[i % n_copies]
+    def decode_layer(l):
+        kc, vc = caches[l]
+        attn.decode_splitkv(dq, kc, vc, dlens, None, num_splits=S, max_kv_len=dec.max_kv_len,
+                            scale=dec.scale, o_partial=op, lse_partial=lp)
+        attn.combine(op, lp, out=do, lse=dl)
+
+    def step(ev=None):
         if ev is not None:
             ev[0].record()
-        attn.prefill(q, k, v, x.scale, True, out=o, lse=lse)
+        for l in range(LP):
+            attn.prefill(q, k, v, x.scale, True, out=o[l & 1], lse=lse[l & 1])
         if ev is not None:
             ev[1].record()
         torch.sum(sweep, dim=0, out=sweep_out)
+        _host_ahead()
         if ev is not None:
-            ev[4].record()
-        # no event between the decode and the combine: one would stop the
-        # combine's programmatic early launch (about 3 us per step)
-        attn.decode_splitkv(dq, kc, vc, dlens, dbt, num_splits=S, max_kv_len=dec.max_kv_len,
-                            scale=dec.scale, o_partial=op, lse_partial=lp)
-        attn.combine(op, lp, out=do, lse=dl)
+            ev[2].record()
+        # decode + combine of every layer, back to back; no event between a
+        # decode and its combine (it would stop the combine's early launch)
+        for l in range(LD):
+            decode_layer(l)
         if ev is not None:
             ev[3].record()
 
     for i in range(args.warmup):
-        step(i)
+        step()
     attn.check_device_status()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[_ev() for _ in range(4)] for _ in range(args.steps)]
     gpu_uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", "") or "")
     sampler = ClockSampler(("GPU-" + gpu_uuid) if gpu_uuid and not gpu_uuid.startswith("GPU-")
                            else (gpu_uuid or str(dev.index)))
@@ -240,116 +264,301 @@ def run_gb300(args, rank: int, world: int, dist):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    t_start, t_end = _ev(), _ev()
     t_start.record()
     for i in range(args.steps):
-        step(i, evs[i])
+        step(evs[i])
     t_end.record()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
     attn.check_device_status()
-    # The decode kernel alone, for its roofline: the same launches with
-    # events around the decode only (the sweep before each, outside them).
-    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    for i, (ea, eb) in enumerate(dev_ev):
-        kc, vc = caches[i % n_copies]
-        torch.sum(sweep, dim=0, out=sweep_out)
-        ea.record()
-        attn.decode_splitkv(dq, kc, vc, dlens, dbt, num_splits=S, max_kv_len=dec.max_kv_len,
-                            scale=dec.scale, o_partial=op, lse_partial=lp)
-        eb.record()
-    torch.cuda.synchronize()
-    attn.check_device_status()
-    dec_alone_ms = [ea.elapsed_time(eb) for ea, eb in dev_ev]
-    app = time_decode_append(args, attn, dq, caches, dec, S, op, lp, sweep, sweep_out, dist, dev)
-    vl = time_prefill_varlen(args, attn, W, dist, dev) if args.workload == "qwen" else None
-    f8 = time_fp8(args, attn, x, q, k, v, o, lse, dist, dev) if args.workload == "qwen" else None
-    d256 = time_d256(args, attn, W, dist, dev) if args.workload == "qwen" else None
-    var = time_variants(args, attn, q, k, v, x.scale, o, lse, dq, caches, dec, S, op, lp, sweep,
-                        sweep_out, dist, dev) if args.workload == "qwen" else None
     total_ms = t_start.elapsed_time(t_end)
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dec_ms = [e[4].elapsed_time(e[3]) for e in evs]  # decode + combine
-    pre_total = sum(pre_ms)
-    dec_total = sum(dec_ms)
-
-    total_ms, pre_total, dec_total = rank_max(dist, [total_ms, pre_total, dec_total], dev)
-    avg_pre = statistics.mean(pre_ms)
-    avg_dec = statistics.mean(dec_alone_ms)
-    prefill_tflops = job_rate(flops, args.steps, world, pre_total) / 1e12
-    decode_gbs = job_rate(dec_bytes, args.steps, world, dec_total) / 1e9
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms, pre_total, dec_total = rank_max(dist, [total_ms, sum(pre_ms), sum(dec_ms)], dev)
+    prefill_tflops = job_rate(flops * LP, args.steps, world, pre_total) / 1e12
+    decode_gbs = job_rate(dec_bytes * LD, args.steps, world, dec_total) / 1e9
+    avg_pre = statistics.mean(pre_ms) / LP
     achieved = flops / (avg_pre * 1e-3) / 1e12
-    dec_achieved = dec_bytes / (avg_dec * 1e-3) / 1e9
-    traffic = profiled_traffic() if args.workload == "qwen" else None
+    traffic = profiled_traffic()
 
     result = {
         "metric": METRIC, "value": round(prefill_tflops, 2), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl["desc"], "batch": 1, "n_q_heads": wl["n_q"],
-                   "n_kv_heads": wl["n_kv"], "seqlen": wl["seqlen"], "head_dim": wl["d"],
-                   "decode_tokens": tokens, "decode_num_splits": S,
-                   "l2": "decode cache rotated over 4 copies (> L2); a read-only sweep of "
-                         "2x L2 between prefill and decode writes back the prefill's dirty "
-                         "output lines (outside the decode's events, inside the step)",
-                   "parallelism": f"replicas x{world}"},
-        "prefill_frac_of_bf16_peak": round(achieved / peaks["bf16_tflops"], 4),
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": traffic,
-                     "kernel": "prefill_kernel<128>", "peak_source": peak_src + " bf16 burst",
-                     "flops_per_launch": flops, "avg_launch_ms": round(avg_pre, 4)},
+        "config": headline_config(world),
+        "roofline": _rooflines(achieved, peaks["bf16_tflops_sustained"], NOMINAL["bf16_tflops"],
+                               "TFLOP/s", "tensor", traffic=traffic,
+                               kernel="prefill_kernel<128, 0, 0>",
+                               peak_source=peak_src + " bf16 sustained (the prefill runs "
+                               "back to back for seconds inside the timed region)",
+                               frac_of_burst_peak=round(achieved / peaks["bf16_tflops"], 4),
+                               flops_per_launch=flops, avg_launch_ms=round(avg_pre, 4),
+                               launches=LP * args.steps),
         "decode": {"value": round(decode_gbs, 1), "unit": "GB/s",
-                   "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 1),
-                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                "frac": round(dec_achieved / peaks["hbm_gbs"], 4),
-                                "kernel": "decode_splitkv_kernel<128>",
-                                "peak_source": peak_src + " hbm copy",
-                                "bytes_per_launch": dec_bytes,
-                                "avg_launch_us": round(avg_dec * 1e3, 2),
-                                "decode_plus_combine_avg_us": round(statistics.mean(dec_ms) * 1e3, 2),
-                                "combine_incremental_us": round(
-                                    (statistics.mean(dec_ms) - avg_dec) * 1e3, 2)}},
-        "gpu_launches": 3 * args.steps,
+                   "what": f"decode + combine per layer, {LD} layers back to back (each its "
+                           f"own {Dc['kv_len']}-token cache), chained by programmatic "
+                           "dependent launch: steady state",
+                   "frac": round(decode_gbs / peaks["hbm_gbs"], 4),
+                   "frac_of_nominal": round(decode_gbs / NOMINAL["hbm_gbs"], 4),
+                   "peak": peaks["hbm_gbs"], "peak_source": peak_src + " hbm copy",
+                   "bytes_per_layer": dec_bytes, "num_splits": S,
+                   "avg_layer_us": round(statistics.mean(dec_ms) / LD * 1e3, 2)},
+        "gpu_launches": (LP + 2 * LD) * args.steps,
         "clocks": clocks,
     }
-    if var is not None:
-        for v_ in var["prefill"].values():
-            v_["frac"] = round(v_["value"] / peaks["bf16_tflops"], 4)
-        var["decode"]["frac"] = round(var["decode"]["value"] / peaks["hbm_gbs"], 4)
-        result["variants"] = var
-    if d256 is not None:
-        d256["roofline"]["peak"] = peaks["bf16_tflops"]
-        d256["roofline"]["frac"] = round(d256["roofline"]["achieved"] / peaks["bf16_tflops"], 4)
-        d256["decode"]["roofline"]["peak"] = peaks["hbm_gbs"]
-        d256["decode"]["roofline"]["frac"] = round(
-            d256["decode"]["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
-        result["prefill_d256"] = d256
-    if f8 is not None:
-        f8_peak = peaks["bf16_tflops"] * 2.0   # nominal dense fp8 / bf16 ratio (4.5 / 2.25)
-        f8["roofline"]["peak"] = round(f8_peak, 1)
-        f8["roofline"]["frac"] = round(f8["roofline"]["achieved"] / f8_peak, 4)
-        f8["roofline"]["peak_source"] = peak_src + " bf16 burst x 2 (nominal fp8 / bf16)"
-        f8["quantize_frac_of_hbm"] = round(f8["quantize_gbs"] / peaks["hbm_gbs"], 4)
-        result["prefill_fp8"] = f8
-    if vl is not None:
-        vl["roofline"]["peak"] = peaks["bf16_tflops"]
-        vl["roofline"]["frac"] = round(vl["roofline"]["achieved"] / peaks["bf16_tflops"], 4)
-        vl["roofline"]["peak_source"] = peak_src + " bf16 burst"
-        result["prefill_varlen"] = vl
+    del caches
+    if args.no_extras:
+        return result
+    configs = {}
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
+    configs["3_llama_long_prefill"] = time_prefill_configs(
+        attn, dev, dist, peaks, [(30720, W.llama_long_prefill)],
+        extra={32768: (achieved, avg_pre)})
+    configs["2_qwen_prefill"] = time_prefill_configs(
+        attn, dev, dist, peaks, [(2048, W.qwen_prefill), (8192, W.qwen_prefill)])
+    configs["4_qwen_decode_30720"] = time_decode_sweep(args, attn, W, dev, dist, peaks, sweep,
+                                                       sweep_out, chain_two=dec_total / args.steps)
+    configs["5_paged_batch16"] = time_paged_batch(args, attn, W, dev, dist, peaks, sweep,
+                                                  sweep_out)
+    result["configs"] = configs
+
+    # ---- the next rows, on the Qwen2.5-7B layer at N = 8192 ----
+    xq = W.qwen_prefill(8192)
+    qq, kq, vq = xq.q.to(dev), xq.k.to(dev), xq.v.to(dev)
+    oq = torch.empty(tuple(xq.q.shape), dtype=torch.float32, device=dev)
+    lq = torch.empty(tuple(xq.q.shape[:3]), dtype=torch.float32, device=dev)
+    dec_caches = [(kc0, vc0)] + [(kc0.clone(), vc0.clone()) for _ in range(3)]
+    app = time_decode_append(args, attn, dq, dec_caches, dec, S, op, lp, sweep, sweep_out, dist,
+                             dev)
+    vl = time_prefill_varlen(args, attn, W, dist, dev)
+    f8 = time_fp8(args, attn, xq, qq, kq, vq, oq, lq, dist, dev)
+    d256 = time_d256(args, attn, W, dist, dev)
+    var = time_variants(args, attn, qq, kq, vq, xq.scale, oq, lq, dq, dec_caches, dec, S, op, lp,
+                        sweep, sweep_out, dist, dev)
+    bf = peaks["bf16_tflops"]
+    for v_ in var["prefill"].values():
+        v_["frac"] = round(v_["value"] / bf, 4)
+    var["decode"]["frac"] = round(var["decode"]["value"] / peaks["hbm_gbs"], 4)
+    result["variants"] = var
+    d256["roofline"]["peak"] = bf
+    d256["roofline"]["frac"] = round(d256["roofline"]["achieved"] / bf, 4)
+    d256["decode"]["roofline"]["peak"] = peaks["hbm_gbs"]
+    d256["decode"]["roofline"]["frac"] = round(
+        d256["decode"]["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
+    result["prefill_d256"] = d256
+    f8_peak = bf * 2.0   # nominal dense fp8 / bf16 ratio (4.5 / 2.25)
+    f8["roofline"]["peak"] = round(f8_peak, 1)
+    f8["roofline"]["frac"] = round(f8["roofline"]["achieved"] / f8_peak, 4)
+    f8["roofline"]["frac_of_bf16_peak"] = round(f8["roofline"]["achieved"] / bf, 4)
+    f8["roofline"]["peak_source"] = peak_src + " bf16 burst x 2 (nominal fp8 / bf16)"
+    f8["quantize_frac_of_hbm"] = round(f8["quantize_gbs"] / peaks["hbm_gbs"], 4)
+    result["prefill_fp8"] = f8
+    vl["roofline"]["peak"] = bf
+    vl["roofline"]["frac"] = round(vl["roofline"]["achieved"] / bf, 4)
+    vl["roofline"]["peak_source"] = peak_src + " bf16 burst"
+    result["prefill_varlen"] = vl
     if app is not None:
         app["roofline"]["peak"] = peaks["hbm_gbs"]
         app["roofline"]["frac"] = round(app["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
         app["roofline"]["peak_source"] = peak_src + " hbm copy"
         result["decode_append"] = app
+    del qq, kq, vq, oq, lq, dec_caches
+    torch.cuda.empty_cache()
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist)
+        result["e2e"] = run_e2e(args, x, dec, dev, world, dist)
     return result
+
+
+def decode_bytes(dec) -> int:
+    """Algorithmic bytes of one decode: the K and V rows attended, q, and the
+    final O and LSE (the split partials are overhead, not credited)."""
+    B, Hq, D = dec.q.shape
+    tokens = int(dec.kv_lens.sum())
+    return tokens * dec.n_kv * D * 2 * 2 + B * Hq * D * 2 + B * Hq * (D + 1) * 4
+
+
+def headline_config(world: int) -> dict:
+    P, Dc = HEADLINE["prefill"], HEADLINE["decode"]
+    return {"workload": HEADLINE["desc"], "batch": 1, "n_q_heads": P["n_q"],
+            "n_kv_heads": P["n_kv"], "seqlen": P["seqlen"], "head_dim": P["d"],
+            "prefill_layers_per_step": P["layers"], "spiked_keys": "1% of keys x8 per kv head",
+            "decode": {"n_q_heads": Dc["n_q"], "n_kv_heads": Dc["n_kv"], "head_dim": 128,
+                       "kv_len": Dc["kv_len"], "layers_per_step": Dc["layers"],
+                       "num_splits": "the library's policy (attn_decode_num_splits)",
+                       "cache": "contiguous, one per layer"},
+            "l2": "inputs larger than L2 (prefill Q+K+V 403 MB, each launch writes a 537 MB "
+                  "output; 28 decode caches of 63 MB); a read-only sweep of 2x L2 between "
+                  "the prefill chain and the decode chain",
+            "parallelism": f"replicas x{world}"}
+
+
+def _timed(fn, n, dist, dev, before=None):
+    """Sum over n launches of fn's CUDA-event time (max over ranks); `before`
+    runs outside the events (an L2 sweep), then the host is put ahead."""
+    import torch
+
+    for i in range(3):
+        fn(i)
+    evs = [(_ev(), _ev()) for _ in range(n)]
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    for i in range(n):
+        if before is not None:
+            before()
+        _host_ahead()
+        evs[i][0].record()
+        fn(i)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    (tot,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
+    return tot
+
+
+def time_prefill_configs(attn, dev, dist, peaks, cases, extra=None):
+    """Causal prefill TFLOP/s per (sequence length, input maker); each launch
+    writes a fresh output larger than L2 (two output buffers alternate)."""
+    import torch
+
+    out = {}
+    for N, make in cases:
+        x = make(N)
+        q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        o = [torch.empty(tuple(x.q.shape), dtype=torch.float32, device=dev) for _ in range(2)]
+        l = [torch.empty(tuple(x.q.shape[:3]), dtype=torch.float32, device=dev) for _ in range(2)]
+        Hq = x.q.shape[1]
+        fl = prefill_flops(Hq, N, x.q.shape[3])
+        n = 20 if N <= 8192 else 6
+        t = _timed(lambda i: attn.prefill(q, k, v, x.scale, True, out=o[i & 1], lse=l[i & 1]), n,
+                   dist, dev)
+        attn.check_device_status()
+        ach = fl / (t / n * 1e-3) / 1e12
+        out[f"N={N}"] = {"value": round(ach, 2), "unit": "TFLOP/s",
+                         "frac": round(ach / peaks["bf16_tflops"], 4),
+                         "frac_of_nominal": round(ach / NOMINAL["bf16_tflops"], 4),
+                         "peak": peaks["bf16_tflops"], "peak_source": "bf16 burst",
+                         "avg_launch_ms": round(t / n, 4), "flops_per_launch": fl,
+                         "heads": f"{Hq}/{x.k.shape[1]}", "launches": n}
+        del q, k, v, o, l
+    for N, (ach, ms) in (extra or {}).items():
+        out[f"N={N}"] = {"value": round(ach, 2), "unit": "TFLOP/s",
+                         "frac": round(ach / peaks["bf16_tflops_sustained"], 4),
+                         "frac_of_burst_peak": round(ach / peaks["bf16_tflops"], 4),
+                         "frac_of_nominal": round(ach / NOMINAL["bf16_tflops"], 4),
+                         "peak": peaks["bf16_tflops_sustained"],
+                         "peak_source": "bf16 sustained (the headline's timed region)",
+                         "avg_launch_ms": round(ms, 4), "heads": "32/8"}
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_decode_sweep(args, attn, W, dev, dist, peaks, sweep, sweep_out, chain_two):
+    """Single-token decode over the 30720-token Qwen2.5-7B-layer cache, for the
+    split counts {1, 16, 64, 148} and the policy's: the decode kernel alone and
+    decode + combine, each single (an L2 sweep before,
+    outside the events) and, for the policy's count, chained over four caches."""
+    import torch
+
+    dec = W.qwen_decode(30720)
+    dq, dlens = dec.q.to(dev), dec.kv_lens.to(dev)
+    kc0, vc0 = dec.k_cache.to(dev), dec.v_cache.to(dev)
+    caches = [(kc0, vc0)] + [(kc0.clone(), vc0.clone()) for _ in range(3)]
+    B, Hq, D = dq.shape
+    nbytes = decode_bytes(dec)
+    hbm = peaks["hbm_gbs"]
+    auto = attn.decode_num_splits(B, dec.n_kv, dec.max_kv_len)
+    n = 20
+    flush = lambda: torch.sum(sweep, dim=0, out=sweep_out)
+    res = {"bytes_per_launch": nbytes, "policy_splits": auto, "peak": hbm,
+           "peak_source": "measured hbm copy",
+           "timing": "CUDA events around each launch group; single = one launch after an L2 "
+                     "sweep with the host ahead; chain = back to back over distinct caches"}
+    for S in (1, 16, 64, 148, auto):
+        op = torch.empty((S, B, Hq, D), dtype=torch.float32, device=dev)
+        lp = torch.empty((S, B, Hq), dtype=torch.float32, device=dev)
+        o = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+        l = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+
+        def alone(i):
+            kc, vc = caches[i % 4]
+            attn.decode_splitkv(dq, kc, vc, dlens, None, num_splits=S, max_kv_len=30720,
+                                scale=dec.scale, o_partial=op, lse_partial=lp)
+
+        def two(i):
+            alone(i)
+            attn.combine(op, lp, out=o, lse=l)
+
+        entry = {}
+        for name, fn in (("decode", alone), ("decode+combine", two)):
+            t = _timed(fn, n, dist, dev, before=flush)
+            gbs = nbytes / (t / n * 1e-3) / 1e9
+            entry[name] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                           "us": round(t / n * 1e3, 2)}
+        attn.check_device_status()
+        res[f"S={S}" + (" (policy)" if S == auto else "")] = entry
+        if S == auto:
+            chain = {}
+            for name, fn in (("decode", alone), ("decode+combine", two)):
+                L = 28
+                t = _timed(lambda i: [fn(j) for j in range(L)], 5, dist, dev, before=flush)
+                gbs = nbytes * L / (t / 5 * 1e-3) / 1e9
+                chain[name] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                               "us_per_layer": round(t / 5 / L * 1e3, 2)}
+            attn.check_device_status()
+            step_gbs = nbytes * HEADLINE["decode"]["layers"] / (chain_two * 1e-3) / 1e9
+            chain["decode+combine (headline step, 28 distinct caches)"] = {
+                "GB/s": round(step_gbs, 1), "frac": round(step_gbs / hbm, 4)}
+            res["chain (4 caches in rotation, 28 layers)"] = chain
+    del caches
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_paged_batch(args, attn, W, dev, dist, peaks, sweep, sweep_out):
+    """Paged decode of 16 sequences (lengths uniform in [1024, 32768]), 32 / 8
+    heads, 16-token blocks, the policy's split count: decode alone and decode +
+    combine, single launches over two device copies of the cache
+    (2.4 GB, each launch reads HBM)."""
+    import torch
+
+    dec = W.llama_paged_decode()
+    dq, dlens, dbt = dec.q.to(dev), dec.kv_lens.to(dev), dec.block_table.to(dev)
+    caches = [(dec.k_cache.to(dev), dec.v_cache.to(dev))]
+    caches.append((caches[0][0].clone(), caches[0][1].clone()))
+    B, Hq, D = dq.shape
+    S = attn.decode_num_splits(B, dec.n_kv, dec.max_kv_len)
+    op = torch.empty((S, B, Hq, D), dtype=torch.float32, device=dev)
+    lp = torch.empty((S, B, Hq), dtype=torch.float32, device=dev)
+    o = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    l = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    nbytes = decode_bytes(dec)
+    hbm = peaks["hbm_gbs"]
+
+    def alone(i):
+        kc, vc = caches[i % 2]
+        attn.decode_splitkv(dq, kc, vc, dlens, dbt, num_splits=S, max_kv_len=dec.max_kv_len,
+                            scale=dec.scale, o_partial=op, lse_partial=lp)
+
+    def two(i):
+        alone(i)
+        attn.combine(op, lp, out=o, lse=l)
+
+    res = {"bytes_per_launch": nbytes, "num_splits": S, "tokens": int(dec.kv_lens.sum()),
+           "peak": hbm, "peak_source": "measured hbm copy"}
+    for name, fn in (("decode", alone), ("decode+combine", two)):
+        t = _timed(fn, 10, dist, dev)
+        gbs = nbytes / (t / 10 * 1e-3) / 1e9
+        res[name] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                     "us": round(t / 10 * 1e3, 2)}
+    attn.check_device_status()
+    del caches
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_variants(args, attn, q, k, v, scale, o, lse, dq, caches, dec, S, op, lp, sweep, sweep_out,
@@ -688,15 +897,17 @@ def time_decode_append(args, attn, dq, caches, dec, S, op, lp, sweep, sweep_out,
             "tokens_attended": tokens, "launches": n}
 
 
-def run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist):
+def run_e2e(args, x, dec, dev, world, dist):
     """Same metric through the public API with pinned host buffers: every step
     copies its inputs host->device and its results device->host.  Steps are
     pipelined as a serving loop runs them: three streams (input copies, the
     library's kernels, result copies) and two device buffer sets, so step
     i+1's inputs travel while step i computes and step i-1's results return.
     The timed region runs from before the first input copy to after the last
-    result copy, so every step's copies are inside it.  Prefill steps and
-    decode steps are timed as two separate loops."""
+    result copy, so every step's copies are inside it.  Prefill steps (one
+    Llama-3-8B layer at N = 32768 each) and decode steps (one Qwen2.5-7B layer
+    over its 30720-token cache, copied from the host each step) are timed as
+    two separate loops."""
     import torch
 
     import exact_io_aware_order_gb300 as attn
@@ -710,7 +921,7 @@ def run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist):
         in_done = [torch.cuda.Event() for _ in range(2)]
         c_done = [torch.cuda.Event() for _ in range(2)]
         out_done = [torch.cuda.Event() for _ in range(2)]
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0, t1 = _ev(), _ev()
         torch.cuda.synchronize()
         t0.record(s_in)
         for i in range(n):
@@ -738,6 +949,7 @@ def run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist):
         return t0.elapsed_time(t1)
 
     two = lambda t: (torch.empty_like(t, device=dev), torch.empty_like(t, device=dev))
+    flops = prefill_flops(x.q.shape[1], x.q.shape[2], x.q.shape[3])
     # ---- prefill ----
     hq, hk, hv = pin(x.q), pin(x.k), pin(x.v)
     ho = [torch.empty(tuple(x.q.shape), dtype=torch.float32).pin_memory() for _ in range(2)]
@@ -750,46 +962,51 @@ def run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist):
     p_out = [(o, ho), (lse, hl)]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho[0].numel() * 4 + hl[0].numel() * 4
+    n = max(3, min(args.steps, args.e2e_steps))
+    pipelined(2, p_in, p_out, pf)            # warm-up
+    if dist is not None:
+        dist.barrier()
+    pre = pipelined(n, p_in, p_out, pf)
+    attn.check_device_status()
+    # the results are the library's: the last step's output equals a direct call
+    ref_o, _ = attn.prefill(q[0], k[0], v[0], x.scale, True)
+    assert torch.equal(ho[(n - 1) & 1], ref_o.cpu()), "pipelined e2e result differs"
+    del q, k, v, o, lse, ref_o, hq, hk, hv, ho, hl
+    torch.cuda.empty_cache()
     # ---- decode ----
     hdq, hkc, hvc, hlen = pin(dec.q), pin(dec.k_cache), pin(dec.v_cache), pin(dec.kv_lens)
-    hbt = pin(dec.block_table) if dec.block_table is not None else None
     B, Hq, D = dec.q.shape
+    S = attn.decode_num_splits(B, dec.n_kv, dec.max_kv_len)
     hdo = [torch.empty((B, Hq, D), dtype=torch.float32).pin_memory() for _ in range(2)]
     hdl = [torch.empty((B, Hq), dtype=torch.float32).pin_memory() for _ in range(2)]
     dq, kc, vc, dlen = two(hdq), two(hkc), two(hvc), two(hlen)
-    dbt = two(hbt) if hbt is not None else (None, None)
     op = tuple(torch.empty((S, B, Hq, D), dtype=torch.float32, device=dev) for _ in range(2))
     lp = tuple(torch.empty((S, B, Hq), dtype=torch.float32, device=dev) for _ in range(2))
     do = tuple(torch.empty((B, Hq, D), dtype=torch.float32, device=dev) for _ in range(2))
     dlo = tuple(torch.empty((B, Hq), dtype=torch.float32, device=dev) for _ in range(2))
 
     def dc(b):
-        attn.decode_splitkv(dq[b], kc[b], vc[b], dlen[b], dbt[b], num_splits=S,
+        attn.decode_splitkv(dq[b], kc[b], vc[b], dlen[b], None, num_splits=S,
                             max_kv_len=dec.max_kv_len, scale=dec.scale, o_partial=op[b],
                             lse_partial=lp[b])
         attn.combine(op[b], lp[b], out=do[b], lse=dlo[b])
 
-    d_in = [(hdq, dq), (hkc, kc), (hvc, vc), (hlen, dlen)] + ([(hbt, dbt)] if hbt is not None else [])
+    d_in = [(hdq, dq), (hkc, kc), (hvc, vc), (hlen, dlen)]
     d_out = [(do, hdo), (dlo, hdl)]
     h2d_dec = sum(h.numel() * h.element_size() for h, _ in d_in)
     d2h_dec = hdo[0].numel() * 4 + hdl[0].numel() * 4
-
-    n = max(3, min(args.steps, args.e2e_steps))
-    pipelined(2, p_in, p_out, pf)            # warm-up
     pipelined(2, d_in, d_out, dc)
     if dist is not None:
         dist.barrier()
-    pre = pipelined(n, p_in, p_out, pf)
     dcd = pipelined(n, d_in, d_out, dc)
     attn.check_device_status()
-    # the results are the library's: the last step's output equals a direct call
-    ref_o, _ = attn.prefill(q[0], k[0], v[0], x.scale, True)
-    assert torch.equal(ho[(n - 1) & 1], ref_o.cpu()), "pipelined e2e result differs"
     pre, dcd = rank_max(dist, [pre, dcd], dev)
     return {"value": round(job_rate(flops, n, world, pre) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "what": "one Llama-3-8B-layer causal prefill at N = 32768 per step, Q/K/V copied "
+                    "in and O/LSE copied out every step",
             "pipelining": "3 streams (H2D / kernels / D2H), 2 buffer sets",
-            "decode_value": round(job_rate(dec_bytes, n, world, dcd) / 1e9, 1),
+            "decode_value": round(job_rate(decode_bytes(dec), n, world, dcd) / 1e9, 1),
             "decode_unit": "GB/s (end to end, cache copied from host each step)",
             "decode_h2d_bytes_per_step": h2d_dec, "decode_d2h_bytes_per_step": d2h_dec}
 
@@ -799,31 +1016,31 @@ def run_e2e(args, x, dec, S, dev, flops, dec_bytes, world, dist):
 # ---------------------------------------------------------------------------
 def _cpu_worker(spec: dict) -> dict:
     """Runs inside a fresh interpreter with BLAS threads pinned: times the
-    oracle on the requested sample and returns throughput figures."""
+    oracle on the requested sample of the headline workload and returns
+    throughput figures."""
     import numpy as np
 
     from exact_io_aware_order_gb300 import workloads as W
     import oracle
 
-    wl = WORKLOADS[spec["workload"]]
-    x = W.make_prefill(1, wl["n_q"], wl["n_kv"], wl["seqlen"], wl["d"], seed=0,
-                       spike_frac=wl["spike"])
-    g = wl["n_q"] // wl["n_kv"]
+    P = HEADLINE["prefill"]
+    x = W.llama_long_prefill(P["seqlen"])
     out = {}
     if spec["kind"] == "heads":
         h = spec["heads"]
+        g = P["n_q"] // P["n_kv"]
         nkv = -(-h // g)
         t0 = time.perf_counter()
         oracle.prefill(x.q[:, :h], x.k[:, :nkv], x.v[:, :nkv], x.scale, True)
         dt = time.perf_counter() - t0
-        fl = prefill_flops(h, wl["seqlen"], wl["d"])
+        fl = prefill_flops(h, P["seqlen"], P["d"])
         out["prefill_tflops"] = fl / dt / 1e12
         out["prefill_s"] = dt
-        out["sample"] = f"all {wl['seqlen']} rows of {h} of {wl['n_q']} query heads"
+        out["sample"] = f"all {P['seqlen']} rows of {h} of {P['n_q']} query heads"
     else:  # per-step sampled rows, repeated
-        N = wl["seqlen"]
+        N = P["seqlen"]
         rows = [(0, 0, int(i)) for i in np.linspace(0, N - 1, spec["rows"]).round()]
-        fl = sum(4.0 * (i + 1) * wl["d"] for _, _, i in rows)
+        fl = sum(4.0 * (i + 1) * P["d"] for _, _, i in rows)
         times = []
         for _ in range(spec["repeats"]):
             t0 = time.perf_counter()
@@ -834,16 +1051,12 @@ def _cpu_worker(spec: dict) -> dict:
         out["step_times"] = times
         out["sample"] = f"{spec['rows']} evenly spaced rows of query head 0 per step"
     if spec.get("decode", True):
-        dec = W.qwen_decode(30720) if wl["decode"] == "qwen30720" else W.llama_paged_decode()
-        nb = spec.get("decode_seqs", dec.q.shape[0])
-        lens = dec.kv_lens.tolist()[:nb]
+        dec = W.qwen_decode(HEADLINE["decode"]["kv_len"])
+        lens = dec.kv_lens.tolist()
         t0 = time.perf_counter()
-        oracle.decode(dec.q[:nb], dec.k_cache, dec.v_cache,
-                      dec.block_table[:nb] if dec.block_table is not None else None,
-                      lens, dec.scale, dec.block_size)
+        oracle.decode(dec.q, dec.k_cache, dec.v_cache, None, lens, dec.scale)
         dt = time.perf_counter() - t0
-        byts = sum(lens) * dec.n_kv * dec.q.shape[2] * 4
-        out["decode_gbs"] = byts / dt / 1e9
+        out["decode_gbs"] = decode_bytes(dec) / dt / 1e9
         out["decode_s"] = dt
     return out
 
@@ -865,23 +1078,21 @@ def run_reference(args, rank: int, world: int):
     """Times the float64 oracle on the host cores, a bounded sample per step."""
     if rank != 0:
         return None
-    wl = WORKLOADS[args.workload]
-    rows = 32 if args.workload == "qwen" else 8
-    spec = {"workload": args.workload, "kind": "rows", "rows": rows,
-            "repeats": args.warmup + args.steps, "decode": False}
-    r = run_cpu(spec)
-    times = r["step_times"][args.warmup:]
     import numpy as np
 
-    fl = sum(4.0 * (i + 1) * wl["d"] for i in np.linspace(0, wl["seqlen"] - 1, rows).round())
+    P = HEADLINE["prefill"]
+    rows = 32
+    spec = {"kind": "rows", "rows": rows, "repeats": args.warmup + args.steps, "decode": False}
+    r = run_cpu(spec)
+    times = r["step_times"][args.warmup:]
+    fl = sum(4.0 * (i + 1) * P["d"] for i in np.linspace(0, P["seqlen"] - 1, rows).round())
     value = fl * len(times) / sum(times) / 1e12
     return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": wl["desc"], "batch": 1, "n_q_heads": wl["n_q"],
-                       "n_kv_heads": wl["n_kv"], "seqlen": wl["seqlen"], "head_dim": wl["d"]},
+            "config": headline_config(world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"],
                              "kind": "oracle", "sample": r["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -892,14 +1103,19 @@ def run_reference(args, rank: int, world: int):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen")
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-heads", type=int, default=8,
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only the timed headline steps (for profiling runs)")
+    ap.add_argument("--seqlen", type=int, default=HEADLINE["prefill"]["seqlen"],
+                    help="prefill length of the timed step (profiling runs use a smaller one)")
+    ap.add_argument("--layers", type=int, default=HEADLINE["prefill"]["layers"],
+                    help="prefill launches per timed step")
+    ap.add_argument("--cpu-heads", type=int, default=2,
                     help="query heads in the cpu_baseline sample (whole rows, N tokens)")
     ap.add_argument("--cpu-worker", type=str, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
@@ -910,6 +1126,11 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
+    HEADLINE["prefill"]["seqlen"] = args.seqlen
+    HEADLINE["prefill"]["layers"] = args.layers
+    if (args.seqlen, args.layers) != (32768, 32):
+        HEADLINE["desc"] = (f"profiling case: Llama-3-8B attention, causal prefill N={args.seqlen} "
+                            f"x {args.layers} layers + the decode chain of the headline")
     rank, world = rank_env()
     if args.impl == "reference":
         res = run_reference(args, rank, world)
@@ -921,7 +1142,7 @@ def main():
     # interpreter either way), on rank 0 at N = 1 only.
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        spec = {"workload": args.workload, "kind": "heads", "heads": args.cpu_heads}
+        spec = {"kind": "heads", "heads": args.cpu_heads}
         r = run_cpu(spec)
         cpu = {"value": round(r["prefill_tflops"], 6), "unit": "TFLOP/s", "cores": r["cores"],
                "kind": "oracle", "sample": r["sample"] + "; float64 numpy, BLAS threads = cores",

@@ -40,7 +40,7 @@ def _rank_main(rank, world, port, q):
         mx = b.rank_max(dist, [1.0 + rank, 10.0 - rank, 5.0 * (rank + 1)])
         rate = b.job_rate(100.0, 4, w, mx[0])
         # the reference arm: only rank 0 works, the others return at once
-        args = argparse.Namespace(workload="qwen", warmup=3, steps=1)
+        args = argparse.Namespace(warmup=3, steps=1)
         ref = b.run_reference(args, r, w) if r != 0 else "skipped"
         dist.barrier()
         q.put((rank, r, w, mx, rate, ref))
