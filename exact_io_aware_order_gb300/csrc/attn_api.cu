@@ -132,7 +132,7 @@ int validate_decode(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_
     return ATTN_ERR_SHAPE;
   if (!paged && max_kv_len < 1) return ATTN_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
-  if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 16) return ATTN_ERR_GQA;
+  if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 64) return ATTN_ERR_GQA;
   if (num_splits < 0 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(o_partial, 16) || !aligned(lse_partial, 4) || !aligned(kv_lens, 4) ||
@@ -150,7 +150,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_NULL: return "ATTN_ERR_NULL: a required pointer is NULL";
     case ATTN_ERR_SHAPE: return "ATTN_ERR_SHAPE: a size or the scale is out of range";
     case ATTN_ERR_HEADDIM: return "ATTN_ERR_HEADDIM: head_dim not supported by this call (see its limits)";
-    case ATTN_ERR_GQA: return "ATTN_ERR_GQA: n_q_heads must be a multiple of n_kv_heads (decode: ratio <= 16)";
+    case ATTN_ERR_GQA: return "ATTN_ERR_GQA: n_q_heads must be a multiple of n_kv_heads (decode: ratio <= 64)";
     case ATTN_ERR_SPLITS: return "ATTN_ERR_SPLITS: num_splits out of range";
     case ATTN_ERR_ALIGN: return "ATTN_ERR_ALIGN: a pointer is misaligned";
     case ATTN_ERR_ARCH: return "ATTN_ERR_ARCH: the current device is not sm_103 (GB300)";

@@ -43,6 +43,7 @@ namespace {
 constexpr int kStageTokens = 64;   // tokens per ring stage
 constexpr int kStages = ATTN_DECODE_STAGES;
 constexpr int kConsumerWarps = 4;  // 16 tokens each per stage
+constexpr int kMaxRowGroups = 4;   // query rows per kv head: up to 4 groups of 16
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -59,10 +60,12 @@ struct DecodeSmem {
   static constexpr int kStageBytes = 2 * kTileBytes;           // K then V
   static constexpr int kQRowBytes = D * 2 + 16;                // padded q rows
   static constexpr int kRing = 0;
-  static constexpr int kQOff = kStages * kStageBytes;
-  static constexpr int kBarOff = kQOff + 16 * kQRowBytes;      // 2*kStages barriers
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kBarOff = kRingBytes;                   // 2*kStages barriers
   static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;
-  static constexpr int kTotal = kMiscOff + 16 + 1024;          // + alignment slack
+  static constexpr int kQOff = kMiscOff + 16;                  // 16 q rows per row group
+  // Dynamic shared memory for `groups` row groups of 16 query rows.
+  static constexpr int total(int groups) { return kQOff + groups * 16 * kQRowBytes + 1024; }
   // Merge scratch reuses the ring once the stream is done: per warp 16 rows of
   // D floats at a padded pitch (64-bit stores from a quad land in distinct
   // bank pairs), then per warp and row m and l, then per row the warps' weights.
@@ -71,7 +74,7 @@ struct DecodeSmem {
   static constexpr int kMergeM = kConsumerWarps * 16 * kMergePitch * 4;  // [warps][16]
   static constexpr int kMergeL = kMergeM + kConsumerWarps * 16 * 4;      // [warps][16]
   static constexpr int kMergeF = kMergeL + kConsumerWarps * 16 * 4;      // [warps][16]
-  static_assert(kMergeF + kConsumerWarps * 16 * 4 <= kQOff, "merge scratch fits in the ring");
+  static_assert(kMergeF + kConsumerWarps * 16 * 4 <= kRingBytes, "merge scratch fits in the ring");
 };
 
 // Byte offset of (row, 16-byte chunk c) inside one 128-byte-swizzled span.
@@ -307,10 +310,18 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
     // ================= consumers =================
     const int cw = warp - 1;
     const int ctid = threadIdx.x - 32;
+    // Row groups: the g query rows in groups of 16 (G = 1, 2 or 4).  The
+    // four warps split into G teams, one per group; a team's warps share the
+    // stage's four 16-token sub-blocks, so every K/V row is still read from
+    // memory once and used for all g rows.
+    const int G = g <= 16 ? 1 : (g <= 32 ? 2 : 4);
+    const int team = 4 / G;              // warps per row group
+    const int rg = cw / team;            // this warp's row group
+    const int rg_row0 = rg * 16;         // its first query row
     uint8_t* sq = smem + L::kQOff;
-    // q rows of this kv head's g query heads; rows g..15 are zero.
+    // q rows of this kv head's g query heads; rows g .. 16 G - 1 are zero.
     const uint16_t* qsrc = a.q + ((size_t)b * a.n_q_heads + (size_t)kvh * g) * D;
-    for (int i = ctid; i < 16 * (D / 8); i += 32 * kConsumerWarps) {
+    for (int i = ctid; i < 16 * G * (D / 8); i += 32 * kConsumerWarps) {
       const int r = i / (D / 8), c = i % (D / 8);
       uint4 val = make_uint4(0, 0, 0, 0);
       if (r < g) val = *reinterpret_cast<const uint4*>(qsrc + (size_t)r * D + c * 8);
@@ -321,7 +332,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint32_t qa[D / 16][4];
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const int r = (lane & 15);
+      const int r = rg_row0 + (lane & 15);
       const int c = kk * 16 + (lane >> 4) * 8;
       ldsm_x4(smem_u32(sq + r * L::kQRowBytes + c * 2), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
     }
@@ -338,7 +349,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
     if (alibi) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const int row = (lane >> 2) + 8 * r;
+        const int row = rg_row0 + (lane >> 2) + 8 * r;
         if (row < g) al2[r] = a.alibi_slopes[kvh * g + row] * kLog2e;
       }
     }
@@ -355,11 +366,15 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (!mbar_wait_warp(full0 + 8 * st, (it / kStages) & 1, ctl)) break;
       const int base = t0 + it * kStageTokens;
       const int cnt = min(kStageTokens, t1 - base);
-      const int vc = min(16, cnt - cw * 16);  // valid tokens of this warp's 16
+      // This warp's 16-token sub-blocks of the stage: one with a single row
+      // group, two or four when its team shares the stage.
+#pragma unroll 1
+      for (int sb = cw % team; sb < 4; sb += team) {
+      const int vc = min(16, cnt - sb * 16);  // valid tokens of this sub-block
       if (vc > 0) {
         uint8_t* sk = smem + L::kRing + st * L::kStageBytes;
         uint8_t* sv = sk + L::kTileBytes;
-        const int r0 = cw * 16;  // this warp's first row in the stage
+        const int r0 = sb * 16;  // the sub-block's first row in the stage
         if (vc < 16) {  // rows past the end: zero V so 0 * (old data) stays 0
           for (int i = lane; i < (16 - vc) * (D / 8); i += 32) {
             const int r = r0 + vc + i / (D / 8), c = i % (D / 8);
@@ -474,6 +489,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         if (vc < 16) fence_proxy_async_smem();  // generic writes above precede the next copy
       }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * st);
     }
@@ -500,33 +516,33 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
           make_float2(acc[j][2], acc[j][3]);
     }
     consumer_sync();
-    // Per row: the common max, each warp's weight e^(m_w - m) / l, and the LSE.
+    // Per row: the common max over its team's warps, each warp's weight
+    // e^(m_w - m) / l, and the LSE.  Row r belongs to row group r / 16, whose
+    // team is warps (r / 16) * team .. + team - 1, at local row r % 16.
     if (ctid < g && !*abort_flag) {
-      const int r = ctid;
+      const int r = ctid, lr = r & 15, w0 = (r >> 4) * team;
       float m = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, mm[w * 16 + r]);
-      float f[kConsumerWarps], lsum = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        f[w] = ex2_approx(mm[w * 16 + r] - m);  // 0 for a warp that saw no token
-        lsum += f[w] * ml[w * 16 + r];
+      for (int w = w0; w < w0 + team; ++w) m = fmaxf(m, mm[w * 16 + lr]);
+      float lsum = 0.f;
+      for (int w = w0; w < w0 + team; ++w) {
+        const float f = ex2_approx(mm[w * 16 + lr] - m);  // 0 for a warp that saw no token
+        lsum += f * ml[w * 16 + lr];
+        mf[w * 16 + lr] = f;
       }
       const float inv = 1.f / lsum;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) mf[w * 16 + r] = f[w] * inv;
+      for (int w = w0; w < w0 + team; ++w) mf[w * 16 + lr] *= inv;
       lse_out[r] = (m + __log2f(lsum)) * kLn2;
     }
     consumer_sync();
     if (!*abort_flag) {
       for (int e = ctid; e < g * (D / 4); e += 32 * kConsumerWarps) {
         const int r = e / (D / 4), c = (e % (D / 4)) * 4;
+        const int lr = r & 15, w0 = (r >> 4) * team;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float fw = mf[w * 16 + r];
+        for (int w = w0; w < w0 + team; ++w) {
+          const float fw = mf[w * 16 + lr];
           const float4 v = *reinterpret_cast<const float4*>(
-              &mo[((size_t)w * 16 + r) * L::kMergePitch + c]);
+              &mo[((size_t)w * 16 + lr) * L::kMergePitch + c]);
           o.x = fmaf(fw, v.x, o.x);
           o.y = fmaf(fw, v.y, o.y);
           o.z = fmaf(fw, v.z, o.z);
@@ -712,10 +728,13 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const LaunchCtx& ctx) {
   cudaGetDevice(&dev);
   if (dev >= 64 || !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::total(kMaxRowGroups));
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
+  const int gq = a.n_q_heads / a.n_kv_heads;  // at most 64 (validated)
+  const int groups = gq <= 16 ? 1 : (gq <= 32 ? 2 : 4);
   DecodeKParams kp;
   kp.a = a;
   kp.err_word = ctx.err_word;
@@ -739,7 +758,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const LaunchCtx& ctx) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_splits, a.n_kv_heads, a.batch);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = L::kTotal;
+  cfg.dynamicSmemBytes = L::total(groups);
   cfg.stream = ctx.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -122,6 +122,7 @@ struct PrefillParams {
   const float* alibi_slopes;  // ALiBi: per query head slope (natural-log units)
   int n_q_tiles;    // ceil(seqlen / 128)
   int total_tiles;  // n_q_tiles * batch * n_q_heads (padded mode)
+  int group_planes; // plain padded mode: query planes per kv-head group of the work list
   const int32_t* cu_seqlens;  // packed mode: (num_seqs + 1) row offsets
   int num_seqs;
   // FP8: dequantisation scales of the e4m3 inputs, per 128-row block of Q and
@@ -170,9 +171,29 @@ template <bool VARLEN, int VARIANT, int kBN>
 __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const SeqTables& st) {
   Tile t;
   if constexpr (!VARLEN) {
-    const int BH = p.batch * p.n_q_heads;
-    const int qt = p.n_q_tiles - 1 - w / BH;
-    const int bh = w % BH;
+    int qt, bh;
+    if constexpr (VARIANT == kPlain) {
+      // The list runs over groups of group_planes consecutive query planes
+      // (whole kv heads), each group's items longest first with heads
+      // fastest, and every other group in the opposite direction so that
+      // lengths do not jump at group boundaries (the snake order below then
+      // still balances).  With one group (the whole batch) this is the plain
+      // longest-first order; several groups keep only a few kv heads' K/V in
+      // use at a time, so that they stay in L2 when all of them would not
+      // fit.  (Only this flavour: the others run close to their register
+      // limit, and the extra index arithmetic measured slower there.)
+      const int P = p.batch * p.n_q_heads;
+      const int grp = w / (p.n_q_tiles * p.group_planes);
+      const int local = w - grp * p.n_q_tiles * p.group_planes;
+      const int gh = min(p.group_planes, P - grp * p.group_planes);
+      const int rank = local / gh;
+      qt = (grp & 1) ? rank : p.n_q_tiles - 1 - rank;
+      bh = grp * p.group_planes + local % gh;
+    } else {
+      const int BH = p.batch * p.n_q_heads;
+      qt = p.n_q_tiles - 1 - w / BH;
+      bh = w % BH;
+    }
     const int bidx = bh / p.n_q_heads, h = bh % p.n_q_heads;
     const int kvh = h / (p.n_q_heads / p.n_kv_heads);
     t.row0 = t.qrel = qt * kBM;
@@ -386,10 +407,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       int nq = 0, nk = 0, nv = 0;  // tiles issued
       // `row`: first row of the tile in the tensor; a transposed tile (FP8
       // V, (plane, d, rows)) takes its rows along the innermost dimension.
+      // L2 policy: Q is read once (evict first); K and V tiles are read again
+      // by the other query tiles of their kv head (evict last).
+      const uint64_t pol_once = l2_policy_evict_first(), pol_keep = l2_policy_evict_last();
       auto load_tile = [&](const CUtensorMap* map, int base, int full, int empty, int R, int cnt,
                            int row, int z, bool transposed) -> bool {
         const int slot = cnt % R;
         const bool is_q = base == L::kQ;
+        const uint64_t pol = is_q ? pol_once : pol_keep;
         const int tile_bytes = is_q ? L::kQTileBytes : L::kTileBytes;
         const int chunk_bytes = is_q ? L::kQChunkBytes : L::kChunkBytes;
         if (cnt >= R && !mbar_wait(bar(empty + slot), ((cnt / R) - 1) & 1, ctl)) return false;
@@ -397,9 +422,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int c = 0; c < L::kChunks; ++c) {
           const uint32_t dst = smem_u32(smem + base + slot * tile_bytes + c * chunk_bytes);
           if (transposed)
-            tma_load_3d(dst, map, bar(full + slot), row, c * 128, z);
+            tma_load_3d_hint(dst, map, bar(full + slot), row, c * 128, z, pol);
           else
-            tma_load_3d(dst, map, bar(full + slot), c * (128 / (FP8 ? 1 : 2)), row, z);
+            tma_load_3d_hint(dst, map, bar(full + slot), c * (128 / (FP8 ? 1 : 2)), row, z, pol);
         }
         return true;
       };
@@ -753,6 +778,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int row = quarter * 32 + lane;
     const uint32_t tOm = tO + ((uint32_t)(quarter * 32) << 16);
     const uint32_t stage = smem_u32(smem + L::kStage + quarter * 4096);
+    const uint64_t pol_out = l2_policy_evict_first();  // O is not read again here
     bool ok = true;
     for (int r = 0; ok; ++r) {
       const int w = item_of(r, total);
@@ -784,7 +810,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && row0 < N) {  // rows past the tensor's end are clipped by the copy
-              tma_store_3d(&tm_o, stage, col0 + c * 32, row0, t.zq);
+              tma_store_3d_hint(&tm_o, stage, col0 + c * 32, row0, t.zq, pol_out);
               bulk_commit_group();
             }
           }
@@ -955,6 +981,18 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   pp.v_scales = a.v_scales;
   pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM;
   pp.total_tiles = pp.n_q_tiles * a.batch * a.n_q_heads;
+  pp.group_planes = a.batch * a.n_q_heads;  // one group: longest first over everything
+  {
+    // When the launch's K and V exceed 96 MB (L2 holds about 126 MB, and Q
+    // and O stream through it too), group whole kv heads so that each group's
+    // K and V take about 24 MB.
+    const long long kv_plane = 2LL * a.seqlen * D * (FP8 ? 1 : 2);
+    const long long kv_total = kv_plane * a.batch * a.n_kv_heads;
+    if (VARIANT == kPlain && !VARLEN && kv_total > (96LL << 20)) {
+      const int kvg = (int)std::max(1LL, (24LL << 20) / kv_plane);
+      pp.group_planes = std::min(kvg * (a.n_q_heads / a.n_kv_heads), a.batch * a.n_q_heads);
+    }
+  }
   pp.cu_seqlens = a.cu_seqlens;
   pp.num_seqs = a.num_seqs;
   pp.err_word = ctx.err_word;

@@ -51,7 +51,7 @@ typedef enum attn_status {
   ATTN_ERR_NULL = 1,     /* a required pointer is NULL                          */
   ATTN_ERR_SHAPE = 2,    /* a size is out of range (batch, heads, seqlen, ...)   */
   ATTN_ERR_HEADDIM = 3,  /* head_dim not supported by the call (see its limits) */
-  ATTN_ERR_GQA = 4,      /* n_q_heads not a multiple of n_kv_heads, or g > 16 in decode */
+  ATTN_ERR_GQA = 4,      /* n_q_heads not a multiple of n_kv_heads, or g > 64 in decode */
   ATTN_ERR_SPLITS = 5,   /* num_splits < 0 or above the supported maximum        */
   ATTN_ERR_ALIGN = 6,    /* a pointer is not aligned as documented               */
   ATTN_ERR_ARCH = 7,     /* the current device is not sm_103 (GB300)             */
@@ -181,7 +181,7 @@ int attn_decode_num_splits(int batch, int n_kv_heads, int max_kv_len, int num_sm
  * Split rule: with c = roundup(ceil(kv_len / S), 16), split s of a sequence
  * covers tokens [s*c, min((s+1)*c, kv_len)); an empty split writes o = 0 and
  * lse = -inf.  Each split's (o, lse) is attention restricted to its tokens.
- * Limits: head_dim in {64, 128, 256}; n_q_heads / n_kv_heads <= 16.
+ * Limits: head_dim in {64, 128, 256}; n_q_heads / n_kv_heads <= 64.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _SPLITS, _ALIGN, _ARCH, _LAUNCH.
  */
 int attn_decode_splitkv(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,

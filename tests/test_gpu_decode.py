@@ -190,3 +190,34 @@ def test_bounded_wait_gives_up_and_reports(dev):
     d = W.make_decode_contiguous(1, 4, 2, 128, 300, seed=3)
     op, lp, o, lse = run_decode(d, dev, 2)
     check_all(d, op, lp, o, lse, 2, "after timeout test")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,lens,S,bs", [
+    (32, 1, 128, [3000], 8, 16),          # g = 32 (multi-query-like)
+    (64, 1, 128, [2500, 17], 5, 16),      # g = 64
+    (40, 2, 64, [1000, 0, 33], 3, 16),    # g = 20: a partly filled second row group
+    (96, 2, 256, [1500], 4, 16),          # g = 48, head_dim 256
+    (64, 2, 128, [700, 1], 7, 7),         # g = 32, odd block size (plain loads)
+])
+def test_large_gqa_ratio_paged(dev, Hq, Hkv, D, lens, S, bs):
+    """Query heads per kv head above 16: the warps split into row groups of 16
+    rows; every K/V row is still read once (page "FlashAttention for
+    inference", section "Decode: a different bottleneck", GQA paragraph)."""
+    d = W.make_decode_paged(len(lens), Hq, Hkv, D, lens, block_size=bs, seed=Hq + D + S,
+                            extra_blocks=2)
+    op, lp, o, lse = run_decode(d, dev, S)
+    check_all(d, op, lp, o, lse, S, f"paged g={Hq // Hkv} D={D} lens={lens}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,kv_len,S", [(64, 1, 30720, 76), (32, 1, 5000, 19), (48, 1, 777, 3)])
+def test_large_gqa_ratio_contiguous(dev, Hq, Hkv, kv_len, S):
+    d = W.make_decode_contiguous(1, Hq, Hkv, 128, kv_len, seed=kv_len + Hq)
+    op, lp, o, lse = run_decode(d, dev, S)
+    check_all(d, op, lp, o, lse, S, f"contig g={Hq // Hkv} len={kv_len}")
+
+
+def test_gqa_ratio_above_64_is_refused(dev):
+    d = W.make_decode_contiguous(1, 65, 1, 64, 32, seed=1)
+    with pytest.raises(AttnError) as e:
+        run_decode(d, dev, 1)
+    assert e.value.status == status_codes()["ATTN_ERR_GQA"]

@@ -85,6 +85,7 @@ def paged_with_room(B, Hq, Hkv, D, lens, bs, seed):
     ([4095], 7, 64, 128, 28, 4),
     ([0, 31, 2000], 4, 16, 256, 16, 8),         # head_dim 256
     ([40, 0], 3, 7, 256, 4, 2),                 # head_dim 256, plain loads
+    ([0, 33, 1500], 4, 16, 128, 64, 1),         # g = 64: four row groups
 ])
 def test_paged_append(dev, lens, S, bs, D, Hq, Hkv):
     d = paged_with_room(len(lens), Hq, Hkv, D, lens, bs, seed=sum(lens) + S)
@@ -174,6 +175,8 @@ def _alibi(n_heads):
     (True, [77, 1500], 5, 7, 128, 8, 2, 64, 50.0, False),          # window + cap, plain loads
     (False, [2048], 33, 0, 128, 8, 2, -1, 0.0, True),              # ALiBi
     (True, [0, 700], 4, 16, 256, 16, 8, 255, 0.0, False),          # head_dim 256 with a window
+    (True, [10, 900], 3, 16, 128, 32, 1, -1, 0.0, True),           # ALiBi, g = 32
+    (False, [1200], 5, 0, 64, 96, 2, 300, 20.0, False),            # window + cap, g = 48
 ])
 def test_append_with_variants(dev, paged, lens, S, bs, D, Hq, Hkv, Wl, cap, alibi):
     """Decode with append and a sliding window, soft-capping or ALiBi

@@ -200,11 +200,25 @@ def test_decode_alibi(dev, paged, lens, S, Wl):
 ])
 def test_decode_variants_other_head_dims(dev, D, paged, lens, S, Wl, cap, alibi):
     """Decode variants at head_dim 64 and 256 (the combined result)."""
+    _decode_variant_case(dev, D, paged, lens, S, Wl, cap, alibi, 8, 4 if paged else 2)
+
+
+@pytest.mark.parametrize("D,paged,lens,S,Wl,cap,alibi,Hq,Hkv", [
+    (128, True, [1700, 40], 6, -1, 0.0, True, 64, 2),      # ALiBi, g = 32
+    (128, False, [3000], 7, 500, 40.0, False, 64, 1),      # window + cap, g = 64
+    (256, True, [900, 2100], 3, 100, 0.0, False, 48, 1),   # window, g = 48, head_dim 256
+])
+def test_decode_variants_large_gqa(dev, D, paged, lens, S, Wl, cap, alibi, Hq, Hkv):
+    """Decode variants with more than 16 query heads per kv head."""
+    _decode_variant_case(dev, D, paged, lens, S, Wl, cap, alibi, Hq, Hkv)
+
+
+def _decode_variant_case(dev, D, paged, lens, S, Wl, cap, alibi, Hq, Hkv):
     if paged:
-        d = W.make_decode_paged(len(lens), 8, 4, D, lens, block_size=16, seed=sum(lens) + D)
+        d = W.make_decode_paged(len(lens), Hq, Hkv, D, lens, block_size=16, seed=sum(lens) + D)
     else:
-        d = W.make_decode_contiguous(len(lens), 8, 2, D, lens[0], seed=lens[0] + D)
-    sl = alibi_slopes(8) if alibi else None
+        d = W.make_decode_contiguous(len(lens), Hq, Hkv, D, lens[0], seed=lens[0] + D)
+    sl = alibi_slopes(Hq) if alibi else None
     q, kc, vc, ln = d.q.to(dev), d.k_cache.to(dev), d.v_cache.to(dev), d.kv_lens.to(dev)
     bt = d.block_table.to(dev) if d.block_table is not None else None
     o, lse = attn.decode(q, kc, vc, ln, bt, num_splits=S, max_kv_len=d.max_kv_len or None,

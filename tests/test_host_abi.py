@@ -148,7 +148,7 @@ def test_decode_validation(L):
     assert _decode(L, d=80) == c["ATTN_ERR_HEADDIM"]
     assert _decode(L, d=512) == c["ATTN_ERR_HEADDIM"]
     assert _decode(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
-    assert _decode(L, hq=34, hkv=2) == c["ATTN_ERR_GQA"]       # g = 17 > 16
+    assert _decode(L, hq=130, hkv=2) == c["ATTN_ERR_GQA"]      # g = 65 > 64
     assert _decode(L, S=-1) == c["ATTN_ERR_SPLITS"]
     assert _decode(L, S=_lib.ATTN_MAX_SPLITS + 1) == c["ATTN_ERR_SPLITS"]
     assert _decode(L, k=P + 8) == c["ATTN_ERR_ALIGN"]
