@@ -316,16 +316,19 @@ def run_gb300(args, rank: int, world: int, dist):
     configs = {}
     del q, k, v, o, lse
     torch.cuda.empty_cache()
-    configs["3_llama_long_prefill"] = time_prefill_configs(
-        attn, dev, dist, peaks, [(30720, W.llama_long_prefill)],
-        extra={32768: (achieved, avg_pre)})
-    configs["2_qwen_prefill"] = time_prefill_configs(
-        attn, dev, dist, peaks, [(2048, W.qwen_prefill), (8192, W.qwen_prefill)])
-    configs["4_qwen_decode_30720"] = time_decode_sweep(args, attn, W, dev, dist, peaks, sweep,
-                                                       sweep_out, chain_two=dec_total / args.steps)
-    configs["5_paged_batch16"] = time_paged_batch(args, attn, W, dev, dist, peaks, sweep,
-                                                  sweep_out)
-    result["configs"] = configs
+    legs = set(("configs,append,varlen,fp8,d256,variants" if args.legs == "all" else args.legs)
+               .split(","))
+    if "configs" in legs:
+        configs["3_llama_long_prefill"] = time_prefill_configs(
+            attn, dev, dist, peaks, [(30720, W.llama_long_prefill)],
+            extra={32768: (achieved, avg_pre)})
+        configs["2_qwen_prefill"] = time_prefill_configs(
+            attn, dev, dist, peaks, [(2048, W.qwen_prefill), (8192, W.qwen_prefill)])
+        configs["4_qwen_decode_30720"] = time_decode_sweep(
+            args, attn, W, dev, dist, peaks, sweep, sweep_out, chain_two=dec_total / args.steps)
+        configs["5_paged_batch16"] = time_paged_batch(args, attn, W, dev, dist, peaks, sweep,
+                                                      sweep_out)
+        result["configs"] = configs
 
     # ---- the next rows, on the Qwen2.5-7B layer at N = 8192 ----
     xq = W.qwen_prefill(8192)
@@ -333,47 +336,53 @@ def run_gb300(args, rank: int, world: int, dist):
     oq = torch.empty(tuple(xq.q.shape), dtype=torch.float32, device=dev)
     lq = torch.empty(tuple(xq.q.shape[:3]), dtype=torch.float32, device=dev)
     dec_caches = [(kc0, vc0)] + [(kc0.clone(), vc0.clone()) for _ in range(3)]
-    app = time_decode_append(args, attn, dq, dec_caches, dec, S, op, lp, sweep, sweep_out, dist,
-                             dev)
-    vl = time_prefill_varlen(args, attn, W, dist, dev)
-    f8 = time_fp8(args, attn, xq, qq, kq, vq, oq, lq, dist, dev)
-    d256 = time_d256(args, attn, W, dist, dev)
-    var = time_variants(args, attn, qq, kq, vq, xq.scale, oq, lq, dq, dec_caches, dec, S, op, lp,
-                        sweep, sweep_out, dist, dev)
     bf = peaks["bf16_tflops"]
-    for v_ in var["prefill"].values():
-        v_["frac"] = round(v_["value"] / bf, 4)
-    var["decode"]["frac"] = round(var["decode"]["value"] / peaks["hbm_gbs"], 4)
-    result["variants"] = var
-    d256["roofline"]["peak"] = bf
-    d256["roofline"]["frac"] = round(d256["roofline"]["achieved"] / bf, 4)
-    d256["decode"]["roofline"]["peak"] = peaks["hbm_gbs"]
-    d256["decode"]["roofline"]["frac"] = round(
-        d256["decode"]["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
-    result["prefill_d256"] = d256
-    f8_meas = measure_fp8_gemm_peak(dev)
-    if f8_meas is not None:
-        f8_peak, f8_src = f8_meas, "measured e4m3 GEMM (torch._scaled_mm, 8192^3, best of 10)"
-    else:
-        f8_peak = bf * 2.0   # nominal dense fp8 / bf16 ratio (4.5 / 2.25)
-        f8_src = peak_src + " bf16 burst x 2 (nominal fp8 / bf16)"
-    f8["roofline"]["peak"] = round(f8_peak, 1)
-    f8["roofline"]["frac"] = round(f8["roofline"]["achieved"] / f8_peak, 4)
-    f8["roofline"]["frac_of_bf16_peak"] = round(f8["roofline"]["achieved"] / bf, 4)
-    f8["roofline"]["peak_source"] = f8_src
-    f8["speedup_over_bf16_prefill"] = round(
-        f8["roofline"]["achieved"] / configs["2_qwen_prefill"]["N=8192"]["value"], 3)
-    f8["quantize_frac_of_hbm"] = round(f8["quantize_gbs"] / peaks["hbm_gbs"], 4)
-    result["prefill_fp8"] = f8
-    vl["roofline"]["peak"] = bf
-    vl["roofline"]["frac"] = round(vl["roofline"]["achieved"] / bf, 4)
-    vl["roofline"]["peak_source"] = peak_src + " bf16 burst"
-    result["prefill_varlen"] = vl
-    if app is not None:
-        app["roofline"]["peak"] = peaks["hbm_gbs"]
-        app["roofline"]["frac"] = round(app["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
-        app["roofline"]["peak_source"] = peak_src + " hbm copy"
-        result["decode_append"] = app
+    if "append" in legs:
+        app = time_decode_append(args, attn, dq, dec_caches, dec, S, op, lp, sweep, sweep_out,
+                                 dist, dev)
+        if app is not None:
+            app["roofline"]["peak"] = peaks["hbm_gbs"]
+            app["roofline"]["frac"] = round(app["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
+            app["roofline"]["peak_source"] = peak_src + " hbm copy"
+            result["decode_append"] = app
+    if "varlen" in legs:
+        vl = time_prefill_varlen(args, attn, W, dist, dev)
+        vl["roofline"]["peak"] = bf
+        vl["roofline"]["frac"] = round(vl["roofline"]["achieved"] / bf, 4)
+        vl["roofline"]["peak_source"] = peak_src + " bf16 burst"
+        result["prefill_varlen"] = vl
+    if "fp8" in legs:
+        f8 = time_fp8(args, attn, xq, qq, kq, vq, oq, lq, dist, dev)
+        f8_meas = measure_fp8_gemm_peak(dev)
+        if f8_meas is not None:
+            f8_peak, f8_src = f8_meas, "measured e4m3 GEMM (torch._scaled_mm, 8192^3, best of 10)"
+        else:
+            f8_peak = bf * 2.0   # nominal dense fp8 / bf16 ratio (4.5 / 2.25)
+            f8_src = peak_src + " bf16 burst x 2 (nominal fp8 / bf16)"
+        f8["roofline"]["peak"] = round(f8_peak, 1)
+        f8["roofline"]["frac"] = round(f8["roofline"]["achieved"] / f8_peak, 4)
+        f8["roofline"]["frac_of_bf16_peak"] = round(f8["roofline"]["achieved"] / bf, 4)
+        f8["roofline"]["peak_source"] = f8_src
+        if "2_qwen_prefill" in configs:
+            f8["speedup_over_bf16_prefill"] = round(
+                f8["roofline"]["achieved"] / configs["2_qwen_prefill"]["N=8192"]["value"], 3)
+        f8["quantize_frac_of_hbm"] = round(f8["quantize_gbs"] / peaks["hbm_gbs"], 4)
+        result["prefill_fp8"] = f8
+    if "d256" in legs:
+        d256 = time_d256(args, attn, W, dist, dev)
+        d256["roofline"]["peak"] = bf
+        d256["roofline"]["frac"] = round(d256["roofline"]["achieved"] / bf, 4)
+        d256["decode"]["roofline"]["peak"] = peaks["hbm_gbs"]
+        d256["decode"]["roofline"]["frac"] = round(
+            d256["decode"]["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
+        result["prefill_d256"] = d256
+    if "variants" in legs:
+        var = time_variants(args, attn, qq, kq, vq, xq.scale, oq, lq, dq, dec_caches, dec, S, op,
+                            lp, sweep, sweep_out, dist, dev)
+        for v_ in var["prefill"].values():
+            v_["frac"] = round(v_["value"] / bf, 4)
+        var["decode"]["frac"] = round(var["decode"]["value"] / peaks["hbm_gbs"], 4)
+        result["variants"] = var
     del qq, kq, vq, oq, lq, dec_caches
     torch.cuda.empty_cache()
     if not args.no_e2e:
@@ -789,36 +798,43 @@ def time_fp8(args, attn, x, q, k, v, o, lse, dist, dev):
         evs[i][1].record()
     torch.cuda.synchronize()
     (tot,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
-    # The quantiser on its own: its three calls (Q, K with block scales and
-    # the rotation, V with a per-head scale, transposed) into preallocated
-    # outputs, captured once in a CUDA graph so that the events time the
-    # kernels rather than the Python calls; L2 is flushed (a write of 2x L2)
-    # outside the events before every replay.
+    # The quantiser on its own, into preallocated outputs, captured in a CUDA
+    # graph so that the events time the kernels rather than the Python calls;
+    # L2 is flushed (a write of 2x L2) outside the events before every replay.
+    # Two forms: the fused call for Q, K and V (attn_quantize_fp8_qkv: three
+    # launches), and the three separate calls (six launches).
+    flush = torch.empty(2 * (int(torch.cuda.get_device_properties(dev).L2_cache_size) or (128 << 20)),
+                        dtype=torch.uint8, device=dev)
+
+    def graph_us(fn):
+        fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(10)]
+        for qa, qb in qev:
+            flush.zero_()
+            qa.record()
+            graph.replay()
+            qb.record()
+        torch.cuda.synchronize()
+        return statistics.median(qa.elapsed_time(qb) for qa, qb in qev) * 1e3
+
     outs = [torch.empty_like(t) for t in qin]
+    fused = tuple(torch.empty_like(t) for t in qin)
 
     def quantize_into():
         attn.quantize_fp8(q, signs, 128, codes=outs[0], scales=outs[3])
         attn.quantize_fp8(k, signs, 128, codes=outs[1], scales=outs[4])
         attn.quantize_fp8(v, None, 0, True, codes=outs[2], scales=outs[5])
 
-    quantize_into()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        quantize_into()
-    flush = torch.empty(2 * (int(torch.cuda.get_device_properties(dev).L2_cache_size) or (128 << 20)),
-                        dtype=torch.uint8, device=dev)
-    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(10)]
-    for qa, qb in qev:
-        flush.zero_()
-        qa.record()
-        graph.replay()
-        qb.record()
-    torch.cuda.synchronize()
-    quant_us = statistics.median(qa.elapsed_time(qb) for qa, qb in qev) * 1e3
+    quant_sep_us = graph_us(quantize_into)
+    quant_us = graph_us(lambda: attn.quantize_fp8_qkv(q, k, v, signs, out=fused))
     assert all(torch.equal(a_, b_) for a_, b_ in zip(outs, qin)), "graph replay differs"
-    del flush, graph
+    assert all(torch.equal(a_, b_) for a_, b_ in zip(fused, qin)), "fused quantiser differs"
+    del flush
     # algorithmic bytes: every element read once (bf16) and written once (e4m3)
     quant_bytes = (q.numel() + k.numel() + v.numel()) * 3
     # accuracy against the bf16 path, on queries and keys with four outlier
@@ -842,6 +858,9 @@ def time_fp8(args, attn, x, q, k, v, o, lse, dist, dev):
             "quantize_us": round(quant_us, 1),
             "quantize_gbs": round(quant_bytes / (quant_us * 1e-6) / 1e9, 1),
             "quantize_bytes": quant_bytes,
+            "quantize_form": "attn_quantize_fp8_qkv (Q, K and V's amax in one launch; then V's "
+                             "codes and scales)",
+            "quantize_separate_calls_us": round(quant_sep_us, 1),
             "rms_vs_bf16": {k_: round(v_, 6) for k_, v_ in rms.items()},
             "error_ratio_naive_over_block_rotation": round(rms["naive"] / rms["block+rotation"], 2)}
 
@@ -1000,6 +1019,19 @@ def run_e2e(args, x, dec, dev, world, dist):
     d2h = ho[0].numel() * 4 + hl[0].numel() * 4
     n = max(3, min(args.steps, args.e2e_steps))
     pipelined(2, p_in, p_out, pf)            # warm-up
+
+    def copy_gbs(pairs, to_dev):
+        """This box's copy rate for one step's inputs (to_dev) or results, alone."""
+        e0, e1 = _ev(), _ev()
+        torch.cuda.synchronize()
+        e0.record()
+        for h, d in pairs:
+            (d[0].copy_(h, non_blocking=True) if to_dev else h[0].copy_(d[0], non_blocking=True))
+        e1.record()
+        torch.cuda.synchronize()
+        return round((h2d if to_dev else d2h) / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+
+    copy_rates = {"h2d_gbs": copy_gbs(p_in, True), "d2h_gbs": copy_gbs(p_out, False)}
     if dist is not None:
         dist.barrier()
     pre = pipelined(n, p_in, p_out, pf)
@@ -1042,6 +1074,7 @@ def run_e2e(args, x, dec, dev, world, dist):
             "what": "one Llama-3-8B-layer causal prefill at N = 32768 per step, Q/K/V copied "
                     "in and O/LSE copied out every step",
             "pipelining": "3 streams (H2D / kernels / D2H), 2 buffer sets",
+            "copy_rates_alone": copy_rates,
             "decode_value": round(job_rate(decode_bytes(dec), n, world, dcd) / 1e9, 1),
             "decode_unit": "GB/s (end to end, cache copied from host each step)",
             "decode_h2d_bytes_per_step": h2d_dec, "decode_d2h_bytes_per_step": d2h_dec}
@@ -1147,6 +1180,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="only the timed headline steps (for profiling runs)")
+    ap.add_argument("--legs", type=str, default="all",
+                    help="comma list of the legs after the timed steps to run: configs, append, "
+                         "varlen, fp8, d256, variants (for profiling runs); default all")
     ap.add_argument("--seqlen", type=int, default=HEADLINE["prefill"]["seqlen"],
                     help="prefill length of the timed step (profiling runs use a smaller one)")
     ap.add_argument("--layers", type=int, default=HEADLINE["prefill"]["layers"],

@@ -19,6 +19,7 @@ from .api import (  # noqa: F401
     decode_append_splitkv,
     decode_append,
     quantize_fp8,
+    quantize_fp8_qkv,
     prefill_fp8,
 )
 from ._lib import AttnError, lib  # noqa: F401

@@ -38,6 +38,7 @@ SIGNATURES = {
                                                        c_void_p]),
     "attn_prefill_fp8": (c_int, [c_void_p] * 8 + [c_int] * 5 + [c_float, c_int, c_void_p]),
     "attn_quantize_fp8": (c_int, [c_void_p] * 4 + [c_int] * 5 + [c_void_p]),
+    "attn_quantize_fp8_qkv": (c_int, [c_void_p] * 10 + [c_int] * 4 + [c_void_p]),
     "attn_combine": (c_int, [c_void_p, c_void_p] + [c_int] * 4 + [c_void_p, c_void_p, c_void_p]),
     "attn_check_device_status": (c_int, [c_void_p]),
     "attn_set_wait_timeout_ns": (c_uint64, [c_uint64]),

@@ -184,6 +184,49 @@ def quantize_fp8(x: torch.Tensor, signs: Optional[torch.Tensor] = None, block_ro
     return codes, scales
 
 
+def quantize_fp8_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                     signs: Optional[torch.Tensor] = None, stream=None, out: Optional[tuple] = None):
+    """FP8 inputs of :func:`prefill_fp8` for Q, K and V in one call
+    (``attn_quantize_fp8_qkv``): Q and K with 128-row block scales and the
+    optional rotation, V with one scale per plane, transposed.  q: (...,
+    rows, d), k and v: (..., rows, d) bf16.  Returns (q8, k8, v8t, q_scales,
+    k_scales, v_scales), written into ``out`` (a tuple of those six tensors)
+    when given; equal bit for bit to three :func:`quantize_fp8` calls."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, name, _BF16, q.dim())
+    rows, d = q.shape[-2], q.shape[-1]
+    if tuple(k.shape) != tuple(v.shape) or k.shape[-2:] != q.shape[-2:]:
+        raise ValueError("k and v must match, and share rows and head_dim with q")
+    lq, lk = tuple(q.shape[:-2]), tuple(k.shape[:-2])
+    pq = pk = 1
+    for n in lq:
+        pq *= n
+    for n in lk:
+        pk *= n
+    nb = -(-rows // 128)
+    shapes = [(lq + (rows, d), torch.uint8), (lk + (rows, d), torch.uint8),
+              (lk + (d, rows), torch.uint8), (lq + (nb,), torch.float32),
+              (lk + (nb,), torch.float32), (lk, torch.float32)]
+    if out is None:
+        out = tuple(torch.empty(sh, dtype=dt, device=q.device) for sh, dt in shapes)
+    for t, (sh, dt), name in zip(out, shapes, ("q8", "k8", "v8t", "q_scales", "k_scales",
+                                               "v_scales")):
+        _need(t, name, dt, len(sh))
+        if tuple(t.shape) != sh:
+            raise ValueError(f"{name} must have shape {sh}")
+    sp = None
+    if signs is not None:
+        _need(signs, "signs", torch.float32, 1)
+        if signs.numel() != d:
+            raise ValueError("signs must have head_dim entries")
+        sp = signs.data_ptr()
+    st = lib().attn_quantize_fp8_qkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                     *(t.data_ptr() for t in out), sp, pq, pk, rows, d,
+                                     _stream(stream))
+    check("attn_quantize_fp8_qkv", st)
+    return out
+
+
 def decode_num_splits(batch: int, n_kv_heads: int, max_kv_len: int, num_sms: int = 0) -> int:
     """The split-count policy (``attn_decode_num_splits``)."""
     return int(lib().attn_decode_num_splits(int(batch), int(n_kv_heads), int(max_kv_len),

@@ -406,6 +406,34 @@ int attn_quantize_fp8(const attn_bf16* x, uint8_t* codes, float* scales, const f
   return ATTN_OK;
 }
 
+int attn_quantize_fp8_qkv(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
+                          uint8_t* q_codes, uint8_t* k_codes, uint8_t* v_codes_t,
+                          float* q_scales, float* k_scales, float* v_scales, const float* signs,
+                          int planes_q, int planes_kv, int rows, int head_dim, void* stream) {
+  if (!q || !k || !v || !q_codes || !k_codes || !v_codes_t || !q_scales || !k_scales ||
+      !v_scales)
+    return ATTN_ERR_NULL;
+  if (planes_q < 1 || planes_q > 65535 || planes_kv < 1 || planes_kv > 65535 || rows < 1 ||
+      rows > (1 << 24) ||
+      (long long)(planes_q + 2LL * planes_kv) * ((rows + 127) / 128) > 0x7fffffffLL)
+    return ATTN_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_codes, 16) ||
+      !aligned(k_codes, 16) || !aligned(v_codes_t, 16) || !aligned(q_scales, 4) ||
+      !aligned(k_scales, 4) || !aligned(v_scales, 4) || !aligned(signs, 4))
+    return ATTN_ERR_ALIGN;
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  const float inv = static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim)));
+  attn::QuantArgs aq{q, q_codes, q_scales, signs, planes_q, rows, head_dim, 128, 0, inv};
+  attn::QuantArgs ak{k, k_codes, k_scales, signs, planes_kv, rows, head_dim, 128, 0, inv};
+  attn::QuantArgs av{v, v_codes_t, v_scales, nullptr, planes_kv, rows, head_dim, 0, 1, inv};
+  if (attn::launch_quantize_qkv(aq, ak, av, make_ctx(stream, ds)) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
 int attn_check_device_status(void* stream) {
   int st = ATTN_OK;
   DeviceState* ds = device_state(&st);

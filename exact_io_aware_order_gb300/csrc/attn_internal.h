@@ -101,6 +101,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_combine(const CombineArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_wait_selftest(const LaunchCtx& ctx);
 cudaError_t launch_quantize(const QuantArgs& a, const LaunchCtx& ctx);
+// Q and K with block scales (128 rows), V with one scale per plane and
+// transposed; the three share rows and head_dim.
+cudaError_t launch_quantize_qkv(const QuantArgs& q, const QuantArgs& k, const QuantArgs& v,
+                                const LaunchCtx& ctx);
 
 // Resolves the current device's launch context (architecture check, error
 // word, SM count) for a call on `stream`; returns an attn_status code.

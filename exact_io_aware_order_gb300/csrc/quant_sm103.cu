@@ -245,34 +245,65 @@ __device__ __forceinline__ void store_codes(const QuantArgs& a, int plane, int r
   }
 }
 
-// One scale per block of 128 rows: amax, scale and codes in one pass.
+// One scale per block of 128 rows: amax, scale and codes in one pass, for
+// block `blk` of `plane` (nblk blocks per plane).
 template <int D, int LPR>
-__global__ void __launch_bounds__(kThreads) quantize_block_kernel(const QuantArgs a) {
+__device__ __forceinline__ void quantize_block(const QuantArgs& a, int plane, int blk, int nblk,
+                                               float* red) {
   using G = Geom<D, LPR>;
-  __shared__ float red[kWarps];
-  const int plane = blockIdx.y, lane = threadIdx.x & 31;
-  const int row0w = blockIdx.x * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
+  const int lane = threadIdx.x & 31;
+  const int row0w = blk * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
   float x[G::RPL][G::E];
   load_rows<D, LPR>(a, plane, row0w, lane, x);
   float amax = block_amax<D, LPR>(x, red);
   if (amax == 0.f) amax = 1.f;
-  if (threadIdx.x == 0) a.scales[(size_t)plane * gridDim.x + blockIdx.x] = __fdiv_rn(amax, kE4M3Max);
+  if (threadIdx.x == 0) a.scales[(size_t)plane * nblk + blk] = __fdiv_rn(amax, kE4M3Max);
   store_codes<D, LPR>(a, plane, row0w, lane, x, __fdiv_rn(kE4M3Max, amax));
 }
 
-// One scale per plane, pass 1: the plane's amax, as float bits in scales[plane]
-// (zeroed before the launch).
 template <int D, int LPR>
-__global__ void __launch_bounds__(kThreads) plane_amax_kernel(const QuantArgs a) {
-  using G = Geom<D, LPR>;
+__global__ void __launch_bounds__(kThreads) quantize_block_kernel(const QuantArgs a) {
   __shared__ float red[kWarps];
-  const int plane = blockIdx.y, lane = threadIdx.x & 31;
-  const int row0w = blockIdx.x * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
+  quantize_block<D, LPR>(a, blockIdx.y, blockIdx.x, gridDim.x, red);
+}
+
+// One scale per plane, pass 1: block `blk`'s amax folded into the plane's,
+// kept as float bits in scales[plane] (zeroed before the launch).
+template <int D>
+__device__ __forceinline__ void plane_amax_block(const QuantArgs& a, int plane, int blk,
+                                                 float* red) {
+  using G = Geom<D, 4>;
+  const int lane = threadIdx.x & 31;
+  const int row0w = blk * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
   float x[G::RPL][G::E];
-  load_rows<D, LPR>(a, plane, row0w, lane, x);
-  const float amax = block_amax<D, LPR>(x, red);
+  load_rows<D, 4>(a, plane, row0w, lane, x);
+  const float amax = block_amax<D, 4>(x, red);
   if (threadIdx.x == 0)
     atomicMax(reinterpret_cast<unsigned int*>(a.scales) + plane, __float_as_uint(amax));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) plane_amax_kernel(const QuantArgs a) {
+  __shared__ float red[kWarps];
+  plane_amax_block<D>(a, blockIdx.y, blockIdx.x, red);
+}
+
+// Q and K with block scales and V's plane amax in one launch: CTA b takes
+// block b of the concatenated lists (Q blocks, then K blocks, then V blocks).
+template <int D>
+__global__ void __launch_bounds__(kThreads) qkv_pass1_kernel(const QuantArgs q, const QuantArgs k,
+                                                             const QuantArgs v, int nblk) {
+  __shared__ float red[kWarps];
+  int b = blockIdx.x;
+  const int nq = q.planes * nblk, nk = k.planes * nblk;
+  if (b < nq) {
+    quantize_block<D, 4>(q, b / nblk, b % nblk, nblk, red);
+  } else if ((b -= nq) < nk) {
+    quantize_block<D, 4>(k, b / nblk, b % nblk, nblk, red);
+  } else {
+    b -= nk;
+    plane_amax_block<D>(v, b / nblk, b % nblk, red);
+  }
 }
 
 // Pass 2: the codes, from the plane's amax.
@@ -306,7 +337,7 @@ cudaError_t launch_quantize_t(const QuantArgs& a, const LaunchCtx& ctx) {
   }
   cudaError_t e = cudaMemsetAsync(a.scales, 0, (size_t)a.planes * sizeof(float), ctx.stream);
   if (e != cudaSuccess) return e;
-  plane_amax_kernel<D, 4><<<grid, kThreads, 0, ctx.stream>>>(a);
+  plane_amax_kernel<D><<<grid, kThreads, 0, ctx.stream>>>(a);
   plane_codes_kernel<D, LPR><<<grid, kThreads, 0, ctx.stream>>>(a);
   plane_scale_kernel<<<(a.planes + 127) / 128, 128, 0, ctx.stream>>>(a);
   return cudaGetLastError();
@@ -317,10 +348,33 @@ cudaError_t launch_quantize_d(const QuantArgs& a, const LaunchCtx& ctx) {
   return a.transpose ? launch_quantize_t<D, 32>(a, ctx) : launch_quantize_t<D, 4>(a, ctx);
 }
 
+// Q, K (block scales, rotated when signs are given) and V (plane scales,
+// transposed): the first pass of all three in one launch, then V's codes and
+// scales.
+template <int D>
+cudaError_t launch_quantize_qkv_d(const QuantArgs& q, const QuantArgs& k, const QuantArgs& v,
+                                  const LaunchCtx& ctx) {
+  const int nblk = (q.rows + kBlockRows - 1) / kBlockRows;
+  cudaError_t e = cudaMemsetAsync(v.scales, 0, (size_t)v.planes * sizeof(float), ctx.stream);
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = (unsigned)((q.planes + k.planes + v.planes) * nblk);
+  qkv_pass1_kernel<D><<<blocks, kThreads, 0, ctx.stream>>>(q, k, v, nblk);
+  const dim3 grid((unsigned)nblk, (unsigned)v.planes);
+  plane_codes_kernel<D, 32><<<grid, kThreads, 0, ctx.stream>>>(v);
+  plane_scale_kernel<<<(v.planes + 127) / 128, 128, 0, ctx.stream>>>(v);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_quantize(const QuantArgs& a, const LaunchCtx& ctx) {
   return a.head_dim == 128 ? launch_quantize_d<128>(a, ctx) : launch_quantize_d<64>(a, ctx);
+}
+
+cudaError_t launch_quantize_qkv(const QuantArgs& q, const QuantArgs& k, const QuantArgs& v,
+                                const LaunchCtx& ctx) {
+  return q.head_dim == 128 ? launch_quantize_qkv_d<128>(q, k, v, ctx)
+                           : launch_quantize_qkv_d<64>(q, k, v, ctx);
 }
 
 }  // namespace attn

@@ -318,6 +318,32 @@ int attn_quantize_fp8(const attn_bf16* x, uint8_t* codes, float* scales, const f
                       void* stream);
 
 /*
+ * attn_quantize_fp8_qkv -- the FP8 inputs of attn_prefill_fp8 for Q, K and V
+ * in one call, with fewer launches than three attn_quantize_fp8 calls (Q, K
+ * and V's amax in one kernel, then V's codes and scales).
+ *
+ * Page: same, section "Interaction with post-trained models" (FlashAttention-3's
+ * FP8 path: block quantisation and incoherent processing).
+ *
+ *   q        : (planes_q, rows, head_dim) bf16; k, v: (planes_kv, rows, head_dim) bf16;
+ *              16-byte aligned
+ *   signs    : (head_dim,) fp32 +-1 for the rotation of q and k, or NULL
+ *   q_codes  : (planes_q, rows, head_dim) e4m3;  q_scales: (planes_q, ceil(rows/128)) fp32
+ *   k_codes  : (planes_kv, rows, head_dim) e4m3; k_scales: (planes_kv, ceil(rows/128)) fp32
+ *   v_codes_t: (planes_kv, head_dim, rows) e4m3; v_scales: (planes_kv,) fp32
+ *   codes 16-byte aligned, scales 4-byte aligned
+ * The results are bit for bit those of attn_quantize_fp8 on q and on k with
+ * block_rows = 128 and these signs, and on v with no rotation, block_rows = 0
+ * and transpose = 1.  Limits: planes_q, planes_kv <= 65535; 1 <= rows <= 2^24;
+ * head_dim 64 or 128.
+ * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _ALIGN, _ARCH, _LAUNCH.
+ */
+int attn_quantize_fp8_qkv(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
+                          uint8_t* q_codes, uint8_t* k_codes, uint8_t* v_codes_t,
+                          float* q_scales, float* k_scales, float* v_scales, const float* signs,
+                          int planes_q, int planes_kv, int rows, int head_dim, void* stream);
+
+/*
  * attn_combine -- merge per-split partial results by their LSE weights.
  *
  * Page: same, section "The online softmax, with every symbol defined" (the

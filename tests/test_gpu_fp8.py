@@ -50,6 +50,49 @@ def test_quantizer_bit_exact(dev, planes, rows, d, rot, block, transpose):
     assert np.array_equal(scales.cpu().numpy().reshape(ref_scales.shape), ref_scales)
 
 
+@pytest.mark.parametrize("pq,pk,rows,d,rot", [
+    (28, 4, 8192, 128, True),     # the Qwen2.5-7B layer's Q, K and V at N = 8192
+    (3, 1, 300, 64, False),
+    (6, 3, 4100, 128, True),      # rows not a multiple of 16
+    (2, 2, 17, 128, True),        # one partial block
+])
+def test_quantizer_qkv_matches_separate_calls_and_oracle(dev, pq, pk, rows, d, rot):
+    """attn_quantize_fp8_qkv: bit for bit the three attn_quantize_fp8 calls
+    (Q, K block-scaled and rotated, V per plane and transposed), and the
+    oracle's codes and scales."""
+    g = torch.Generator().manual_seed(pq + rows)
+    mk = lambda p: (torch.randn(p, rows, d, generator=g) *
+                    torch.exp(torch.randn(p, rows, 1, generator=g))).to(torch.bfloat16)
+    q, k, v = mk(pq), mk(pk), mk(pk)
+    k[0, :, 5] *= 25                                           # an outlier channel
+    sg = signs_for(d, 7) if rot else None
+    sgd = torch.from_numpy(sg).to(dev) if rot else None
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    fused = attn.quantize_fp8_qkv(qd, kd, vd, sgd)
+    sep = (*attn.quantize_fp8(qd, sgd, block_rows=128)[:1], *attn.quantize_fp8(kd, sgd, 128)[:1],
+           *attn.quantize_fp8(vd, None, 0, True)[:1])
+    sep_s = (attn.quantize_fp8(qd, sgd, 128)[1], attn.quantize_fp8(kd, sgd, 128)[1],
+             attn.quantize_fp8(vd, None, 0, True)[1])
+    attn.check_device_status()
+    for a, b in zip(fused[:3], sep):
+        assert torch.equal(a, b)
+    for a, b in zip(fused[3:], sep_s):
+        assert torch.equal(a, b)
+    # against the oracle
+    for x, codes, scales, block, tr, rot_ in ((q, fused[0], fused[3], 128, False, rot),
+                                              (k, fused[1], fused[4], 128, False, rot),
+                                              (v, fused[2], fused[5], rows, True, False)):
+        x32 = x.float().numpy()
+        if rot_:
+            x32 = F.hadamard_rotate(x32, sg)
+        ref_codes, ref_scales = F.quantize_blocks(x32, block)
+        got = e4m3_values(codes)
+        if tr:
+            got = got.transpose(0, 2, 1)
+        assert np.array_equal(got, ref_codes)
+        assert np.array_equal(scales.cpu().numpy().reshape(ref_scales.shape), ref_scales)
+
+
 @pytest.mark.parametrize("block", [128, 0])
 def test_quantizer_all_zero_plane(dev, block):
     """A block (or plane) of zeros: amax 0 counts as 1, so its scale is 1/448
