@@ -77,8 +77,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max grows > 2^8
 
-// ESZ: bytes per element of Q, K and V (2: bf16; 1: e4m3).
-template <int D, bool VARLEN, int ESZ = 2>
+// ESZ: bytes per element of Q, K and V (2: bf16; 1: e4m3).  XB: the ALiBi
+// bias's extra k-step operands (two constant 4 KB key chunks, a 256-byte
+// query atom per Q slot).
+template <int D, bool VARLEN, int ESZ = 2, bool XB = false>
 struct PrefillSmem {
   static constexpr int kBNt = key_tile<D>();
   static constexpr int kQTileBytes = 128 * D * ESZ;    // one Q tile (128 rows)
@@ -93,7 +95,13 @@ struct PrefillSmem {
   static constexpr int kK = kQ + kQSlots * kQTileBytes;
   static constexpr int kV = kK + kKSlots * kTileBytes;
   static constexpr int kStage = kV + kVSlots * kTileBytes;     // O staging: 4 warps x 32 rows x 128 B
-  static constexpr int kBar = kStage + 4 * 4096;
+  // ALiBi: K'+ and K'- (128 rows x 32 B each), then Q' per Q slot (8 rows x
+  // 32 B: all 128 rows of Q' are equal, so its 8-row groups share one atom).
+  static constexpr int kKxPos = kStage + 4 * 4096;
+  static constexpr int kKxNeg = kKxPos + 4096;
+  static constexpr int kQx = kKxNeg + 4096;
+  static constexpr int kQxBytes = 256;
+  static constexpr int kBar = kKxPos + (XB ? 2 * 4096 + kQSlots * kQxBytes : 0);
   // barriers: q_full/q_empty, k_full/k_empty, v_full/v_empty (one pair per
   // slot), s_full/p_full/pv_done [3], o_full, o_empty, stats_full/stats_empty [2],
   // drain_s, drain_pv
@@ -260,7 +268,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const PrefillParams p) {
   constexpr bool FP8 = VARIANT == kFp8;
   constexpr int kBN = key_tile<D>();
-  using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2>;
+  // ALiBi at head_dim <= 128: the tensor core adds the bias's per-key part.
+  constexpr bool XB = VARIANT == kWindowAlibi && D <= 128;
+  using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2, XB>;
   constexpr int RQ = L::kQSlots, RK = L::kKSlots, RV = L::kVSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -360,6 +370,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err_word, kErrSeqLens);
     }
   }
+  if constexpr (XB) {
+    // ALiBi's key chunks K'+ and K'-: row r (a key's offset in its tile) is
+    // 32 bytes, two equal 16-byte halves of bf16 (+-r, +-r, +-r, 0, 0, 0, 0, 0),
+    // so that any 32-byte swizzle of the halves reads the same values.
+    for (int i = threadIdx.x; i < 2 * 256; i += kThreads) {
+      const int which = i >> 8, u = i & 255, r = u >> 1;
+      const float v = which ? -static_cast<float>(r) : static_cast<float>(r);
+      st_shared_v4(smem_u32(smem + (which ? L::kKxNeg : L::kKxPos) + u * 16),
+                   make_float4(__uint_as_float(pack_bf16x2(v, v)), __uint_as_float(pack_bf16x2(v, 0.f)),
+                               0.f, 0.f));
+    }
+    fence_proxy_async_smem();  // read by the MMAs (async proxy)
+  }
   const SeqTables seqt{seq_start, seq_len, item_prefix};
   tc_fence_before();
   __syncthreads();
@@ -418,6 +441,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int tile_bytes = is_q ? L::kQTileBytes : L::kTileBytes;
         const int chunk_bytes = is_q ? L::kQChunkBytes : L::kChunkBytes;
         if (cnt >= R && !mbar_wait(bar(empty + slot), ((cnt / R) - 1) & 1, ctl)) return false;
+        if constexpr (XB) {
+          if (is_q) {
+            // ALiBi's query atom Q' for this slot: every row (h, m, l, 0, ...) / 2
+            // in both 16-byte halves, where h + m + l (three bf16 terms) is
+            // slope log2(e) / (scale log2(e)), so that Q' K'+- scaled by
+            // scale log2(e) is +- slope (j - kv0) log2(e).
+            const float tgt = p.alibi_slopes[z % p.n_q_heads] * kLog2e / p.sl2;
+            const float h = bf16_round(tgt), mid = bf16_round(tgt - h), lo = bf16_round(tgt - h - mid);
+            const float4 u = make_float4(__uint_as_float(pack_bf16x2(0.5f * h, 0.5f * mid)),
+                                         __uint_as_float(pack_bf16x2(0.5f * lo, 0.f)), 0.f, 0.f);
+            const uint32_t qx = smem_u32(smem + L::kQx + slot * L::kQxBytes);
+            for (int i = 0; i < L::kQxBytes / 16; ++i) st_shared_v4(qx + i * 16, u);
+            fence_proxy_async_smem();  // visible to the MMAs before the slot is announced
+          }
+        }
         mbar_arrive_expect_tx(bar(full + slot), (uint32_t)tile_bytes);
         for (int c = 0; c < L::kChunks; ++c) {
           const uint32_t dst = smem_u32(smem + base + slot * tile_bytes + c * chunk_bytes);
@@ -495,6 +533,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             else
               mma_ss_lo(dS, q_lo + qoff, kb + koff, dhi, id_s, kk > 0);
           }
+          if constexpr (XB) {
+            // One more k step adds slope (j - kv0) with the sign of j - i
+            // (Q' K'+ below the diagonal, Q' K'- above it).  A non-causal
+            // tile on the diagonal holds both signs: its softmax adds the
+            // whole bias itself.
+            const int kv0 = key_tile_at<VARIANT>(t, j, p.causal) * kBN;
+            if (p.causal || kv0 != t.qrel) {
+              // 32-byte swizzle, K-major; A (Q') with an 8-row stride of 0
+              // (one atom for all rows), B (K'+-) with 256 bytes.
+              const uint32_t qx = sw128_desc_lo(smem_u32(smem + L::kQx + qs * L::kQxBytes), 16);
+              const uint32_t kx = sw128_desc_lo(
+                  smem_u32(smem + ((p.causal || kv0 < t.qrel) ? L::kKxPos : L::kKxNeg)), 16);
+              mma_ss_lo2(dS, qx, sw32_desc_hi(0), kx, sw32_desc_hi(256), id_s, 1u);
+            }
+          }
           mma_commit(bar(kSFull + b));
           mma_commit(bar(kKEmpty + slot));
         }
@@ -567,12 +620,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const Tile t = tile_of<VARLEN, VARIANT, kBN>(w, p, seqt);
       const int q0 = t.qrel, q_row = q0 + row;  // indices within the sequence
       float m = -INFINITY, l = 0.f;   // running max (log2 domain) and sum of the row
-      // ALiBi: this head's slope in log2 units; the scores are then biased
-      // and scaled in place, so the passes below use a unit scale.
-      float alibi_l2 = 0.f, sl2 = p.sl2;
+      // ALiBi: this head's slope in log2 units.  At head_dim <= 128 the
+      // tensor core has added its per-key part to S and each row adds a
+      // constant per tile; otherwise the scores are biased and scaled in
+      // place, so the passes below use a unit scale.
+      float alibi_l2 = 0.f, sl2 = p.sl2, alibi_s = 0.f;
       if constexpr (VARIANT == kWindowAlibi) {
         alibi_l2 = p.alibi_slopes[t.zq % p.n_q_heads] * kLog2e;
-        sl2 = 1.f;
+        if constexpr (XB)
+          alibi_s = alibi_l2 / p.sl2;  // the slope in units of S
+        else
+          sl2 = 1.f;
       }
       // FP8: the scores carry the Q block's scale (here) and the K block's
       // (per key tile, below).
@@ -598,6 +656,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[c][i]);
         }
         const int kv0 = key_tile_at<VARIANT>(t, j, p.causal) * kBN;  // first key of the tile
+        float c_row = 0.f;  // ALiBi (head_dim <= 128): the row's bias constant for this tile
         if constexpr (VARIANT != kPlain) {
           if constexpr (VARIANT == kWindowCap) {
             // This flavour requires softcap > 0 (cap_in2 != 0): with a zero
@@ -618,11 +677,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
           }
           if constexpr (VARIANT == kWindowAlibi) {
-            // s -> s scale log2 e - slope log2 e |i - j|
             const float dist0 = static_cast<float>(kv0 - q_row);  // key c is at j - i = dist0 + c
+            if constexpr (XB) {
+              // -slope |i - j| = -slope |i - kv0| +- slope (j - kv0): the
+              // second term is in S already, the first is the row's constant.
+              if (p.causal || kv0 != q0) {
+                c_row = -alibi_l2 * fabsf(dist0);
+              } else {
 #pragma unroll
-            for (int c = 0; c < kBN; ++c)
-              s[c] = fmaf(s[c], p.sl2, -alibi_l2 * fabsf(dist0 + static_cast<float>(c)));
+                for (int c = 0; c < kBN; ++c)
+                  s[c] = fmaf(-alibi_s, fabsf(dist0 + static_cast<float>(c)), s[c]);
+              }
+            } else {
+              // s -> s scale log2 e - slope log2 e |i - j|
+#pragma unroll
+              for (int c = 0; c < kBN; ++c)
+                s[c] = fmaf(s[c], p.sl2, -alibi_l2 * fabsf(dist0 + static_cast<float>(c)));
+            }
           }
           const bool hi_edge = p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > t.len);
           const bool lo_edge = p.window_left >= 0 && kv0 < q0 + kBM - 1 - p.window_left;
@@ -664,7 +735,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
                      fmaxf(mxa[6], mxa[7]));
         }
-        const float m_new = fmaxf(m, mx * sl2);
+        const float m_new = fmaxf(m, XB ? fmaf(mx, sl2, c_row) : mx * sl2);
         // Rescale only when some row of the warp gained more than 2^8; otherwise
         // keep the stale max for both l and O (exact either way).
         float corr = 1.f;
@@ -686,7 +757,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // A row whose keys in this item's tiles so far were all outside its
         // window has m = -inf (all its P are 0): take 0 as its reference.
         const float m_ref = (VARIANT != kPlain && m == -INFINITY) ? 0.f : m;
-        const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m_ref, -m_ref);
+        const float nm = XB ? c_row - m_ref : -m_ref;
+        const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(nm, nm);
         // soft-capping: exponent sl2 (1 - 2 r) - m = -2 sl2 r + (sl2 - m)
         const float2 cap_a = make_float2(-2.f * sl2, -2.f * sl2), cap_b = make_float2(sl2 - m_ref, sl2 - m_ref);
         float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -939,7 +1011,7 @@ bool make_out_map(CUtensorMap* m, void* base, int D, int rows, int planes) {
 template <int D, bool VARLEN, int VARIANT>
 cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   constexpr bool FP8 = VARIANT == kFp8;
-  using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2>;
+  using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2, VARIANT == kWindowAlibi && D <= 128>;
   // The soft-cap flavour drops the factor's zero test from its hot loop.
   if (VARIANT == kWindowCap && !(a.softcap > 0.f)) return cudaErrorInvalidValue;
   static bool configured[64] = {};

@@ -241,6 +241,18 @@ __device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32
       "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// As mma_ss_lo, with separate high words for A and B.
+__device__ __forceinline__ void mma_ss_lo2(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                           uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                           uint32_t desc_hi, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -293,6 +305,12 @@ __host__ __device__ constexpr uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lb
 }
 __host__ __device__ constexpr uint32_t sw128_desc_hi(uint32_t sbo_bytes) {
   return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+// High word of a 32-byte-swizzle descriptor (K-major rows of 32 bytes,
+// 8-row atoms of 256 bytes; swizzle mode 6).
+__host__ __device__ constexpr uint32_t sw32_desc_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (6u << 29);
 }
 
 // The mbarrier receives one arrival once every tcgen05.mma issued so far by
@@ -486,6 +504,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// x rounded to the nearest bf16, as a float.
+__device__ __forceinline__ float bf16_round(float x) {
+  return __uint_as_float((pack_bf16x2(x, 0.f) & 0xFFFFu) << 16);
+}
 __device__ __forceinline__ bool elect_one_lane() { return (threadIdx.x & 31u) == 0u; }
 
 }  // namespace attn

@@ -145,6 +145,25 @@ def test_prefill_alibi_full(dev, N, Hq, Hkv, D, causal, Wl):
     compare(o, lse, o_ref, lse_ref, f"alibi prefill N={N} W={Wl}")
 
 
+@pytest.mark.parametrize("N,Hq,Hkv,D,causal,Wl,slopes", [
+    (700, 4, 2, 64, False, -1, None),        # head_dim 64, tiles on both sides of the diagonal
+    (1100, 8, 2, 128, False, 300, None),     # non-causal window: keys on both sides within it
+    (640, 8, 4, 128, True, -1, [1.0, 0.9, 0.02, 0.25, 0.5, 0.001, 0.75, 0.33]),
+    (640, 8, 4, 128, False, -1, [1.0, -0.05, 0.02, 0.25, 0.5, 0.001, 0.75, 0.0]),
+])
+def test_prefill_alibi_bias_forms(dev, N, Hq, Hkv, D, causal, Wl, slopes):
+    """At head_dim <= 128 the kernel splits -slope |i - j| per key tile into
+    a row constant and a per-key part that the tensor core adds (the slope
+    carried as three bf16 terms); these cases cover tiles below, above and on
+    the diagonal, steep, zero and negative slopes."""
+    x = W.make_prefill(1, Hq, Hkv, N, D, seed=N + 11, causal=causal)
+    sl = alibi_slopes(Hq) if slopes is None else torch.tensor(slopes, dtype=torch.float32)
+    o, lse = run_prefill(x, dev, window_left=Wl, alibi_slopes=sl.to(dev))
+    o_ref, lse_ref = oracle.prefill(x.q, x.k, x.v, x.scale, causal, window_left=Wl,
+                                    alibi_slopes=sl.tolist())
+    compare(o, lse, o_ref, lse_ref, f"alibi bias forms N={N} D={D} causal={causal} W={Wl}")
+
+
 def test_prefill_alibi_qwen_8192_sampled(dev):
     x = W.qwen_prefill(8192)
     sl = alibi_slopes(28)
