@@ -230,9 +230,12 @@ def run_gb300(args, rank: int, world: int, dist):
     sweep_out = torch.empty((), dtype=torch.float32, device=dev)
 
     def decode_layer(l):
+        # Early cache streaming: each layer has its own cache, so the kernel
+        # before a decode (the previous layer's combine, or the L2 sweep)
+        # writes none of what the decode reads before its wait.
         kc, vc = caches[l]
         attn.decode_splitkv(dq, kc, vc, dlens, None, num_splits=S, max_kv_len=dec.max_kv_len,
-                            scale=dec.scale, o_partial=op, lse_partial=lp)
+                            scale=dec.scale, o_partial=op, lse_partial=lp, early_cache=True)
         attn.combine(op, lp, out=do, lse=dl)
 
     def step(ev=None):
@@ -435,7 +438,9 @@ def headline_config(world: int) -> dict:
             "decode": {"n_q_heads": Dc["n_q"], "n_kv_heads": Dc["n_kv"], "head_dim": 128,
                        "kv_len": Dc["kv_len"], "layers_per_step": Dc["layers"],
                        "num_splits": "the library's policy (attn_decode_num_splits)",
-                       "cache": "contiguous, one per layer"},
+                       "cache": "contiguous, one per layer",
+                       "launch": "decode with ATTN_DECODE_EARLY_CACHE, then attn_combine, "
+                                 "layer after layer on one stream"},
             "l2": "inputs larger than L2 (prefill Q+K+V 403 MB, each launch writes a 537 MB "
                   "output; 28 decode caches of 63 MB); a read-only sweep of 2x L2 between "
                   "the prefill chain and the decode chain",
@@ -538,6 +543,15 @@ def time_decode_sweep(args, attn, W, dev, dist, peaks, sweep, sweep_out, chain_t
             alone(i)
             attn.combine(op, lp, out=o, lse=l)
 
+        def alone_early(i):
+            kc, vc = caches[i % 4]
+            attn.decode_splitkv(dq, kc, vc, dlens, None, num_splits=S, max_kv_len=30720,
+                                scale=dec.scale, o_partial=op, lse_partial=lp, early_cache=True)
+
+        def two_early(i):
+            alone_early(i)
+            attn.combine(op, lp, out=o, lse=l)
+
         entry = {}
         for name, fn in (("decode", alone), ("decode+combine", two)):
             t = _timed(fn, n, dist, dev, before=flush)
@@ -548,7 +562,9 @@ def time_decode_sweep(args, attn, W, dev, dist, peaks, sweep, sweep_out, chain_t
         res[f"S={S}" + (" (policy)" if S == auto else "")] = entry
         if S == auto:
             chain = {}
-            for name, fn in (("decode", alone), ("decode+combine", two)):
+            for name, fn in (("decode", alone), ("decode+combine", two),
+                             ("decode, early cache streaming", alone_early),
+                             ("decode+combine, early cache streaming", two_early)):
                 L = 28
                 t = _timed(lambda i: [fn(j) for j in range(L)], 5, dist, dev, before=flush)
                 gbs = nbytes * L / (t / 5 * 1e-3) / 1e9

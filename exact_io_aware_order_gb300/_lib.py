@@ -17,6 +17,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "attn.h")
 
 c_int, c_float, c_void_p, c_uint64, c_char_p = (ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
                                                  ctypes.c_uint64, ctypes.c_char_p)
+c_uint = ctypes.c_uint
 
 # name -> (restype, argtypes); pointers are passed as c_void_p (raw addresses).
 SIGNATURES = {
@@ -27,6 +28,8 @@ SIGNATURES = {
                                                                 c_void_p, c_void_p]),
     "attn_decode_splitkv_ex": (c_int, [c_void_p] * 5 + [c_int] + [c_void_p] * 2 + [c_int] * 8
                                + [c_float, c_int, c_float, c_void_p, c_void_p]),
+    "attn_decode_splitkv_ex2": (c_int, [c_void_p] * 5 + [c_int] + [c_void_p] * 2 + [c_int] * 8
+                                + [c_float, c_int, c_float, c_void_p, c_uint, c_void_p]),
     "attn_prefill_varlen": (c_int, [c_void_p] * 6 + [c_int] * 5 + [c_float, c_int, c_void_p]),
     "attn_decode_num_splits": (c_int, [c_int] * 4),
     "attn_decode_splitkv": (c_int, [c_void_p] * 5 + [c_int] + [c_void_p] * 2 + [c_int] * 8

@@ -17,6 +17,10 @@ from ._lib import check, lib
 _BF16 = torch.bfloat16
 
 
+# attn_decode_splitkv_ex2 flag (include/attn.h ATTN_DECODE_EARLY_CACHE).
+EARLY_CACHE = 1
+
+
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -235,7 +239,7 @@ def decode_num_splits(batch: int, n_kv_heads: int, max_kv_len: int, num_sms: int
 
 def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
                  o_partial, lse_partial, stream, new_kv=None, window_left=-1, softcap=0.0,
-                 alibi_slopes=None):
+                 alibi_slopes=None, early_cache=False):
     """Shape checks and marshalling shared by the plain and appending decode."""
     _need(q, "q", _BF16, 3)
     _need(k_cache, "k_cache", _BF16, 4)
@@ -289,7 +293,12 @@ def _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_l
         if alibi_slopes.numel() != n_q:
             raise ValueError("alibi_slopes must have one slope per query head")
         al = alibi_slopes.data_ptr()
-    if new_kv is None and variant:
+    if new_kv is None and early_cache:
+        name = "attn_decode_splitkv_ex2"
+        st = lib().attn_decode_splitkv_ex2(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                           bt_ptr, *tail[:-1], int(window_left), float(softcap),
+                                           al, EARLY_CACHE, tail[-1])
+    elif new_kv is None and variant:
         name = "attn_decode_splitkv_ex"
         st = lib().attn_decode_splitkv_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                           bt_ptr, *tail[:-1], int(window_left), float(softcap),
@@ -318,9 +327,14 @@ def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                    num_splits: int = 0, max_kv_len: Optional[int] = None,
                    scale: Optional[float] = None, o_partial: Optional[torch.Tensor] = None,
                    lse_partial: Optional[torch.Tensor] = None, stream=None, window_left: int = -1,
-                   softcap: float = 0.0, alibi_slopes: Optional[torch.Tensor] = None):
+                   softcap: float = 0.0, alibi_slopes: Optional[torch.Tensor] = None,
+                   early_cache: bool = False):
     """Split-KV single-token decode (``attn_decode_splitkv``; with a sliding
-    window or soft-capping, ``attn_decode_splitkv_ex``).
+    window or soft-capping, ``attn_decode_splitkv_ex``; with
+    ``early_cache=True``, ``attn_decode_splitkv_ex2`` with
+    ATTN_DECODE_EARLY_CACHE: the kernel may start streaming the cache before
+    the previous kernel on the stream has finished, which must then write
+    none of kv_lens, block_table and the caches).
 
     q: (B, n_q, d) bf16.  Paged: k_cache, v_cache (num_blocks, block_size,
     n_kv, d) with block_table (B, max_blocks) int32; contiguous (block_table
@@ -329,7 +343,7 @@ def decode_splitkv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     """
     return _decode_call(q, k_cache, v_cache, kv_lens, block_table, num_splits, max_kv_len, scale,
                         o_partial, lse_partial, stream, window_left=window_left, softcap=softcap,
-                        alibi_slopes=alibi_slopes)
+                        alibi_slopes=alibi_slopes, early_cache=early_cache)
 
 
 def decode_append_splitkv(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,

@@ -267,7 +267,8 @@ int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_n
                 int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                 int max_blocks_per_seq, int num_blocks, int max_kv_len, float scale,
                 void* stream, bool append, int window_left = -1, float softcap = 0.f,
-                const float* alibi_slopes = nullptr) {
+                const float* alibi_slopes = nullptr, unsigned flags = 0u) {
+  if ((flags & ~ATTN_DECODE_EARLY_CACHE) != 0u || (append && flags != 0u)) return ATTN_ERR_SHAPE;
   const int vst = attn::validate_decode(q, k_new, v_new, k_cache, v_cache, block_table, kv_lens,
                                         num_splits, o_partial, lse_partial, batch, n_q_heads,
                                         n_kv_heads, head_dim, block_size, max_blocks_per_seq,
@@ -289,6 +290,7 @@ int decode_impl(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_n
   a.window_left = window_left;
   a.softcap = softcap;
   a.alibi_slopes = alibi_slopes;
+  a.early_cache = (flags & ATTN_DECODE_EARLY_CACHE) ? 1 : 0;
   if (attn::launch_decode(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
@@ -315,6 +317,19 @@ int attn_decode_splitkv_ex(const attn_bf16* q, const attn_bf16* k_cache, const a
                      o_partial, lse_partial, batch, n_q_heads, n_kv_heads, head_dim, block_size,
                      max_blocks_per_seq, num_blocks, max_kv_len, scale, stream, false, window_left,
                      softcap, alibi_slopes);
+}
+
+int attn_decode_splitkv_ex2(const attn_bf16* q, const attn_bf16* k_cache,
+                            const attn_bf16* v_cache, const int32_t* block_table,
+                            const int32_t* kv_lens, int num_splits, float* o_partial,
+                            float* lse_partial, int batch, int n_q_heads, int n_kv_heads,
+                            int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                            int max_kv_len, float scale, int window_left, float softcap,
+                            const float* alibi_slopes, unsigned flags, void* stream) {
+  return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_table, kv_lens, num_splits,
+                     o_partial, lse_partial, batch, n_q_heads, n_kv_heads, head_dim, block_size,
+                     max_blocks_per_seq, num_blocks, max_kv_len, scale, stream, false, window_left,
+                     softcap, alibi_slopes, flags);
 }
 
 int attn_decode_append_splitkv(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,

@@ -73,6 +73,11 @@ struct DecodeArgs {
   int window_left = -1;
   float softcap = 0.f;
   const float* alibi_slopes = nullptr;  // (n_q_heads,): adds -slope_h * (kv_len - 1 - j)
+  // Early cache streaming (never with append): kv_lens, the block table and
+  // the cache are read, and the ring filled, before the wait for the previous
+  // grid on the stream; q and the slopes are read and the partials written
+  // after it.
+  int early_cache = 0;
 };
 
 struct CombineArgs {

@@ -140,8 +140,12 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
 
   // Inputs may come from the previous kernel on the stream: wait for it before
   // the first global read; then let the next kernel (the combine) begin its
-  // launch while this grid streams.
-  grid_dep_wait();
+  // launch while this grid streams.  Early cache streaming: the caller has
+  // stated that the previous kernel writes neither kv_lens, the block table
+  // nor the cache, so the wait moves to the reads of q (consumers) and the
+  // first write; the producer fills the ring meanwhile.
+  const bool early = a.early_cache != 0;
+  if (!early) grid_dep_wait();
   grid_dep_launch();
   // ---- this split's token range (split rule: see the C header) ----
   const bool paged = a.block_table != nullptr;
@@ -172,6 +176,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
   float* o_out = a.o_partial + (((size_t)split * a.batch + b) * a.n_q_heads + (size_t)kvh * g) * D;
   float* lse_out = a.lse_partial + ((size_t)split * a.batch + b) * a.n_q_heads + (size_t)kvh * g;
   if (n_tok <= 0) {  // empty split: o = 0, lse = -inf
+    if (early) grid_dep_wait();
     for (int i = threadIdx.x; i < g * D; i += blockDim.x) o_out[i] = 0.f;
     for (int i = threadIdx.x; i < g; i += blockDim.x) lse_out[i] = -INFINITY;
     return;
@@ -320,6 +325,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int rg_row0 = rg * 16;         // its first query row
     uint8_t* sq = smem + L::kQOff;
     // q rows of this kv head's g query heads; rows g .. 16 G - 1 are zero.
+    if (early) grid_dep_wait();  // q (and below, the slopes) may come from the previous grid
     const uint16_t* qsrc = a.q + ((size_t)b * a.n_q_heads + (size_t)kvh * g) * D;
     for (int i = ctid; i < 16 * G * (D / 8); i += 32 * kConsumerWarps) {
       const int r = i / (D / 8), c = i % (D / 8);
@@ -577,8 +583,11 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const Combi
   const int sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
   __shared__ float s_max[kCombineWarps], s_sum[kCombineWarps];
   __shared__ float4 s_o[kCombineWarps][kRowsPerWarp][kVec];
-  grid_dep_wait();    // the partials come from the decode kernel before us
+  // The next kernel may begin its launch at once: it waits for this grid
+  // before it reads what this grid writes or overwrites the partials (a decode
+  // with early cache streaming only fills its ring before that wait).
   grid_dep_launch();
+  grid_dep_wait();    // the partials come from the decode kernel before us
 
   float m = -INFINITY, wsum = 0.f;  // running max / weight sum (natural-log domain)
   float4 acc[kPerLane];

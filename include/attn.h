@@ -209,6 +209,35 @@ int attn_decode_splitkv_ex(const attn_bf16* q, const attn_bf16* k_cache,
                            const float* alibi_slopes, void* stream);
 
 /*
+ * attn_decode_splitkv_ex2 -- attn_decode_splitkv_ex with flags.
+ *
+ * Page: same, section "Decode: a different bottleneck" (the decode is bound
+ * by streaming the cache, so the stream should start as early as possible).
+ *
+ *   flags: 0, or ATTN_DECODE_EARLY_CACHE.  With it, when the call follows
+ *          another kernel on the same stream, the decode grid may begin
+ *          while that kernel is still running (programmatic dependent
+ *          launch): it reads kv_lens and the block table and copies cache
+ *          rows into its shared-memory ring before that kernel has finished,
+ *          and reads q and alibi_slopes and writes o_partial / lse_partial
+ *          only after it.  The CALLER GUARANTEES that the kernel immediately
+ *          before the call on the stream writes none of kv_lens, block_table,
+ *          k_cache and v_cache (for example: a layer's decode right after the
+ *          previous layer's attn_combine, each layer with its own cache).
+ *          Results are the same as without the flag.
+ * Other arguments, limits and errors as attn_decode_splitkv_ex; unknown flag
+ * bits are ATTN_ERR_SHAPE.
+ */
+#define ATTN_DECODE_EARLY_CACHE 1u
+int attn_decode_splitkv_ex2(const attn_bf16* q, const attn_bf16* k_cache,
+                            const attn_bf16* v_cache, const int32_t* block_table,
+                            const int32_t* kv_lens, int num_splits, float* o_partial,
+                            float* lse_partial, int batch, int n_q_heads, int n_kv_heads,
+                            int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                            int max_kv_len, float scale, int window_left, float softcap,
+                            const float* alibi_slopes, unsigned flags, void* stream);
+
+/*
  * attn_decode_append_splitkv -- split-KV single-token decode that first
  * appends each sequence's new key and value to its cache.
  *

@@ -221,3 +221,53 @@ def test_gqa_ratio_above_64_is_refused(dev):
     with pytest.raises(AttnError) as e:
         run_decode(d, dev, 1)
     assert e.value.status == status_codes()["ATTN_ERR_GQA"]
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_early_cache_chain(dev, paged):
+    """Layers chained on one stream, each decode (ATTN_DECODE_EARLY_CACHE)
+    right after the previous layer's combine, each layer with its own cache
+    and query (so the previous kernel writes none of what the decode reads
+    early): every layer's combined result against the oracle, and equal, bit
+    for bit, to the same decode without the flag."""
+    layers = 3
+    if paged:
+        ds = [W.make_decode_paged(3, 8, 2, 128, [3000, 17, 1024], block_size=16, seed=40 + i)
+              for i in range(layers)]
+    else:
+        ds = [W.make_decode_contiguous(2, 8, 2, 128, 3000, seed=40 + i, max_kv_len=3100)
+              for i in range(layers)]
+    S = 7
+    dev_in = []
+    for d in ds:
+        dev_in.append((d.q.to(dev), d.k_cache.to(dev), d.v_cache.to(dev), d.kv_lens.to(dev),
+                       d.block_table.to(dev) if d.block_table is not None else None))
+    B, Hq, D = ds[0].q.shape
+    op = torch.empty((S, B, Hq, D), dtype=torch.float32, device=dev)
+    lp = torch.empty((S, B, Hq), dtype=torch.float32, device=dev)
+    outs = {}
+    for early in (True, False):
+        res = []
+        for i, d in enumerate(ds):
+            q, kc, vc, lens, bt = dev_in[i]
+            attn.decode_splitkv(q, kc, vc, lens, bt, num_splits=S, max_kv_len=d.max_kv_len,
+                                scale=d.scale, o_partial=op, lse_partial=lp, early_cache=early)
+            o, lse = nan_like((B, Hq, D), dev), nan_like((B, Hq), dev)
+            attn.combine(op, lp, out=o, lse=lse)
+            res.append((o, lse))
+        torch.cuda.synchronize()
+        attn.check_device_status()
+        outs[early] = res
+    for i, d in enumerate(ds):
+        o, lse = outs[True][i]
+        o_ref, lse_ref = oracle.decode(d.q, d.k_cache, d.v_cache, d.block_table,
+                                       d.kv_lens.tolist(), d.scale, d.block_size)
+        compare(o, lse, o_ref, lse_ref, f"early chain layer {i} paged={paged}")
+        assert torch.equal(o, outs[False][i][0]) and torch.equal(lse, outs[False][i][1])
+
+
+def test_early_cache_refused_with_append(dev):
+    """The appending decode writes the cache itself: no early streaming there
+    (the C entry points that append take no flags; the binding has none)."""
+    import inspect
+    assert "early_cache" not in inspect.signature(attn.decode_append_splitkv).parameters

@@ -156,6 +156,26 @@ def test_decode_validation(L):
     assert _decode(L, bt=P + 2) == c["ATTN_ERR_ALIGN"]
 
 
+def _decode_ex2(L, flags, **kw):
+    a = dict(q=P, k=P, v=P, bt=P, lens=P, S=4, op=P, lp=P, B=2, hq=8, hkv=2, d=128, bs=16, mb=8,
+             nb=16, maxlen=128, scale=0.1)
+    a.update(kw)
+    return L.attn_decode_splitkv_ex2(a["q"], a["k"], a["v"], a["bt"], a["lens"], a["S"], a["op"],
+                                     a["lp"], a["B"], a["hq"], a["hkv"], a["d"], a["bs"], a["mb"],
+                                     a["nb"], a["maxlen"], a["scale"], -1, 0.0, None, flags, None)
+
+
+def test_decode_flags_validation(L):
+    """Unknown flag bits are refused before anything is launched; the
+    argument checks of attn_decode_splitkv_ex apply with the early flag too."""
+    c = _lib.status_codes()
+    assert _decode_ex2(L, 2) == c["ATTN_ERR_SHAPE"]
+    assert _decode_ex2(L, 0x80000000) == c["ATTN_ERR_SHAPE"]
+    assert _decode_ex2(L, 1, q=None) == c["ATTN_ERR_NULL"]
+    assert _decode_ex2(L, 1, hq=130, hkv=2) == c["ATTN_ERR_GQA"]
+    assert _decode_ex2(L, 1, d=80) == c["ATTN_ERR_HEADDIM"]
+
+
 def _append(L, **kw):
     a = dict(q=P, kn=P, vn=P, k=P, v=P, bt=P, lens=P, S=4, op=P, lp=P, B=2, hq=8, hkv=2, d=128,
              bs=16, mb=8, nb=16, maxlen=128, scale=0.1)
