@@ -674,14 +674,19 @@ def time_variants(args, attn, q, k, v, scale, o, lse, dq, caches, dec, S, op, lp
     lens = dec.kv_lens.to(dev)
     att = sum(min(int(n_), Wl + 1) for n_ in dec.kv_lens.tolist())
     dbytes = att * dec.n_kv * Dd * 2 * 2 + dq.numel() * 2 + Bd * Hqd * (Dd + 1) * 4
+    # The split count for the tokens the window keeps (the policy on the
+    # attended length), not for the whole cache.
+    Sw = attn.decode_num_splits(Bd, dec.n_kv, min(int(dec.kv_lens.max()), Wl + 1))
+    opw = torch.empty((Sw, Bd, Hqd, Dd), dtype=torch.float32, device=dev)
+    lpw = torch.empty((Sw, Bd, Hqd), dtype=torch.float32, device=dev)
     t_dec = timed(lambda i: attn.decode_splitkv(dq, caches[i % len(caches)][0],
                                                 caches[i % len(caches)][1], lens, None,
-                                                num_splits=S, scale=dec.scale, o_partial=op,
-                                                lse_partial=lp, window_left=Wl),
+                                                num_splits=Sw, scale=dec.scale, o_partial=opw,
+                                                lse_partial=lpw, window_left=Wl),
                   before=lambda: torch.sum(sweep, dim=0, out=sweep_out))
     return {"prefill": pre,
             "decode": {"value": round(job_rate(dbytes, n, world, t_dec) / 1e9, 1), "unit": "GB/s",
-                       "window_left": Wl, "bytes_per_launch": dbytes,
+                       "window_left": Wl, "bytes_per_launch": dbytes, "num_splits": Sw,
                        "avg_launch_us": round(t_dec / n * 1e3, 2)}}
 
 
