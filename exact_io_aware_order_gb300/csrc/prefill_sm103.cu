@@ -102,6 +102,8 @@ struct PrefillSmem {
   static constexpr int kQx = kKxNeg + 4096;
   static constexpr int kQxBytes = 256;
   static constexpr int kBar = kKxPos + (XB ? 2 * 4096 + kQSlots * kQxBytes : 0);
+  static_assert(!XB || (kKxNeg == kKxPos + 4096 && kQx + kQSlots * kQxBytes == kBar),
+                "ALiBi operand layout");
   // barriers: q_full/q_empty, k_full/k_empty, v_full/v_empty (one pair per
   // slot), s_full/p_full/pv_done [3], o_full, o_empty, stats_full/stats_empty [2],
   // drain_s, drain_pv

@@ -131,3 +131,17 @@ def test_head_dim_256(dev, B, Hq, Hkv, N, causal):
     o, lse = run_prefill(x, dev)
     o_ref, lse_ref = oracle.prefill(x.q, x.k, x.v, x.scale, causal)
     compare(o, lse, o_ref, lse_ref, f"d=256 B={B} N={N}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_head_dim_256_8192_spiky_sampled(dev, causal):
+    """The benchmarked head_dim-256 shape (N = 8192, 16 / 8 heads) with 1% of
+    the keys x8 (the running max jumps, so O is rescaled part-way): 400
+    sampled rows against the oracle."""
+    x = W.make_prefill(1, 16, 8, 8192, 256, seed=5, spike_frac=0.01, causal=causal)
+    o, lse = run_prefill(x, dev, causal)
+    rng = np.random.default_rng(9)
+    rows = [(0, int(h), int(i)) for h, i in zip(rng.integers(0, 16, 400), rng.integers(0, 8192, 400))]
+    o_ref, lse_ref = oracle.prefill_rows(x.q, x.k, x.v, x.scale, causal, rows)
+    idx = tuple(torch.tensor(c) for c in zip(*rows))
+    compare(o[idx], lse[idx], o_ref, lse_ref, f"d=256 N=8192 spiky causal={causal}")
