@@ -419,16 +419,18 @@ def _seq_bounds(cu_seqlens) -> list:
     return list(zip(cu[:-1], cu[1:]))
 
 
-def prefill_varlen(q, k, v, cu_seqlens, scale: float, causal: bool = True):
+def prefill_varlen(q, k, v, cu_seqlens, scale: float, causal: bool = True,
+                   window_left: int = -1, softcap: float = 0.0, alibi_slopes=None):
     """Prefill of sequences packed end to end (page §"Interaction with
     post-trained models", packed data and variable-length batches: examples
     packed into one sequence must not attend to each other).
 
     q: (n_q, total, d); k, v: (n_kv, total, d); cu_seqlens: (num_seqs + 1,)
     with sequence s occupying rows [cu[s], cu[s+1]).  Each sequence is the
-    plain prefill of :func:`prefill` on its own rows.  Rows past cu[-1] are
-    not part of any sequence and come back as O = 0, LSE = -inf.
-    Returns O (n_q, total, d) and LSE (n_q, total), float64.
+    prefill of :func:`prefill` on its own rows, with the same variants
+    (window, soft cap, ALiBi; positions counted from the sequence's first
+    row).  Rows past cu[-1] are not part of any sequence and come back as
+    O = 0, LSE = -inf.  Returns O (n_q, total, d) and LSE (n_q, total), float64.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     n_q, total, d = q.shape
@@ -437,7 +439,8 @@ def prefill_varlen(q, k, v, cu_seqlens, scale: float, causal: bool = True):
     for a, b in _seq_bounds(cu_seqlens):
         if b == a:
             continue
-        os_, ls_ = prefill(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], scale, causal)
+        os_, ls_ = prefill(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], scale, causal,
+                           window_left=window_left, softcap=softcap, alibi_slopes=alibi_slopes)
         o[:, a:b] = os_[0]
         lse[:, a:b] = ls_[0]
     return o, lse

@@ -488,6 +488,40 @@ def test_varlen_prefill_matches_block_diagonal_mask_and_brute_force():
     assert _pin_varlen() <= TOL
 
 
+def _pin_varlen_variants():
+    """Packed prefill with a window, a soft cap or ALiBi against scalar brute
+    force on each sequence's own rows (positions counted from the sequence's
+    first row); rows past the last sequence stay O = 0, LSE = -inf."""
+    lens = [7, 0, 12, 5]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, nq, nkv, d = int(cu[-1]) + 2, 4, 2, 8
+    rng = np.random.default_rng(23)
+    q = rng.standard_normal((nq, T, d)) * 1.5
+    k = rng.standard_normal((nkv, T, d))
+    v = rng.standard_normal((nkv, T, d))
+    slopes = [2.0 ** (-8.0 * (h + 1) / nq) for h in range(nq)]
+    worst = 0.0
+    for causal, W, cap, sl in [(True, 3, 0.0, None), (False, 4, 0.0, None), (True, -1, 1.3, None),
+                               (False, 2, 0.9, None), (True, -1, 0.0, slopes),
+                               (False, 5, 0.0, slopes)]:
+        o, lse = oracle.prefill_varlen(q, k, v, cu, 0.8, causal, window_left=W, softcap=cap,
+                                       alibi_slopes=sl)
+        for a, b in zip(cu[:-1], cu[1:]):
+            if b == a:
+                continue
+            ob, lb = _brute_prefill(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], 0.8, causal,
+                                    W, cap, sl)
+            worst = max(worst, float(np.abs(ob[0] - o[:, a:b]).max()),
+                        float(np.abs(lb[0] - lse[:, a:b]).max()))
+        if not (np.all(o[:, cu[-1]:] == 0) and np.all(np.isneginf(lse[:, cu[-1]:]))):
+            return math.inf
+    return worst
+
+
+def test_varlen_variants_brute_force():
+    assert _pin_varlen_variants() <= TOL
+
+
 def test_varlen_sampled_rows_match_full():
     lens = [130, 7, 300]
     cu = np.concatenate([[0], np.cumsum(lens)])
@@ -662,7 +696,8 @@ def _pins():
             "closed": (_pin_closed_forms, TOL), "gqa": (_pin_gqa, TOL),
             "combine": (_pin_combine, TOL), "partials": (_pin_partials_bruteforce, TOL),
             "append": (_pin_append, TOL),
-            "varlen": (_pin_varlen, TOL), "variants": (_pin_variants, TOL)}
+            "varlen": (_pin_varlen, TOL), "variants": (_pin_variants, TOL),
+            "varlen_variants": (_pin_varlen_variants, TOL)}
 
 
 def _any_pin_fails():
