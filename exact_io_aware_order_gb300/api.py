@@ -87,8 +87,11 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[f
 def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
                    scale: Optional[float] = None, causal: bool = True,
                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                   stream=None):
-    """Prefill of sequences packed end to end (``attn_prefill_varlen``).
+                   stream=None, window_left: int = -1, softcap: float = 0.0,
+                   alibi_slopes: Optional[torch.Tensor] = None):
+    """Prefill of sequences packed end to end (``attn_prefill_varlen``; with a
+    sliding window, soft-capping or ALiBi slopes, ``attn_prefill_varlen_ex``,
+    positions counted from each sequence's first row).
 
     q: (n_q, total, d) bf16; k, v: (n_kv, total, d) bf16; cu_seqlens:
     (num_seqs + 1,) int32 on the device.  Returns (O (n_q, total, d) fp32,
@@ -111,11 +114,23 @@ def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
         lse = torch.empty((n_q, T), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32, 3)
     _need(lse, "lse", torch.float32, 2)
-    st = lib().attn_prefill_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                   lse.data_ptr(), cu_seqlens.data_ptr(), cu_seqlens.numel() - 1,
-                                   T, n_q, n_kv, d, float(scale), int(bool(causal)),
-                                   _stream(stream))
-    check("attn_prefill_varlen", st)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, T, n_q, n_kv, d, float(scale),
+            int(bool(causal)))
+    if window_left != -1 or softcap != 0.0 or alibi_slopes is not None:
+        al = None
+        if alibi_slopes is not None:
+            _need(alibi_slopes, "alibi_slopes", torch.float32, 1)
+            if alibi_slopes.numel() != n_q:
+                raise ValueError("alibi_slopes must have one slope per query head")
+            al = alibi_slopes.data_ptr()
+        name = "attn_prefill_varlen_ex"
+        st = lib().attn_prefill_varlen_ex(*args, int(window_left), float(softcap), al,
+                                          _stream(stream))
+    else:
+        name = "attn_prefill_varlen"
+        st = lib().attn_prefill_varlen(*args, _stream(stream))
+    check(name, st)
     return out, lse
 
 

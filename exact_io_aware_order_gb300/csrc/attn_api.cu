@@ -229,22 +229,25 @@ int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, 
                       causal, window_left, softcap, alibi_slopes, stream);
 }
 
-int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+namespace {
+
+int prefill_varlen_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
                         float* lse, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
                         int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
-                        void* stream) {
+                        int window_left, float softcap, const float* alibi_slopes, void* stream) {
   if (!q || !k || !v || !o || !lse || !cu_seqlens) return ATTN_ERR_NULL;
   if (num_seqs < 1 || num_seqs > attn::kMaxVarlenSeqs || n_q_heads < 1 || n_kv_heads < 1 ||
       n_q_heads > (1 << 20) || total_tokens < 1 || total_tokens > (1 << 24) ||
-      !valid_scale(scale))
+      !valid_scale(scale) || !valid_variant(window_left, softcap))
     return ATTN_ERR_SHAPE;
+  if (alibi_slopes && softcap > 0.f) return ATTN_ERR_SHAPE;  // not combined
   // work items (at most total/128 + num_seqs query tiles per head) are counted in 32 bits
   if ((long long)n_q_heads * ((total_tokens + 127) / 128 + num_seqs) > 0x7fffffffLL)
     return ATTN_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-      !aligned(lse, 4) || !aligned(cu_seqlens, 4))
+      !aligned(lse, 4) || !aligned(cu_seqlens, 4) || !aligned(alibi_slopes, 4))
     return ATTN_ERR_ALIGN;
   int st = ATTN_OK;
   DeviceState* ds = device_state(&st);
@@ -253,8 +256,31 @@ int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16*
                       causal ? 1 : 0};
   a.cu_seqlens = cu_seqlens;
   a.num_seqs = num_seqs;
+  a.window_left = window_left;
+  a.softcap = softcap;
+  a.alibi_slopes = alibi_slopes;
   if (attn::launch_prefill(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
+}
+
+}  // namespace
+
+int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+                        float* lse, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                        int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
+                        void* stream) {
+  return prefill_varlen_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, n_q_heads,
+                             n_kv_heads, head_dim, scale, causal, -1, 0.f, nullptr, stream);
+}
+
+int attn_prefill_varlen_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+                           float* lse, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                           int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
+                           int window_left, float softcap, const float* alibi_slopes,
+                           void* stream) {
+  return prefill_varlen_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, n_q_heads,
+                             n_kv_heads, head_dim, scale, causal, window_left, softcap,
+                             alibi_slopes, stream);
 }
 
 namespace {

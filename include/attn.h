@@ -141,6 +141,25 @@ int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16*
                         void* stream);
 
 /*
+ * attn_prefill_varlen_ex -- attn_prefill_varlen with the variants of
+ * attn_prefill_ex (sliding window, logit soft-capping, ALiBi).
+ *
+ * Page: same, section "Interaction with post-trained models" (packed batches
+ * and the variants models are trained with).  Each sequence is attended on
+ * its own rows with the variant applied as in attn_prefill_ex, positions i, j
+ * counted from the sequence's first row: the window keeps keys j >= i -
+ * window_left, ALiBi adds -alibi_slopes[h] * |i - j|.
+ *   window_left, softcap, alibi_slopes: as attn_prefill_ex (ALiBi and
+ *          soft-capping together are ATTN_ERR_SHAPE; alibi_slopes 4-byte aligned).
+ * Other arguments, limits and errors as attn_prefill_varlen.
+ */
+int attn_prefill_varlen_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+                           float* lse, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                           int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
+                           int window_left, float softcap, const float* alibi_slopes,
+                           void* stream);
+
+/*
  * attn_decode_num_splits -- the split-count policy for single-token decode.
  *
  * Page: same, section "Decode: a different bottleneck": splitting the key/value

@@ -82,3 +82,39 @@ def test_bad_cu_seqlens_is_reported(dev):
         attn.check_device_status()
     assert e.value.status == status_codes()["ATTN_ERR_DEVICE"]
     attn.check_device_status()                                          # cleared
+
+
+def _slopes(n):
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / n) for h in range(n)], dtype=torch.float32)
+
+
+@pytest.mark.parametrize("lens,hq,hkv,d,causal,variant", [
+    ([300, 0, 129, 1000, 7], 8, 2, 128, True, {"window_left": 100}),
+    ([300, 0, 129, 1000, 7], 8, 2, 128, False, {"window_left": 200}),
+    ([513, 64, 200], 4, 2, 64, True, {"softcap": 30.0}),
+    ([513, 64, 200], 4, 2, 128, False, {"softcap": 20.0, "window_left": 150}),
+    ([700, 90, 33], 8, 4, 128, True, {"alibi": True}),
+    ([700, 90, 33], 8, 4, 128, False, {"alibi": True}),
+    ([400, 129], 4, 2, 256, True, {"alibi": True, "window_left": 90}),
+    ([400, 129, 1], 4, 2, 64, False, {"alibi": True}),
+])
+def test_varlen_variants(dev, lens, hq, hkv, d, causal, variant):
+    """Packed prefill with a sliding window, soft-capping or ALiBi
+    (``attn_prefill_varlen_ex``): every sequence on its own rows, positions
+    from its first row, against the oracle."""
+    x = W.make_prefill_varlen(lens, hq, hkv, d, seed=sum(lens) + d, extra_rows=2, causal=causal)
+    kw = {k: v for k, v in variant.items() if k != "alibi"}
+    okw = dict(kw)
+    if variant.get("alibi"):
+        sl = _slopes(hq)
+        kw["alibi_slopes"] = sl.to(dev)
+        okw["alibi_slopes"] = sl.tolist()
+    n_q, T, dd = x.q.shape
+    o, lse = nan_like((n_q, T, dd), dev), nan_like((n_q, T), dev)
+    attn.prefill_varlen(x.q.to(dev), x.k.to(dev), x.v.to(dev), x.cu_seqlens.to(dev), x.scale,
+                        causal, out=o, lse=lse, **kw)
+    attn.check_device_status()
+    o_ref, lse_ref = oracle.prefill_varlen(x.q, x.k, x.v, x.cu_seqlens, x.scale, causal, **okw)
+    T0 = int(x.cu_seqlens[-1])
+    compare(o[:, :T0], lse[:, :T0], o_ref[:, :T0], lse_ref[:, :T0], f"varlen {lens} {variant}")
+    assert torch.isnan(o[:, T0:]).all() and torch.isnan(lse[:, T0:]).all()

@@ -127,6 +127,26 @@ def test_prefill_varlen_validation(L):
     assert _varlen(L, q=P + 8) == c["ATTN_ERR_ALIGN"]
 
 
+def _varlen_ex(L, w=-1, cap=0.0, al=None, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, cu=P, S=3, T=1000, hq=8, hkv=2, d=128, scale=0.1, causal=1)
+    a.update(kw)
+    return L.attn_prefill_varlen_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu"], a["S"],
+                                    a["T"], a["hq"], a["hkv"], a["d"], a["scale"], a["causal"],
+                                    w, cap, al, None)
+
+
+def test_prefill_varlen_ex_validation(L):
+    """The packed prefill's variant arguments are checked as attn_prefill_ex's."""
+    c = _lib.status_codes()
+    assert _varlen_ex(L, w=-2) == c["ATTN_ERR_SHAPE"]
+    assert _varlen_ex(L, cap=-1.0) == c["ATTN_ERR_SHAPE"]
+    assert _varlen_ex(L, cap=float("nan")) == c["ATTN_ERR_SHAPE"]
+    assert _varlen_ex(L, cap=2.0, al=P) == c["ATTN_ERR_SHAPE"]      # ALiBi with soft-capping
+    assert _varlen_ex(L, al=P + 2) == c["ATTN_ERR_ALIGN"]
+    assert _varlen_ex(L, w=5, cu=None) == c["ATTN_ERR_NULL"]
+    assert _varlen_ex(L, w=5, S=513) == c["ATTN_ERR_SHAPE"]
+
+
 def _decode(L, **kw):
     a = dict(q=P, k=P, v=P, bt=P, lens=P, S=4, op=P, lp=P, B=2, hq=8, hkv=2, d=128, bs=16,
              mb=8, nb=16, maxlen=128, scale=0.1)
