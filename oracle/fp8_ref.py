@@ -34,10 +34,11 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention_ref import _f64, prefill
+from .attention_ref import _f64, _seq_bounds, prefill, prefill_varlen
 
 __all__ = ["E4M3_MAX", "round_e4m3", "hadamard_rotate", "quantize_blocks",
-           "quantize_for_attention", "prefill_fp8"]
+           "quantize_for_attention", "prefill_fp8", "quantize_for_attention_varlen",
+           "prefill_fp8_varlen"]
 
 E4M3_MAX = 448.0
 _BLOCK = 128
@@ -139,3 +140,71 @@ def prefill_fp8(qz: dict, scale: float, causal: bool = True, block: int = _BLOCK
     kd = dequantize(qz["kc"], qz["ks"], block)
     vd = qz["vc"] * np.asarray(qz["vs"], dtype=np.float64)[..., None, None]
     return prefill(qd, kd, vd, scale, causal)
+
+
+def packed_tile_count(cu_seqlens, block: int = _BLOCK) -> list:
+    """Per packed sequence, the first index of its tiles in the scale arrays
+    of :func:`quantize_for_attention_varlen`: sequence s's tile t is column
+    prefix[s] + t, prefix[s] = sum over the earlier sequences of
+    ceil(len / block).  Returns the prefix list (num_seqs + 1 entries)."""
+    prefix = [0]
+    for a, b in _seq_bounds(cu_seqlens):
+        prefix.append(prefix[-1] + -(-(b - a) // block))
+    return prefix
+
+
+def quantize_for_attention_varlen(q, k, v, cu_seqlens, signs=None, block: int = _BLOCK):
+    """The FP8 inputs of a packed prefill: q (n_q, total, d), k, v (n_kv,
+    total, d) with sequence s on rows [cu[s], cu[s+1]).  Q and K (rotated
+    with `signs` first) are quantised per tile of `block` rows of each
+    sequence, tiles starting at the sequence's first row, so that a tile of
+    the attention never straddles two scales; the scale of sequence s's tile
+    t is column prefix[s] + t (:func:`packed_tile_count`) of an array with
+    ceil(total / block) + num_seqs columns (the rest stay 0).  Rows outside
+    every sequence are not quantised (codes 0).  V: one scale per head over
+    all its rows, as in :func:`quantize_for_attention`.
+    Returns dict: qc (n_q, total, d), qs (n_q, width), kc, ks likewise,
+    vc (n_kv, total, d), vs (n_kv,)."""
+    q32 = _f64(q).astype(np.float32)
+    k32 = _f64(k).astype(np.float32)
+    v32 = _f64(v).astype(np.float32)
+    if signs is not None:
+        q32 = hadamard_rotate(q32, signs)
+        k32 = hadamard_rotate(k32, signs)
+    nq, T, d = q32.shape
+    nkv = k32.shape[0]
+    bounds = _seq_bounds(cu_seqlens)
+    width = -(-T // block) + len(bounds)
+    prefix = packed_tile_count(cu_seqlens, block)
+    out = {}
+    for name, x in (("q", q32), ("k", k32)):
+        codes = np.zeros(x.shape, dtype=np.float64)
+        scales = np.zeros((x.shape[0], width), dtype=np.float32)
+        for s_, (a, b) in enumerate(bounds):
+            if b == a:
+                continue
+            c, sc = quantize_blocks(x[:, a:b], block)     # tiles aligned to the sequence start
+            codes[:, a:b] = c
+            scales[:, prefix[s_]:prefix[s_] + sc.shape[1]] = sc
+        out[name + "c"], out[name + "s"] = codes, scales
+    vc, vs = quantize_blocks(v32, T)
+    out["vc"], out["vs"] = vc, vs.reshape(nkv)
+    out["cu"] = [int(x) for x in np.asarray(cu_seqlens).reshape(-1)]
+    return out
+
+
+def prefill_fp8_varlen(qz: dict, scale: float, causal: bool = True, block: int = _BLOCK):
+    """Packed attention (:func:`attention_ref.prefill_varlen`) on the
+    dequantised inputs of :func:`quantize_for_attention_varlen`."""
+    cu = qz["cu"]
+    prefix = packed_tile_count(cu, block)
+    qd = np.zeros(qz["qc"].shape)
+    kd = np.zeros(qz["kc"].shape)
+    for s_, (a, b) in enumerate(_seq_bounds(cu)):
+        if b == a:
+            continue
+        nt = prefix[s_ + 1] - prefix[s_]
+        qd[:, a:b] = dequantize(qz["qc"][:, a:b], qz["qs"][:, prefix[s_]:prefix[s_] + nt], block)
+        kd[:, a:b] = dequantize(qz["kc"][:, a:b], qz["ks"][:, prefix[s_]:prefix[s_] + nt], block)
+    vd = qz["vc"] * np.asarray(qz["vs"], dtype=np.float64)[:, None, None]
+    return prefill_varlen(qd, kd, vd, cu, scale, causal)

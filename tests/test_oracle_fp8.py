@@ -113,3 +113,58 @@ def test_block_and_rotation_lower_the_error():
     naive = score_err(F.quantize_for_attention(q, k, x.v, None, block=512), 512)
     ours = score_err(F.quantize_for_attention(q, k, x.v, signs, block=128), 128)
     assert naive / ours > 1.5, (naive, ours)
+
+
+def test_packed_quantisation_matches_each_sequence_alone():
+    """Packed FP8 inputs: each sequence's codes and scales equal those of the
+    sequence quantised on its own (tiles aligned to its first row), its scales
+    sit at the tile prefix of the earlier sequences, rows outside every
+    sequence stay 0, and V's per-head scale covers all rows."""
+    lens = [130, 0, 16, 257, 5]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1]) + 7
+    g = torch.Generator().manual_seed(31)
+    q = torch.randn(4, T, 64, generator=g).to(torch.bfloat16)
+    k = torch.randn(2, T, 64, generator=g).to(torch.bfloat16)
+    v = torch.randn(2, T, 64, generator=g).to(torch.bfloat16)
+    signs = np.where(np.random.default_rng(3).random(64) < 0.5, -1.0, 1.0).astype(np.float32)
+    qz = F.quantize_for_attention_varlen(q, k, v, cu, signs)
+    prefix = F.packed_tile_count(cu)
+    assert prefix == [0, 2, 2, 3, 6, 7]
+    assert qz["qs"].shape == (4, -(-T // 128) + len(lens))
+    for s_, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        if b == a:
+            continue
+        alone = F.quantize_for_attention(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], signs)
+        nt = prefix[s_ + 1] - prefix[s_]
+        assert np.array_equal(qz["qc"][:, a:b], alone["qc"][0])
+        assert np.array_equal(qz["kc"][:, a:b], alone["kc"][0])
+        assert np.array_equal(qz["qs"][:, prefix[s_]:prefix[s_] + nt], alone["qs"][0])
+        assert np.array_equal(qz["ks"][:, prefix[s_]:prefix[s_] + nt], alone["ks"][0])
+    assert not qz["qc"][:, int(cu[-1]):].any() and not qz["qs"][:, prefix[-1]:].any()
+    whole = F.quantize_for_attention(q[None], k[None], v[None])
+    assert np.array_equal(qz["vc"], whole["vc"][0]) and np.array_equal(qz["vs"], whole["vs"][0])
+
+
+def test_packed_fp8_attention_equals_per_sequence_fp8_attention():
+    """The packed FP8 attention is, sequence by sequence, the FP8 attention of
+    the sequence alone with V's scale of the whole packed tensor."""
+    lens = [40, 0, 97]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(2, T, 16, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, T, 16, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, T, 16, generator=g).to(torch.bfloat16)
+    qz = F.quantize_for_attention_varlen(q, k, v, cu)
+    for causal in (True, False):
+        o, lse = F.prefill_fp8_varlen(qz, 0.25, causal)
+        for a, b in zip(cu[:-1], cu[1:]):
+            if b == a:
+                continue
+            alone = F.quantize_for_attention(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b])
+            alone["vc"] = qz["vc"][None, :, a:b]
+            alone["vs"] = qz["vs"][None]
+            oa, la = F.prefill_fp8(alone, 0.25, causal)
+            assert np.abs(oa[0] - o[:, a:b]).max() <= 1e-12
+            assert np.abs(la[0] - lse[:, a:b]).max() <= 1e-12
