@@ -20,6 +20,8 @@ from .api import (  # noqa: F401
     decode_append,
     quantize_fp8,
     quantize_fp8_qkv,
+    quantize_fp8_varlen,
     prefill_fp8,
+    prefill_fp8_varlen,
 )
 from ._lib import AttnError, lib  # noqa: F401

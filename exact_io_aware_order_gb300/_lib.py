@@ -42,6 +42,9 @@ SIGNATURES = {
                                       + [c_int] * 8 + [c_float, c_int, c_float, c_void_p,
                                                        c_void_p]),
     "attn_prefill_fp8": (c_int, [c_void_p] * 8 + [c_int] * 5 + [c_float, c_int, c_void_p]),
+    "attn_prefill_fp8_varlen": (c_int, [c_void_p] * 9 + [c_int] * 5
+                                + [c_float, c_int, c_void_p]),
+    "attn_quantize_fp8_varlen": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_void_p]),
     "attn_quantize_fp8": (c_int, [c_void_p] * 4 + [c_int] * 5 + [c_void_p]),
     "attn_quantize_fp8_qkv": (c_int, [c_void_p] * 10 + [c_int] * 4 + [c_void_p]),
     "attn_combine": (c_int, [c_void_p, c_void_p] + [c_int] * 4 + [c_void_p, c_void_p, c_void_p]),

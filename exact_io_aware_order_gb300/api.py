@@ -162,6 +162,64 @@ def prefill_fp8(q8: torch.Tensor, k8: torch.Tensor, v8t: torch.Tensor, q_scales:
     return out, lse
 
 
+def prefill_fp8_varlen(q8: torch.Tensor, k8: torch.Tensor, v8t: torch.Tensor,
+                       q_scales: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                       cu_seqlens: torch.Tensor, scale: float, causal: bool = True,
+                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                       stream=None):
+    """Packed prefill on FP8 inputs (``attn_prefill_fp8_varlen``): q8 (n_q,
+    total, 128) and k8 (n_kv, total, 128) from :func:`quantize_fp8_varlen`,
+    v8t (n_kv, 128, total) from :func:`quantize_fp8` (block_rows=0,
+    transpose=True); every non-empty sequence must start at a multiple of 16
+    rows.  Returns (O (n_q, total, 128) fp32, LSE (n_q, total) fp32); rows
+    outside every sequence are left as they were in ``out`` / ``lse``."""
+    for t, name in ((q8, "q8"), (k8, "k8"), (v8t, "v8t")):
+        _need(t, name, torch.uint8, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    n_q, T, d = q8.shape
+    n_kv = k8.shape[0]
+    if k8.shape != (n_kv, T, d) or v8t.shape != (n_kv, d, T):
+        raise ValueError("k8 must be (n_kv, total, d) and v8t (n_kv, d, total)")
+    for t, name in ((q_scales, "q_scales"), (k_scales, "k_scales"), (v_scales, "v_scales")):
+        _need(t, name, torch.float32, t.dim())
+    if out is None:
+        out = torch.empty((n_q, T, d), dtype=torch.float32, device=q8.device)
+    if lse is None:
+        lse = torch.empty((n_q, T), dtype=torch.float32, device=q8.device)
+    st = lib().attn_prefill_fp8_varlen(q8.data_ptr(), k8.data_ptr(), v8t.data_ptr(),
+                                       q_scales.data_ptr(), k_scales.data_ptr(),
+                                       v_scales.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                       cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, T, n_q,
+                                       n_kv, d, float(scale), int(bool(causal)), _stream(stream))
+    check("attn_prefill_fp8_varlen", st)
+    return out, lse
+
+
+def quantize_fp8_varlen(x: torch.Tensor, cu_seqlens: torch.Tensor,
+                        signs: Optional[torch.Tensor] = None, stream=None):
+    """Block quantisation of packed rows (``attn_quantize_fp8_varlen``):
+    x (planes, total, d) bf16; each sequence in tiles of 128 rows from its
+    first row.  Returns (codes uint8 (planes, total, d), scales fp32
+    (planes, ceil(total / 128) + num_seqs)); rows outside every sequence and
+    the columns past the last tile are zero."""
+    _need(x, "x", _BF16, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    planes, T, d = x.shape
+    ns = cu_seqlens.numel() - 1
+    codes = torch.zeros((planes, T, d), dtype=torch.uint8, device=x.device)
+    scales = torch.zeros((planes, -(-T // 128) + ns), dtype=torch.float32, device=x.device)
+    sp = None
+    if signs is not None:
+        _need(signs, "signs", torch.float32, 1)
+        if signs.numel() != d:
+            raise ValueError("signs must have head_dim entries")
+        sp = signs.data_ptr()
+    st = lib().attn_quantize_fp8_varlen(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), sp,
+                                        cu_seqlens.data_ptr(), ns, T, planes, d, _stream(stream))
+    check("attn_quantize_fp8_varlen", st)
+    return codes, scales
+
+
 def quantize_fp8(x: torch.Tensor, signs: Optional[torch.Tensor] = None, block_rows: int = 128,
                  transpose: bool = False, stream=None, codes: Optional[torch.Tensor] = None,
                  scales: Optional[torch.Tensor] = None):

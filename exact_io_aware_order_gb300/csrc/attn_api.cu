@@ -447,6 +447,64 @@ int attn_quantize_fp8(const attn_bf16* x, uint8_t* codes, float* scales, const f
   return ATTN_OK;
 }
 
+int attn_prefill_fp8_varlen(const uint8_t* q, const uint8_t* k, const uint8_t* v_t,
+                            const float* q_scales, const float* k_scales, const float* v_scales,
+                            float* o, float* lse, const int32_t* cu_seqlens, int num_seqs,
+                            int total_tokens, int n_q_heads, int n_kv_heads, int head_dim,
+                            float scale, int causal, void* stream) {
+  if (!q || !k || !v_t || !q_scales || !k_scales || !v_scales || !o || !lse || !cu_seqlens)
+    return ATTN_ERR_NULL;
+  if (num_seqs < 1 || num_seqs > attn::kMaxVarlenSeqs || n_q_heads < 1 || n_kv_heads < 1 ||
+      n_q_heads > (1 << 20) || total_tokens < 16 || total_tokens > (1 << 24) ||
+      total_tokens % 16 != 0 || !valid_scale(scale))
+    return ATTN_ERR_SHAPE;  // v_t rows are total_tokens bytes: a multiple of 16 for the copies
+  if ((long long)n_q_heads * ((total_tokens + 127) / 128 + num_seqs) > 0x7fffffffLL)
+    return ATTN_ERR_SHAPE;
+  if (head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v_t, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(q_scales, 4) || !aligned(k_scales, 4) ||
+      !aligned(v_scales, 4) || !aligned(cu_seqlens, 4))
+    return ATTN_ERR_ALIGN;
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  attn::PrefillArgs a{reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint16_t*>(k),
+                      reinterpret_cast<const uint16_t*>(v_t), o, lse, 1, n_q_heads, n_kv_heads,
+                      total_tokens, head_dim, scale, causal ? 1 : 0};
+  a.cu_seqlens = cu_seqlens;
+  a.num_seqs = num_seqs;
+  a.fp8 = 1;
+  a.q_scales = q_scales;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
+  if (attn::launch_prefill(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+int attn_quantize_fp8_varlen(const attn_bf16* x, uint8_t* codes, float* scales,
+                             const float* signs, const int32_t* cu_seqlens, int num_seqs,
+                             int total_tokens, int planes, int head_dim, void* stream) {
+  if (!x || !codes || !scales || !cu_seqlens) return ATTN_ERR_NULL;
+  if (planes < 1 || planes > 65535 || num_seqs < 1 || num_seqs > attn::kMaxVarlenSeqs ||
+      total_tokens < 1 || total_tokens > (1 << 24))
+    return ATTN_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4) || !aligned(signs, 4) ||
+      !aligned(cu_seqlens, 4))
+    return ATTN_ERR_ALIGN;
+  int st = ATTN_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  attn::QuantArgs a{x, codes, scales, signs, planes, total_tokens, head_dim, 128, 0,
+                    static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim)))};
+  a.cu_seqlens = cu_seqlens;
+  a.num_seqs = num_seqs;
+  a.tiles = (total_tokens + 127) / 128 + num_seqs;
+  if (attn::launch_quantize(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
 int attn_quantize_fp8_qkv(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
                           uint8_t* q_codes, uint8_t* k_codes, uint8_t* v_codes_t,
                           float* q_scales, float* k_scales, float* v_scales, const float* signs,

@@ -97,6 +97,13 @@ struct QuantArgs {
   int block_rows;       // 128: one scale per 128 rows; 0: one scale per plane
   int transpose;
   float inv_sqrt_d;     // float32 value of 1 / sqrt(head_dim)
+  // Packed sequences (block scales only): sequence s is rows [cu[s], cu[s+1]);
+  // its tiles of 128 rows start at its first row and tile t's scale is column
+  // prefix[s] + t of a (planes, tiles) array (prefix: tiles of the earlier
+  // sequences).
+  const int32_t* cu_seqlens = nullptr;
+  int num_seqs = 0;
+  int tiles = 0;        // columns of the scale array: ceil(rows / 128) + num_seqs
 };
 
 // Each returns cudaSuccess or the launch error.  Arguments are already

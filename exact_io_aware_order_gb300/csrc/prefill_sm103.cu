@@ -154,6 +154,7 @@ struct Tile {
   int zk;    // K / V tensor-map plane
   int j0;    // first key tile visited (> 0 only with a sliding window)
   int n;     // key tiles visited (>= 1)
+  int tile0; // FP8 scales: the sequence's first 128-row tile in the scale arrays
 };
 
 // Shared-memory tables of the packed variable-length mode.
@@ -211,6 +212,7 @@ __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const Seq
     t.len = p.seqlen;
     t.zq = bidx * p.n_q_heads + h;
     t.zk = bidx * p.n_kv_heads + kvh;
+    t.tile0 = 0;
     t.n = p.causal ? (qt + 1) * kBM / kBN : (p.seqlen + kBN - 1) / kBN;
   } else {
     // The sequence: the last one whose first item is at or before w (a
@@ -230,6 +232,7 @@ __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const Seq
     t.len = st.len[lo];
     t.zq = h;
     t.zk = h / (p.n_q_heads / p.n_kv_heads);
+    t.tile0 = st.prefix[lo] / p.n_q_heads;  // items per sequence = its tiles x heads
     t.n = p.causal ? (qt + 1) * kBM / kBN : (t.len + kBN - 1) / kBN;
   }
   // A sliding window skips the key tiles left of every row's window: the
@@ -340,7 +343,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // per-sequence item counts (n_q_heads x query tiles).
     if (warp == kEpiWarp0) {
       int carry = 0, prev_end = 0;
-      bool bad = false;
+      bool bad = false, misaligned = false;
       for (int base = 0; base < p.num_seqs; base += 32) {
         const int s = base + lane;
         int a = 0, e = 0;
@@ -352,6 +355,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int lower = lane == 0 ? prev_end : a_prev;  // the previous sequence's end
         int a_c = min(max(a, 0), N), e_c = min(max(e, a_c), N);
         if (s < p.num_seqs && (a != a_c || e != e_c || a < lower || (s == 0 && a != 0))) bad = true;
+        // FP8: V^T's copies take tokens along the innermost coordinate, which
+        // a TMA copy of bytes needs at a multiple of 16: every non-empty
+        // sequence must start there (else the launch does nothing, flagged).
+        if (FP8 && s < p.num_seqs && e_c > a_c && (a_c & 15) != 0) misaligned = true;
         if (s >= p.num_seqs) a_c = e_c = 0;
         const int items = ((e_c - a_c + kBM - 1) / kBM) * p.n_q_heads;
         int incl = items;
@@ -370,6 +377,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       if (lane == 0) item_prefix[0] = 0;
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err_word, kErrSeqLens);
+      if (__any_sync(0xffffffffu, misaligned)) {
+        for (int s = lane; s <= p.num_seqs; s += 32) item_prefix[s] = 0;  // no work, no copies
+        if (lane == 0) atomicOr(p.err_word, kErrSeqLens);
+      }
     }
   }
   if constexpr (XB) {
@@ -637,11 +648,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // FP8: the scores carry the Q block's scale (here) and the K block's
       // (per key tile, below).
       float q_scale = 1.f;
-      if constexpr (FP8) q_scale = p.q_scales[(size_t)t.zq * p.n_q_tiles + t.qrel / kBM];
+      if constexpr (FP8) q_scale = p.q_scales[(size_t)t.zq * p.n_q_tiles + t.tile0 + t.qrel / kBM];
       for (int j = 0; j < t.n; ++j, ++g) {
         const int b = g % kSBuf;
         if constexpr (FP8)
-          sl2 = p.sl2 * q_scale * p.k_scales[(size_t)t.zk * p.n_q_tiles + t.j0 + j];
+          sl2 = p.sl2 * q_scale * p.k_scales[(size_t)t.zk * p.n_q_tiles + t.tile0 + t.j0 + j];
         if (!mbar_wait_warp(bar(kSFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tSm = tmem + (uint32_t)(b * kBN) + lane_base;
@@ -1053,7 +1064,9 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   pp.q_scales = a.q_scales;
   pp.k_scales = a.k_scales;
   pp.v_scales = a.v_scales;
-  pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM;
+  // Padded: query tiles per sequence.  Packed: the columns of the FP8 scale
+  // arrays (every sequence's tiles, at most ceil(total / 128) + num_seqs).
+  pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM + (VARLEN ? a.num_seqs : 0);
   pp.total_tiles = pp.n_q_tiles * a.batch * a.n_q_heads;
   pp.group_planes = a.batch * a.n_q_heads;  // one group: longest first over everything
   {
@@ -1092,8 +1105,9 @@ cudaError_t launch_prefill_cap(const PrefillArgs& a, const LaunchCtx& ctx) {
 
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx) {
   if (a.fp8) {
-    if (a.head_dim != 128 || a.cu_seqlens) return cudaErrorInvalidValue;
-    return launch_prefill_t<128, false, kFp8>(a, ctx);
+    if (a.head_dim != 128) return cudaErrorInvalidValue;
+    return a.cu_seqlens ? launch_prefill_t<128, true, kFp8>(a, ctx)
+                        : launch_prefill_t<128, false, kFp8>(a, ctx);
   }
   const bool varlen = a.cu_seqlens != nullptr;
   if (a.head_dim == 256)

@@ -62,18 +62,19 @@ struct Geom {
   static_assert(E % 2 == 0 && RPL >= 1, "lane geometry");
 };
 
-// The lane's rows (row0w + k RW + lane / LPR, k < RPL; zero past the end),
+// The lane's rows (row0w + k RW + lane / LPR, k < RPL; zero from row_end on),
 // rotated when signs are given: x[k][e] is element E (lane % LPR) + e.
 template <int D, int LPR>
 __device__ __forceinline__ void load_rows(const QuantArgs& a, int plane, int row0w, int lane,
-                                          float (&x)[Geom<D, LPR>::RPL][Geom<D, LPR>::E]) {
+                                          float (&x)[Geom<D, LPR>::RPL][Geom<D, LPR>::E],
+                                          int row_end) {
   using G = Geom<D, LPR>;
   constexpr int E = G::E;
   const int c = lane % LPR;
 #pragma unroll
   for (int k = 0; k < G::RPL; ++k) {
     const int row = row0w + k * G::RW + lane / LPR;
-    if (row < a.rows) {
+    if (row < row_end) {
       const uint16_t* src = a.x + ((size_t)plane * a.rows + row) * D + c * E;
       uint32_t w[E / 2];
       if constexpr (E >= 8) {
@@ -188,7 +189,7 @@ __device__ __forceinline__ float block_amax(const float (&x)[Geom<D, LPR>::RPL][
 template <int D, int LPR>
 __device__ __forceinline__ void store_codes(const QuantArgs& a, int plane, int row0w, int lane,
                                             const float (&x)[Geom<D, LPR>::RPL][Geom<D, LPR>::E],
-                                            float inv) {
+                                            float inv, int row_end) {
   using G = Geom<D, LPR>;
   constexpr int E = G::E;
   const int c = lane % LPR;
@@ -206,7 +207,7 @@ __device__ __forceinline__ void store_codes(const QuantArgs& a, int plane, int r
 #pragma unroll
     for (int k = 0; k < G::RPL; ++k) {
       const int row = row0w + k * G::RW + lane / LPR;
-      if (row >= a.rows) continue;
+      if (row >= row_end) continue;
       uint8_t* dst = a.codes + ((size_t)plane * a.rows + row) * D + c * E;
       uint32_t wd[E / 4];
 #pragma unroll
@@ -254,11 +255,65 @@ __device__ __forceinline__ void quantize_block(const QuantArgs& a, int plane, in
   const int lane = threadIdx.x & 31;
   const int row0w = blk * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
   float x[G::RPL][G::E];
-  load_rows<D, LPR>(a, plane, row0w, lane, x);
+  load_rows<D, LPR>(a, plane, row0w, lane, x, a.rows);
   float amax = block_amax<D, LPR>(x, red);
   if (amax == 0.f) amax = 1.f;
   if (threadIdx.x == 0) a.scales[(size_t)plane * nblk + blk] = __fdiv_rn(amax, kE4M3Max);
-  store_codes<D, LPR>(a, plane, row0w, lane, x, __fdiv_rn(kE4M3Max, amax));
+  store_codes<D, LPR>(a, plane, row0w, lane, x, __fdiv_rn(kE4M3Max, amax), a.rows);
+}
+
+// Packed sequences: CTA (T, plane) quantises tile T of the list of every
+// sequence's 128-row tiles (tiles start at their sequence's first row), its
+// scale at column T.  One warp first reads cu_seqlens, clamps each sequence
+// into [0, rows] as the packed prefill does, and scans the tile counts.
+template <int D>
+__global__ void __launch_bounds__(kThreads) packed_block_kernel(const QuantArgs a) {
+  using G = Geom<D, 4>;
+  __shared__ float red[kWarps];
+  __shared__ int seq_start[kMaxVarlenSeqs], seq_end[kMaxVarlenSeqs], prefix[kMaxVarlenSeqs + 1];
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int base = 0; base < a.num_seqs; base += 32) {
+      const int s = base + lane;
+      int st = 0, en = 0;
+      if (s < a.num_seqs) {
+        st = min(max(a.cu_seqlens[s], 0), a.rows);
+        en = min(max(a.cu_seqlens[s + 1], st), a.rows);
+      }
+      int incl = (en - st + kBlockRows - 1) / kBlockRows;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (s < a.num_seqs) {
+        seq_start[s] = st;
+        seq_end[s] = en;
+        prefix[s + 1] = carry + incl;
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  __syncthreads();
+  const int T = blockIdx.x, plane = blockIdx.y;
+  if (T >= prefix[a.num_seqs]) return;  // beyond the last tile
+  int lo = 0, hi = a.num_seqs - 1;       // the last sequence whose tiles start at or before T
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= T) lo = mid; else hi = mid - 1;
+  }
+  const int r0 = seq_start[lo] + (T - prefix[lo]) * kBlockRows;
+  const int r1 = min(r0 + kBlockRows, seq_end[lo]);
+  const int lane = threadIdx.x & 31;
+  const int row0w = r0 + (threadIdx.x >> 5) * kWarpRows;
+  float x[G::RPL][G::E];
+  load_rows<D, 4>(a, plane, row0w, lane, x, r1);
+  float amax = block_amax<D, 4>(x, red);
+  if (amax == 0.f) amax = 1.f;
+  if (threadIdx.x == 0) a.scales[(size_t)plane * a.tiles + T] = __fdiv_rn(amax, kE4M3Max);
+  store_codes<D, 4>(a, plane, row0w, lane, x, __fdiv_rn(kE4M3Max, amax), r1);
 }
 
 template <int D, int LPR>
@@ -276,7 +331,7 @@ __device__ __forceinline__ void plane_amax_block(const QuantArgs& a, int plane, 
   const int lane = threadIdx.x & 31;
   const int row0w = blk * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
   float x[G::RPL][G::E];
-  load_rows<D, 4>(a, plane, row0w, lane, x);
+  load_rows<D, 4>(a, plane, row0w, lane, x, a.rows);
   const float amax = block_amax<D, 4>(x, red);
   if (threadIdx.x == 0)
     atomicMax(reinterpret_cast<unsigned int*>(a.scales) + plane, __float_as_uint(amax));
@@ -313,10 +368,10 @@ __global__ void __launch_bounds__(kThreads) plane_codes_kernel(const QuantArgs a
   const int plane = blockIdx.y, lane = threadIdx.x & 31;
   const int row0w = blockIdx.x * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
   float x[G::RPL][G::E];
-  load_rows<D, LPR>(a, plane, row0w, lane, x);
+  load_rows<D, LPR>(a, plane, row0w, lane, x, a.rows);
   float amax = __uint_as_float(reinterpret_cast<const unsigned int*>(a.scales)[plane]);
   if (amax == 0.f) amax = 1.f;
-  store_codes<D, LPR>(a, plane, row0w, lane, x, __fdiv_rn(kE4M3Max, amax));
+  store_codes<D, LPR>(a, plane, row0w, lane, x, __fdiv_rn(kE4M3Max, amax), a.rows);
 }
 
 // Pass 3: amax -> scale, in place.
@@ -345,6 +400,11 @@ cudaError_t launch_quantize_t(const QuantArgs& a, const LaunchCtx& ctx) {
 
 template <int D>
 cudaError_t launch_quantize_d(const QuantArgs& a, const LaunchCtx& ctx) {
+  if (a.cu_seqlens) {
+    packed_block_kernel<D><<<dim3((unsigned)a.tiles, (unsigned)a.planes), kThreads, 0,
+                             ctx.stream>>>(a);
+    return cudaGetLastError();
+  }
   return a.transpose ? launch_quantize_t<D, 32>(a, ctx) : launch_quantize_t<D, 4>(a, ctx);
 }
 

@@ -392,6 +392,58 @@ int attn_quantize_fp8_qkv(const attn_bf16* q, const attn_bf16* k, const attn_bf1
                           int planes_q, int planes_kv, int rows, int head_dim, void* stream);
 
 /*
+ * attn_quantize_fp8_varlen -- attn_quantize_fp8 with block scales for
+ * sequences packed end to end (the Q and K of attn_prefill_fp8_varlen).
+ *
+ * Page: same, section "Interaction with post-trained models" (packed batches;
+ * FP8 block quantisation).  Each sequence is cut into tiles of 128 rows
+ * starting at its first row, so that no attention tile straddles two scales;
+ * tile t of sequence s gets the scale in column prefix(s) + t, prefix(s) the
+ * number of tiles of the sequences before it.
+ *   x      : (planes, total_tokens, head_dim) bf16, 16-byte aligned
+ *   codes  : (planes, total_tokens, head_dim) e4m3 output, 16-byte aligned; rows
+ *            outside every sequence are not written
+ *   scales : (planes, ceil(total_tokens / 128) + num_seqs) fp32 output, the
+ *            columns past the last tile not written
+ *   signs  : as attn_quantize_fp8 (NULL: no rotation)
+ *   cu_seqlens, num_seqs: as attn_prefill_varlen (clamped the same way)
+ * V takes one scale per head: attn_quantize_fp8 with block_rows 0 and
+ * transpose 1 over the packed rows.
+ * Limits: head_dim in {64, 128}; 1 <= num_seqs <= 512; 1 <= total_tokens <= 2^24.
+ * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _ALIGN, _ARCH, _LAUNCH.
+ */
+int attn_quantize_fp8_varlen(const attn_bf16* x, uint8_t* codes, float* scales,
+                             const float* signs, const int32_t* cu_seqlens, int num_seqs,
+                             int total_tokens, int planes, int head_dim, void* stream);
+
+/*
+ * attn_prefill_fp8_varlen -- attn_prefill_fp8 over sequences packed end to
+ * end (attn_prefill_varlen's layout and rules).
+ *
+ * Page: same, sections "Interaction with post-trained models" (packed batches,
+ * FP8) and "Prefill: tiles, loop order and the tensor cores".
+ *   q, k     : (n_q_heads / n_kv_heads, total_tokens, 128) e4m3 from
+ *              attn_quantize_fp8_varlen (the same signs for both)
+ *   v_t      : (n_kv_heads, 128, total_tokens) e4m3 from attn_quantize_fp8
+ *              (block_rows 0, transpose 1)
+ *   q_scales, k_scales: (planes, ceil(total_tokens / 128) + num_seqs) fp32
+ *   v_scales : (n_kv_heads,) fp32
+ *   o, lse, cu_seqlens, num_seqs, scale, causal: as attn_prefill_varlen
+ * V^T is copied with the tokens along the innermost coordinate, so EVERY
+ * NON-EMPTY SEQUENCE MUST START AT A MULTIPLE OF 16 ROWS: otherwise nothing
+ * is computed and the launch is flagged (ATTN_ERR_DEVICE from
+ * attn_check_device_status), as for a cu_seqlens that breaks its rule.
+ * Limits: head_dim 128; total_tokens a multiple of 16 (16 .. 2^24); the other
+ * limits of attn_prefill_varlen.
+ * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
+ */
+int attn_prefill_fp8_varlen(const uint8_t* q, const uint8_t* k, const uint8_t* v_t,
+                            const float* q_scales, const float* k_scales, const float* v_scales,
+                            float* o, float* lse, const int32_t* cu_seqlens, int num_seqs,
+                            int total_tokens, int n_q_heads, int n_kv_heads, int head_dim,
+                            float scale, int causal, void* stream);
+
+/*
  * attn_combine -- merge per-split partial results by their LSE weights.
  *
  * Page: same, section "The online softmax, with every symbol defined" (the

@@ -2,6 +2,8 @@
 (oracle/fp8_ref.py): the quantiser's e4m3 codes and scales bit for bit
 (rotated or not, per block or per plane, row-major or transposed)."""
 
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -181,3 +183,90 @@ def test_fp8_block_quantisation_and_rotation_lower_the_error(dev):
         errs[name] = np.sqrt(np.mean((o.double().cpu().numpy() - o_exact) ** 2))
     attn.check_device_status()
     assert errs["naive"] / errs["block+rotation"] > 1.5, errs
+
+
+def test_packed_quantizer_bit_exact(dev):
+    """attn_quantize_fp8_varlen: codes and scales of packed rows equal the
+    oracle's bit for bit (tiles from each sequence's first row; scale columns
+    at the tile prefix); rows outside every sequence and unused columns stay
+    zero."""
+    lens = [130, 0, 16, 257, 5]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1]) + 9
+    g = torch.Generator().manual_seed(12)
+    for d, rot in ((128, True), (64, False)):
+        x = torch.randn(3, T, d, generator=g).to(torch.bfloat16)
+        signs = signs_for(d, 4) if rot else None
+        sg = torch.from_numpy(signs).to(dev) if rot else None
+        codes, scales = attn.quantize_fp8_varlen(x.to(dev), torch.from_numpy(cu).to(dev), sg)
+        attn.check_device_status()
+        ref = F.quantize_for_attention_varlen(x, x[:1], x[:1], cu, signs)
+        assert np.array_equal(e4m3_values(codes), ref["qc"])
+        assert np.array_equal(scales.cpu().numpy(), ref["qs"])
+
+
+def packed_sigma(qz, scale, causal):
+    """p_rounding_sigma sequence by sequence (each with its own tiles' scales)."""
+    prefix = F.packed_tile_count(qz["cu"])
+    sig = np.zeros(qz["qc"].shape)
+    for s_, (a, b) in enumerate(zip(qz["cu"][:-1], qz["cu"][1:])):
+        if b == a:
+            continue
+        nt = prefix[s_ + 1] - prefix[s_]
+        one = {"qc": qz["qc"][None, :, a:b], "qs": qz["qs"][None, :, prefix[s_]:prefix[s_] + nt],
+               "kc": qz["kc"][None, :, a:b], "ks": qz["ks"][None, :, prefix[s_]:prefix[s_] + nt],
+               "vc": qz["vc"][None, :, a:b], "vs": qz["vs"][None]}
+        sig[:, a:b] = p_rounding_sigma(one, scale, causal)[0]
+    return sig
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,causal", [([256, 0, 48, 144, 37], 8, 2, True),
+                                                ([512, 16, 160], 4, 4, False),
+                                                ([32, 1000], 4, 1, True)])
+def test_prefill_fp8_varlen_parity(dev, lens, Hq, Hkv, causal):
+    """Packed FP8 prefill (every sequence starting at a multiple of 16 rows)
+    against the oracle's packed FP8 attention: LSE within 1e-3, O within the
+    P-rounding bound, rows past the last sequence untouched."""
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = -(-int(cu[-1]) // 16) * 16 + 16
+    g = torch.Generator().manual_seed(sum(lens) + Hq)
+    q = torch.randn(Hq, T, 128, generator=g).to(torch.bfloat16)
+    k = torch.randn(Hkv, T, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(Hkv, T, 128, generator=g).to(torch.bfloat16)
+    signs = signs_for(128, 21)
+    sg = torch.from_numpy(signs).to(dev)
+    cud = torch.from_numpy(cu).to(dev)
+    q8, qs = attn.quantize_fp8_varlen(q.to(dev), cud, sg)
+    k8, ks = attn.quantize_fp8_varlen(k.to(dev), cud, sg)
+    v8t, vs = attn.quantize_fp8(v.to(dev), None, block_rows=0, transpose=True)
+    scale = 1.0 / math.sqrt(128)
+    o = torch.full((Hq, T, 128), float("nan"), device=dev)
+    lse = torch.full((Hq, T), float("nan"), device=dev)
+    attn.prefill_fp8_varlen(q8, k8, v8t, qs, ks, vs, cud, scale, causal, out=o, lse=lse)
+    attn.check_device_status()
+    qz = F.quantize_for_attention_varlen(q, k, v, cu, signs)
+    o_ref, lse_ref = F.prefill_fp8_varlen(qz, scale, causal)
+    T0 = int(cu[-1])
+    lerr = np.abs(lse[:, :T0].double().cpu().numpy() - lse_ref[:, :T0]).max()
+    assert lerr <= 1e-3, lerr
+    sig = packed_sigma(qz, scale, causal)[:, :T0]
+    z = np.abs(o[:, :T0].double().cpu().numpy() - o_ref[:, :T0]) / (sig + 1e-6)
+    assert z.max() <= 6.0 and z.mean() <= 1.0, (z.max(), z.mean())
+    assert torch.isnan(o[:, T0:]).all() and torch.isnan(lse[:, T0:]).all()
+
+
+def test_prefill_fp8_varlen_misaligned_start_is_refused(dev):
+    """A non-empty sequence that starts off a multiple of 16 rows: the kernel
+    checks cu_seqlens before any copy, computes nothing and flags the launch."""
+    T, d = 64, 128
+    cu = torch.tensor([0, 20, 64], dtype=torch.int32, device=dev)   # second sequence at row 20
+    z8 = torch.zeros((2, T, d), dtype=torch.uint8, device=dev)
+    v8t = torch.zeros((2, d, T), dtype=torch.uint8, device=dev)
+    sc = torch.ones((2, 3), dtype=torch.float32, device=dev)
+    vs = torch.ones(2, dtype=torch.float32, device=dev)
+    o = torch.full((2, T, d), float("nan"), device=dev)
+    lse = torch.full((2, T), float("nan"), device=dev)
+    attn.prefill_fp8_varlen(z8, z8, v8t, sc, sc, vs, cu, 0.1, True, out=o, lse=lse)
+    with pytest.raises(attn.AttnError):
+        attn.check_device_status()
+    assert torch.isnan(o).all() and torch.isnan(lse).all()

@@ -301,3 +301,43 @@ def test_header_documents_each_entry_point():
         block = text[:text.index(name + "(")]
         doc = block[block.rindex("/*"):]
         assert "Page:" in doc or "section" in doc, f"{name} lacks its citation"
+
+
+def _fp8_varlen(L, **kw):
+    a = dict(q=P, k=P, v=P, qs=P, ks=P, vs=P, o=P, lse=P, cu=P, S=3, T=512, hq=8, hkv=2, d=128,
+             scale=0.1, causal=1)
+    a.update(kw)
+    return L.attn_prefill_fp8_varlen(a["q"], a["k"], a["v"], a["qs"], a["ks"], a["vs"], a["o"],
+                                     a["lse"], a["cu"], a["S"], a["T"], a["hq"], a["hkv"], a["d"],
+                                     a["scale"], a["causal"], None)
+
+
+def test_prefill_fp8_varlen_validation(L):
+    c = _lib.status_codes()
+    assert _fp8_varlen(L, cu=None) == c["ATTN_ERR_NULL"]
+    assert _fp8_varlen(L, vs=None) == c["ATTN_ERR_NULL"]
+    assert _fp8_varlen(L, T=500) == c["ATTN_ERR_SHAPE"]      # V^T rows must be 16-byte multiples
+    assert _fp8_varlen(L, T=0) == c["ATTN_ERR_SHAPE"]
+    assert _fp8_varlen(L, S=513) == c["ATTN_ERR_SHAPE"]
+    assert _fp8_varlen(L, d=64) == c["ATTN_ERR_HEADDIM"]
+    assert _fp8_varlen(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
+    assert _fp8_varlen(L, cu=P + 2) == c["ATTN_ERR_ALIGN"]
+    assert _fp8_varlen(L, v=P + 8) == c["ATTN_ERR_ALIGN"]
+
+
+def _quant_varlen(L, **kw):
+    a = dict(x=P, codes=P, scales=P, signs=None, cu=P, S=3, T=500, planes=4, d=128)
+    a.update(kw)
+    return L.attn_quantize_fp8_varlen(a["x"], a["codes"], a["scales"], a["signs"], a["cu"], a["S"],
+                                      a["T"], a["planes"], a["d"], None)
+
+
+def test_quantize_fp8_varlen_validation(L):
+    c = _lib.status_codes()
+    assert _quant_varlen(L, cu=None) == c["ATTN_ERR_NULL"]
+    assert _quant_varlen(L, S=0) == c["ATTN_ERR_SHAPE"]
+    assert _quant_varlen(L, planes=0) == c["ATTN_ERR_SHAPE"]
+    assert _quant_varlen(L, T=(1 << 24) + 1) == c["ATTN_ERR_SHAPE"]
+    assert _quant_varlen(L, d=256) == c["ATTN_ERR_HEADDIM"]
+    assert _quant_varlen(L, codes=P + 8) == c["ATTN_ERR_ALIGN"]
+    assert _quant_varlen(L, signs=P + 2) == c["ATTN_ERR_ALIGN"]
