@@ -916,11 +916,53 @@ def time_prefill_varlen(args, attn, W, dist, dev):
     (tot,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
     world = dist.get_world_size() if dist is not None else 1
     avg_ms = tot / n
-    return {"value": round(job_rate(flops, n, world, tot) / 1e12, 2), "unit": "TFLOP/s",
-            "roofline": {"bound": "tensor", "achieved": round(flops / (avg_ms * 1e-3) / 1e12, 2),
-                         "unit": "TFLOP/s", "kernel": "prefill_kernel<128, packed>",
-                         "flops_per_launch": flops, "avg_launch_ms": round(avg_ms, 4)},
-            "num_seqs": len(lens), "total_tokens": T, "launches": n}
+    res = {"value": round(job_rate(flops, n, world, tot) / 1e12, 2), "unit": "TFLOP/s",
+           "roofline": {"bound": "tensor", "achieved": round(flops / (avg_ms * 1e-3) / 1e12, 2),
+                        "unit": "TFLOP/s", "kernel": "prefill_kernel<128, packed>",
+                        "flops_per_launch": flops, "avg_launch_ms": round(avg_ms, 4)},
+           "num_seqs": len(lens), "total_tokens": T, "launches": n}
+    del q, k, v, o, lse
+    # Packed FP8 on the same prompts with their lengths rounded up to 16 rows
+    # (the FP8 path needs every sequence to start at a multiple of 16), beside
+    # the bf16 packed kernel on those lengths; the quantiser runs outside the
+    # events.
+    lens16 = [-(-n_ // 16) * 16 for n_ in lens]
+    x16 = W.make_prefill_varlen(lens16, n_q, x.k.shape[0], d, seed=0)
+    q, k, v, cu = x16.q.to(dev), x16.k.to(dev), x16.v.to(dev), x16.cu_seqlens.to(dev)
+    T16 = x16.q.shape[1]
+    o = torch.empty((n_q, T16, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((n_q, T16), dtype=torch.float32, device=dev)
+    g = torch.Generator().manual_seed(11)
+    signs = torch.where(torch.rand(d, generator=g) < 0.5, -1.0, 1.0).to(torch.float32).to(dev)
+    q8, qs = attn.quantize_fp8_varlen(q, cu, signs)
+    k8, ks = attn.quantize_fp8_varlen(k, cu, signs)
+    v8t, vs = attn.quantize_fp8(v, None, block_rows=0, transpose=True)
+    flops16 = sum(prefill_flops(n_q, n_, d) for n_ in lens16)
+    t16 = {}
+    for name, fn in (("bf16", lambda: attn.prefill_varlen(q, k, v, cu, x16.scale, True, out=o,
+                                                           lse=lse)),
+                     ("fp8", lambda: attn.prefill_fp8_varlen(q8, k8, v8t, qs, ks, vs, cu,
+                                                              x16.scale, True, out=o, lse=lse))):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        torch.cuda.synchronize()
+        for i in range(n):
+            evs[i][0].record()
+            fn()
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        (t16[name],) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
+    attn.check_device_status()
+    res["fp8_packed"] = {
+        "value": round(job_rate(flops16, n, world, t16["fp8"]) / 1e12, 2), "unit": "TFLOP/s",
+        "bf16_same_lengths": round(job_rate(flops16, n, world, t16["bf16"]) / 1e12, 2),
+        "speedup_over_bf16": round(t16["bf16"] / t16["fp8"], 3),
+        "lengths": "the packed prompts' lengths rounded up to multiples of 16",
+        "kernel": "prefill_kernel<128, packed, fp8>", "flops_per_launch": flops16,
+        "avg_launch_ms": round(t16["fp8"] / n, 4)}
+    return res
 
 
 def time_decode_append(args, attn, dq, caches, dec, S, op, lp, sweep, sweep_out, dist, dev):
