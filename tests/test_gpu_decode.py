@@ -271,3 +271,51 @@ def test_early_cache_refused_with_append(dev):
     (the C entry points that append take no flags; the binding has none)."""
     import inspect
     assert "early_cache" not in inspect.signature(attn.decode_append_splitkv).parameters
+
+
+@pytest.mark.parametrize("paged,D,Hq,Hkv,variant", [
+    (True, 128, 8, 2, {"window_left": 200}),
+    (False, 128, 8, 2, {"alibi": True}),
+    (True, 256, 4, 2, {"softcap": 30.0}),
+    (False, 64, 4, 4, {}),
+    (True, 128, 32, 1, {}),                    # 32 query heads per kv head (row-group teams)
+])
+def test_early_cache_chain_variants(dev, paged, D, Hq, Hkv, variant):
+    """Early cache streaming with the decode variants, head_dims and GQA
+    ratios: two chained layers equal, bit for bit, the same decodes without
+    the flag, and match the oracle."""
+    import oracle as O
+    kw = {k: v for k, v in variant.items() if k != "alibi"}
+    okw = dict(kw)
+    if variant.get("alibi"):
+        sl = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)], dtype=torch.float32)
+        kw["alibi_slopes"] = sl.to(dev)
+        okw["alibi_slopes"] = sl.tolist()
+    if paged:
+        ds = [W.make_decode_paged(2, Hq, Hkv, D, [900, 33], block_size=16, seed=60 + i)
+              for i in range(2)]
+    else:
+        ds = [W.make_decode_contiguous(2, Hq, Hkv, D, 700, seed=60 + i) for i in range(2)]
+    S = 5
+    B = ds[0].q.shape[0]
+    outs = {}
+    for early in (True, False):
+        res = []
+        for d in ds:
+            op = torch.empty((S, B, Hq, D), dtype=torch.float32, device=dev)
+            lp = torch.empty((S, B, Hq), dtype=torch.float32, device=dev)
+            bt = d.block_table.to(dev) if d.block_table is not None else None
+            attn.decode_splitkv(d.q.to(dev), d.k_cache.to(dev), d.v_cache.to(dev),
+                                d.kv_lens.to(dev), bt, num_splits=S, max_kv_len=d.max_kv_len,
+                                scale=d.scale, o_partial=op, lse_partial=lp, early_cache=early,
+                                **kw)
+            res.append(attn.combine(op, lp))
+        torch.cuda.synchronize()
+        attn.check_device_status()
+        outs[early] = res
+    for i, d in enumerate(ds):
+        o, lse = outs[True][i]
+        assert torch.equal(o, outs[False][i][0]) and torch.equal(lse, outs[False][i][1])
+        o_ref, lse_ref = O.decode(d.q, d.k_cache, d.v_cache, d.block_table, d.kv_lens.tolist(),
+                                  d.scale, d.block_size, **okw)
+        compare(o, lse, o_ref, lse_ref, f"early variants {variant} paged={paged} D={D}")
