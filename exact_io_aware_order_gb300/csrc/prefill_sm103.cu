@@ -275,6 +275,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   constexpr int kBN = key_tile<D>();
   // ALiBi at head_dim <= 128: the tensor core adds the bias's per-key part.
   constexpr bool XB = VARIANT == kWindowAlibi && D <= 128;
+  // Edge tiles: masked per 32-column chunk, with a warp-wide test first (the
+  // warp's rows are consecutive, so its smallest last-allowed column is its
+  // first row's and its largest first-allowed column its last row's; a chunk
+  // inside both for every row needs no per-score test), or per score.  Which
+  // form schedules better depends on the flavour: measured, the chunked form
+  // is faster in the plain and soft-capping flavours, slower in the others.
+  constexpr bool kChunkMask = (VARIANT == kPlain && !VARLEN) || VARIANT == kWindowCap;
   using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2, XB>;
   constexpr int RQ = L::kQSlots, RK = L::kKSlots, RV = L::kVSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -713,15 +720,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           if (hi_edge || lo_edge) {
             const int lim = !hi_edge ? kBN : p.causal ? (q_row - kv0) : (t.len - 1 - kv0);
             const int lo = lo_edge ? (q_row - p.window_left - kv0) : -1;  // first allowed column
+            if constexpr (kChunkMask) {
+              const int lim_w = (hi_edge && p.causal) ? lim - lane : lim;
+              const int lo_w = lo_edge ? lo + (31 - lane) : -1;
 #pragma unroll
-            for (int c = 0; c < kBN; ++c)
-              if (c > lim || c < lo) s[c] = VARIANT == kWindowCap ? INFINITY : -INFINITY;
+              for (int ch = 0; ch < kBN / 32; ++ch)
+                if (ch * 32 + 31 > lim_w || ch * 32 < lo_w)
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) {
+                    const int c = ch * 32 + i;
+                    if (c > lim || c < lo) s[c] = VARIANT == kWindowCap ? INFINITY : -INFINITY;
+                  }
+            } else {
+#pragma unroll
+              for (int c = 0; c < kBN; ++c)
+                if (c > lim || c < lo) s[c] = VARIANT == kWindowCap ? INFINITY : -INFINITY;
+            }
           }
         } else if (p.causal ? (kv0 + kBN - 1 > q0) : (kv0 + kBN > t.len)) {
           const int lim = p.causal ? (q_row - kv0) : (t.len - 1 - kv0);  // last allowed column
+          if constexpr (kChunkMask) {
+            const int lim_w = p.causal ? lim - lane : lim;  // the warp's first row's limit
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c > lim) s[c] = -INFINITY;
+            for (int ch = 0; ch < kBN / 32; ++ch)
+              if (ch * 32 + 31 > lim_w)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (ch * 32 + i > lim) s[ch * 32 + i] = -INFINITY;
+          } else {
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+              if (c > lim) s[c] = -INFINITY;
+          }
         }
         // Row max: eight independent chains of 3-input max, then a small tree
         // (soft-capping: the smallest r, the largest tanh = 1 - 2 r).
@@ -753,6 +783,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // keep the stale max for both l and O (exact either way).
         float corr = 1.f;
         bool rescale_o = false;
+        if constexpr (VARIANT != kPlain && VARIANT != kFp8) {
+          // A row that has seen no allowed key yet (its keys so far were all
+          // outside its window) has O = 0 and l = 0: it takes the new max
+          // without a rescale.
+          if (m == -INFINITY) m = m_new;
+        }
         if (j == 0) {
           m = m_new;  // O is written fresh by the item's first P V product
         } else if (__any_sync(0xffffffffu, m_new - m > kRescaleThreshold)) {
