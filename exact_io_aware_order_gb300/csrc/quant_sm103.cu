@@ -8,13 +8,16 @@
 // Sylvester Hadamard matrix; the same rotation for Q and K leaves Q K^T
 // unchanged), then quantise blocks of rows to e4m3 with scale amax / 448.
 //
-// Layout of the work: one CTA per block of 128 rows of a plane, eight warps
-// of 16 rows each.  Within a warp, LPR consecutive lanes share a row: lane l
-// holds elements [E c, E c + E) (c = l % LPR, E = d / LPR) of the rows
-// l / LPR + k (32 / LPR), k = 0, 1, ...  Row-major output takes LPR = 4 (32
-// elements per lane at head_dim 128: 64-byte loads, five of the rotation's
-// seven butterfly stages inside the lane); the transposed output takes
-// LPR = 32, so that a lane holds 16 consecutive rows of each of its
+// Layout of the work: blocks of 128 rows of a plane, eight warps of 16 rows
+// each.  Within a warp, LPR consecutive lanes share a row: lane l holds
+// elements [E c, E c + E) (c = l % LPR, E = d / LPR) of the rows l / LPR +
+// k (32 / LPR), k = 0, 1, ...  Row-major codes take LPR = 2 (64 elements per
+// lane at head_dim 128: six of the rotation's seven butterfly stages inside
+// the lane), in persistent CTAs that walk a list of blocks and stage each in
+// shared memory with asynchronous copies, two blocks ahead, so that loads
+// overlap the arithmetic.  Packed sequences take LPR = 4 with direct loads.
+// The transposed output takes LPR = 32, one CTA per block, so that a lane
+// holds 16 consecutive rows of each of its
 // elements and writes them as 16 consecutive bytes.  Butterflies with
 // stride h < E pair elements inside a lane; larger strides pair lane l with
 // lane l ^ (h / E) through a shuffle, the lower index taking u + v and the
@@ -30,6 +33,7 @@
 // them per plane with an integer atomic max on the float's bits (amax >= 0,
 // where the bit patterns order like the values); the second pass quantises;
 // a last, one-thread-per-plane pass turns the stored amax into the scale.
+#include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -62,12 +66,13 @@ struct Geom {
   static_assert(E % 2 == 0 && RPL >= 1, "lane geometry");
 };
 
-// The lane's rows (row0w + k RW + lane / LPR, k < RPL; zero from row_end on),
-// rotated when signs are given: x[k][e] is element E (lane % LPR) + e.
+// The lane's rows (row0w + k RW + lane / LPR, k < RPL) as raw bf16 pairs from
+// global memory: w[k][i] holds elements E c + 2 i and E c + 2 i + 1 (c = lane %
+// LPR) of row k; zero from row_end on.
 template <int D, int LPR>
-__device__ __forceinline__ void load_rows(const QuantArgs& a, int plane, int row0w, int lane,
-                                          float (&x)[Geom<D, LPR>::RPL][Geom<D, LPR>::E],
-                                          int row_end) {
+__device__ __forceinline__ void load_raw(const QuantArgs& a, int plane, int row0w, int lane,
+                                         uint32_t (&w)[Geom<D, LPR>::RPL][Geom<D, LPR>::E / 2],
+                                         int row_end) {
   using G = Geom<D, LPR>;
   constexpr int E = G::E;
   const int c = lane % LPR;
@@ -76,37 +81,123 @@ __device__ __forceinline__ void load_rows(const QuantArgs& a, int plane, int row
     const int row = row0w + k * G::RW + lane / LPR;
     if (row < row_end) {
       const uint16_t* src = a.x + ((size_t)plane * a.rows + row) * D + c * E;
-      uint32_t w[E / 2];
       if constexpr (E >= 8) {
 #pragma unroll
         for (int i = 0; i < E / 8; ++i) {
           const uint4 u = reinterpret_cast<const uint4*>(src)[i];
-          w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+          w[k][4 * i] = u.x; w[k][4 * i + 1] = u.y; w[k][4 * i + 2] = u.z; w[k][4 * i + 3] = u.w;
         }
       } else if constexpr (E == 4) {
         const uint2 u = *reinterpret_cast<const uint2*>(src);
-        w[0] = u.x; w[1] = u.y;
+        w[k][0] = u.x; w[k][1] = u.y;
       } else {
-        w[0] = *reinterpret_cast<const uint32_t*>(src);
-      }
-#pragma unroll
-      for (int i = 0; i < E / 2; ++i) {
-        x[k][2 * i] = __uint_as_float(w[i] << 16);
-        x[k][2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        w[k][0] = *reinterpret_cast<const uint32_t*>(src);
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) x[k][e] = 0.f;
+      for (int i = 0; i < E / 2; ++i) w[k][i] = 0u;
     }
   }
-  if (a.signs == nullptr) return;
+}
+
+// Blocks of 128 rows staged in shared memory: row r of the block takes D * 2
+// bytes, its 16-byte chunk j stored at chunk stage_chunk<D>(r, j) of the row.
+// The reads below give two lanes to a row, so the eight lanes of a 16-byte
+// load phase read the same chunk slot of four consecutive rows, which would
+// all fall on the same banks (rows are 128 or 256 bytes); the permutation
+// (an XOR within each group of eight chunks, by the row and the half of the
+// row) puts those eight reads, and the copies' writes, on distinct banks.
+template <int D>
+__device__ __forceinline__ int stage_chunk(int r, int j) {
+  if constexpr (D == 128)
+    return j ^ (((r & 3) << 1) | (j >> 3));
+  else
+    return j ^ (r & 3);
+}
+
+template <int D>
+constexpr int stage_bytes() {
+  return kBlockRows * D * 2;
+}
+
+// Copies rows [r0, r1) of a plane into a stage (r0 is the block's first row),
+// one 16-byte chunk per thread and step; the caller commits the group.
+template <int D>
+__device__ __forceinline__ void stage_rows(const QuantArgs& a, int plane, int r0, int r1,
+                                           uint32_t sbuf) {
+  constexpr int kCpr = D * 2 / 16;  // chunks per row
+  const int n = (r1 - r0) * kCpr;
+  const uint16_t* src = a.x + ((size_t)plane * a.rows + r0) * D;
+  for (int idx = threadIdx.x; idx < n; idx += kThreads) {
+    const int r = idx / kCpr, j = idx % kCpr;
+    cp_async16(sbuf + (uint32_t)(r * D * 2 + stage_chunk<D>(r, j) * 16),
+               src + (size_t)r * D + j * 8);
+  }
+}
+
+// load_raw's result (two lanes per row) from a staged block; lrow0w is
+// row0w's row within the block.
+template <int D>
+__device__ __forceinline__ void load_raw_staged(const uint8_t* stage, int lrow0w, int row0w,
+                                                int lane,
+                                                uint32_t (&w)[Geom<D, 2>::RPL][Geom<D, 2>::E / 2],
+                                                int row_end) {
+  using G = Geom<D, 2>;
+  constexpr int E = G::E;  // whole chunks: 64 or 32 elements
+  const int c = lane % 2;
+#pragma unroll
+  for (int k = 0; k < G::RPL; ++k) {
+    const int dr = k * G::RW + lane / 2;
+    if (row0w + dr < row_end) {
+      const int lr = lrow0w + dr;
+      const uint8_t* rowp = stage + lr * (D * 2);
+#pragma unroll
+      for (int i = 0; i < E / 8; ++i) {
+        const uint4 u =
+            *reinterpret_cast<const uint4*>(rowp + stage_chunk<D>(lr, c * (E / 8) + i) * 16);
+        w[k][4 * i] = u.x; w[k][4 * i + 1] = u.y; w[k][4 * i + 2] = u.z; w[k][4 * i + 3] = u.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) w[k][i] = 0u;
+    }
+  }
+}
+
+// The rows as float32, rotated when signs (global memory, or shared memory
+// and 16-byte aligned when SMEM_SIGNS) are given: x[k][e] is element
+// E (lane % LPR) + e of the lane's row k.
+template <int D, int LPR, bool SMEM_SIGNS = false>
+__device__ __forceinline__ void rotate_rows(const float* signs, float inv_sqrt_d, int lane,
+                                            const uint32_t (&w)[Geom<D, LPR>::RPL][Geom<D, LPR>::E / 2],
+                                            float (&x)[Geom<D, LPR>::RPL][Geom<D, LPR>::E]) {
+  using G = Geom<D, LPR>;
+  constexpr int E = G::E;
+  const int c = lane % LPR;
+#pragma unroll
+  for (int k = 0; k < G::RPL; ++k)
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      x[k][2 * i] = __uint_as_float(w[k][i] << 16);
+      x[k][2 * i + 1] = __uint_as_float(w[k][i] & 0xffff0000u);
+    }
+  if (signs == nullptr) return;
   // Pairs of elements go through the packed two-lane float32 instructions
   // (each half rounded on its own, as the scalar operation).
   float2 sg[E / 2];
+  if constexpr (SMEM_SIGNS) {
 #pragma unroll
-  for (int e = 0; e < E; e += 2) sg[e / 2] = make_float2(a.signs[c * E + e], a.signs[c * E + e + 1]);
+    for (int e = 0; e < E; e += 4) {
+      const float4 t = *reinterpret_cast<const float4*>(signs + c * E + e);
+      sg[e / 2] = make_float2(t.x, t.y);
+      sg[e / 2 + 1] = make_float2(t.z, t.w);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; e += 2) sg[e / 2] = make_float2(signs[c * E + e], signs[c * E + e + 1]);
+  }
   const float2 neg1 = make_float2(-1.f, -1.f);
-  const float2 isd = make_float2(a.inv_sqrt_d, a.inv_sqrt_d);
+  const float2 isd = make_float2(inv_sqrt_d, inv_sqrt_d);
 #pragma unroll
   for (int k = 0; k < G::RPL; ++k) {
     float* xr = x[k];
@@ -162,6 +253,17 @@ __device__ __forceinline__ void load_rows(const QuantArgs& a, int plane, int row
       xr[e + 1] = t.y;
     }
   }
+}
+
+// The lane's rows from global memory, rotated when signs are given (zero from
+// row_end on).
+template <int D, int LPR>
+__device__ __forceinline__ void load_rows(const QuantArgs& a, int plane, int row0w, int lane,
+                                          float (&x)[Geom<D, LPR>::RPL][Geom<D, LPR>::E],
+                                          int row_end) {
+  uint32_t w[Geom<D, LPR>::RPL][Geom<D, LPR>::E / 2];
+  load_raw<D, LPR>(a, plane, row0w, lane, w, row_end);
+  rotate_rows<D, LPR>(a.signs, a.inv_sqrt_d, lane, w, x);
 }
 
 // Largest |x| over the CTA's rows (every thread gets it).
@@ -322,43 +424,112 @@ __global__ void __launch_bounds__(kThreads) quantize_block_kernel(const QuantArg
   quantize_block<D, LPR>(a, blockIdx.y, blockIdx.x, gridDim.x, red);
 }
 
-// One scale per plane, pass 1: block `blk`'s amax folded into the plane's,
-// kept as float bits in scales[plane] (zeroed before the launch).
-template <int D>
-__device__ __forceinline__ void plane_amax_block(const QuantArgs& a, int plane, int blk,
-                                                 float* red) {
-  using G = Geom<D, 4>;
-  const int lane = threadIdx.x & 31;
-  const int row0w = blk * kBlockRows + (threadIdx.x >> 5) * kWarpRows;
-  float x[G::RPL][G::E];
-  load_rows<D, 4>(a, plane, row0w, lane, x, a.rows);
-  const float amax = block_amax<D, 4>(x, red);
-  if (threadIdx.x == 0)
-    atomicMax(reinterpret_cast<unsigned int*>(a.scales) + plane, __float_as_uint(amax));
-}
+// Blocks of 128 rows with two lanes per row, staged through shared memory:
+// block b of the concatenated lists (q's blocks, then k's: codes and one
+// scale per block; then v's: the block's amax folded into its plane's).  Any
+// list may be empty (planes = 0).  Persistent CTAs walk the blocks b =
+// blockIdx.x + i gridDim.x; kStages stages keep the copies of the next
+// blocks in flight while a block is rotated, reduced and written.
+constexpr int kStages = 3;
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) plane_amax_kernel(const QuantArgs a) {
+__global__ void __launch_bounds__(kThreads, 2)
+staged_blocks_kernel(const __grid_constant__ QuantArgs q, const __grid_constant__ QuantArgs k,
+                     const __grid_constant__ QuantArgs v, int nblk) {
+  using G = Geom<D, 2>;
+  extern __shared__ __align__(16) uint8_t stage_mem[];
   __shared__ float red[kWarps];
-  plane_amax_block<D>(a, blockIdx.y, blockIdx.x, red);
-}
-
-// Q and K with block scales and V's plane amax in one launch: CTA b takes
-// block b of the concatenated lists (Q blocks, then K blocks, then V blocks).
-template <int D>
-__global__ void __launch_bounds__(kThreads) qkv_pass1_kernel(const QuantArgs q, const QuantArgs k,
-                                                             const QuantArgs v, int nblk) {
-  __shared__ float red[kWarps];
-  int b = blockIdx.x;
-  const int nq = q.planes * nblk, nk = k.planes * nblk;
-  if (b < nq) {
-    quantize_block<D, 4>(q, b / nblk, b % nblk, nblk, red);
-  } else if ((b -= nq) < nk) {
-    quantize_block<D, 4>(k, b / nblk, b % nblk, nblk, red);
-  } else {
-    b -= nk;
-    plane_amax_block<D>(v, b / nblk, b % nblk, red);
+  __shared__ __align__(16) float sgn[3][D];  // each list's signs, read 4 at a time
+  const uint32_t sbase = smem_u32(stage_mem);
+  for (int i = threadIdx.x; i < 3 * D; i += kThreads) {
+    const float* g = i < D ? q.signs : (i < 2 * D ? k.signs : v.signs);
+    sgn[i / D][i % D] = g != nullptr ? g[i % D] : 0.f;
+  }  // visible after the first __syncthreads below
+  // 64-bit list indices: planes x blocks may exceed the int range
+  const long long nq = (long long)q.planes * nblk, nk = (long long)k.planes * nblk;
+  const long long total = nq + nk + (long long)v.planes * nblk;
+  const long long step = gridDim.x;
+  // list index -> (tensor, plane, block)
+  auto locate = [&](long long b, int& which, int& plane, int& blk) {
+    which = b < nq ? 0 : (b < nq + nk ? 1 : 2);
+    const long long lb = which == 0 ? b : (which == 1 ? b - nq : b - nq - nk);
+    plane = static_cast<int>(lb / nblk);
+    blk = static_cast<int>(lb - (long long)plane * nblk);
+  };
+  auto args = [&](int which) -> const QuantArgs& { return which == 0 ? q : (which == 1 ? k : v); };
+  auto issue = [&](long long b, int stage) {
+    int which, plane, blk;
+    locate(b, which, plane, blk);
+    const QuantArgs& a = args(which);
+    const int r0 = blk * kBlockRows;
+    stage_rows<D>(a, plane, r0, min(r0 + kBlockRows, a.rows),
+                  sbase + (uint32_t)(stage * stage_bytes<D>()));
+  };
+#pragma unroll 1
+  for (int s = 0; s < kStages - 1; ++s) {
+    const long long b = blockIdx.x + s * step;
+    if (b < total) issue(b, s);
+    cp_async_commit();  // possibly empty: every thread counts the same groups
   }
+  const int lane = threadIdx.x & 31;
+  const int lrow0w = (threadIdx.x >> 5) * kWarpRows;
+  int it = 0;
+#pragma unroll 1
+  for (long long b = blockIdx.x; b < total; ++it, b += step) {
+    cp_async_wait<kStages - 2>();  // this thread's copies of block b have landed
+    __syncthreads();               // everyone's have; the stage read in the last round is free
+    {
+      const long long bn = b + (kStages - 1) * step;
+      if (bn < total) issue(bn, (it + kStages - 1) % kStages);
+      cp_async_commit();
+    }
+    int which, plane, blk;
+    locate(b, which, plane, blk);
+    const QuantArgs& a = args(which);
+    const int row0w = blk * kBlockRows + lrow0w;
+    float x[G::RPL][G::E];
+    {
+      uint32_t w[G::RPL][G::E / 2];
+      load_raw_staged<D>(stage_mem + (it % kStages) * stage_bytes<D>(), lrow0w, row0w, lane, w,
+                         a.rows);
+      if (a.signs != nullptr)
+        rotate_rows<D, 2, true>(sgn[which], a.inv_sqrt_d, lane, w, x);
+      else
+        rotate_rows<D, 2>(nullptr, a.inv_sqrt_d, lane, w, x);
+    }
+    float amax = block_amax<D, 2>(x, red);
+    if (which == 2) {
+      if (threadIdx.x == 0)
+        atomicMax(reinterpret_cast<unsigned int*>(a.scales) + plane, __float_as_uint(amax));
+    } else {
+      if (amax == 0.f) amax = 1.f;
+      if (threadIdx.x == 0) a.scales[(size_t)plane * nblk + blk] = __fdiv_rn(amax, kE4M3Max);
+      store_codes<D, 2>(a, plane, row0w, lane, x, __fdiv_rn(kE4M3Max, amax), a.rows);
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// Launches staged_blocks_kernel over the three lists: at most two CTAs per SM
+// (the stages take 3 x 32 KB at head_dim 128), no more CTAs than blocks.
+template <int D>
+cudaError_t launch_staged(const QuantArgs& q, const QuantArgs& k, const QuantArgs& v, int nblk,
+                          const LaunchCtx& ctx) {
+  constexpr int kSmem = kStages * stage_bytes<D>();
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(staged_blocks_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = true;
+  }
+  const long long total = (long long)(q.planes + k.planes + v.planes) * nblk;
+  const int grid = (int)std::min<long long>(total, 2LL * std::max(ctx.num_sms, 1));
+  if (grid < 1) return cudaSuccess;
+  staged_blocks_kernel<D><<<grid, kThreads, kSmem, ctx.stream>>>(q, k, v, nblk);
+  return cudaGetLastError();
 }
 
 // Pass 2: the codes, from the plane's amax.
@@ -385,14 +556,22 @@ __global__ void plane_scale_kernel(const QuantArgs a) {
 
 template <int D, int LPR>
 cudaError_t launch_quantize_t(const QuantArgs& a, const LaunchCtx& ctx) {
-  const dim3 grid((unsigned)((a.rows + kBlockRows - 1) / kBlockRows), (unsigned)a.planes);
+  const int nblk = (a.rows + kBlockRows - 1) / kBlockRows;
+  const dim3 grid((unsigned)nblk, (unsigned)a.planes);
+  QuantArgs none = a;
+  none.planes = 0;
   if (a.block_rows > 0) {
-    quantize_block_kernel<D, LPR><<<grid, kThreads, 0, ctx.stream>>>(a);
-    return cudaGetLastError();
+    if constexpr (LPR == 4) {
+      return launch_staged<D>(a, none, none, nblk, ctx);
+    } else {
+      quantize_block_kernel<D, LPR><<<grid, kThreads, 0, ctx.stream>>>(a);
+      return cudaGetLastError();
+    }
   }
   cudaError_t e = cudaMemsetAsync(a.scales, 0, (size_t)a.planes * sizeof(float), ctx.stream);
   if (e != cudaSuccess) return e;
-  plane_amax_kernel<D><<<grid, kThreads, 0, ctx.stream>>>(a);
+  e = launch_staged<D>(none, none, a, nblk, ctx);
+  if (e != cudaSuccess) return e;
   plane_codes_kernel<D, LPR><<<grid, kThreads, 0, ctx.stream>>>(a);
   plane_scale_kernel<<<(a.planes + 127) / 128, 128, 0, ctx.stream>>>(a);
   return cudaGetLastError();
@@ -417,8 +596,8 @@ cudaError_t launch_quantize_qkv_d(const QuantArgs& q, const QuantArgs& k, const 
   const int nblk = (q.rows + kBlockRows - 1) / kBlockRows;
   cudaError_t e = cudaMemsetAsync(v.scales, 0, (size_t)v.planes * sizeof(float), ctx.stream);
   if (e != cudaSuccess) return e;
-  const unsigned blocks = (unsigned)((q.planes + k.planes + v.planes) * nblk);
-  qkv_pass1_kernel<D><<<blocks, kThreads, 0, ctx.stream>>>(q, k, v, nblk);
+  e = launch_staged<D>(q, k, v, nblk, ctx);
+  if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)nblk, (unsigned)v.planes);
   plane_codes_kernel<D, 32><<<grid, kThreads, 0, ctx.stream>>>(v);
   plane_scale_kernel<<<(v.planes + 127) / 128, 128, 0, ctx.stream>>>(v);

@@ -31,6 +31,9 @@ def signs_for(d, seed):
     (3, 4100, 64, True, 0, True),      # per-plane scale, transposed, rows not a multiple of 16
     (2, 8192, 128, True, 0, True),
     (5, 17, 128, True, 128, True),     # one partial block
+    (40, 2000, 128, True, 128, False),  # more blocks than CTAs (staged, several per CTA), ragged ends
+    (48, 1100, 64, False, 128, False),  # the same at head_dim 64
+    (24, 3000, 64, True, 0, True),      # per-plane amax over many staged blocks
 ])
 def test_quantizer_bit_exact(dev, planes, rows, d, rot, block, transpose):
     g = torch.Generator().manual_seed(rows + d)
