@@ -1099,6 +1099,13 @@ def run_e2e(args, x, dec, dev, world, dist):
         dist.barrier()
     pre = pipelined(n, p_in, p_out, pf)
     attn.check_device_status()
+    # The same loop with the kernels alone and with the copies alone: whether
+    # this box overlapped the copies with the kernels (their sum against the
+    # whole) is part of the end-to-end number.
+    parts = {"kernels_only": pipelined(n, [], [], pf) / n,
+             "copies_only": pipelined(n, p_in, p_out, lambda b: None) / n,
+             "whole": pre / n}
+    parts = {k_: round(v_, 3) for k_, v_ in parts.items()}
     # the results are the library's: the last step's output equals a direct call
     ref_o, _ = attn.prefill(q[0], k[0], v[0], x.scale, True)
     assert torch.equal(ho[(n - 1) & 1], ref_o.cpu()), "pipelined e2e result differs"
@@ -1138,6 +1145,7 @@ def run_e2e(args, x, dec, dev, world, dist):
                     "in and O/LSE copied out every step",
             "pipelining": "3 streams (H2D / kernels / D2H), 2 buffer sets",
             "copy_rates_alone": copy_rates,
+            "ms_per_step_parts": parts,
             "decode_value": round(job_rate(decode_bytes(dec), n, world, dcd) / 1e9, 1),
             "decode_unit": "GB/s (end to end, cache copied from host each step)",
             "decode_h2d_bytes_per_step": h2d_dec, "decode_d2h_bytes_per_step": d2h_dec}
