@@ -474,8 +474,9 @@ int attn_check_device_status(void* stream);
 /*
  * attn_set_wait_timeout_ns -- upper bound, in nanoseconds, on any single
  * kernel-side wait (default 2e9).  Values below 1000 are raised to 1000.
- * Host-side setting read at each launch; not thread-safe against concurrent
- * launches.  Returns the previous value.
+ * One process-wide value, read and written atomically: each launch takes the
+ * value current when it is issued, so a change made from another thread
+ * applies to the launches issued after it.  Returns the previous value.
  */
 uint64_t attn_set_wait_timeout_ns(uint64_t timeout_ns);
 
