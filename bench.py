@@ -1146,6 +1146,9 @@ def run_e2e(args, x, dec, dev, world, dist):
             "pipelining": "3 streams (H2D / kernels / D2H), 2 buffer sets",
             "copy_rates_alone": copy_rates,
             "ms_per_step_parts": parts,
+            # settings that decide whether streams can overlap (unset: the defaults)
+            "stream_env": {k_: os.environ.get(k_) for k_ in ("CUDA_DEVICE_MAX_CONNECTIONS",
+                                                              "CUDA_LAUNCH_BLOCKING")},
             "decode_value": round(job_rate(decode_bytes(dec), n, world, dcd) / 1e9, 1),
             "decode_unit": "GB/s (end to end, cache copied from host each step)",
             "decode_h2d_bytes_per_step": h2d_dec, "decode_d2h_bytes_per_step": d2h_dec}
