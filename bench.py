@@ -379,6 +379,10 @@ def run_gb300(args, rank: int, world: int, dist):
         d256["decode"]["roofline"]["frac"] = round(
             d256["decode"]["roofline"]["achieved"] / peaks["hbm_gbs"], 4)
         result["prefill_d256"] = d256
+        d64 = time_d64(args, attn, W, dist, dev)
+        d64["roofline"]["peak"] = bf
+        d64["roofline"]["frac"] = round(d64["roofline"]["achieved"] / bf, 4)
+        result["prefill_d64"] = d64
     if "variants" in legs:
         var = time_variants(args, attn, qq, kq, vq, xq.scale, oq, lq, dq, dec_caches, dec, S, op,
                             lp, sweep, sweep_out, dist, dev)
@@ -776,6 +780,42 @@ def time_d256(args, attn, W, dist, dev):
                                   "avg_launch_us": round(avg_d * 1e3, 2),
                                   "decode_plus_combine_avg_us": round(statistics.mean(both_ms) * 1e3, 2)}}
     return res
+
+
+def time_d64(args, attn, W, dist, dev):
+    """Causal prefill with head_dim 64 (N = 8192, 32 query / 8 kv heads).
+    Against head_dim 128 the products per key tile halve while the softmax's
+    cost per score stays, so the softmax sets the rate."""
+    import torch
+
+    Hq, Hkv, N, D = 32, 8, 8192, 64
+    x = W.make_prefill(1, Hq, Hkv, N, D, seed=0)
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    o = torch.empty((1, Hq, N, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((1, Hq, N), dtype=torch.float32, device=dev)
+    flops = prefill_flops(Hq, N, D)
+    n = max(3, min(args.steps, 100))
+    for _ in range(3):
+        attn.prefill(q, k, v, x.scale, True, out=o, lse=lse)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    for i in range(n):
+        evs[i][0].record()
+        attn.prefill(q, k, v, x.scale, True, out=o, lse=lse)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    attn.check_device_status()
+    (tot,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
+    world = dist.get_world_size() if dist is not None else 1
+    avg_ms = tot / n
+    return {"value": round(job_rate(flops, n, world, tot) / 1e12, 2), "unit": "TFLOP/s",
+            "shape": "N=8192, 32/8 heads, head_dim 64, causal",
+            "roofline": {"bound": "tensor", "achieved": round(flops / (avg_ms * 1e-3) / 1e12, 2),
+                         "unit": "TFLOP/s", "kernel": "prefill_kernel<64>",
+                         "flops_per_launch": flops, "avg_launch_ms": round(avg_ms, 4)}}
 
 
 def time_fp8(args, attn, x, q, k, v, o, lse, dist, dev):
@@ -1256,7 +1296,8 @@ def main():
                     help="only the timed headline steps (for profiling runs)")
     ap.add_argument("--legs", type=str, default="all",
                     help="comma list of the legs after the timed steps to run: configs, append, "
-                         "varlen, fp8, d256, variants (for profiling runs); default all")
+                         "varlen, fp8, d256 (head_dims 256 and 64), variants (for profiling "
+                         "runs); default all")
     ap.add_argument("--seqlen", type=int, default=HEADLINE["prefill"]["seqlen"],
                     help="prefill length of the timed step (profiling runs use a smaller one)")
     ap.add_argument("--layers", type=int, default=HEADLINE["prefill"]["layers"],
