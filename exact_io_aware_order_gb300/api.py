@@ -139,9 +139,9 @@ def prefill_fp8(q8: torch.Tensor, k8: torch.Tensor, v8t: torch.Tensor, q_scales:
                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                 stream=None):
     """Prefill on FP8 inputs from :func:`quantize_fp8` (``attn_prefill_fp8``):
-    q8 (B, n_q, N, 128) and k8 (B, n_kv, N, 128) e4m3 codes (uint8), v8t
-    (B, n_kv, 128, N) transposed, their block / head scales.  Returns
-    (O (B, n_q, N, 128) fp32, LSE (B, n_q, N) fp32)."""
+    q8 (B, n_q, N, d) and k8 (B, n_kv, N, d) e4m3 codes (uint8), v8t
+    (B, n_kv, d, N) transposed, their block / head scales; d is 64 or 128.
+    Returns (O (B, n_q, N, d) fp32, LSE (B, n_q, N) fp32)."""
     for t, name in ((q8, "q8"), (k8, "k8"), (v8t, "v8t")):
         _need(t, name, torch.uint8, 4)
     B, n_q, N, d = q8.shape
@@ -168,11 +168,12 @@ def prefill_fp8_varlen(q8: torch.Tensor, k8: torch.Tensor, v8t: torch.Tensor,
                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                        stream=None):
     """Packed prefill on FP8 inputs (``attn_prefill_fp8_varlen``): q8 (n_q,
-    total, 128) and k8 (n_kv, total, 128) from :func:`quantize_fp8_varlen`,
-    v8t (n_kv, 128, total) from :func:`quantize_fp8` (block_rows=0,
-    transpose=True); every non-empty sequence must start at a multiple of 16
-    rows.  Returns (O (n_q, total, 128) fp32, LSE (n_q, total) fp32); rows
-    outside every sequence are left as they were in ``out`` / ``lse``."""
+    total, d) and k8 (n_kv, total, d) from :func:`quantize_fp8_varlen`, v8t
+    (n_kv, d, total) from :func:`quantize_fp8` (block_rows=0,
+    transpose=True), d 64 or 128; every non-empty sequence must start at a
+    multiple of 16 rows.  Returns (O (n_q, total, d) fp32, LSE (n_q, total)
+    fp32); rows outside every sequence are left as they were in ``out`` /
+    ``lse``."""
     for t, name in ((q8, "q8"), (k8, "k8"), (v8t, "v8t")):
         _need(t, name, torch.uint8, 3)
     _need(cu_seqlens, "cu_seqlens", torch.int32, 1)

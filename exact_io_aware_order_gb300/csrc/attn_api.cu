@@ -409,7 +409,7 @@ int attn_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_t* v_t,
       seqlen % 16 != 0 || (long long)batch * n_q_heads > (1LL << 20) || !valid_scale(scale))
     return ATTN_ERR_SHAPE;  // v_t rows are seqlen bytes: a multiple of 16 for the copies
   if ((long long)batch * n_q_heads * ((seqlen + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-  if (head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v_t, 16) || !aligned(o, 16) ||
       !aligned(lse, 4) || !aligned(q_scales, 4) || !aligned(k_scales, 4) || !aligned(v_scales, 4))
@@ -460,7 +460,7 @@ int attn_prefill_fp8_varlen(const uint8_t* q, const uint8_t* k, const uint8_t* v
     return ATTN_ERR_SHAPE;  // v_t rows are total_tokens bytes: a multiple of 16 for the copies
   if ((long long)n_q_heads * ((total_tokens + 127) / 128 + num_seqs) > 0x7fffffffLL)
     return ATTN_ERR_SHAPE;
-  if (head_dim != 128) return ATTN_ERR_HEADDIM;
+  if (head_dim != 64 && head_dim != 128) return ATTN_ERR_HEADDIM;
   if (n_q_heads % n_kv_heads != 0) return ATTN_ERR_GQA;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v_t, 16) || !aligned(o, 16) ||
       !aligned(lse, 4) || !aligned(q_scales, 4) || !aligned(k_scales, 4) ||

@@ -140,6 +140,10 @@ struct PrefillParams {
   const float* q_scales;
   const float* k_scales;
   const float* v_scales;
+  // FP8: O's columns (head_dim 64 or 128).  At 64 the copies of Q, K and V^T
+  // fill the tiles' second half with zeros, which add nothing to S and give
+  // zero columns 64..127 of O; only the first 64 are stored.
+  int d_out;
   uint32_t* err_word;
   uint64_t timeout_ns;
 };
@@ -915,10 +919,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int in_seq = t.len - (t.qrel + quarter * 32);
       // O is read kEC columns at a time (all of it for head_dim <= 128).
       constexpr int kEC = D > 128 ? 128 : D;
+      const int d_out = FP8 ? p.d_out : D;  // O's columns in memory
       auto store_cols = [&](const uint32_t (&acc)[kEC / 32][32], int col0, float inv_l) {
         if (!VARLEN || in_seq >= 32) {
 #pragma unroll
           for (int c = 0; c < kEC / 32; ++c) {
+            if (FP8 && col0 + c * 32 >= d_out) break;
             if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
             __syncwarp();
 #pragma unroll
@@ -936,16 +942,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
           }
         } else if (lane < in_seq) {
-          float* orow = p.o + ((size_t)t.zq * N + (size_t)(row0 + lane)) * D + col0;
+          float* orow = p.o + ((size_t)t.zq * N + (size_t)(row0 + lane)) * d_out + col0;
 #pragma unroll
           for (int c = 0; c < kEC / 32; ++c)
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
+              if (FP8 && col0 + c * 32 >= d_out) continue;
               reinterpret_cast<float4*>(orow + c * 32)[i] =
                   make_float4(__uint_as_float(acc[c][4 * i]) * inv_l,
                               __uint_as_float(acc[c][4 * i + 1]) * inv_l,
                               __uint_as_float(acc[c][4 * i + 2]) * inv_l,
                               __uint_as_float(acc[c][4 * i + 3]) * inv_l);
+            }
         }
       };
       float2 ml;
@@ -1073,18 +1081,21 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
     if (dev < 64) configured[dev] = true;
   }
   CUtensorMap mq, mk, mv, mo;
+  // FP8 at head_dim 64 runs this 128-column kernel: the maps cover the real
+  // 64 columns (rows of V^T) and the 128-wide boxes read zeros beyond them.
+  const int d_io = FP8 ? a.head_dim : D;
   if (FP8) {
-    // Q, K (planes, rows, D) and V transposed (planes, D, rows), e4m3
-    if (!make_map_u8(&mq, a.q, D, a.seqlen, a.batch * a.n_q_heads) ||
-        !make_map_u8(&mk, a.k, D, a.seqlen, a.batch * a.n_kv_heads) ||
-        !make_map_u8(&mv, a.v, a.seqlen, D, a.batch * a.n_kv_heads))
+    // Q, K (planes, rows, d_io) and V transposed (planes, d_io, rows), e4m3
+    if (!make_map_u8(&mq, a.q, d_io, a.seqlen, a.batch * a.n_q_heads) ||
+        !make_map_u8(&mk, a.k, d_io, a.seqlen, a.batch * a.n_kv_heads) ||
+        !make_map_u8(&mv, a.v, a.seqlen, d_io, a.batch * a.n_kv_heads))
       return cudaErrorInvalidValue;
   } else if (!make_map(&mq, a.q, D, a.seqlen, a.batch * a.n_q_heads) ||
              !make_map(&mk, a.k, D, a.seqlen, a.batch * a.n_kv_heads, key_tile<D>()) ||
              !make_map(&mv, a.v, D, a.seqlen, a.batch * a.n_kv_heads, key_tile<D>())) {
     return cudaErrorInvalidValue;
   }
-  if (!make_out_map(&mo, a.o, D, a.seqlen, a.batch * a.n_q_heads)) return cudaErrorInvalidValue;
+  if (!make_out_map(&mo, a.o, d_io, a.seqlen, a.batch * a.n_q_heads)) return cudaErrorInvalidValue;
   PrefillParams pp;
   pp.o = a.o;
   pp.lse = a.lse;
@@ -1100,6 +1111,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   pp.q_scales = a.q_scales;
   pp.k_scales = a.k_scales;
   pp.v_scales = a.v_scales;
+  pp.d_out = d_io;
   // Padded: query tiles per sequence.  Packed: the columns of the FP8 scale
   // arrays (every sequence's tiles, at most ceil(total / 128) + num_seqs).
   pp.n_q_tiles = (a.seqlen + kBM - 1) / kBM + (VARLEN ? a.num_seqs : 0);
@@ -1141,7 +1153,7 @@ cudaError_t launch_prefill_cap(const PrefillArgs& a, const LaunchCtx& ctx) {
 
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx) {
   if (a.fp8) {
-    if (a.head_dim != 128) return cudaErrorInvalidValue;
+    if (a.head_dim != 128 && a.head_dim != 64) return cudaErrorInvalidValue;
     return a.cu_seqlens ? launch_prefill_t<128, true, kFp8>(a, ctx)
                         : launch_prefill_t<128, false, kFp8>(a, ctx);
   }

@@ -319,17 +319,19 @@ int attn_decode_append_splitkv_ex(const attn_bf16* q, const attn_bf16* k_new,
  * FP8 path: block quantisation and incoherent processing) and section "Prefill:
  * tiles, loop order and the tensor cores" for everything else.
  *
- *   q        : (batch, n_q_heads,  seqlen, 128) e4m3, 16-byte aligned (rotated if
- *              k is: pass the same signs to attn_quantize_fp8 for both)
- *   k        : (batch, n_kv_heads, seqlen, 128) e4m3
- *   v_t      : (batch, n_kv_heads, 128, seqlen) e4m3 (transposed)
+ *   q        : (batch, n_q_heads,  seqlen, head_dim) e4m3, 16-byte aligned (rotated
+ *              if k is: pass the same signs to attn_quantize_fp8 for both)
+ *   k        : (batch, n_kv_heads, seqlen, head_dim) e4m3
+ *   v_t      : (batch, n_kv_heads, head_dim, seqlen) e4m3 (transposed)
  *   q_scales : (batch, n_q_heads,  ceil(seqlen/128)) fp32 block scales
  *   k_scales : (batch, n_kv_heads, ceil(seqlen/128)) fp32 block scales
  *   v_scales : (batch, n_kv_heads) fp32 per-head scales
  *   o, lse, scale, causal: as attn_prefill (o is the attention of the
  *              dequantised inputs).  P is rounded to e4m3 for the P V product.
- * Limits: head_dim 128; seqlen a multiple of 16 (the rows of v_t are
- *   seqlen bytes); the other limits of attn_prefill.
+ * Limits: head_dim 64 or 128 (64 runs the 128-column kernel, its copies
+ *   reading zeros past the 64 columns: the same time per score as 128);
+ *   seqlen a multiple of 16 (the rows of v_t are seqlen bytes); the other
+ *   limits of attn_prefill.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
  */
 int attn_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_t* v_t,
@@ -422,9 +424,9 @@ int attn_quantize_fp8_varlen(const attn_bf16* x, uint8_t* codes, float* scales,
  *
  * Page: same, sections "Interaction with post-trained models" (packed batches,
  * FP8) and "Prefill: tiles, loop order and the tensor cores".
- *   q, k     : (n_q_heads / n_kv_heads, total_tokens, 128) e4m3 from
+ *   q, k     : (n_q_heads / n_kv_heads, total_tokens, head_dim) e4m3 from
  *              attn_quantize_fp8_varlen (the same signs for both)
- *   v_t      : (n_kv_heads, 128, total_tokens) e4m3 from attn_quantize_fp8
+ *   v_t      : (n_kv_heads, head_dim, total_tokens) e4m3 from attn_quantize_fp8
  *              (block_rows 0, transpose 1)
  *   q_scales, k_scales: (planes, ceil(total_tokens / 128) + num_seqs) fp32
  *   v_scales : (n_kv_heads,) fp32
@@ -433,8 +435,8 @@ int attn_quantize_fp8_varlen(const attn_bf16* x, uint8_t* codes, float* scales,
  * NON-EMPTY SEQUENCE MUST START AT A MULTIPLE OF 16 ROWS: otherwise nothing
  * is computed and the launch is flagged (ATTN_ERR_DEVICE from
  * attn_check_device_status), as for a cu_seqlens that breaks its rule.
- * Limits: head_dim 128; total_tokens a multiple of 16 (16 .. 2^24); the other
- * limits of attn_prefill_varlen.
+ * Limits: head_dim 64 or 128 (as attn_prefill_fp8); total_tokens a multiple
+ * of 16 (16 .. 2^24); the other limits of attn_prefill_varlen.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
  */
 int attn_prefill_fp8_varlen(const uint8_t* q, const uint8_t* k, const uint8_t* v_t,

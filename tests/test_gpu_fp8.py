@@ -147,13 +147,16 @@ def p_rounding_sigma(qz, scale, causal):
     return sig
 
 
-@pytest.mark.parametrize("N,Hq,Hkv,causal", [(1024, 8, 2, True), (768, 4, 4, False),
-                                             (2048, 4, 1, True)])
-def test_prefill_fp8_parity(dev, N, Hq, Hkv, causal):
+@pytest.mark.parametrize("N,Hq,Hkv,causal,d", [(1024, 8, 2, True, 128), (768, 4, 4, False, 128),
+                                               (2048, 4, 1, True, 128),
+                                               (1024, 8, 2, True, 64),    # 64 columns: the
+                                               (640, 4, 4, False, 64),    # 128-wide tiles read zeros
+                                               (336, 6, 3, True, 64)])   # past them
+def test_prefill_fp8_parity(dev, N, Hq, Hkv, causal, d):
     from exact_io_aware_order_gb300 import workloads as W
 
-    x = W.make_prefill(1, Hq, Hkv, N, 128, seed=N + Hq, causal=causal)
-    signs = signs_for(128, 11)
+    x = W.make_prefill(1, Hq, Hkv, N, d, seed=N + Hq, causal=causal)
+    signs = signs_for(d, 11)
     q8, k8, v8t, qs, ks, vs = fp8_inputs(x, dev, signs)
     o, lse = attn.prefill_fp8(q8, k8, v8t, qs, ks, vs, x.scale, causal)
     attn.check_device_status()
@@ -223,27 +226,29 @@ def packed_sigma(qz, scale, causal):
     return sig
 
 
-@pytest.mark.parametrize("lens,Hq,Hkv,causal", [([256, 0, 48, 144, 37], 8, 2, True),
-                                                ([512, 16, 160], 4, 4, False),
-                                                ([32, 1000], 4, 1, True)])
-def test_prefill_fp8_varlen_parity(dev, lens, Hq, Hkv, causal):
+@pytest.mark.parametrize("lens,Hq,Hkv,causal,d", [([256, 0, 48, 144, 37], 8, 2, True, 128),
+                                                  ([512, 16, 160], 4, 4, False, 128),
+                                                  ([32, 1000], 4, 1, True, 128),
+                                                  ([256, 0, 48, 144, 37], 8, 2, True, 64),
+                                                  ([512, 16, 160], 4, 4, False, 64)])
+def test_prefill_fp8_varlen_parity(dev, lens, Hq, Hkv, causal, d):
     """Packed FP8 prefill (every sequence starting at a multiple of 16 rows)
     against the oracle's packed FP8 attention: LSE within 1e-3, O within the
     P-rounding bound, rows past the last sequence untouched."""
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     T = -(-int(cu[-1]) // 16) * 16 + 16
     g = torch.Generator().manual_seed(sum(lens) + Hq)
-    q = torch.randn(Hq, T, 128, generator=g).to(torch.bfloat16)
-    k = torch.randn(Hkv, T, 128, generator=g).to(torch.bfloat16)
-    v = torch.randn(Hkv, T, 128, generator=g).to(torch.bfloat16)
-    signs = signs_for(128, 21)
+    q = torch.randn(Hq, T, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(Hkv, T, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(Hkv, T, d, generator=g).to(torch.bfloat16)
+    signs = signs_for(d, 21)
     sg = torch.from_numpy(signs).to(dev)
     cud = torch.from_numpy(cu).to(dev)
     q8, qs = attn.quantize_fp8_varlen(q.to(dev), cud, sg)
     k8, ks = attn.quantize_fp8_varlen(k.to(dev), cud, sg)
     v8t, vs = attn.quantize_fp8(v.to(dev), None, block_rows=0, transpose=True)
-    scale = 1.0 / math.sqrt(128)
-    o = torch.full((Hq, T, 128), float("nan"), device=dev)
+    scale = 1.0 / math.sqrt(d)
+    o = torch.full((Hq, T, d), float("nan"), device=dev)
     lse = torch.full((Hq, T), float("nan"), device=dev)
     attn.prefill_fp8_varlen(q8, k8, v8t, qs, ks, vs, cud, scale, causal, out=o, lse=lse)
     attn.check_device_status()

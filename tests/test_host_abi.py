@@ -319,7 +319,8 @@ def test_prefill_fp8_varlen_validation(L):
     assert _fp8_varlen(L, T=500) == c["ATTN_ERR_SHAPE"]      # V^T rows must be 16-byte multiples
     assert _fp8_varlen(L, T=0) == c["ATTN_ERR_SHAPE"]
     assert _fp8_varlen(L, S=513) == c["ATTN_ERR_SHAPE"]
-    assert _fp8_varlen(L, d=64) == c["ATTN_ERR_HEADDIM"]
+    assert _fp8_varlen(L, d=96) == c["ATTN_ERR_HEADDIM"]
+    assert _fp8_varlen(L, d=256) == c["ATTN_ERR_HEADDIM"]
     assert _fp8_varlen(L, hq=6, hkv=4) == c["ATTN_ERR_GQA"]
     assert _fp8_varlen(L, cu=P + 2) == c["ATTN_ERR_ALIGN"]
     assert _fp8_varlen(L, v=P + 8) == c["ATTN_ERR_ALIGN"]
