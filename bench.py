@@ -811,11 +811,35 @@ def time_d64(args, attn, W, dist, dev):
     (tot,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
     world = dist.get_world_size() if dist is not None else 1
     avg_ms = tot / n
-    return {"value": round(job_rate(flops, n, world, tot) / 1e12, 2), "unit": "TFLOP/s",
-            "shape": "N=8192, 32/8 heads, head_dim 64, causal",
-            "roofline": {"bound": "tensor", "achieved": round(flops / (avg_ms * 1e-3) / 1e12, 2),
-                         "unit": "TFLOP/s", "kernel": "prefill_kernel<64>",
-                         "flops_per_launch": flops, "avg_launch_ms": round(avg_ms, 4)}}
+    res = {"value": round(job_rate(flops, n, world, tot) / 1e12, 2), "unit": "TFLOP/s",
+           "shape": "N=8192, 32/8 heads, head_dim 64, causal",
+           "roofline": {"bound": "tensor", "achieved": round(flops / (avg_ms * 1e-3) / 1e12, 2),
+                        "unit": "TFLOP/s", "kernel": "prefill_kernel<64>",
+                        "flops_per_launch": flops, "avg_launch_ms": round(avg_ms, 4)}}
+    # The same shape in FP8 (block scales, rotation): the 128-column FP8
+    # kernel, its copies reading zeros past column 64.
+    g = torch.Generator().manual_seed(1)
+    signs = torch.where(torch.rand(D, generator=g) < 0.5, -1.0, 1.0).to(torch.float32).to(dev)
+    q8, qs = attn.quantize_fp8(q, signs, block_rows=128)
+    k8, ks = attn.quantize_fp8(k, signs, block_rows=128)
+    v8t, vs = attn.quantize_fp8(v, None, block_rows=0, transpose=True)
+    for _ in range(3):
+        attn.prefill_fp8(q8, k8, v8t, qs, ks, vs, x.scale, True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    for i in range(n):
+        evs[i][0].record()
+        attn.prefill_fp8(q8, k8, v8t, qs, ks, vs, x.scale, True, out=o, lse=lse)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    attn.check_device_status()
+    (tot8,) = rank_max(dist, [sum(a.elapsed_time(b) for a, b in evs)], dev)
+    res["fp8"] = {"value": round(job_rate(flops, n, world, tot8) / 1e12, 2), "unit": "TFLOP/s",
+                  "kernel": "prefill_kernel<128, fp8> over 64 columns",
+                  "avg_launch_ms": round(tot8 / n, 4),
+                  "vs_bf16": round(tot / tot8, 3)}
+    return res
 
 
 def time_fp8(args, attn, x, q, k, v, o, lse, dist, dev):
