@@ -14,7 +14,7 @@ The headline value is causal-prefill attention TFLOP/s (4 N^2 d heads, halved
 for causal); the decode's HBM GB/s per layer is reported beside it.  Inputs
 are resident in HBM when the timed region starts and exceed L2.  After the
 timed region every other workload is measured once and reported under
-"configs" (Qwen prefill at N = 2048 and 8192, Llama prefill at N = 30720, the
+"workloads" (Qwen prefill at N = 2048 and 8192, Llama prefill at N = 30720, the
 decode split sweep single and chained, the paged batch decode), followed by
 the next rows (append, packed, FP8, head_dim 256, variants).
 
@@ -316,22 +316,22 @@ def run_gb300(args, rank: int, world: int, dist):
     del caches
     if args.no_extras:
         return result
-    configs = {}
+    workloads = {}
     del q, k, v, o, lse
     torch.cuda.empty_cache()
-    legs = set(("configs,append,varlen,fp8,d256,variants" if args.legs == "all" else args.legs)
+    legs = set(("workloads,append,varlen,fp8,d256,variants" if args.legs == "all" else args.legs)
                .split(","))
-    if "configs" in legs:
-        configs["3_llama_long_prefill"] = time_prefill_configs(
+    if "workloads" in legs:
+        workloads["llama_prefill_long"] = time_prefill_lengths(
             attn, dev, dist, peaks, [(30720, W.llama_long_prefill)],
             extra={32768: (achieved, avg_pre)})
-        configs["2_qwen_prefill"] = time_prefill_configs(
+        workloads["qwen_prefill"] = time_prefill_lengths(
             attn, dev, dist, peaks, [(2048, W.qwen_prefill), (8192, W.qwen_prefill)])
-        configs["4_qwen_decode_30720"] = time_decode_sweep(
+        workloads["qwen_decode_30720"] = time_decode_sweep(
             args, attn, W, dev, dist, peaks, sweep, sweep_out, chain_two=dec_total / args.steps)
-        configs["5_paged_batch16"] = time_paged_batch(args, attn, W, dev, dist, peaks, sweep,
+        workloads["paged_decode_batch16"] = time_paged_batch(args, attn, W, dev, dist, peaks, sweep,
                                                       sweep_out)
-        result["configs"] = configs
+        result["workloads"] = workloads
 
     # ---- the next rows, on the Qwen2.5-7B layer at N = 8192 ----
     xq = W.qwen_prefill(8192)
@@ -366,9 +366,9 @@ def run_gb300(args, rank: int, world: int, dist):
         f8["roofline"]["frac"] = round(f8["roofline"]["achieved"] / f8_peak, 4)
         f8["roofline"]["frac_of_bf16_peak"] = round(f8["roofline"]["achieved"] / bf, 4)
         f8["roofline"]["peak_source"] = f8_src
-        if "2_qwen_prefill" in configs:
+        if "qwen_prefill" in workloads:
             f8["speedup_over_bf16_prefill"] = round(
-                f8["roofline"]["achieved"] / configs["2_qwen_prefill"]["N=8192"]["value"], 3)
+                f8["roofline"]["achieved"] / workloads["qwen_prefill"]["N=8192"]["value"], 3)
         f8["quantize_frac_of_hbm"] = round(f8["quantize_gbs"] / peaks["hbm_gbs"], 4)
         result["prefill_fp8"] = f8
     if "d256" in legs:
@@ -474,7 +474,7 @@ def _timed(fn, n, dist, dev, before=None):
     return tot
 
 
-def time_prefill_configs(attn, dev, dist, peaks, cases, extra=None):
+def time_prefill_lengths(attn, dev, dist, peaks, cases, extra=None):
     """Causal prefill TFLOP/s per (sequence length, input maker); each launch
     writes a fresh output larger than L2 (two output buffers alternate)."""
     import torch
@@ -1319,7 +1319,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="only the timed headline steps (for profiling runs)")
     ap.add_argument("--legs", type=str, default="all",
-                    help="comma list of the legs after the timed steps to run: configs, append, "
+                    help="comma list of the legs after the timed steps to run: workloads, append, "
                          "varlen, fp8, d256 (head_dims 256 and 64), variants (for profiling "
                          "runs); default all")
     ap.add_argument("--seqlen", type=int, default=HEADLINE["prefill"]["seqlen"],
