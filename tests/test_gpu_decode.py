@@ -92,6 +92,19 @@ def test_contiguous_edge_cases(dev, kv_len, L, S):
     check_all(d, op, lp, o, lse, S, f"contig len={kv_len} L={L} S={S}")
 
 
+@pytest.mark.parametrize("paged", [False, True])
+def test_long_cache_262144(dev, paged):
+    """One sequence of 262144 cached tokens (8 / 2 heads; 16384 blocks when
+    paged), the policy's split count: every split's partials and the
+    combined result against the oracle."""
+    L = 262144
+    d = (W.make_decode_paged(1, 8, 2, 128, [L], seed=21) if paged
+         else W.make_decode_contiguous(1, 8, 2, 128, L, seed=21))
+    S = attn.decode_num_splits(1, 2, L)
+    op, lp, o, lse = run_decode(d, dev, S)
+    check_all(d, op, lp, o, lse, S, f"len={L} paged={paged} S={S}")
+
+
 @pytest.mark.parametrize("kv_len,L,S", [(1, 1, 1), (4100, 4200, 5), (30720, 30720, 60)])
 def test_contiguous_head_dim_256(dev, kv_len, L, S):
     """head_dim 256 (four 128-byte swizzle spans per cached row), 16 / 8 heads."""

@@ -90,6 +90,22 @@ def test_llama_long_spiky_sampled_rows(dev, N):
     _sampled(x, o, lse, heads_full=set(), rows_per_head=48, seed=N)
 
 
+def test_long_sequence_131072_sampled(dev):
+    """N = 131072 (1024 query tiles per plane, row indices past 2^16, a
+    causal row reading up to 1024 key tiles), 1% of the keys x8: sampled rows,
+    among them the first and last rows and the tile and 2^16 boundaries,
+    against the oracle."""
+    N = 131072
+    x = W.make_prefill(1, 2, 1, N, 128, seed=13, spike_frac=0.01)
+    o, lse = run_prefill(x, dev)
+    rows = [(0, h, i) for h in (0, 1) for i in (0, 1, 127, 128, 65535, 65536, N - 2, N - 1)]
+    rng = np.random.default_rng(13)
+    rows += [(0, int(h), int(i)) for h, i in zip(rng.integers(0, 2, 100), rng.integers(0, N, 100))]
+    o_ref, lse_ref = oracle.prefill_rows(x.q, x.k, x.v, x.scale, True, rows)
+    idx = tuple(torch.tensor(c) for c in zip(*rows))
+    compare(o[idx], lse[idx], o_ref, lse_ref, "N=131072 spiky")
+
+
 def test_closed_forms_on_gpu(dev):
     """q = 0 gives LSE_i = ln(i+1) and O_i = mean(v_0..v_i); V = 1 gives O = 1."""
     x = W.make_prefill(1, 2, 1, 700, 128, seed=3)
