@@ -110,6 +110,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// L2 prefetch of one box: a hint, with no shared memory and no barrier.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -147,6 +155,22 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
   const bool early = a.early_cache != 0;
   if (!early) grid_dep_wait();
   grid_dep_launch();
+  // Contiguous cache: before kv_lens arrives, ask L2 for the first stage of
+  // this split as the host's max_kv_len places it (kv_len's placement when
+  // the two are equal).  A hint only: the copies below read whatever range
+  // kv_len gives.
+  if (kp.mode == kLoadBox64 && a.k_new == nullptr && a.window_left < 0 && threadIdx.x == 0) {
+    const int per_h = (a.max_kv_len + S - 1) / S;
+    const int chunk_h = (per_h + kSplitGranule - 1) / kSplitGranule * kSplitGranule;
+    const long long t0_h = (long long)split * chunk_h;
+    if (t0_h < a.max_kv_len) {
+#pragma unroll
+      for (int h = 0; h < L::kHalves; ++h) {
+        tma_prefetch_4d(&tm_k, h * 64, kvh, (int)t0_h, b);
+        tma_prefetch_4d(&tm_v, h * 64, kvh, (int)t0_h, b);
+      }
+    }
+  }
   // ---- this split's token range (split rule: see the C header) ----
   const bool paged = a.block_table != nullptr;
   const bool append = a.k_new != nullptr;
