@@ -147,15 +147,18 @@ def p_rounding_sigma(qz, scale, causal):
     return sig
 
 
-@pytest.mark.parametrize("N,Hq,Hkv,causal,d", [(1024, 8, 2, True, 128), (768, 4, 4, False, 128),
-                                               (2048, 4, 1, True, 128),
-                                               (1024, 8, 2, True, 64),    # 64 columns: the
-                                               (640, 4, 4, False, 64),    # 128-wide tiles read zeros
-                                               (336, 6, 3, True, 64)])   # past them
-def test_prefill_fp8_parity(dev, N, Hq, Hkv, causal, d):
+@pytest.mark.parametrize("B,N,Hq,Hkv,causal,d", [(1, 1024, 8, 2, True, 128),
+                                                 (1, 768, 4, 4, False, 128),
+                                                 (1, 2048, 4, 1, True, 128),
+                                                 (2, 640, 6, 2, True, 128),   # a batch: scales per
+                                                 (3, 400, 4, 1, False, 64),   # (sequence, head, tile)
+                                                 (1, 1024, 8, 2, True, 64),   # 64 columns: the
+                                                 (1, 640, 4, 4, False, 64),   # 128-wide tiles read
+                                                 (1, 336, 6, 3, True, 64)])   # zeros past them
+def test_prefill_fp8_parity(dev, B, N, Hq, Hkv, causal, d):
     from exact_io_aware_order_gb300 import workloads as W
 
-    x = W.make_prefill(1, Hq, Hkv, N, d, seed=N + Hq, causal=causal)
+    x = W.make_prefill(B, Hq, Hkv, N, d, seed=N + Hq + B, causal=causal)
     signs = signs_for(d, 11)
     q8, k8, v8t, qs, ks, vs = fp8_inputs(x, dev, signs)
     o, lse = attn.prefill_fp8(q8, k8, v8t, qs, ks, vs, x.scale, causal)
