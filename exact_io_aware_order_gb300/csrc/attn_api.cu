@@ -1,6 +1,7 @@
 // C ABI of the attention library: argument validation, per-device state
 // (error word, architecture check) and kernel launches on the caller's stream.
 // The operations themselves are defined in include/attn.h.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -236,8 +237,8 @@ int prefill_varlen_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16*
                         int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
                         int window_left, float softcap, const float* alibi_slopes, void* stream) {
   if (!q || !k || !v || !o || !lse || !cu_seqlens) return ATTN_ERR_NULL;
-  if (num_seqs < 1 || num_seqs > attn::kMaxVarlenSeqs || n_q_heads < 1 || n_kv_heads < 1 ||
-      n_q_heads > (1 << 20) || total_tokens < 1 || total_tokens > (1 << 24) ||
+  if (num_seqs < 1 || num_seqs > attn::kMaxVarlenSeqsPerCall || n_q_heads < 1 ||
+      n_kv_heads < 1 || n_q_heads > (1 << 20) || total_tokens < 1 || total_tokens > (1 << 24) ||
       !valid_scale(scale) || !valid_variant(window_left, softcap))
     return ATTN_ERR_SHAPE;
   if (alibi_slopes && softcap > 0.f) return ATTN_ERR_SHAPE;  // not combined
@@ -254,12 +255,19 @@ int prefill_varlen_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16*
   if (!ds) return st;
   attn::PrefillArgs a{q, k, v, o, lse, 1, n_q_heads, n_kv_heads, total_tokens, head_dim, scale,
                       causal ? 1 : 0};
-  a.cu_seqlens = cu_seqlens;
-  a.num_seqs = num_seqs;
   a.window_left = window_left;
   a.softcap = softcap;
   a.alibi_slopes = alibi_slopes;
-  if (attn::launch_prefill(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  // One launch per slice of at most kMaxVarlenSeqs sequences, in order on the
+  // stream: the entries of cu_seqlens are absolute row offsets, so a slice is
+  // the same array from its first sequence on.
+  const attn::LaunchCtx ctx = make_ctx(stream, ds);
+  for (int g = 0; g < num_seqs; g += attn::kMaxVarlenSeqs) {
+    a.cu_seqlens = cu_seqlens + g;
+    a.num_seqs = std::min(attn::kMaxVarlenSeqs, num_seqs - g);
+    a.seq_base = g;
+    if (attn::launch_prefill(a, ctx) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  }
   return ATTN_OK;
 }
 

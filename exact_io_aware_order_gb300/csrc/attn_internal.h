@@ -32,6 +32,7 @@ struct PrefillArgs {
   // of packed rows and sequence s occupies rows [cu_seqlens[s], cu_seqlens[s+1]).
   const int32_t* cu_seqlens = nullptr;
   int num_seqs = 0;
+  int seq_base = 0;  // index of cu_seqlens[0] in the caller's list (0: its start)
   // Variants: a sliding window (row i sees keys j >= i - window_left; -1 =
   // none) and logit soft-capping (s -> softcap * tanh(s / softcap); 0 = off).
   int window_left = -1;
@@ -46,8 +47,13 @@ struct PrefillArgs {
   const float* v_scales = nullptr;
 };
 
-// Largest number of packed sequences per variable-length prefill call.
+// Packed sequences per prefill launch (the kernel keeps a table per sequence
+// in shared memory); a bf16 packed prefill runs longer lists as one launch per
+// slice of at most this many, up to kMaxVarlenSeqsPerCall.  The FP8 packed
+// prefill and its quantiser number their scale columns across the whole list
+// and take one launch, so at most kMaxVarlenSeqs.
 constexpr int kMaxVarlenSeqs = 512;
+constexpr int kMaxVarlenSeqsPerCall = 1 << 20;
 
 struct DecodeArgs {
   const uint16_t* q;

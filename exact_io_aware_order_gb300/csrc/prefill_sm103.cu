@@ -135,6 +135,7 @@ struct PrefillParams {
   int group_planes; // plain padded mode: query planes per kv-head group of the work list
   const int32_t* cu_seqlens;  // packed mode: (num_seqs + 1) row offsets
   int num_seqs;
+  int seq_base;     // packed mode: cu_seqlens[0]'s index in the caller's list
   // FP8: dequantisation scales of the e4m3 inputs, per 128-row block of Q and
   // K ((plane, n_q_tiles)) and per head of V ((plane,)).
   const float* q_scales;
@@ -365,7 +366,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int a_prev = __shfl_up_sync(0xffffffffu, e, 1);
         const int lower = lane == 0 ? prev_end : a_prev;  // the previous sequence's end
         int a_c = min(max(a, 0), N), e_c = min(max(e, a_c), N);
-        if (s < p.num_seqs && (a != a_c || e != e_c || a < lower || (s == 0 && a != 0))) bad = true;
+        // (only the list's first entry must be 0: a later slice starts where
+        // the previous launch's last sequence ended)
+        if (s < p.num_seqs &&
+            (a != a_c || e != e_c || a < lower || (s == 0 && p.seq_base == 0 && a != 0)))
+          bad = true;
         // FP8: V^T's copies take tokens along the innermost coordinate, which
         // a TMA copy of bytes needs at a multiple of 16: every non-empty
         // sequence must start there (else the launch does nothing, flagged).
@@ -1130,6 +1135,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   }
   pp.cu_seqlens = a.cu_seqlens;
   pp.num_seqs = a.num_seqs;
+  pp.seq_base = a.seq_base;
   pp.err_word = ctx.err_word;
   pp.timeout_ns = ctx.timeout_ns;
   // Persistent: one CTA per SM (shared memory and TMEM admit one), each

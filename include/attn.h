@@ -131,8 +131,10 @@ int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, 
  * Rows outside every sequence are not written.  A cu_seqlens that breaks the
  * rule above is clamped into it and flagged (ATTN_ERR_DEVICE from
  * attn_check_device_status).
- * Limits: 1 <= num_seqs <= 512; head_dim in {64, 128, 256}; 1 <= total_tokens <= 2^24;
- *   n_q_heads % n_kv_heads == 0; n_q_heads * (ceil(total_tokens/128) + num_seqs) < 2^31.
+ * Limits: 1 <= num_seqs <= 2^20 (more than 512 run as one launch per slice of
+ *   512 sequences, in order on the stream); head_dim in {64, 128, 256};
+ *   1 <= total_tokens <= 2^24; n_q_heads % n_kv_heads == 0;
+ *   n_q_heads * (ceil(total_tokens/128) + num_seqs) < 2^31.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
  */
 int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
@@ -435,8 +437,9 @@ int attn_quantize_fp8_varlen(const attn_bf16* x, uint8_t* codes, float* scales,
  * NON-EMPTY SEQUENCE MUST START AT A MULTIPLE OF 16 ROWS: otherwise nothing
  * is computed and the launch is flagged (ATTN_ERR_DEVICE from
  * attn_check_device_status), as for a cu_seqlens that breaks its rule.
- * Limits: head_dim 64 or 128 (as attn_prefill_fp8); total_tokens a multiple
- * of 16 (16 .. 2^24); the other limits of attn_prefill_varlen.
+ * Limits: head_dim 64 or 128 (as attn_prefill_fp8); 1 <= num_seqs <= 512 (one
+ * launch: the scale columns are numbered across the whole list); total_tokens
+ * a multiple of 16 (16 .. 2^24); the other limits of attn_prefill_varlen.
  * Errors: ATTN_ERR_NULL, _SHAPE, _HEADDIM, _GQA, _ALIGN, _ARCH, _LAUNCH.
  */
 int attn_prefill_fp8_varlen(const uint8_t* q, const uint8_t* k, const uint8_t* v_t,

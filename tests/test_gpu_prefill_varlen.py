@@ -118,3 +118,29 @@ def test_varlen_variants(dev, lens, hq, hkv, d, causal, variant):
     T0 = int(x.cu_seqlens[-1])
     compare(o[:, :T0], lse[:, :T0], o_ref[:, :T0], lse_ref[:, :T0], f"varlen {lens} {variant}")
     assert torch.isnan(o[:, T0:]).all() and torch.isnan(lse[:, T0:]).all()
+
+
+@pytest.mark.parametrize("n_seqs,d,variant", [(1100, 64, {}), (1030, 128, {"window_left": 20}),
+                                              (700, 64, {"alibi": True})])
+def test_more_sequences_than_one_launch(dev, n_seqs, d, variant):
+    """More than 512 packed sequences (lengths 0 .. 48, some empty): the call
+    runs one launch per slice of 512 on the stream; every row against the
+    oracle, no device flag raised, rows past the last sequence untouched."""
+    rng = np.random.default_rng(n_seqs + d)
+    lens = [int(n) for n in rng.integers(0, 49, n_seqs)]
+    x = W.make_prefill_varlen(lens, 4, 2, d, seed=n_seqs, extra_rows=3)
+    kw = {k: v for k, v in variant.items() if k != "alibi"}
+    okw = dict(kw)
+    if variant.get("alibi"):
+        sl = _slopes(4)
+        kw["alibi_slopes"] = sl.to(dev)
+        okw["alibi_slopes"] = sl.tolist()
+    n_q, T, dd = x.q.shape
+    o, lse = nan_like((n_q, T, dd), dev), nan_like((n_q, T), dev)
+    attn.prefill_varlen(x.q.to(dev), x.k.to(dev), x.v.to(dev), x.cu_seqlens.to(dev), x.scale,
+                        True, out=o, lse=lse, **kw)
+    attn.check_device_status()
+    o_ref, lse_ref = oracle.prefill_varlen(x.q, x.k, x.v, x.cu_seqlens, x.scale, True, **okw)
+    T0 = int(x.cu_seqlens[-1])
+    compare(o[:, :T0], lse[:, :T0], o_ref[:, :T0], lse_ref[:, :T0], f"{n_seqs} sequences {variant}")
+    assert torch.isnan(o[:, T0:]).all() and torch.isnan(lse[:, T0:]).all()

@@ -116,7 +116,7 @@ def test_prefill_varlen_validation(L):
     c = _lib.status_codes()
     assert _varlen(L, cu=None) == c["ATTN_ERR_NULL"]
     assert _varlen(L, S=0) == c["ATTN_ERR_SHAPE"]
-    assert _varlen(L, S=513) == c["ATTN_ERR_SHAPE"]
+    assert _varlen(L, S=(1 << 20) + 1) == c["ATTN_ERR_SHAPE"]   # 513 .. 2^20 run in slices
     assert _varlen(L, hq=1 << 20, hkv=1, T=1 << 24) == c["ATTN_ERR_SHAPE"]   # item count > 2^31
     assert _varlen(L, T=0) == c["ATTN_ERR_SHAPE"]
     assert _varlen(L, T=(1 << 24) + 1) == c["ATTN_ERR_SHAPE"]
@@ -144,7 +144,7 @@ def test_prefill_varlen_ex_validation(L):
     assert _varlen_ex(L, cap=2.0, al=P) == c["ATTN_ERR_SHAPE"]      # ALiBi with soft-capping
     assert _varlen_ex(L, al=P + 2) == c["ATTN_ERR_ALIGN"]
     assert _varlen_ex(L, w=5, cu=None) == c["ATTN_ERR_NULL"]
-    assert _varlen_ex(L, w=5, S=513) == c["ATTN_ERR_SHAPE"]
+    assert _varlen_ex(L, w=5, S=(1 << 20) + 1) == c["ATTN_ERR_SHAPE"]
 
 
 def _decode(L, **kw):
