@@ -38,7 +38,8 @@ def test_tiny_causal_prefill(dev):
     (1, 1, 1, 128, 64, True), (1, 1, 1, 129, 128, True), (2, 4, 2, 300, 128, True),
     (1, 3, 3, 383, 64, True), (1, 2, 2, 511, 128, True), (1, 2, 1, 1000, 128, True),
     (1, 7, 1, 640, 128, True), (1, 2, 1, 700, 128, False), (2, 2, 2, 256, 64, False),
-    (1, 1, 1, 5, 128, False), (3, 2, 1, 257, 64, True)])
+    (1, 1, 1, 5, 128, False), (3, 2, 1, 257, 64, True),
+    (16, 32, 8, 200, 128, True)])              # 512 planes: several items per CTA
 def test_ragged_and_small_shapes(dev, B, Hq, Hkv, N, D, causal):
     x = W.make_prefill(B, Hq, Hkv, N, D, seed=N + 7 * D + B)
     o, lse = run_prefill(x, dev, causal)
@@ -104,6 +105,22 @@ def test_long_sequence_131072_sampled(dev):
     o_ref, lse_ref = oracle.prefill_rows(x.q, x.k, x.v, x.scale, True, rows)
     idx = tuple(torch.tensor(c) for c in zip(*rows))
     compare(o[idx], lse[idx], o_ref, lse_ref, "N=131072 spiky")
+
+
+def test_batch_with_l2_grouping_sampled(dev):
+    """Batch 2 of Llama-3-8B layers at N = 16384 (32 / 8 heads): K and V take
+    134 MB, so the work list runs in groups of two kv heads (8 query planes)
+    for L2 locality, eight groups over the batch; sampled rows of both
+    sequences against the oracle."""
+    x = W.make_prefill(2, 32, 8, 16384, 128, seed=17, spike_frac=0.01)
+    o, lse = run_prefill(x, dev)
+    rng = np.random.default_rng(17)
+    rows = [(int(b), int(h), int(i)) for b, h, i in
+            zip(rng.integers(0, 2, 160), rng.integers(0, 32, 160), rng.integers(0, 16384, 160))]
+    rows += [(1, 31, 16383), (1, 0, 0), (0, 31, 16383)]
+    o_ref, lse_ref = oracle.prefill_rows(x.q, x.k, x.v, x.scale, True, rows)
+    idx = tuple(torch.tensor(c) for c in zip(*rows))
+    compare(o[idx], lse[idx], o_ref, lse_ref, "B=2 N=16384 grouped")
 
 
 def test_closed_forms_on_gpu(dev):
