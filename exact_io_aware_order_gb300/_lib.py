@@ -33,6 +33,10 @@ SIGNATURES = {
     "attn_prefill_varlen": (c_int, [c_void_p] * 6 + [c_int] * 5 + [c_float, c_int, c_void_p]),
     "attn_prefill_varlen_ex": (c_int, [c_void_p] * 6 + [c_int] * 5
                                + [c_float, c_int, c_int, c_float, c_void_p, c_void_p]),
+    "attn_prefill_ex2": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_int, c_float,
+                                                                 c_void_p, c_uint, c_void_p]),
+    "attn_prefill_varlen_ex2": (c_int, [c_void_p] * 6 + [c_int] * 5
+                                + [c_float, c_int, c_int, c_float, c_void_p, c_uint, c_void_p]),
     "attn_decode_num_splits": (c_int, [c_int] * 4),
     "attn_decode_splitkv": (c_int, [c_void_p] * 5 + [c_int] + [c_void_p] * 2 + [c_int] * 8
                             + [c_float, c_void_p]),

@@ -19,6 +19,7 @@ _BF16 = torch.bfloat16
 
 # attn_decode_splitkv_ex2 flag (include/attn.h ATTN_DECODE_EARLY_CACHE).
 EARLY_CACHE = 1
+OUT_BF16 = 1  # ATTN_PREFILL_OUT_BF16
 
 
 def _stream(stream) -> int:
@@ -45,13 +46,15 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
 def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
             causal: bool = True, out: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, stream=None, window_left: int = -1,
-            softcap: float = 0.0, alibi_slopes: Optional[torch.Tensor] = None):
+            softcap: float = 0.0, alibi_slopes: Optional[torch.Tensor] = None,
+            out_dtype: torch.dtype = torch.float32):
     """Attention forward over whole sequences (``attn_prefill``; with a
     sliding window, soft-capping or ALiBi slopes ((n_q,) fp32 on the device),
-    ``attn_prefill_ex``).
+    ``attn_prefill_ex``; with ``out_dtype=torch.bfloat16``,
+    ``attn_prefill_ex2`` with ATTN_PREFILL_OUT_BF16).
 
     q: (B, n_q, N, d) bf16; k, v: (B, n_kv, N, d) bf16.  Returns
-    (O (B, n_q, N, d) fp32, LSE (B, n_q, N) fp32, natural log).
+    (O (B, n_q, N, d) fp32 or bf16, LSE (B, n_q, N) fp32, natural log).
     """
     _need(q, "q", _BF16, 4)
     _need(k, "k", _BF16, 4)
@@ -62,15 +65,26 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[f
         raise ValueError("k and v must be (B, n_kv, N, d) matching q")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if out_dtype not in (torch.float32, _BF16):
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
     if out is None:
-        out = torch.empty((B, n_q, N, d), dtype=torch.float32, device=q.device)
+        out = torch.empty((B, n_q, N, d), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, n_q, N), dtype=torch.float32, device=q.device)
-    _need(out, "out", torch.float32, 4)
+    _need(out, "out", out_dtype, 4)
     _need(lse, "lse", torch.float32, 3)
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, n_q, n_kv,
             N, d, float(scale), int(bool(causal)))
-    if window_left == -1 and softcap == 0.0 and alibi_slopes is None:
+    if out_dtype == _BF16:
+        al = None
+        if alibi_slopes is not None:
+            _need(alibi_slopes, "alibi_slopes", torch.float32, 1)
+            if alibi_slopes.numel() != n_q:
+                raise ValueError("alibi_slopes must have one slope per query head")
+            al = alibi_slopes.data_ptr()
+        check("attn_prefill_ex2", lib().attn_prefill_ex2(*args, int(window_left), float(softcap),
+                                                         al, OUT_BF16, _stream(stream)))
+    elif window_left == -1 and softcap == 0.0 and alibi_slopes is None:
         check("attn_prefill", lib().attn_prefill(*args, _stream(stream)))
     else:
         al = None
@@ -88,15 +102,17 @@ def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
                    scale: Optional[float] = None, causal: bool = True,
                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                    stream=None, window_left: int = -1, softcap: float = 0.0,
-                   alibi_slopes: Optional[torch.Tensor] = None):
+                   alibi_slopes: Optional[torch.Tensor] = None,
+                   out_dtype: torch.dtype = torch.float32):
     """Prefill of sequences packed end to end (``attn_prefill_varlen``; with a
     sliding window, soft-capping or ALiBi slopes, ``attn_prefill_varlen_ex``,
-    positions counted from each sequence's first row).
+    positions counted from each sequence's first row; with
+    ``out_dtype=torch.bfloat16``, ``attn_prefill_varlen_ex2``).
 
     q: (n_q, total, d) bf16; k, v: (n_kv, total, d) bf16; cu_seqlens:
-    (num_seqs + 1,) int32 on the device.  Returns (O (n_q, total, d) fp32,
-    LSE (n_q, total) fp32); rows outside every sequence are left as they were
-    in ``out`` / ``lse``.
+    (num_seqs + 1,) int32 on the device.  Returns (O (n_q, total, d) fp32 or
+    bf16, LSE (n_q, total) fp32); rows outside every sequence are left as
+    they were in ``out`` / ``lse``.
     """
     _need(q, "q", _BF16, 3)
     _need(k, "k", _BF16, 3)
@@ -108,16 +124,28 @@ def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
         raise ValueError("k and v must be (n_kv, total, d) matching q")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if out_dtype not in (torch.float32, _BF16):
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
     if out is None:
-        out = torch.empty((n_q, T, d), dtype=torch.float32, device=q.device)
+        out = torch.empty((n_q, T, d), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((n_q, T), dtype=torch.float32, device=q.device)
-    _need(out, "out", torch.float32, 3)
+    _need(out, "out", out_dtype, 3)
     _need(lse, "lse", torch.float32, 2)
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
             cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, T, n_q, n_kv, d, float(scale),
             int(bool(causal)))
-    if window_left != -1 or softcap != 0.0 or alibi_slopes is not None:
+    if out_dtype == _BF16:
+        al = None
+        if alibi_slopes is not None:
+            _need(alibi_slopes, "alibi_slopes", torch.float32, 1)
+            if alibi_slopes.numel() != n_q:
+                raise ValueError("alibi_slopes must have one slope per query head")
+            al = alibi_slopes.data_ptr()
+        name = "attn_prefill_varlen_ex2"
+        st = lib().attn_prefill_varlen_ex2(*args, int(window_left), float(softcap), al, OUT_BF16,
+                                           _stream(stream))
+    elif window_left != -1 or softcap != 0.0 or alibi_slopes is not None:
         al = None
         if alibi_slopes is not None:
             _need(alibi_slopes, "alibi_slopes", torch.float32, 1)

@@ -184,11 +184,12 @@ int attn_decode_num_splits(int batch, int n_kv_heads, int max_kv_len, int num_sm
 
 namespace {
 
-int prefill_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o, float* lse,
+int prefill_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, void* o, float* lse,
                  int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim, float scale,
                  int causal, int window_left, float softcap, const float* alibi_slopes,
-                 void* stream) {
+                 unsigned flags, void* stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (flags & ~ATTN_PREFILL_OUT_BF16) return ATTN_ERR_SHAPE;
   if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || seqlen < 1 || seqlen > (1 << 24) ||
       (long long)batch * n_q_heads > (1LL << 20) || !valid_scale(scale) ||
       !valid_variant(window_left, softcap))
@@ -209,6 +210,7 @@ int prefill_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
   a.window_left = window_left;
   a.softcap = softcap;
   a.alibi_slopes = alibi_slopes;
+  a.o_bf16 = (flags & ATTN_PREFILL_OUT_BF16) ? 1 : 0;
   if (attn::launch_prefill(a, make_ctx(stream, ds)) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
@@ -219,7 +221,7 @@ int attn_prefill(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, flo
                  int batch, int n_q_heads, int n_kv_heads, int seqlen, int head_dim, float scale,
                  int causal, void* stream) {
   return prefill_impl(q, k, v, o, lse, batch, n_q_heads, n_kv_heads, seqlen, head_dim, scale,
-                      causal, -1, 0.f, nullptr, stream);
+                      causal, -1, 0.f, nullptr, 0u, stream);
 }
 
 int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
@@ -227,16 +229,26 @@ int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, 
                     float scale, int causal, int window_left, float softcap,
                     const float* alibi_slopes, void* stream) {
   return prefill_impl(q, k, v, o, lse, batch, n_q_heads, n_kv_heads, seqlen, head_dim, scale,
-                      causal, window_left, softcap, alibi_slopes, stream);
+                      causal, window_left, softcap, alibi_slopes, 0u, stream);
+}
+
+int attn_prefill_ex2(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, void* o,
+                     float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen,
+                     int head_dim, float scale, int causal, int window_left, float softcap,
+                     const float* alibi_slopes, unsigned flags, void* stream) {
+  return prefill_impl(q, k, v, o, lse, batch, n_q_heads, n_kv_heads, seqlen, head_dim, scale,
+                      causal, window_left, softcap, alibi_slopes, flags, stream);
 }
 
 namespace {
 
-int prefill_varlen_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
+int prefill_varlen_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, void* o,
                         float* lse, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
                         int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
-                        int window_left, float softcap, const float* alibi_slopes, void* stream) {
+                        int window_left, float softcap, const float* alibi_slopes, unsigned flags,
+                        void* stream) {
   if (!q || !k || !v || !o || !lse || !cu_seqlens) return ATTN_ERR_NULL;
+  if (flags & ~ATTN_PREFILL_OUT_BF16) return ATTN_ERR_SHAPE;
   if (num_seqs < 1 || num_seqs > attn::kMaxVarlenSeqsPerCall || n_q_heads < 1 ||
       n_kv_heads < 1 || n_q_heads > (1 << 20) || total_tokens < 1 || total_tokens > (1 << 24) ||
       !valid_scale(scale) || !valid_variant(window_left, softcap))
@@ -258,6 +270,7 @@ int prefill_varlen_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16*
   a.window_left = window_left;
   a.softcap = softcap;
   a.alibi_slopes = alibi_slopes;
+  a.o_bf16 = (flags & ATTN_PREFILL_OUT_BF16) ? 1 : 0;
   // One launch per slice of at most kMaxVarlenSeqs sequences, in order on the
   // stream: the entries of cu_seqlens are absolute row offsets, so a slice is
   // the same array from its first sequence on.
@@ -278,7 +291,7 @@ int attn_prefill_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16*
                         int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
                         void* stream) {
   return prefill_varlen_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, n_q_heads,
-                             n_kv_heads, head_dim, scale, causal, -1, 0.f, nullptr, stream);
+                             n_kv_heads, head_dim, scale, causal, -1, 0.f, nullptr, 0u, stream);
 }
 
 int attn_prefill_varlen_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* o,
@@ -288,7 +301,17 @@ int attn_prefill_varlen_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf
                            void* stream) {
   return prefill_varlen_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, n_q_heads,
                              n_kv_heads, head_dim, scale, causal, window_left, softcap,
-                             alibi_slopes, stream);
+                             alibi_slopes, 0u, stream);
+}
+
+int attn_prefill_varlen_ex2(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, void* o,
+                            float* lse, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                            int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
+                            int window_left, float softcap, const float* alibi_slopes,
+                            unsigned flags, void* stream) {
+  return prefill_varlen_impl(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, n_q_heads,
+                             n_kv_heads, head_dim, scale, causal, window_left, softcap,
+                             alibi_slopes, flags, stream);
 }
 
 namespace {

@@ -23,7 +23,7 @@ struct PrefillArgs {
   const uint16_t* q;
   const uint16_t* k;
   const uint16_t* v;
-  float* o;
+  void* o;     // fp32, or bf16 with o_bf16
   float* lse;
   int batch, n_q_heads, n_kv_heads, seqlen, head_dim;
   float scale;
@@ -33,6 +33,7 @@ struct PrefillArgs {
   const int32_t* cu_seqlens = nullptr;
   int num_seqs = 0;
   int seq_base = 0;  // index of cu_seqlens[0] in the caller's list (0: its start)
+  int o_bf16 = 0;    // O written as bf16 (O / l in fp32, rounded once) instead of fp32
   // Variants: a sliding window (row i sees keys j >= i - window_left; -1 =
   // none) and logit soft-capping (s -> softcap * tanh(s / softcap); 0 = off).
   int window_left = -1;

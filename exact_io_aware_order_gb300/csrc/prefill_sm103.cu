@@ -122,7 +122,7 @@ struct PrefillSmem {
 };
 
 struct PrefillParams {
-  float* o;
+  void* o;          // fp32, or bf16 in the OBF16 kernels
   float* lse;
   int batch, n_q_heads, n_kv_heads, seqlen;
   float sl2;  // scale * log2(e); with soft-capping, softcap * log2(e)
@@ -271,7 +271,9 @@ __device__ __forceinline__ int item_of(int r, int total) {
 
 // VARIANT selects the flavour (see Variant): the plain kernel has neither a
 // window nor soft-capping in its code, the window kernel no soft-capping.
-template <int D, bool VARLEN, int VARIANT>
+// OBF16: O is written as bf16 (acc / l in fp32, rounded once); a template
+// parameter, so that the fp32 kernels carry none of that code.
+template <int D, bool VARLEN, int VARIANT, bool OBF16>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -926,6 +928,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       constexpr int kEC = D > 128 ? 128 : D;
       const int d_out = FP8 ? p.d_out : D;  // O's columns in memory
       auto store_cols = [&](const uint32_t (&acc)[kEC / 32][32], int col0, float inv_l) {
+        if constexpr (OBF16) {
+          // bf16 O: 64 columns make one 128-byte row of the staging box.
+          auto pk = [&](int c, int b) {  // columns b, b+1 of 32-column chunk c, as bf16x2
+            return __uint_as_float(pack_bf16x2(__uint_as_float(acc[c][b]) * inv_l,
+                                               __uint_as_float(acc[c][b + 1]) * inv_l));
+          };
+          if (!VARLEN || in_seq >= 32) {
+#pragma unroll
+            for (int c2 = 0; c2 < kEC / 64; ++c2) {
+              if (FP8 && col0 + c2 * 64 >= d_out) break;
+              if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {  // 8 columns per 16-byte piece
+                const int c = 2 * c2 + (i >> 2), b = (i & 3) * 8;
+                st_shared_v4(stage + lane * 128 + ((i ^ (lane & 7)) << 4),
+                             make_float4(pk(c, b), pk(c, b + 2), pk(c, b + 4), pk(c, b + 6)));
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0 && row0 < N) {  // rows past the tensor's end are clipped by the copy
+                tma_store_3d_hint(&tm_o, stage, col0 + c2 * 64, row0, t.zq, pol_out);
+                bulk_commit_group();
+              }
+            }
+          } else if (lane < in_seq) {
+            uint16_t* orow = static_cast<uint16_t*>(p.o) +
+                             ((size_t)t.zq * N + (size_t)(row0 + lane)) * d_out + col0;
+#pragma unroll
+            for (int c = 0; c < kEC / 32; ++c) {
+              if (FP8 && col0 + c * 32 >= d_out) continue;
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                reinterpret_cast<float4*>(orow + c * 32)[i] =
+                    make_float4(pk(c, 8 * i), pk(c, 8 * i + 2), pk(c, 8 * i + 4), pk(c, 8 * i + 6));
+            }
+          }
+          return;
+        }
         if (!VARLEN || in_seq >= 32) {
 #pragma unroll
           for (int c = 0; c < kEC / 32; ++c) {
@@ -947,7 +988,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
           }
         } else if (lane < in_seq) {
-          float* orow = p.o + ((size_t)t.zq * N + (size_t)(row0 + lane)) * d_out + col0;
+          float* orow = static_cast<float*>(p.o) + ((size_t)t.zq * N + (size_t)(row0 + lane)) * d_out + col0;
 #pragma unroll
           for (int c = 0; c < kEC / 32; ++c)
 #pragma unroll
@@ -1057,20 +1098,23 @@ bool make_map_u8(CUtensorMap* m, const void* base, int inner, int rows, int plan
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 output (planes, rows, D): box = 32 x 32 x 1 (128-byte rows), 128-byte swizzle.
-bool make_out_map(CUtensorMap* m, void* base, int D, int rows, int planes) {
+// Output (planes, rows, D), fp32 (box 32 x 32 x 1) or bf16 (box 64 x 32 x 1):
+// 128-byte rows, 128-byte swizzle.
+bool make_out_map(CUtensorMap* m, void* base, int D, int rows, int planes, bool bf16 = false) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
+  const cuuint64_t esz = bf16 ? 2 : 4;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * 4 * (cuuint64_t)rows};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)D * esz * (cuuint64_t)rows};
+  cuuint32_t box[3] = {bf16 ? 64u : 32u, 32, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base,
+             dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool VARLEN, int VARIANT>
+template <int D, bool VARLEN, int VARIANT, bool OBF16 = false>
 cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   constexpr bool FP8 = VARIANT == kFp8;
   using L = PrefillSmem<D, VARLEN, FP8 ? 1 : 2, VARIANT == kWindowAlibi && D <= 128>;
@@ -1080,7 +1124,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VARLEN, VARIANT>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VARLEN, VARIANT, OBF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
@@ -1100,7 +1144,8 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
              !make_map(&mv, a.v, D, a.seqlen, a.batch * a.n_kv_heads, key_tile<D>())) {
     return cudaErrorInvalidValue;
   }
-  if (!make_out_map(&mo, a.o, d_io, a.seqlen, a.batch * a.n_q_heads)) return cudaErrorInvalidValue;
+  if (!make_out_map(&mo, a.o, d_io, a.seqlen, a.batch * a.n_q_heads, OBF16))
+    return cudaErrorInvalidValue;
   PrefillParams pp;
   pp.o = a.o;
   pp.lse = a.lse;
@@ -1143,23 +1188,30 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const LaunchCtx& ctx) {
   // on the device, so every SM gets a CTA (those without items exit at once).
   const int sms = std::max(ctx.num_sms, 1);
   const unsigned grid = (unsigned)(VARLEN ? sms : std::min(pp.total_tiles, sms));
-  prefill_kernel<D, VARLEN, VARIANT><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, mo, pp);
+  prefill_kernel<D, VARLEN, VARIANT, OBF16><<<grid, kThreads, L::kAlloc, ctx.stream>>>(mq, mk, mv, mo,
+                                                                                        pp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+template <int D, bool VARLEN, bool OBF16>
+cudaError_t launch_prefill_flavour(const PrefillArgs& a, const LaunchCtx& ctx) {
+  if (a.alibi_slopes) return launch_prefill_t<D, VARLEN, kWindowAlibi, OBF16>(a, ctx);
+  if (a.softcap > 0.f) return launch_prefill_t<D, VARLEN, kWindowCap, OBF16>(a, ctx);
+  if (a.window_left >= 0) return launch_prefill_t<D, VARLEN, kWindow, OBF16>(a, ctx);
+  return launch_prefill_t<D, VARLEN, kPlain, OBF16>(a, ctx);
+}
+
 template <int D, bool VARLEN>
 cudaError_t launch_prefill_cap(const PrefillArgs& a, const LaunchCtx& ctx) {
-  if (a.alibi_slopes) return launch_prefill_t<D, VARLEN, kWindowAlibi>(a, ctx);
-  if (a.softcap > 0.f) return launch_prefill_t<D, VARLEN, kWindowCap>(a, ctx);
-  if (a.window_left >= 0) return launch_prefill_t<D, VARLEN, kWindow>(a, ctx);
-  return launch_prefill_t<D, VARLEN, kPlain>(a, ctx);
+  return a.o_bf16 ? launch_prefill_flavour<D, VARLEN, true>(a, ctx)
+                  : launch_prefill_flavour<D, VARLEN, false>(a, ctx);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const LaunchCtx& ctx) {
   if (a.fp8) {
-    if (a.head_dim != 128 && a.head_dim != 64) return cudaErrorInvalidValue;
+    if ((a.head_dim != 128 && a.head_dim != 64) || a.o_bf16) return cudaErrorInvalidValue;
     return a.cu_seqlens ? launch_prefill_t<128, true, kFp8>(a, ctx)
                         : launch_prefill_t<128, false, kFp8>(a, ctx);
   }

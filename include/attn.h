@@ -111,6 +111,25 @@ int attn_prefill_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, 
                     const float* alibi_slopes, void* stream);
 
 /*
+ * attn_prefill_ex2 -- attn_prefill_ex with flags; ATTN_PREFILL_OUT_BF16 writes
+ * O as bf16.
+ *
+ * Page: same, section "Prefill: tiles, loop order and the tensor cores" (the
+ * output tile O_i = acc / l written once per query tile).
+ *   o     : (batch, n_q_heads, seqlen, head_dim), fp32, or bf16 with
+ *           ATTN_PREFILL_OUT_BF16: each value acc / l is computed in fp32 and
+ *           rounded to the nearest bf16 (ties to even) once, so the bf16 O
+ *           equals the fp32 O of the same call rounded; 16-byte aligned
+ *   flags : 0 or ATTN_PREFILL_OUT_BF16; any other bit is ATTN_ERR_SHAPE
+ * lse stays fp32.  Everything else, and the errors, as attn_prefill_ex.
+ */
+#define ATTN_PREFILL_OUT_BF16 1u
+int attn_prefill_ex2(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, void* o,
+                     float* lse, int batch, int n_q_heads, int n_kv_heads, int seqlen,
+                     int head_dim, float scale, int causal, int window_left, float softcap,
+                     const float* alibi_slopes, unsigned flags, void* stream);
+
+/*
  * attn_prefill_varlen -- prefill of several sequences packed end to end
  * without padding (variable-length batch).
  *
@@ -160,6 +179,18 @@ int attn_prefill_varlen_ex(const attn_bf16* q, const attn_bf16* k, const attn_bf
                            int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
                            int window_left, float softcap, const float* alibi_slopes,
                            void* stream);
+
+/*
+ * attn_prefill_varlen_ex2 -- attn_prefill_varlen_ex with the flags of
+ * attn_prefill_ex2 (ATTN_PREFILL_OUT_BF16: o is (n_q_heads, total_tokens,
+ * head_dim) bf16).  Rows outside every sequence are not written.  Everything
+ * else as attn_prefill_varlen_ex.
+ */
+int attn_prefill_varlen_ex2(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, void* o,
+                            float* lse, const int32_t* cu_seqlens, int num_seqs, int total_tokens,
+                            int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
+                            int window_left, float softcap, const float* alibi_slopes,
+                            unsigned flags, void* stream);
 
 /*
  * attn_decode_num_splits -- the split-count policy for single-token decode.

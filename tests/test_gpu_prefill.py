@@ -123,6 +123,33 @@ def test_batch_with_l2_grouping_sampled(dev):
     compare(o[idx], lse[idx], o_ref, lse_ref, "B=2 N=16384 grouped")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,N,D,causal,variant", [
+    (1, 4, 2, 1000, 128, True, {}),
+    (2, 2, 1, 300, 64, False, {}),
+    (1, 2, 2, 700, 256, True, {}),
+    (1, 4, 1, 900, 128, True, {"window_left": 200}),
+    (1, 4, 2, 600, 128, True, {"softcap": 30.0}),
+    (1, 4, 2, 640, 128, False, {"alibi": True}),
+])
+def test_bf16_output_is_the_rounded_fp32_output(dev, B, Hq, Hkv, N, D, causal, variant):
+    """attn_prefill_ex2 with ATTN_PREFILL_OUT_BF16: O is acc / l rounded once
+    to bf16, so it equals the fp32 O of the same inputs rounded to nearest,
+    bit for bit, and the LSE is unchanged."""
+    x = W.make_prefill(B, Hq, Hkv, N, D, seed=N + D + B, causal=causal)
+    kw = {k_: v_ for k_, v_ in variant.items() if k_ != "alibi"}
+    if variant.get("alibi"):
+        kw["alibi_slopes"] = torch.tensor([2.0 ** (-(h + 1)) for h in range(Hq)],
+                                          dtype=torch.float32, device=dev)
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    o32, l32 = attn.prefill(q, k, v, x.scale, causal, **kw)
+    o16 = torch.full((B, Hq, N, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    o16, l16 = attn.prefill(q, k, v, x.scale, causal, out=o16, out_dtype=torch.bfloat16, **kw)
+    attn.check_device_status()
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(l16, l32)
+
+
 def test_closed_forms_on_gpu(dev):
     """q = 0 gives LSE_i = ln(i+1) and O_i = mean(v_0..v_i); V = 1 gives O = 1."""
     x = W.make_prefill(1, 2, 1, 700, 128, seed=3)

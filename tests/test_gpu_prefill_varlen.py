@@ -144,3 +144,25 @@ def test_more_sequences_than_one_launch(dev, n_seqs, d, variant):
     T0 = int(x.cu_seqlens[-1])
     compare(o[:, :T0], lse[:, :T0], o_ref[:, :T0], lse_ref[:, :T0], f"{n_seqs} sequences {variant}")
     assert torch.isnan(o[:, T0:]).all() and torch.isnan(lse[:, T0:]).all()
+
+
+@pytest.mark.parametrize("lens,d,variant", [([1, 127, 0, 129, 300, 45], 128, {}),
+                                            ([700, 33, 64], 64, {"window_left": 50}),
+                                            ([400, 129, 1], 256, {})])
+def test_varlen_bf16_output_is_the_rounded_fp32_output(dev, lens, d, variant):
+    """attn_prefill_varlen_ex2 with bf16 O: the rounded fp32 O of the same
+    call, bit for bit, including the last boxes of sequences that are written
+    row by row; rows outside every sequence untouched."""
+    x = W.make_prefill_varlen(lens, 4, 2, d, seed=sum(lens) + d, extra_rows=5)
+    q, k, v, cu = x.q.to(dev), x.k.to(dev), x.v.to(dev), x.cu_seqlens.to(dev)
+    n_q, T, _ = x.q.shape
+    o32, l32 = attn.prefill_varlen(q, k, v, cu, x.scale, True, **variant)
+    o16 = torch.full((n_q, T, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    l16 = torch.full((n_q, T), float("nan"), device=dev)
+    attn.prefill_varlen(q, k, v, cu, x.scale, True, out=o16, lse=l16, out_dtype=torch.bfloat16,
+                        **variant)
+    attn.check_device_status()
+    T0 = int(x.cu_seqlens[-1])
+    assert torch.equal(o16[:, :T0], o32[:, :T0].to(torch.bfloat16))
+    assert torch.equal(l16[:, :T0], l32[:, :T0])
+    assert torch.isnan(o16[:, T0:].float()).all()

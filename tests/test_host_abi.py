@@ -54,6 +54,22 @@ def _prefill(L, **kw):
                           a["n"], a["d"], a["scale"], a["causal"], None)
 
 
+def test_prefill_ex2_flags(L):
+    """attn_prefill_ex2 / attn_prefill_varlen_ex2: unknown flag bits are
+    refused before any launch; the rest of the validation is the _ex calls'."""
+    c = _lib.status_codes()
+    f = L.attn_prefill_ex2
+    base = (P, P, P, P, P, 1, 4, 2, 128, 128, 0.1, 1, -1, 0.0, None)
+    assert f(*base, 2, None) == c["ATTN_ERR_SHAPE"]
+    assert f(*base, 1 << 31, None) == c["ATTN_ERR_SHAPE"]
+    assert f(P, P, P, None, P, 1, 4, 2, 128, 128, 0.1, 1, -1, 0.0, None, 1, None) == c["ATTN_ERR_NULL"]
+    assert f(P, P, P, P + 8, P, 1, 4, 2, 128, 128, 0.1, 1, -1, 0.0, None, 1, None) == c["ATTN_ERR_ALIGN"]
+    g = L.attn_prefill_varlen_ex2
+    vbase = (P, P, P, P, P, P, 3, 512, 8, 2, 128, 0.1, 1, -1, 0.0, None)
+    assert g(*vbase, 4, None) == c["ATTN_ERR_SHAPE"]
+    assert g(P, P, P, P, P, P, 3, 512, 8, 2, 96, 0.1, 1, -1, 0.0, None, 1, None) == c["ATTN_ERR_HEADDIM"]
+
+
 def test_prefill_validation(L):
     c = _lib.status_codes()
     assert _prefill(L, q=None) == c["ATTN_ERR_NULL"]
