@@ -167,3 +167,73 @@ def test_decode_append_fuzz(dev, case):
     bits = lambda t: t.detach().cpu().contiguous().view(torch.int16)
     assert torch.equal(bits(kc), bits(kc_ref)), what + ": K cache"
     assert torch.equal(bits(vc), bits(vc_ref)), what + ": V cache"
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_prefill_fp8_fuzz(dev, case):
+    """FP8 prefill (block scales, rotation) on random shapes: LSE within 1e-3
+    of exact attention on the dequantised inputs, O within the P-rounding
+    bound (as the FP8 parity tests)."""
+    from test_gpu_fp8 import fp8_inputs, p_rounding_sigma, signs_for
+    from oracle import fp8_ref as F
+
+    rng = np.random.default_rng(5000 + case)
+    d = int(rng.choice([64, 128]))
+    B = int(rng.integers(1, 3))
+    hkv = int(rng.choice([1, 2, 4]))
+    hq = hkv * int(rng.choice([1, 2, 4, 7]))
+    N = 16 * int(rng.integers(1, 65))
+    causal = bool(rng.integers(0, 2))
+    x = W.make_prefill(B, hq, hkv, N, d, seed=case, causal=causal)
+    signs = signs_for(d, case)
+    q8, k8, v8t, qs, ks, vs = fp8_inputs(x, dev, signs)
+    o, lse = attn.prefill_fp8(q8, k8, v8t, qs, ks, vs, x.scale, causal)
+    attn.check_device_status()
+    qz = F.quantize_for_attention(x.q, x.k, x.v, signs)
+    o_ref, lse_ref = F.prefill_fp8(qz, x.scale, causal)
+    what = f"case {case}: B{B} H{hq}/{hkv} N{N} d{d} causal={causal}"
+    assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= 1e-3, what
+    z = np.abs(o.double().cpu().numpy() - o_ref) / (p_rounding_sigma(qz, x.scale, causal) + 1e-6)
+    assert z.max() <= 6.0 and z.mean() <= 1.0, (what, z.max(), z.mean())
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_prefill_fp8_varlen_fuzz(dev, case):
+    """Packed FP8 prefill on random sequence lists (every sequence starting
+    at a multiple of 16 rows; the last one of any length)."""
+    import math
+
+    from test_gpu_fp8 import packed_sigma, signs_for
+    from oracle import fp8_ref as F
+
+    rng = np.random.default_rng(6000 + case)
+    d = int(rng.choice([64, 128]))
+    hkv = int(rng.choice([1, 2, 4]))
+    hq = hkv * int(rng.choice([1, 2, 4]))
+    n_seqs = int(rng.integers(1, 7))
+    lens = [16 * int(n) for n in rng.integers(0, 41, n_seqs - 1)] + [int(rng.integers(1, 500))]
+    causal = bool(rng.integers(0, 2))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = -(-int(cu[-1]) // 16) * 16 + 16
+    g = torch.Generator().manual_seed(case)
+    q = torch.randn(hq, T, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(hkv, T, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(hkv, T, d, generator=g).to(torch.bfloat16)
+    signs = signs_for(d, case)
+    sg, cud = torch.from_numpy(signs).to(dev), torch.from_numpy(cu).to(dev)
+    q8, qs = attn.quantize_fp8_varlen(q.to(dev), cud, sg)
+    k8, ks = attn.quantize_fp8_varlen(k.to(dev), cud, sg)
+    v8t, vs = attn.quantize_fp8(v.to(dev), None, block_rows=0, transpose=True)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = nan_like((hq, T, d), dev), nan_like((hq, T), dev)
+    attn.prefill_fp8_varlen(q8, k8, v8t, qs, ks, vs, cud, scale, causal, out=o, lse=lse)
+    attn.check_device_status()
+    qz = F.quantize_for_attention_varlen(q, k, v, cu, signs)
+    o_ref, lse_ref = F.prefill_fp8_varlen(qz, scale, causal)
+    T0 = int(cu[-1])
+    what = f"case {case}: lens {lens} H{hq}/{hkv} d{d} causal={causal}"
+    assert np.abs(lse[:, :T0].double().cpu().numpy() - lse_ref[:, :T0]).max() <= 1e-3, what
+    z = np.abs(o[:, :T0].double().cpu().numpy() - o_ref[:, :T0]) / (
+        packed_sigma(qz, scale, causal)[:, :T0] + 1e-6)
+    assert z.max() <= 6.0 and z.mean() <= 1.0, (what, z.max(), z.mean())
+    assert torch.isnan(o[:, T0:]).all()
