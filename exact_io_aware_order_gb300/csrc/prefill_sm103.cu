@@ -64,6 +64,24 @@ constexpr int kBM = 128;                 // rows per query tile
 // 64 columns and O's 256 columns then fit the 512 TMEM columns).
 template <int D>
 constexpr int key_tile() { return D == 256 ? 64 : 128; }
+
+// TMEM buffers: SB S buffers (kBN columns each; P aliases S) and OB O
+// accumulators (D columns each), within 512 columns.  With two O buffers an
+// item's first P V product need not wait for the epilogue to read the last
+// item's O; two S buffers make S(j + 2) wait for P V(j).  head_dim 64: three
+// S and two O (384 + 128).  128: three S and one O (384 + 128) in bf16, where
+// the softmax leaves the S-after-P V chain too little slack (measured 15%
+// slower with two and two); two S and two O (256 + 256) in FP8, whose halved
+// products leave enough (measured 1.3% faster).  256: three S of 64 keys and
+// one O (192 + 256).
+template <int D, bool FP8>
+__host__ __device__ constexpr int s_bufs() {
+  return (D == 128 && FP8) ? 2 : 3;
+}
+template <int D, bool FP8>
+__host__ __device__ constexpr int o_bufs() {
+  return (D == 256 || (D == 128 && !FP8)) ? 1 : 2;
+}
 constexpr int kThreads = 352;            // 11 warps
 constexpr int kSoftmaxThreads = 128;     // warps 0-3: one query row per thread
 constexpr int kProducerWarp = 4;
@@ -71,7 +89,8 @@ constexpr int kSWarp = 5;                // issues S = Q K^T
 constexpr int kPVWarp = 6;               // issues O += P V
 constexpr int kEpiWarp0 = 7;             // warps 7-10: O / LSE epilogue
 constexpr int kEpiThreads = 128;
-constexpr int kSBuf = 3;                 // S buffers in TMEM
+constexpr int kSBuf = 3;                 // most S buffers in TMEM (barrier layout)
+constexpr int kOBufMax = 2;              // most O buffers in TMEM (barrier layout)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -108,7 +127,7 @@ struct PrefillSmem {
   // slot), s_full/p_full/pv_done [3], o_full, o_empty, stats_full/stats_empty [2],
   // drain_s, drain_pv
   static constexpr int kNumBars =
-      2 * kQSlots + 2 * kKSlots + 2 * kVSlots + 3 * kSBuf + 2 + 4 + 2;
+      2 * kQSlots + 2 * kKSlots + 2 * kVSlots + 3 * kSBuf + 2 * kOBufMax + 4 + 2;
   static constexpr int kStats = kBar + kNumBars * 8;           // float2 (m, l) [2][128]
   static constexpr int kMisc = kStats + 2 * 128 * 8;           // tmem base, abort flag
   // Packed variable-length mode: per sequence its first row, its length and
@@ -280,6 +299,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const PrefillParams p) {
   constexpr bool FP8 = VARIANT == kFp8;
   constexpr int kBN = key_tile<D>();
+  constexpr int SB = s_bufs<D, FP8>(), OB = o_bufs<D, FP8>();
+  static_assert(SB <= kSBuf && OB <= kOBufMax && SB * kBN + OB * D <= (int)kTmemCols,
+                "TMEM budget");
   // ALiBi at head_dim <= 128: the tensor core adds the bias's per-key part.
   constexpr bool XB = VARIANT == kWindowAlibi && D <= 128;
   // Edge tiles: masked per 32-column chunk, with a warp-wide test first (the
@@ -303,7 +325,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int kQFull = 0, kQEmpty = kQFull + RQ, kKFull = kQEmpty + RQ, kKEmpty = kKFull + RK,
             kVFull = kKEmpty + RK, kVEmpty = kVFull + RV, kSFull = kVEmpty + RV,
             kPFull = kSFull + kSBuf, kPVDone = kPFull + kSBuf, kOFull = kPVDone + kSBuf,
-            kOEmpty = kOFull + 1, kStFull = kOEmpty + 1, kStEmpty = kStFull + 2,
+            kOEmpty = kOFull + kOBufMax, kStFull = kOEmpty + kOBufMax, kStEmpty = kStFull + 2,
             kDrainS = kStEmpty + 2, kDrainPV = kDrainS + 1;
   float2* stats = reinterpret_cast<float2*>(smem + L::kStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -323,13 +345,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(bar(kVFull + i), 1);
       mbar_init(bar(kVEmpty + i), 1);
     }
-    for (int i = 0; i < kSBuf; ++i) {
+    for (int i = 0; i < SB; ++i) {
       mbar_init(bar(kSFull + i), 1);
       mbar_init(bar(kPFull + i), kSoftmaxThreads);
       mbar_init(bar(kPVDone + i), 1);
     }
-    mbar_init(bar(kOFull), 1);
-    mbar_init(bar(kOEmpty), kEpiThreads);
+    for (int i = 0; i < OB; ++i) {
+      mbar_init(bar(kOFull + i), 1);
+      mbar_init(bar(kOEmpty + i), kEpiThreads);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kStFull + i), kSoftmaxThreads);
       mbar_init(bar(kStEmpty + i), kEpiThreads);
@@ -419,8 +443,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S buffers [0, kBN), [kBN, 2 kBN), [2 kBN, 3 kBN) | O [3 kBN, 3 kBN + D)
-  const uint32_t tO = tmem + 3u * kBN;
+  // TMEM columns: SB S buffers of kBN columns, then OB O buffers of D columns
+  // (item r accumulates into O buffer r % OB, so with two the next item's
+  // products need not wait for the epilogue to read the last item's O).
+  const uint32_t tO = tmem + (uint32_t)(SB * kBN);
+  auto o_buf = [&](int r) { return tO + (uint32_t)((r % OB) * D); };
   const WaitCtl ctl{abort_flag, p.err_word, p.timeout_ns};
   const int total = VARLEN ? item_prefix[p.num_seqs] : p.total_tiles;
 
@@ -548,9 +575,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!mbar_wait(bar(kQFull + qs), (r / RQ) & 1, ctl)) { ok = false; break; }
         const uint32_t q_lo = sw128_desc_lo(smem_u32(smem + L::kQ + qs * L::kQTileBytes), 16);
         for (int j = 0; j < t.n; ++j, ++g) {
-          const int b = g % kSBuf, slot = g % RK;
-          // Buffer b last held P(g-3): PV(g-3) must have read it.
-          if (g >= kSBuf && !mbar_wait(bar(kPVDone + b), ((g / kSBuf) - 1) & 1, ctl)) { ok = false; break; }
+          const int b = g % SB, slot = g % RK;
+          // Buffer b last held P(g - SB): PV(g - SB) must have read it.
+          if (g >= SB && !mbar_wait(bar(kPVDone + b), ((g / SB) - 1) & 1, ctl)) { ok = false; break; }
           if (!mbar_wait(bar(kKFull + slot), (g / RK) & 1, ctl)) { ok = false; break; }
           const uint32_t kb = k_lo0 + (uint32_t)((slot * L::kTileBytes) >> 4);
           const uint32_t dS = tmem + (uint32_t)(b * kBN);
@@ -603,12 +630,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int w = item_of(r, total);
         if (w < 0) break;
         const int n = tile_of<VARLEN, VARIANT, kBN>(w, p, seqt).n;
+        const int ob = r % OB;
+        const uint32_t tOr = o_buf(r);
         for (int j = 0; j < n; ++j, ++g) {
-          const int b = g % kSBuf, slot = g % RV;
-          if (!mbar_wait(bar(kPFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
-          // The first product of an item overwrites O: the epilogue must have
-          // read the previous item's O out of TMEM.
-          if (j == 0 && r > 0 && !mbar_wait(bar(kOEmpty), (r - 1) & 1, ctl)) { ok = false; break; }
+          const int b = g % SB, slot = g % RV;
+          if (!mbar_wait(bar(kPFull + b), (g / SB) & 1, ctl)) { ok = false; break; }
+          // The first product of an item overwrites its O buffer: the epilogue
+          // must have read that buffer's previous item (r - OB) out of TMEM.
+          if (j == 0 && r >= OB && !mbar_wait(bar(kOEmpty + ob), ((r / OB) - 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();  // P(g) was written to TMEM by the softmax threads
           if (!mbar_wait(bar(kVFull + slot), (g / RV) & 1, ctl)) { ok = false; break; }
           // B = V tile rows [16kk, 16kk+16): 16 rows x 128 B per k step; the
@@ -620,16 +652,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // 32 keys per step: 8 columns of P (four e4m3 per column), 32 bytes of each V^T row
 #pragma unroll
             for (int kk = 0; kk < kBN / 32; ++kk)
-              mma_ts_lo_f8(tO, aP + kk * 8, vb + ((kk * 32) >> 4), dhi, id_pv, kk > 0 ? 1u : acc0);
+              mma_ts_lo_f8(tOr, aP + kk * 8, vb + ((kk * 32) >> 4), dhi, id_pv, kk > 0 ? 1u : acc0);
           } else {
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts_lo(tO, aP + kk * 8, vb + ((kk * 16 * 128) >> 4), dhi, id_pv,
+              mma_ts_lo(tOr, aP + kk * 8, vb + ((kk * 16 * 128) >> 4), dhi, id_pv,
                         kk > 0 ? 1u : acc0);
           }
           mma_commit(bar(kVEmpty + slot));
           mma_commit(bar(kPVDone + b));
-          if (j == n - 1) mma_commit(bar(kOFull));
+          if (j == n - 1) mma_commit(bar(kOFull + ob));
         }
       }
       mma_commit(bar(kDrainPV));
@@ -642,13 +674,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // ============================ softmax warps ============================
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int row = warp * 32 + lane;               // row within the tile (= TMEM lane)
-    const uint32_t tOm = tO + lane_base;
     bool ok = true;
     int g = 0;
     for (int r = 0; ok; ++r) {
       const int w = item_of(r, total);
       if (w < 0) break;
       const Tile t = tile_of<VARLEN, VARIANT, kBN>(w, p, seqt);
+      const uint32_t tOm = o_buf(r) + lane_base;  // this item's O buffer
       const int q0 = t.qrel, q_row = q0 + row;  // indices within the sequence
       float m = -INFINITY, l = 0.f;   // running max (log2 domain) and sum of the row
       // ALiBi: this head's slope in log2 units.  At head_dim <= 128 the
@@ -668,10 +700,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       float q_scale = 1.f;
       if constexpr (FP8) q_scale = p.q_scales[(size_t)t.zq * p.n_q_tiles + t.tile0 + t.qrel / kBM];
       for (int j = 0; j < t.n; ++j, ++g) {
-        const int b = g % kSBuf;
+        const int b = g % SB;
         if constexpr (FP8)
           sl2 = p.sl2 * q_scale * p.k_scales[(size_t)t.zk * p.n_q_tiles + t.tile0 + t.j0 + j];
-        if (!mbar_wait_warp(bar(kSFull + b), (g / kSBuf) & 1, ctl)) { ok = false; break; }
+        if (!mbar_wait_warp(bar(kSFull + b), (g / SB) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tSm = tmem + (uint32_t)(b * kBN) + lane_base;
         // The whole S row: four 32-column loads in flight, one wait.
@@ -869,8 +901,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         l += rsum.x + rsum.y;
         if (rescale_o) {
           // O must hold every P V product up to key tile j-1 before it is rescaled.
-          const int bp = (g - 1) % kSBuf;
-          if (!mbar_wait_warp(bar(kPVDone + bp), ((g - 1) / kSBuf) & 1, ctl)) { ok = false; break; }
+          const int bp = (g - 1) % SB;
+          if (!mbar_wait_warp(bar(kPVDone + bp), ((g - 1) / SB) & 1, ctl)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -908,7 +940,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // whole lines and the load/store unit stays free for the softmax warps.
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const uint32_t tOm = tO + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t lane_q = (uint32_t)(quarter * 32) << 16;
     const uint32_t stage = smem_u32(smem + L::kStage + quarter * 4096);
     const uint64_t pol_out = l2_policy_evict_first();  // O is not read again here
     bool ok = true;
@@ -916,7 +948,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int w = item_of(r, total);
       if (w < 0) break;
       const Tile t = tile_of<VARLEN, VARIANT, kBN>(w, p, seqt);
-      if (!mbar_wait_warp(bar(kOFull), r & 1, ctl)) { ok = false; break; }
+      const int ob = r % OB;
+      const uint32_t tOm = o_buf(r) + lane_q;  // this item's O buffer
+      if (!mbar_wait_warp(bar(kOFull + ob), (r / OB) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       const int ss = r & 1;
       const int row0 = t.row0 + quarter * 32;  // tensor row of this warp's box
@@ -1009,7 +1043,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int c = 0; c < D / 32; ++c) tmem_ld32(tOm + c * 32, acc[c]);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar(kOEmpty));  // O may now be overwritten by the next item
+        mbar_arrive(bar(kOEmpty + ob));  // this O buffer may now take item r + OB
         if (!mbar_wait_warp(bar(kStFull + ss), (r >> 1) & 1, ctl)) { ok = false; break; }
         ml = stats[ss * 128 + row];
         mbar_arrive(bar(kStEmpty + ss));
@@ -1029,7 +1063,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           tmem_wait_ld();
           if (h == D / kEC - 1) {
             tc_fence_before();
-            mbar_arrive(bar(kOEmpty));
+            mbar_arrive(bar(kOEmpty + ob));
           }
           store_cols(acc, h * kEC, inv_l);
         }
