@@ -19,13 +19,15 @@
 //   * key/value tiles of 128 keys (64 at head_dim 256), streamed by TMA
 //     (128-byte swizzle, 3-D tensor maps so rows past the end read as zero)
 //     into a K ring and a V ring in shared memory; Q tiles double-buffered;
-//   * TMEM (512 columns): three S buffers and O.  S is triple-buffered, so the
-//     tensor core computes S(j+1), S(j+2) while the softmax works on S(j).
+//   * TMEM (512 columns): S buffers and O accumulators (see s_bufs / o_bufs):
+//     three S buffers and one O in bf16 at head_dim 128, so the tensor core
+//     computes S(j+1), S(j+2) while the softmax works on S(j); two O (items
+//     alternating) at head_dim 64 and in FP8.
 //     P(j) is written as bf16 over the first half of S(j)'s buffer and feeds
 //     O += P V straight from TMEM (A operand in tensor memory), V from shared
 //     memory (MN-major);
 //   * two threads issue tcgen05.mma: warp 5 the S products (S(j) as soon as
-//     K_j is in and the P V product three tiles back has freed the buffer),
+//     K_j is in and the P V product that last read its buffer has finished),
 //     warp 6 the P V products (as soon as P(j) and V_j are ready).  Every
 //     wait or commit stalls its issuing thread for longer than one
 //     128x128x16 MMA runs, so one thread alone leaves the tensor core idle
@@ -43,7 +45,8 @@
 //   * flavours compiled separately, so the plain kernel carries none of the
 //     others' code: sliding window, window and/or soft-capping, ALiBi (with
 //     an optional window), FP8 (e4m3 operands, kind::f8f6f4, per-block
-//     scales), each padded or packed (variable-length sequences);
+//     scales), each padded or packed (variable-length sequences), and each
+//     with an fp32 or a bf16 O;
 //   * every wait is bounded; on a timeout all roles leave their loops, the
 //     CTA waits for in-flight copies and MMAs, frees TMEM and exits.
 #include <cstdint>
