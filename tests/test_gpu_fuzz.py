@@ -60,8 +60,13 @@ def test_prefill_fuzz(dev, case):
     attn.prefill(x.q.to(dev), x.k.to(dev), x.v.to(dev), x.scale, causal, out=o, lse=lse, **kw)
     attn.check_device_status()
     o_ref, lse_ref = oracle.prefill(x.q, x.k, x.v, x.scale, causal, **okw)
-    compare(o, lse, o_ref, lse_ref,
-            f"case {case}: B{B} H{hq}/{hkv} N{N} d{d} causal={causal} {variant}")
+    what = f"case {case}: B{B} H{hq}/{hkv} N{N} d{d} causal={causal} {variant}"
+    compare(o, lse, o_ref, lse_ref, what)
+    # the same call with a bf16 O: the fp32 O rounded once, bit for bit
+    o16, l16 = attn.prefill(x.q.to(dev), x.k.to(dev), x.v.to(dev), x.scale, causal,
+                            out_dtype=torch.bfloat16, **kw)
+    attn.check_device_status()
+    assert torch.equal(o16, o.to(torch.bfloat16)) and torch.equal(l16, lse), what + " (bf16 O)"
 
 
 @pytest.mark.parametrize("case", range(32))
@@ -84,9 +89,15 @@ def test_prefill_varlen_fuzz(dev, case):
     attn.check_device_status()
     o_ref, lse_ref = oracle.prefill_varlen(x.q, x.k, x.v, x.cu_seqlens, x.scale, causal, **okw)
     T0 = int(x.cu_seqlens[-1])
-    compare(o[:, :T0], lse[:, :T0], o_ref[:, :T0], lse_ref[:, :T0],
-            f"case {case}: lens {lens} H{hq}/{hkv} d{d} causal={causal} {variant}")
+    what = f"case {case}: lens {lens} H{hq}/{hkv} d{d} causal={causal} {variant}"
+    compare(o[:, :T0], lse[:, :T0], o_ref[:, :T0], lse_ref[:, :T0], what)
     assert torch.isnan(o[:, T0:]).all() and torch.isnan(lse[:, T0:]).all()
+    o16 = torch.full((n_q, T, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    attn.prefill_varlen(x.q.to(dev), x.k.to(dev), x.v.to(dev), x.cu_seqlens.to(dev), x.scale,
+                        causal, out=o16, out_dtype=torch.bfloat16, **kw)
+    attn.check_device_status()
+    assert torch.equal(o16[:, :T0], o[:, :T0].to(torch.bfloat16)), what + " (bf16 O)"
+    assert torch.isnan(o16[:, T0:].float()).all(), what + " (bf16 O past the end)"
 
 
 @pytest.mark.parametrize("case", range(48))
